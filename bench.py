@@ -1,0 +1,333 @@
+"""Benchmark of the DSA decode layer step on GB300.
+
+Workload: batch-8 decode, 65,536-token context per request, FP8 index keys and
+latents in a 1 GiB packed pool with a randomly permuted block table, top-2048
+(the 64K decode configuration of the benchmark definition; seeded synthetic
+data).  One step = one dsa_layer_step call for the whole batch: indexer scores,
+exact top-2048, sparse MLA (96 heads), split-K LSE combine.
+
+Prints one JSON line (rank 0).  `value` is layer-steps/s over all ranks
+(replicas: each rank runs its own batch; weak scaling).  The L2 is flushed
+(256 MiB write) before every timed step, outside the timed events.  The step is
+replayed from a CUDA graph captured from the C-ABI call; `e2e` instead runs the
+plain C-ABI call each step with the step's query tensors copied from pinned host
+memory and the output copied back inside the timed region.
+
+`--impl reference` times the float64 CPU oracle on the same workload (the
+reference arm of this build; there is no other runnable implementation).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+WORKLOAD = "decode b8 x 65536 ctx, FP8 keys+latents, 1 GiB packed pool, permuted block table, top-2048"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    return rank, world, local
+
+
+def algorithmic_bytes(wl, idx):
+    """Bytes the method must move for one step: every index key of each context,
+    the latents of the union of selected tokens per request, the query tensors
+    and the output (intermediate scores/candidates are not counted)."""
+    key_b = 132 if wl.idx_fmt == 0 else 68
+    lat_b = 576 if wl.lat_fmt == 0 else 352
+    total = 0
+    for b in range(wl.num_reqs):
+        toks = np.nonzero(wl.q_req == b)[0]
+        L = int(wl.ctx_lens[b])
+        sel = np.unique(idx[toks][idx[toks] >= 0]) if toks.size else np.zeros(0)
+        total += L * key_b + sel.size * lat_b
+    total += wl.num_tokens * (4096 + 128 + 96 * 576 * 2 + 96 * 512 * 2)
+    return total
+
+
+def scorer_bytes(wl):
+    key_b = 132 if wl.idx_fmt == 0 else 68
+    return int(sum(int(L) for L in wl.ctx_lens)) * key_b + wl.num_tokens * (4096 + 128)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The float64 oracle, as it stands, on whole steps of the same workload."""
+    from oracle import dsa_oracle as O
+    lay = O.Layout(wl.pool, wl.row_stride, wl.idx_page_offset, wl.lat_page_offset, wl.block_size, wl.idx_fmt,
+                   wl.lat_fmt)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        O.layer_step(lay, wl.block_table, wl.ctx_lens, wl.q_req, wl.q_pos, wl.q_idx, wl.w, wl.q, topk=wl.topk,
+                     sm_scale=wl.sm_scale)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or steps >= 50:
+            break
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    return {"value": steps / dt, "unit": "layer-steps/s", "cores": int(threads), "kind": "oracle",
+            "sample": f"{steps} whole steps ({wl.num_tokens} queries each) in {dt:.1f} s; numpy float64, "
+                      f"BLAS threads = {threads} of {os.cpu_count()} host cores"}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    # K timed steps of the oracle, each a bounded sample: one query of the batch
+    # (the per-step value is extrapolated to the 8-query step).
+    from oracle import dsa_oracle as O
+    lay = O.Layout(wl.pool, wl.row_stride, wl.idx_page_offset, wl.lat_page_offset, wl.block_size, wl.idx_fmt,
+                   wl.lat_fmt)
+    for i in range(args.warmup):
+        O.layer_step(lay, wl.block_table, wl.ctx_lens, wl.q_req, wl.q_pos, wl.q_idx, wl.w, wl.q, tokens=[i % 8])
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        O.layer_step(lay, wl.block_table, wl.ctx_lens, wl.q_req, wl.q_pos, wl.q_idx, wl.w, wl.q, tokens=[i % 8])
+        times.append((time.perf_counter() - t0) * wl.num_tokens)
+    ms = 1000 * statistics.mean(times)
+    value = 1000.0 / ms
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or str(os.cpu_count())
+    line = {"impl": "reference", "metric": "DSA decode layer-steps/s (64K context, batch 8)", "value": value,
+            "unit": "layer-steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "layer-steps/s", "cores": int(threads), "kind": "oracle",
+                             "sample": "one query of the 8-query step per timed step, times 8"},
+            "e2e": {"value": value, "unit": "layer-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    from dsa_sparse_attention_gb300 import workloads as W
+    wl = W.config(1, seed=0)
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    from dsa_sparse_attention_gb300.build import build
+    build()
+    import dsa_sparse_attention_gb300 as dsa
+    from dsa_sparse_attention_gb300.harness import DeviceWorkload
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    dw = DeviceWorkload(wl)
+    stream = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        dw.layer_step(stream)           # eager warm-up (sets kernel attributes)
+    stream.synchronize()
+    assert dsa.dsa_check(dw.ws, stream) == 0
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        dw.layer_step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    n_kernels_per_step = 9   # plan, scorer, 3 histogram passes, count, emit, mla, combine
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for s in range(args.steps):
+            flush.zero_()
+            evs[s][0].record(stream)
+            graph.replay()
+            evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * 1000.0 / ms
+
+    # dominant kernel (indexer scorer) timed alone, same stream, L2 flushed
+    scores = torch.empty(wl.num_tokens, dw.ld, dtype=torch.float32, device="cuda")
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    with torch.cuda.stream(stream):
+        for i in range(23):
+            flush.zero_()
+            if i >= 3:
+                sev[i - 3][0].record(stream)
+            dsa.dsa_indexer_score(dw.layout, dw.batch, dw.q_idx, dw.w, scores, dw.ld, dw.ws, stream)
+            if i >= 3:
+                sev[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    sc_ms = statistics.mean(a.elapsed_time(b) for a, b in sev)
+    peak, peak_kind = load_peaks()
+    sc_gbs = scorer_bytes(wl) / (sc_ms * 1e-3) / 1e9
+
+    # whole-step algorithmic bytes
+    idx_np = dw.idx.cpu().numpy()
+    alg = algorithmic_bytes(wl, idx_np)
+    step_tbs = alg / (ms / world * 1e-3) / 1e12 if world == 1 else alg / (ms * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers
+    pin = {k: v.cpu().pin_memory() for k, v in
+           dict(q_idx=dw.q_idx, w=dw.w, q=dw.q, q_req=dw.q_req, q_pos=dw.q_pos, ctx=dw.ctx, bt=dw.bt).items()}
+    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = out_host.numel() * out_host.element_size()
+    dev = dict(q_idx=dw.q_idx, w=dw.w, q=dw.q, q_req=dw.q_req, q_pos=dw.q_pos, ctx=dw.ctx, bt=dw.bt)
+
+    def e2e_step():
+        for k, v in pin.items():
+            dev[k].copy_(v, non_blocking=True)
+        dw.layer_step(stream)
+        out_host.copy_(dw.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            flush.zero_()
+            stream.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            stream.synchronize()
+            e2e_ms.append((time.perf_counter() - t0) * 1000)
+    e2e_value = world * 1000.0 / statistics.mean(e2e_ms)
+    assert dsa.dsa_check(dw.ws, stream) == 0
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        line = {
+            "metric": "DSA decode layer-steps/s (64K context, batch 8)", "value": value, "unit": "layer-steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8/bf16/fp16 (fp32 acc)",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": wl.num_reqs, "ctx_len": int(wl.ctx_lens[0]), "topk": wl.topk,
+                       "l2": "flushed (256 MiB write) before every timed step", "graph": "CUDA graph replay",
+                       "parallelism": f"replicas x{world}"},
+            "achieved_hbm_tbs_step": step_tbs,
+            "achieved_frac_of_8tbs": step_tbs / 8.0,
+            "algorithmic_bytes_per_step": alg,
+            "roofline": {"bound": "hbm", "kernel": "indexer scorer (dsa_indexer_score: plan + scorer)",
+                         "achieved": sc_gbs, "peak": peak, "unit": "GB/s", "frac": sc_gbs / peak,
+                         "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                         "traffic": None, "launch_ms": sc_ms},
+            "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": n_kernels_per_step * args.steps,
+            "clocks": clk, "wall_s_timed": t_wall,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,390 @@
+// capi.cu — the extern "C" entry points declared in include/dsa.h: host-side
+// validation, workspace carving, TMA descriptor encoding and kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dsa.h"
+
+#include "params.cuh"
+
+using namespace dsa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kTopkChunk = 4096;
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Ws {
+  size_t status = 0;
+  size_t plan_hdr = 0, groups = 0;
+  size_t hist = 0, counts = 0;
+  size_t scores = 0;
+  int64_t ld = 0;
+  size_t idx = 0;
+  size_t part_o = 0, part_ml = 0;
+  int nsplit = 1, tps = 16;
+  int topk_nchunks = 1;
+  size_t total = 0;
+};
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+dsa_status check_layout(const dsa_kv_layout* l, bool need_pool = true) {
+  if (!l) return DSA_ERR_INVALID_ARG;
+  if (need_pool && !l->pool) return DSA_ERR_INVALID_ARG;
+  if (l->reserved != 0 || l->num_rows <= 0 || l->num_rows > (int64_t(1) << 31) - 1) return DSA_ERR_INVALID_ARG;
+  if (!is_pow2(l->block_size) || l->block_size < 16 || l->block_size > 256) return DSA_ERR_UNSUPPORTED;
+  if (l->idx_fmt != DSA_IDX_FP8 && l->idx_fmt != DSA_IDX_MXFP4) return DSA_ERR_INVALID_ARG;
+  if (l->lat_fmt != DSA_LAT_FP8 && l->lat_fmt != DSA_LAT_NVFP4) return DSA_ERR_INVALID_ARG;
+  if (l->idx_fmt != DSA_IDX_FP8 || l->lat_fmt != DSA_LAT_FP8) return DSA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(l->pool) & 15) || (l->row_stride_bytes & 15) || (l->idx_page_offset & 15) ||
+      (l->lat_page_offset & 15))
+    return DSA_ERR_INVALID_ARG;
+  const int64_t idx_pb = int64_t(l->block_size) * (l->idx_fmt == DSA_IDX_FP8 ? 132 : 68);
+  const int64_t lat_pb = int64_t(l->block_size) * (l->lat_fmt == DSA_LAT_FP8 ? 576 : 352);
+  if (l->idx_page_offset < 0 || l->lat_page_offset < 0 || l->idx_page_offset + idx_pb > l->row_stride_bytes ||
+      l->lat_page_offset + lat_pb > l->row_stride_bytes)
+    return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status check_batch(const dsa_batch* b, int block_size) {
+  if (!b) return DSA_ERR_INVALID_ARG;
+  if (b->num_tokens < 0 || b->num_reqs < 1 || (b->flags & ~DSA_BATCH_INVARIANT) || b->bt_stride < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (b->num_tokens > 0 && (!b->q_req || !b->q_pos)) return DSA_ERR_INVALID_ARG;
+  if (!b->ctx_lens || !b->block_table) return DSA_ERR_INVALID_ARG;
+  if (b->max_ctx_len < 1 || b->max_ctx_len > (int64_t(1) << 30)) return DSA_ERR_INVALID_ARG;
+  if (block_size > 0 && b->max_ctx_len > int64_t(b->bt_stride) * block_size) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+Ws plan_ws(const dsa_kv_layout* l, const dsa_batch* b, int topk) {
+  Ws w;
+  const int64_t T = b->num_tokens;
+  size_t off = 0;
+  w.status = off;
+  off += kStatusBytes;
+  w.plan_hdr = off;
+  off = align_up(off + sizeof(PlanHeader));
+  w.groups = off;
+  off = align_up(off + size_t(T > 0 ? T : 1) * sizeof(ScoreGroup));
+  w.topk_nchunks = static_cast<int>(cdiv(b->max_ctx_len, kTopkChunk));
+  w.hist = off;
+  off = align_up(off + size_t(T) * (2048 + 2048 + 1024) * 4);
+  w.counts = off;
+  off = align_up(off + size_t(T) * w.topk_nchunks * 2 * 4);
+  w.ld = (b->max_ctx_len + 3) / 4 * 4;
+  w.scores = off;
+  off = align_up(off + size_t(T) * size_t(w.ld) * 4);
+  w.idx = off;
+  off = align_up(off + size_t(T) * size_t(topk > 0 ? topk : 1) * 4);
+  // MLA split: enough CTAs to cover the GPU about twice
+  const int ntiles = static_cast<int>(cdiv(topk > 0 ? topk : 1, kSelTile));
+  int nsplit = 1;
+  if (b->flags & DSA_BATCH_INVARIANT)
+    nsplit = ntiles;   // fixed split: independent of the batch
+  else if (T > 0)
+    nsplit = static_cast<int>(cdiv(2 * num_sms(), T));
+  if (nsplit > ntiles) nsplit = ntiles;
+  if (nsplit < 1) nsplit = 1;
+  w.tps = static_cast<int>(cdiv(ntiles, nsplit));
+  w.nsplit = static_cast<int>(cdiv(ntiles, w.tps));
+  w.part_o = off;
+  if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * kVDim * 4);
+  w.part_ml = off;
+  if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * 8);
+  w.total = off;
+  (void)l;
+  return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over the index-key value bytes of every page: {128 B, block slots, rows}.
+bool make_key_map(CUtensorMap* m, const dsa_kv_layout* l) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const int box_rows = l->block_size < kKeyTile ? l->block_size : kKeyTile;
+  cuuint64_t dims[3] = {128, cuuint64_t(l->block_size), cuuint64_t(l->num_rows)};
+  cuuint64_t strides[2] = {128, cuuint64_t(l->row_stride_bytes)};
+  cuuint32_t box[3] = {128, cuuint32_t(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(l->pool)) + l->idx_page_offset;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q_idx [T*32 rows, 128 B], box = one token's 32 heads.
+bool make_qidx_map(CUtensorMap* m, const void* q_idx, int T) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, cuuint64_t(T) * kIdxHeads};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, kIdxHeads};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(q_idx), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q [T*96 rows, 576 bf16], box = 64 dims x 96 heads.
+bool make_q_map(CUtensorMap* m, const void* q, int T) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {kLatDim, cuuint64_t(T) * kMlaHeads};
+  cuuint64_t strides[1] = {kLatDim * 2};
+  cuuint32_t box[2] = {64, kMlaHeads};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+PoolView pool_view(const dsa_kv_layout* l) {
+  PoolView v;
+  v.pool = static_cast<const uint8_t*>(l->pool);
+  v.num_rows = l->num_rows;
+  v.row_stride = l->row_stride_bytes;
+  v.idx_off = l->idx_page_offset;
+  v.lat_off = l->lat_page_offset;
+  v.bs = l->block_size;
+  int lg = 0;
+  while ((1 << lg) < l->block_size) ++lg;
+  v.log2_bs = lg;
+  v.idx_fmt = l->idx_fmt;
+  v.lat_fmt = l->lat_fmt;
+  return v;
+}
+
+BatchView batch_view(const dsa_batch* b) {
+  BatchView v;
+  v.T = b->num_tokens;
+  v.B = b->num_reqs;
+  v.q_req = b->q_req;
+  v.q_pos = b->q_pos;
+  v.ctx_lens = b->ctx_lens;
+  v.bt = b->block_table;
+  v.bt_stride = b->bt_stride;
+  v.max_ctx = static_cast<int32_t>(b->max_ctx_len);
+  return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+dsa_status check_ws(void* ws, size_t bytes, const Ws& w) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return DSA_ERR_WORKSPACE;
+  if (bytes < w.total) return DSA_ERR_WORKSPACE;
+  return DSA_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q_idx, const float* w, float* scores,
+                       int64_t ld, void* ws, const Ws& wl, cudaStream_t st) {
+  const int T = b->num_tokens;
+  if (T == 0) return DSA_OK;
+  CUtensorMap kmap, qmap;
+  if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return DSA_ERR_CUDA;
+  const int G = (T == b->num_reqs) ? 1 : 8;
+  uint32_t* status = at<uint32_t>(ws, wl.status);
+  cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, wl.plan_hdr), 0, wl.hist - wl.plan_hdr, st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  BatchView bv = batch_view(b);
+  e = launch_plan_groups(bv, G, at<ScoreGroup>(ws, wl.groups), at<PlanHeader>(ws, wl.plan_hdr), status, st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  IndexerParams p;
+  p.pool = pool_view(l);
+  p.b = bv;
+  p.w = w;
+  p.scores = scores;
+  p.ld = ld;
+  p.hdr = at<PlanHeader>(ws, wl.plan_hdr);
+  p.groups = at<ScoreGroup>(ws, wl.groups);
+  p.status = status;
+  return cuda_status(launch_indexer_fp8(kmap, qmap, p, G, num_sms(), st));
+}
+
+dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* scores, int64_t ld, int topk,
+                    int32_t* idx, int32_t* phys, void* ws, const Ws& wl, cudaStream_t st) {
+  if (b->num_tokens == 0) return DSA_OK;
+  TopkParams p;
+  p.b = batch_view(b);
+  p.scores = scores;
+  p.ld = ld;
+  p.k = topk;
+  p.chunk = kTopkChunk;
+  p.hist1 = at<uint32_t>(ws, wl.hist);
+  p.hist2 = p.hist1 + size_t(b->num_tokens) * 2048;
+  p.hist3 = p.hist2 + size_t(b->num_tokens) * 2048;
+  p.counts = at<uint32_t>(ws, wl.counts);
+  p.nchunks = wl.topk_nchunks;
+  p.idx = idx;
+  p.phys = phys;
+  int lg = 0;
+  if (l)
+    while ((1 << lg) < l->block_size) ++lg;
+  p.log2_bs = lg;
+  p.status = at<uint32_t>(ws, wl.status);
+  return cuda_status(launch_topk(p, st));
+}
+
+dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, const int32_t* idx, int topk,
+                   float sm_scale, void* out, float* lse, void* ws, const Ws& wl, cudaStream_t st) {
+  const int T = b->num_tokens;
+  if (T == 0) return DSA_OK;
+  CUtensorMap qmap;
+  if (!make_q_map(&qmap, q, T)) return DSA_ERR_CUDA;
+  MlaParams p;
+  p.pool = pool_view(l);
+  p.b = batch_view(b);
+  p.idx = idx;
+  p.topk = topk;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.tps = wl.tps;
+  p.nsplit = wl.nsplit;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.part_o = at<float>(ws, wl.part_o);
+  p.part_ml = at<float2>(ws, wl.part_ml);
+  p.status = at<uint32_t>(ws, wl.status);
+  return cuda_status(launch_sparse_mla(qmap, p, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_DEVICE_CHECK: return "DSA_ERR_DEVICE_CHECK";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+size_t dsa_workspace_size(const dsa_kv_layout* layout, const dsa_batch* batch, int32_t topk) {
+  if (check_layout(layout, false) != DSA_OK) return 0;
+  if (check_batch(batch, layout->block_size) != DSA_OK) return 0;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return 0;
+  return plan_ws(layout, batch, topk).total;
+}
+
+dsa_status dsa_indexer_score(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
+                             float* scores, int64_t ld_scores, void* workspace, size_t workspace_bytes,
+                             dsa_stream_t stream) {
+  dsa_status s = check_layout(layout);
+  if (s != DSA_OK) return s;
+  if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
+  if (batch->num_tokens > 0 && (!q_idx || !w || !scores || !aligned16(q_idx) || !aligned16(w) || !aligned16(scores)))
+    return DSA_ERR_INVALID_ARG;
+  if (ld_scores < batch->max_ctx_len || (ld_scores & 3)) return DSA_ERR_INVALID_ARG;
+  const Ws wl = plan_ws(layout, batch, 1);
+  if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
+  return run_indexer(layout, batch, q_idx, w, scores, ld_scores, workspace, wl, stream);
+}
+
+dsa_status dsa_topk(const dsa_kv_layout* layout, const dsa_batch* batch, const float* scores, int64_t ld_scores,
+                    int32_t topk, int32_t* idx, int32_t* phys_slots, void* workspace, size_t workspace_bytes,
+                    dsa_stream_t stream) {
+  dsa_status s;
+  if (phys_slots && (s = check_layout(layout, false)) != DSA_OK) return s;
+  if ((s = check_batch(batch, layout ? layout->block_size : 0)) != DSA_OK) return s;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_INVALID_ARG;
+  if (batch->num_tokens > 0 && (!scores || !idx || !aligned16(scores))) return DSA_ERR_INVALID_ARG;
+  if (ld_scores < batch->max_ctx_len || (ld_scores & 3)) return DSA_ERR_INVALID_ARG;
+  dsa_kv_layout dummy{};
+  dummy.num_rows = 1;
+  dummy.block_size = 64;
+  const Ws wl = plan_ws(layout ? layout : &dummy, batch, topk);
+  if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
+  return run_topk(layout, batch, scores, ld_scores, topk, idx, phys_slots, workspace, wl, stream);
+}
+
+dsa_status dsa_sparse_mla(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q, const int32_t* idx,
+                          int32_t topk, float sm_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          dsa_stream_t stream) {
+  dsa_status s = check_layout(layout);
+  if (s != DSA_OK) return s;
+  if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
+  if (topk < 1 || topk > DSA_MAX_TOPK || !std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  if (batch->num_tokens > 0 && (!q || !idx || !out || !aligned16(q) || !aligned16(out))) return DSA_ERR_INVALID_ARG;
+  const Ws wl = plan_ws(layout, batch, topk);
+  if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
+  return run_mla(layout, batch, q, idx, topk, sm_scale, out, lse, workspace, wl, stream);
+}
+
+dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
+                          const void* q, int32_t topk, float sm_scale, int32_t* idx_out, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  dsa_status s = check_layout(layout);
+  if (s != DSA_OK) return s;
+  if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
+  if (topk < 1 || topk > DSA_MAX_TOPK || !std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  if (batch->num_tokens > 0 && (!q_idx || !w || !q || !out || !aligned16(q_idx) || !aligned16(w) ||
+                                !aligned16(q) || !aligned16(out)))
+    return DSA_ERR_INVALID_ARG;
+  const Ws wl = plan_ws(layout, batch, topk);
+  if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
+  float* scores = at<float>(workspace, wl.scores);
+  int32_t* idx = idx_out ? idx_out : at<int32_t>(workspace, wl.idx);
+  if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream)) != DSA_OK) return s;
+  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, nullptr, workspace, wl, stream)) != DSA_OK) return s;
+  return run_mla(layout, batch, q, idx, topk, sm_scale, out, lse, workspace, wl, stream);
+}
+
+dsa_status dsa_check(void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  if (!workspace || workspace_bytes < kStatusBytes) return DSA_ERR_WORKSPACE;
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  if (word == 0) return DSA_OK;
+  if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (word & DEV_TIMEOUT) return DSA_ERR_TIMEOUT;
+  return DSA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

@@ -1,0 +1,409 @@
+// indexer.cu — lightning-indexer scoring on the 5th-generation tensor cores.
+//
+// vLLM K3.1 Pro day-0 post, "Sparse Attention in K3.1 Pro": every earlier token
+// is scored for each query with 32 light heads against one FP8 index key,
+//   score(t, s) = sum_h w[t,h] * ReLU(q_idx[t,h,:] . key(s)),  key(s) = code(s) * scale(s).
+// "Low-latency decode: a fused DSA decode path" describes the scorer as
+// key-balanced; "AMD / Quantization" notes keys are reused across query rows
+// during speculative verification.  Both hold here:
+//  * The contraction is a dense GEMM per 128-key tile: D[key, (token,head)] =
+//    keys[128 x 128 B e4m3] x q_idx^T, M = 128 keys, N = 32 heads x (tokens of
+//    the group, 1..8), K = 128, tcgen05.mma kind::f8f6f4 with fp32 accumulation
+//    in TMEM.  A group's tokens share every key tile (one HBM read per key).
+//  * The grid is persistent; each CTA takes an equal contiguous range of the
+//    global key-tile enumeration (key-balanced across requests and groups).
+//  * Warp roles: warp 0 streams key pages with TMA (3-D map over the packed pool:
+//    128 B x block slots x rows, 128-byte swizzle) plus the per-token scales with
+//    bulk copies; warp 1 issues the MMAs; warps 2..9 read the accumulators
+//    (thread = key) and reduce sum_h w * ReLU(acc) * scale into fp32 scores.
+// Page translation (row = block_table[req][s / bs]) happens in the producer.
+#include <cuda.h>
+
+#include "params.cuh"
+
+namespace dsa {
+
+// ------------------------------------------------------------------ planning
+
+struct PlanParams {
+  BatchView b;
+  int G;                 // max tokens per group
+  ScoreGroup* groups;    // [T], zeroed by the host
+  PlanHeader* hdr;
+  uint32_t* status;
+};
+
+template <typename Op>
+__device__ int block_inclusive_scan(int v, int* sh, Op op, int identity) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int x = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = op(v, x);
+  }
+  if (lane == 31) sh[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int x = lane < nw ? sh[lane] : identity;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x = op(x, y);
+    }
+    sh[lane] = x;
+  }
+  __syncthreads();
+  if (warp > 0) v = op(v, sh[warp - 1]);
+  __syncthreads();
+  return v;
+}
+
+struct OpAdd { __device__ int operator()(int a, int b) const { return a + b; } };
+struct OpMax { __device__ int operator()(int a, int b) const { return a > b ? a : b; } };
+
+// Splits the tokens into groups: maximal runs of consecutive tokens of the same
+// request, cut into pieces of at most G; then counts each group's key tiles.
+__global__ void __launch_bounds__(1024) plan_groups_kernel(PlanParams p) {
+  __shared__ int sh[32];
+  __shared__ int carry_run, carry_groups;
+  if (threadIdx.x == 0) { carry_run = 0; carry_groups = 0; }
+  __syncthreads();
+  const int T = p.b.T;
+  for (int base = 0; base < T; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    const bool valid = t < T;
+    int req = 0, pos = 0, prev = -1;
+    if (valid) {
+      load_token(p.b, t, p.status, req, pos);
+      if (t > 0) {
+        int pr = p.b.q_req[t - 1];
+        prev = (pr < 0 || pr >= p.b.B) ? (pr < 0 ? 0 : p.b.B - 1) : pr;
+      }
+    }
+    const int rs = (valid && (t == 0 || req != prev)) ? t : -1;
+    int run_start = block_inclusive_scan(rs, sh, OpMax(), -1);
+    run_start = run_start > carry_run ? run_start : carry_run;
+    const int is_start = (valid && ((t - run_start) % p.G == 0)) ? 1 : 0;
+    const int incl = block_inclusive_scan(is_start, sh, OpAdd(), 0);
+    const int g = carry_groups + incl - 1;
+    if (valid) {
+      if (is_start) { p.groups[g].t0 = t; p.groups[g].req = req; }
+      atomicAdd(&p.groups[g].n, 1);
+      atomicMax(&p.groups[g].L, pos + 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) {
+      carry_run = run_start;
+      carry_groups += incl;
+    }
+    __syncthreads();
+  }
+  __syncthreads();
+  const int ng = carry_groups;
+  __shared__ int chunk_total;
+  int carry_tiles = 0;
+  for (int base = 0; base < ng; base += blockDim.x) {
+    const int g = base + threadIdx.x;
+    const int tiles = g < ng ? static_cast<int>(cdiv(__ldcg(&p.groups[g].L), kKeyTile)) : 0;
+    const int incl = block_inclusive_scan(tiles, sh, OpAdd(), 0);
+    if (g < ng) p.groups[g].tile_begin = carry_tiles + incl - tiles;
+    if (threadIdx.x == blockDim.x - 1) chunk_total = incl;
+    __syncthreads();
+    carry_tiles += chunk_total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    p.hdr->n_groups = ng;
+    p.hdr->total_tiles = carry_tiles;
+  }
+}
+
+// ------------------------------------------------------------------- scorer
+
+
+template <int G>
+struct ScorerCfg {
+  static constexpr int STAGES = (G == 1) ? 8 : 6;
+  static constexpr int ACC_COLS = 32 * G;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;          // 64 or 512 (powers of two)
+  static constexpr int KEY_BYTES = kKeyTile * kIdxDim;    // 16 KB
+  static constexpr int SCALE_BYTES = kKeyTile * 4;
+  static constexpr int Q_BYTES = G * kIdxHeads * kIdxDim;
+  static constexpr int OFF_Q = STAGES * KEY_BYTES;
+  static constexpr int OFF_SCALES = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_BARS = OFF_SCALES + STAGES * SCALE_BYTES;
+  static constexpr int N_BARS = 2 * STAGES + 9;
+  static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int THREADS = 320;
+  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// Wait ignoring the CTA abort flag, for draining copies/MMAs in flight before exit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(addr, parity)) {
+    if (globaltimer() - t0 > 200000000ull) break;   // 0.2 s
+  }
+}
+
+__device__ __forceinline__ int find_group(const ScoreGroup* groups, int ng, int tile) {
+  int lo = 0, hi = ng - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (groups[mid].tile_begin <= tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int G>
+__global__ void __launch_bounds__(320, 1)
+    indexer_fp8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                       IndexerParams p) {
+  using C = ScorerCfg<G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* qfull = tempty + 2;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* drain = qempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  int* abortf = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int total = p.hdr->total_tiles;
+  const int ng = p.hdr->n_groups;
+  const int tile_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
+  const int tile_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + 8);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abortf = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const Abort ab{abortf, p.status};
+  const int bs = p.pool.bs;
+  const int box = bs < kKeyTile ? bs : kKeyTile;   // keys per TMA box
+  const int nbox = kKeyTile / box;
+
+  if (tile_lo < tile_hi) {
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&qmap);
+      int g = find_group(p.groups, ng, tile_lo);
+      ScoreGroup grp = p.groups[g];
+      int next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
+      int gcount = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int i = tile_lo; i < tile_hi && ok; ++i) {
+        if (i == next_begin) {
+          ++g;
+          grp = p.groups[g];
+          next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
+          ++gcount;
+        }
+        if (i == tile_lo || i == grp.tile_begin) {
+          const int qb = gcount & 1;
+          if (gcount >= 2 && !(ok = mbar_wait(&qempty[qb], ((gcount - 2) >> 1) & 1, ab))) break;
+          mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * kIdxHeads * kIdxDim);
+          for (int j = 0; j < grp.n; ++j)
+            tma_load_2d(smem + C::OFF_Q + qb * C::Q_BYTES + j * kIdxHeads * kIdxDim, &qmap, &qfull[qb], 0,
+                        (grp.t0 + j) * kIdxHeads);
+        }
+        const int it = i - tile_lo;
+        const int s = it % C::STAGES;
+        if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
+        const int64_t key0 = static_cast<int64_t>(i - grp.tile_begin) * kKeyTile;
+        int rows[kKeyTile / 16];
+#pragma unroll
+        for (int bx = 0; bx < kKeyTile / 16; ++bx) rows[bx] = -1;
+        uint32_t bytes = 0;
+        for (int bx = 0; bx < nbox; ++bx) {
+          const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
+          if (k0 >= grp.L) break;
+          const int row = p.b.bt[static_cast<int64_t>(grp.req) * p.b.bt_stride + (k0 >> p.pool.log2_bs)];
+          if (row < 0 || row >= p.pool.num_rows) {
+            atomicOr(p.status, DEV_BAD_BLOCK);
+            continue;
+          }
+          rows[bx] = row;
+          bytes += static_cast<uint32_t>(box) * (kIdxDim + 4);
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        for (int bx = 0; bx < nbox; ++bx) {
+          if (rows[bx] < 0) continue;
+          const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
+          const int slot0 = static_cast<int>(k0 & (bs - 1));
+          tma_load_3d(smem + s * C::KEY_BYTES + bx * box * kIdxDim, &kmap, &full[s], 0, slot0, rows[bx]);
+          const uint8_t* src = p.pool.pool + static_cast<int64_t>(rows[bx]) * p.pool.row_stride + p.pool.idx_off +
+                               static_cast<int64_t>(bs) * kIdxDim + static_cast<int64_t>(slot0) * 4;
+          bulk_load(smem + C::OFF_SCALES + s * C::SCALE_BYTES + bx * box * 4, src, box * 4, &full[s]);
+        }
+        ++issued;
+      }
+      if (!ok) {   // drain the copies still in flight before the CTA exits
+        for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it)
+          drain_wait(&full[it % C::STAGES], (it / C::STAGES) & 1);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      int g = find_group(p.groups, ng, tile_lo);
+      ScoreGroup grp = p.groups[g];
+      int next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
+      int gcount = 0;
+      uint32_t idesc = make_idesc(0, 0, false, false, kKeyTile, grp.n * kIdxHeads);
+      bool ok = mbar_wait(&qfull[0], 0, ab);
+      for (int i = tile_lo; i < tile_hi && ok; ++i) {
+        if (i == next_begin) {
+          ++g;
+          grp = p.groups[g];
+          next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
+          ++gcount;
+          idesc = make_idesc(0, 0, false, false, kKeyTile, grp.n * kIdxHeads);
+          if (!(ok = mbar_wait(&qfull[gcount & 1], (gcount >> 1) & 1, ab))) break;
+        }
+        const int it = i - tile_lo;
+        const int s = it % C::STAGES;
+        const int acc = it & 1;
+        if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
+        if (it >= 2 && !(ok = mbar_wait(&tempty[acc], ((it >> 1) - 1) & 1, ab))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * C::ACC_COLS;
+        const uint32_t a0 = smem_u32(smem + s * C::KEY_BYTES);
+        const uint32_t b0 = smem_u32(smem + C::OFF_Q + (gcount & 1) * C::Q_BYTES);
+#pragma unroll
+        for (int k = 0; k < kIdxDim / 32; ++k)
+          mma_f8f6f4(d, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
+                     k > 0 ? 1u : 0u);
+        tc_commit(&empty[s]);
+        tc_commit(&tfull[acc]);
+        if (i + 1 == next_begin || i + 1 == tile_hi) tc_commit(&qempty[gcount & 1]);
+      }
+      if (!ok) {
+        tc_commit(drain);
+        drain_wait(drain, 0);
+      }
+    } else if (warp >= 2) {
+      // ------------------------------------------------------------ epilogue
+      const int e = warp - 2;
+      const int quarter = warp & 3;
+      const int half = e >> 2;
+      int g = find_group(p.groups, ng, tile_lo);
+      ScoreGroup grp = p.groups[g];
+      int next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
+      for (int i = tile_lo; i < tile_hi; ++i) {
+        if (i == next_begin) {
+          ++g;
+          grp = p.groups[g];
+          next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
+        }
+        const int it = i - tile_lo;
+        const int s = it % C::STAGES;
+        const int acc = it & 1;
+        if (!mbar_wait(&tfull[acc], (it >> 1) & 1, ab)) break;
+        if (!mbar_wait(&full[s], (it / C::STAGES) & 1, ab)) break;
+        tc_fence_after();
+        const int kloc = quarter * 32 + lane;
+        const int key = (i - grp.tile_begin) * kKeyTile + kloc;
+        const float scale = reinterpret_cast<const float*>(smem + C::OFF_SCALES + s * C::SCALE_BYTES)[kloc];
+        for (int j = half; j < grp.n; j += 2) {
+          uint32_t r[32];
+          DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + j * kIdxHeads + (static_cast<uint32_t>(quarter * 32) << 16), r);
+          tmem_wait_ld();
+          const int t = grp.t0 + j;
+          int req, pos;
+          load_token(p.b, t, p.status, req, pos);
+          const float4* wv = reinterpret_cast<const float4*>(p.w + static_cast<int64_t>(t) * kIdxHeads);
+          float sum = 0.f;
+          if (scale >= 0.f) {
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 w4 = __ldg(wv + h4);
+              sum = fmaf(w4.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), sum);
+              sum = fmaf(w4.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), sum);
+              sum = fmaf(w4.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), sum);
+              sum = fmaf(w4.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), sum);
+            }
+          } else {   // ReLU(c * x) = c * min(x, 0) for c < 0
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 w4 = __ldg(wv + h4);
+              sum = fmaf(w4.x, fminf(__uint_as_float(r[4 * h4 + 0]), 0.f), sum);
+              sum = fmaf(w4.y, fminf(__uint_as_float(r[4 * h4 + 1]), 0.f), sum);
+              sum = fmaf(w4.z, fminf(__uint_as_float(r[4 * h4 + 2]), 0.f), sum);
+              sum = fmaf(w4.w, fminf(__uint_as_float(r[4 * h4 + 3]), 0.f), sum);
+            }
+          }
+          if (key <= pos) p.scores[static_cast<int64_t>(t) * p.ld + key] = scale * sum;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[acc]);
+          mbar_arrive(&empty[s]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ----------------------------------------------------------------- launchers
+
+cudaError_t launch_plan_groups(const BatchView& b, int G, ScoreGroup* groups, PlanHeader* hdr, uint32_t* status,
+                               cudaStream_t st) {
+  PlanParams p{b, G, groups, hdr, status};
+  plan_groups_kernel<<<1, 1024, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int G>
+static cudaError_t launch_scorer_g(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p,
+                                   int grid, cudaStream_t st) {
+  using C = ScorerCfg<G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(indexer_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  indexer_fp8_kernel<G><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(kmap, qmap, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_fp8(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,
+                               int grid, cudaStream_t st) {
+  if (G == 1) return launch_scorer_g<1>(kmap, qmap, p, grid, st);
+  return launch_scorer_g<8>(kmap, qmap, p, grid, st);
+}
+
+}  // namespace dsa

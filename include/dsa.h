@@ -1,0 +1,214 @@
+/*
+ * dsa.h — C ABI of the GB300 (sm_103a) DSA layer-step library.
+ *
+ * The computation (vLLM blog post "vLLM delivers day-0 support for Kimi K3.1 Pro",
+ * section "Sparse Attention in K3.1 Pro" and Figure 1): a lightning indexer keeps
+ * one FP8 key per token (132 bytes with its scale) and scores every earlier token
+ * for each query with 32 light heads; the 2,048 best tokens are kept; MLA
+ * attention with 96 absorbed query heads then runs exactly, but only over those
+ * tokens' 576-byte latents.  The cache layout follows "A KV cache for three kinds
+ * of state": one contiguous row per cache block holds that block's index-key page
+ * and latent page at fixed offsets, and block tables are translated into page
+ * addresses (here: inside the kernels).  MXFP4 index keys (68 B/token) follow
+ * "AMD / Quantization: Native MXFP4 indexer"; NVFP4 latents (352 B/token) follow
+ * "KV cache footprint".
+ *
+ * Conventions for every call:
+ *  - Pointers documented "device" must point to device memory of the current
+ *    CUDA device; the caller owns every buffer, including the workspace.  The
+ *    library allocates no memory and keeps no state across calls.
+ *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; 0 = legacy
+ *    default stream).  A return value of DSA_OK means the work was validated
+ *    and enqueued; device-side findings (a block id outside the pool, a wait
+ *    that timed out) are recorded in the workspace's status word and reported
+ *    by dsa_check().
+ *  - Arguments are validated on the host before anything is enqueued; on an
+ *    error nothing is enqueued.  No C++ exception crosses this interface.
+ *  - Shapes: T query tokens, B requests, k = topk <= 2048, indexer 32 heads x
+ *    128 dims, MLA 96 heads, latent 576 dims of which the first 512 are the value.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dsa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = -1,  /* a null pointer, bad size, misaligned address or range */
+  DSA_ERR_UNSUPPORTED = -2,  /* a valid but unsupported format / block size / device */
+  DSA_ERR_CUDA = -3,         /* a CUDA runtime or driver call failed */
+  DSA_ERR_WORKSPACE = -4,    /* workspace null, misaligned or smaller than required */
+  DSA_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (dsa_check) */
+  DSA_ERR_DEVICE_CHECK = -6  /* a device-side range check failed (dsa_check) */
+} dsa_status;
+
+enum { DSA_IDX_FP8 = 0, DSA_IDX_MXFP4 = 1 };  /* index-key page formats */
+enum { DSA_LAT_FP8 = 0, DSA_LAT_NVFP4 = 1 };  /* latent page formats */
+
+#define DSA_IDX_HEADS 32
+#define DSA_IDX_DIM 128
+#define DSA_MLA_HEADS 96
+#define DSA_LAT_DIM 576
+#define DSA_V_DIM 512
+#define DSA_MAX_TOPK 2048
+#define DSA_ABI_VERSION 1
+
+/*
+ * One DSA layer's view of the packed KV pool.
+ *
+ * Row r starts at pool + r * row_stride_bytes.  For a block of `block_size`
+ * tokens (a power of two, 16..256) the index page at row + idx_page_offset is
+ *   FP8  : block_size x 128 e4m3 value bytes, then block_size x fp32 scales
+ *          (little endian); key(s) = e4m3(code) * scale(s)          (132 B/token)
+ *   MXFP4: block_size x 64 bytes of packed e2m1 (element 2i in the low nibble of
+ *          byte i), then block_size x 4 E8M0 bytes (scale j covers dims 32j..32j+31)
+ *                                                                   (68 B/token)
+ * and the latent page at row + lat_page_offset is
+ *   FP8  : block_size x 576 e4m3 bytes                              (576 B/token)
+ *   NVFP4: block_size x 352-byte records: 288 bytes packed e2m1, 36 e4m3 scales
+ *          (scale j covers dims 16j..16j+15), 28 bytes of padding (352 B/token)
+ * Token s of request b lives in row block_table[b][s / block_size], slot
+ * s % block_size.  pool, row_stride_bytes and both offsets must be multiples of
+ * 16 bytes.  Index-key scales must be finite; latents and keys must hold no NaN
+ * codes.  The pool is device memory owned by the caller and only read.
+ */
+typedef struct {
+  const void *pool;          /* device */
+  int64_t num_rows;          /* rows in the pool; block ids must lie in [0, num_rows) */
+  int64_t row_stride_bytes;
+  int64_t idx_page_offset;
+  int64_t lat_page_offset;
+  int32_t block_size;
+  int32_t idx_fmt;           /* DSA_IDX_* */
+  int32_t lat_fmt;           /* DSA_LAT_* */
+  int32_t reserved;          /* must be 0 */
+} dsa_kv_layout;
+
+/*
+ * The query batch.  Query token t belongs to request q_req[t] and sits at
+ * absolute position q_pos[t] of that request; it attends to positions
+ * 0..q_pos[t] (causal and inclusive: the new tokens' keys and latents are in the
+ * cache before the call).  Requirements (checked on the device; a violation sets
+ * DSA_ERR_DEVICE_CHECK): 0 <= q_req[t] < num_reqs, 0 <= q_pos[t] < ctx_lens[q_req[t]]
+ * <= max_ctx_len <= bt_stride * block_size.  All pointers are device memory.
+ * Tokens of one request should be contiguous in t so the indexer can share key
+ * reads across them; any order is correct.
+ *
+ * Batch invariance ("Zero-mismatch RL on day 0": a token's result must not
+ * depend on its batch).  The indexer scores and the top-k selection of a token
+ * never depend on the rest of the batch.  The attention output is split over
+ * the selected list into a number of partials chosen from the batch size (to
+ * fill the GPU); with DSA_BATCH_INVARIANT set the split is fixed (one partial
+ * per 128 selected tokens) so the output is bit-identical for any batch, at the
+ * cost of more partial traffic for large batches.
+ */
+#define DSA_BATCH_INVARIANT 1
+typedef struct {
+  int32_t num_tokens;        /* T >= 0 */
+  int32_t num_reqs;          /* B >= 1 */
+  const int32_t *q_req;      /* [T] */
+  const int32_t *q_pos;      /* [T] */
+  const int32_t *ctx_lens;   /* [B] */
+  const int32_t *block_table;/* [B, bt_stride] row ids */
+  int32_t bt_stride;
+  int32_t flags;             /* DSA_BATCH_* bits; 0 = default */
+  int64_t max_ctx_len;       /* host-side upper bound of ctx_lens, used for sizing */
+} dsa_batch;
+
+/* ABI version of the loaded library (DSA_ABI_VERSION). */
+int32_t dsa_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char *dsa_status_string(dsa_status status);
+
+/*
+ * Bytes of device workspace the calls below need for this layout/batch/topk
+ * (the maximum over all calls; 256-byte aligned).  0 on invalid arguments.
+ * The first 256 bytes hold the status word, which persists across calls until
+ * dsa_check() clears it: zero the workspace once after allocating it.
+ */
+size_t dsa_workspace_size(const dsa_kv_layout *layout, const dsa_batch *batch, int32_t topk);
+
+/*
+ * Indexer scores ("Sparse Attention in K3.1 Pro"):
+ *   scores[t * ld_scores + s] = sum_{h<32} w[t,h] * ReLU(q_idx[t,h,:] . key(s)),
+ * for s = 0..q_pos[t], with key(s) the dequantised index key of token s of
+ * request q_req[t].  Entries beyond q_pos[t] are not written.
+ *  q_idx : device, e4m3 codes [T, 32, 128] (16-byte aligned); used as-is (any
+ *          query-side scale belongs in w)
+ *  w     : device, fp32 [T, 32]
+ *  scores: device, fp32 [T, ld_scores], ld_scores >= max_ctx_len, 16-byte aligned rows
+ * Keys are scored with FP8 tensor-core MMAs (fp32 accumulation); the key scale
+ * is applied after the head reduction (exact for a positive or negative scale).
+ */
+dsa_status dsa_indexer_score(const dsa_kv_layout *layout, const dsa_batch *batch,
+                             const void *q_idx, const float *w, float *scores,
+                             int64_t ld_scores, void *workspace, size_t workspace_bytes,
+                             dsa_stream_t stream);
+
+/*
+ * Exact top-k ("Then it keeps the top 2,048 tokens"): for each token t, the k
+ * largest of scores[t, 0..q_pos[t]]; equal scores are ordered by lower position
+ * first (-0.0 equals +0.0).  idx[t, :] receives the selected positions in
+ * ascending order; when q_pos[t] + 1 < k every position is selected and the
+ * tail is filled with -1.  The result is deterministic and independent of the
+ * rest of the batch.
+ *  scores    : device fp32 [T, ld_scores] (not modified); NaN scores are unsupported
+ *  idx       : device int32 [T, topk]
+ *  phys_slots: device int32 [T, topk] or NULL: for each selected position s the
+ *              physical cache slot block_table[b][s/bs] * bs + s % bs (-1 for padding);
+ *              needs `layout` (only its block_size is read); `layout` may be NULL
+ *              when phys_slots is NULL.
+ */
+dsa_status dsa_topk(const dsa_kv_layout *layout, const dsa_batch *batch, const float *scores,
+                    int64_t ld_scores, int32_t topk, int32_t *idx, int32_t *phys_slots,
+                    void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * Sparse MLA ("MLA attention then runs exactly, but only over those 2,048 tokens"):
+ * for each token t and head h < 96, over the positions S_t = {idx[t, i] >= 0}:
+ *   logit(s) = sm_scale * q[t,h,:] . c(s)          (all 576 dims)
+ *   out[t,h,:] = sum_s softmax(logit)(s) * c(s)[0:512]
+ *   lse[t,h]  = ln sum_s exp(logit(s))
+ * with c(s) the dequantised latent of position s of request q_req[t].
+ *  q  : device bf16 [T, 96, 576] (16-byte aligned)
+ *  idx: device int32 [T, topk]; valid entries first, then -1 (as dsa_topk writes
+ *       them); every valid entry must be <= q_pos[t]; at least one per token
+ *  out: device bf16 [T, 96, 512];  lse: device fp32 [T, 96] or NULL
+ * QK runs as bf16 x bf16 (the e4m3 latent is exact in bf16) and PV as fp16 P x
+ * fp16 V on the tensor cores with fp32 accumulation; per-split partials are
+ * merged by log-sum-exp in fp32.
+ */
+dsa_status dsa_sparse_mla(const dsa_kv_layout *layout, const dsa_batch *batch, const void *q,
+                          const int32_t *idx, int32_t topk, float sm_scale, void *out,
+                          float *lse, void *workspace, size_t workspace_bytes,
+                          dsa_stream_t stream);
+
+/*
+ * The whole DSA layer step: indexer scores -> exact top-k -> sparse MLA, with
+ * the intermediate scores and indices kept in the workspace.
+ *  idx_out: device int32 [T, topk] or NULL — receives the selected positions
+ *  other arguments as in the three calls above.
+ */
+dsa_status dsa_layer_step(const dsa_kv_layout *layout, const dsa_batch *batch,
+                          const void *q_idx, const float *w, const void *q, int32_t topk,
+                          float sm_scale, int32_t *idx_out, void *out, float *lse,
+                          void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the workspace status word written by earlier
+ * calls, clears it, and returns DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK.
+ */
+dsa_status dsa_check(void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_GB300_H */

@@ -1,0 +1,183 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small cases span several key tiles, ragged tails and the degenerate cases
+(context 1, contexts straddling a 64-token block and the 2048 boundary, fewer
+tokens than k); the full-size decode configuration runs in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+from dsa_sparse_attention_gb300 import workloads as W
+from tests.parity import OracleCache, check_mla, check_scores, check_topk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from dsa_sparse_attention_gb300.build import build
+    build()
+
+
+def _dev(wl, topk=None, flags=0):
+    from dsa_sparse_attention_gb300.harness import DeviceWorkload
+    return DeviceWorkload(wl, topk=topk, flags=flags)
+
+
+def _np(x):
+    return x.float().cpu().numpy() if x.dtype == torch.bfloat16 else x.cpu().numpy()
+
+
+def _run_all(wl, topk=None, tokens=None, check_split=True):
+    from dsa_sparse_attention_gb300 import dsa_check
+    dw = _dev(wl, topk)
+    k = dw.topk
+    idx, out, lse = dw.layer_step()
+    torch.cuda.synchronize()
+    assert dsa_check(dw.ws) == 0
+    oc = OracleCache(wl)
+    tokens = list(range(wl.num_tokens)) if tokens is None else tokens
+    g_idx, g_out, g_lse = _np(idx), _np(out), _np(lse)
+    scores = dw.indexer_scores()
+    torch.cuda.synchronize()
+    worst_s = check_scores(oc, _np(scores), tokens)
+    subs = check_topk(oc, g_idx, tokens, k)
+    worst_m = check_mla(oc, g_idx, g_out, g_lse, tokens)
+    if check_split:
+        # the three separate calls give exactly what the fused step gives
+        idx2 = dw.topk_of(scores)
+        out2, lse2 = dw.sparse_mla_of(idx2)
+        torch.cuda.synchronize()
+        assert np.array_equal(_np(idx2), g_idx)
+        assert np.array_equal(_np(out2), g_out) and np.array_equal(_np(lse2), g_lse)
+    assert dsa_check(dw.ws) == 0
+    return dict(score_err=worst_s, tie_subs=subs, mla=worst_m)
+
+
+def test_cfg0_tiny_decode():
+    r = _run_all(W.config(0))
+    print(r)
+
+
+def test_ragged_multi_request_decode():
+    lens = [5000, 1, 64, 65, 2047, 2048, 2049, 3000, 129]
+    wl = W.make_workload(lens, 1, seed=11, permute=True, pool_rows=300)
+    _run_all(wl)
+
+
+def test_mtp_groups_of_six():
+    wl = W.make_workload([3000, 5000, 9001], 6, seed=12, permute=True, pool_rows=300)
+    _run_all(wl)
+
+
+def test_prefill_chunk():
+    base, new = 3000, 300
+    wl = W.make_workload([base + new], new, seed=13, permute=True)
+    _run_all(wl, tokens=[0, 1, 2, 7, 8, 150, 298, 299])
+
+
+@pytest.mark.parametrize("bs", [16, 32, 128, 256])
+def test_block_sizes(bs):
+    wl = W.make_workload([3001, 700], 1, seed=14, block_size=bs, permute=True, pool_rows=400)
+    _run_all(wl)
+
+
+@pytest.mark.parametrize("k", [1, 7, 100, 1000])
+def test_topk_sizes(k):
+    wl = W.make_workload([4000, 90, 5], 1, seed=15, permute=True)
+    _run_all(wl, topk=k)
+
+
+def test_all_scores_tied_takes_lowest_positions():
+    # w = 0 makes every score exactly 0: the top-k is then positions 0..k-1.
+    wl = W.make_workload([3000, 2500], 1, seed=16)
+    wl.w[:] = 0
+    dw = _dev(wl)
+    idx, out, lse = dw.layer_step()
+    g = _np(idx)
+    assert np.array_equal(g[0], np.arange(2048)) and np.array_equal(g[1], np.arange(2048))
+    check_mla(OracleCache(wl), g, _np(out), _np(lse), [0, 1])
+
+
+def _embed(big, b, alone):
+    """Give request b of `big` exactly the cache and queries of request 0 of `alone`."""
+    nb = (int(alone.ctx_lens[0]) + 63) // 64
+    rb = big.pool.reshape(big.num_rows, big.row_stride)
+    ra = alone.pool.reshape(alone.num_rows, alone.row_stride)
+    rb[big.block_table[b, :nb]] = ra[alone.block_table[0, :nb]]
+    t = int(np.nonzero(big.q_req == b)[0][0])
+    big.q_idx[t], big.w[t], big.q[t] = alone.q_idx[0], alone.w[0], alone.q[0]
+    return t
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_batch_invariance_bitwise(flags):
+    # Selection never depends on the batch; with DSA_BATCH_INVARIANT (flags=1)
+    # the output does not either, even when the batch size changes the default
+    # split plan (40 tokens -> 8 splits by default, 1 token -> 16).
+    alone = W.make_workload([3000], 1, seed=17, permute=False)
+    lens = [3000 + 37 * i for i in range(40)]
+    lens[5] = 3000
+    big = W.make_workload(lens, 1, seed=27, permute=True)
+    t = _embed(big, 5, alone)
+    i1, o1, l1 = [_np(x).copy() for x in _dev(big, flags=flags).layer_step()]
+    i2, o2, l2 = [_np(x).copy() for x in _dev(alone, flags=flags).layer_step()]
+    assert np.array_equal(i1[t], i2[0])
+    if flags:
+        assert np.array_equal(o1[t], o2[0]) and np.array_equal(l1[t], l2[0])
+    else:
+        oc = OracleCache(alone)
+        check_mla(oc, i1[t:t + 1].repeat(1, 0), o1[t:t + 1], l1[t:t + 1], [0])
+
+
+def test_batch_invariance_same_split_plan_default_mode():
+    # With the same split plan (batch sizes 3 and 1 both use 16 splits) the
+    # default mode is bit-identical as well.
+    alone = W.make_workload([3000], 1, seed=17, permute=False)
+    big = W.make_workload([6000, 3000, 7000], 1, seed=37, permute=True)
+    t = _embed(big, 1, alone)
+    i1, o1, l1 = [_np(x).copy() for x in _dev(big).layer_step()]
+    i2, o2, l2 = [_np(x).copy() for x in _dev(alone).layer_step()]
+    assert np.array_equal(i1[t], i2[0])
+    assert np.array_equal(o1[t], o2[0]) and np.array_equal(l1[t], l2[0])
+
+
+def test_block_table_permutation_bitwise():
+    a = W.make_workload([5000, 3000], 2, seed=18, permute=False, pool_rows=200)
+    b = W.make_workload([5000, 3000], 2, seed=18, permute=True, pool_rows=200)
+    ra = [_np(x).copy() for x in _dev(a).layer_step()]
+    rb = [_np(x).copy() for x in _dev(b).layer_step()]
+    for x, y in zip(ra, rb):
+        assert np.array_equal(x, y)
+
+
+def test_phys_slots():
+    wl = W.make_workload([3000, 100], 1, seed=19, permute=True, pool_rows=100)
+    dw = _dev(wl)
+    scores = dw.indexer_scores()
+    idx, phys = dw.topk_of(scores, with_phys=True)
+    gi, gp = _np(idx), _np(phys)
+    for t in range(2):
+        b = wl.q_req[t]
+        v = gi[t] >= 0
+        exp = wl.block_table[b][gi[t][v] // 64] * 64 + gi[t][v] % 64
+        assert np.array_equal(gp[t][v], exp) and np.all(gp[t][~v] == -1)
+
+
+def test_bad_block_id_is_reported_not_faulted():
+    from dsa_sparse_attention_gb300 import dsa_check
+    wl = W.make_workload([3000], 1, seed=20, pool_rows=60)
+    wl.block_table[0, 5] = wl.num_rows + 7          # outside the pool
+    dw = _dev(wl)
+    dw.layer_step()
+    assert dsa_check(dw.ws) == -6                    # DSA_ERR_DEVICE_CHECK
+    assert dsa_check(dw.ws) == 0                     # cleared
+
+
+@pytest.mark.slow
+def test_full_cfg1_decode_b8_64k():
+    wl = W.config(1)
+    r = _run_all(wl, check_split=False)
+    print(r)
