@@ -203,6 +203,32 @@ dsa_status dsa_layer_step(const dsa_kv_layout *layout, const dsa_batch *batch,
                           void *workspace, size_t workspace_bytes, dsa_stream_t stream);
 
 /*
+ * dsa_topk without a workspace, for callers that cannot allocate device memory
+ * (code running in a stream callback or host-function node, plugins whose host
+ * framework owns all allocations, loops that forbid allocator use after start-up).
+ * The pages describe no such call; it exists only for those callers.
+ *
+ * Same arguments, results and guarantees as dsa_topk, minus the workspace: the
+ * scratch (256 B + T x 20 KiB of histograms + T x ceil(max_ctx_len / 4096) x 8 B
+ * of counts) lives in a fixed DSA_NOALLOC_SCRATCH_BYTES array of device memory
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  Batches that need more return DSA_ERR_WORKSPACE (for example
+ * T <= 128 fits at a 1M-token context).  The call allocates nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call uses the same array: the call clears the part that must start at
+ *    zero on `stream`, but calls that overlap on the GPU (other streams, other
+ *    host threads) race on it; issue them in order on one stream.
+ *  - Device-side range findings are not reported (there is no workspace status
+ *    word); out-of-range positions are clamped so nothing is read out of bounds.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (4u << 20)
+dsa_status dsa_topk_noalloc(const dsa_kv_layout *layout, const dsa_batch *batch, const float *scores,
+                            int64_t ld_scores, int32_t topk, int32_t *idx, int32_t *phys_slots,
+                            dsa_stream_t stream);
+
+/*
  * Synchronises `stream`, reads the workspace status word written by earlier
  * calls, clears it, and returns DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK.
  */
