@@ -17,7 +17,6 @@ using namespace dsa;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kTopkChunk = 4096;
 constexpr size_t kStatusBytes = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -25,7 +24,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Ws {
   size_t status = 0;
   size_t plan_hdr = 0, groups = 0;
-  size_t hist = 0, counts = 0;
+  size_t topk = 0;
   size_t scores = 0;
   int64_t ld = 0;
   size_t idx = 0;
@@ -88,10 +87,8 @@ Ws plan_ws(const dsa_kv_layout* l, const dsa_batch* b, int topk) {
   w.groups = off;
   off = align_up(off + size_t(T > 0 ? T : 1) * sizeof(ScoreGroup));
   w.topk_nchunks = static_cast<int>(cdiv(b->max_ctx_len, kTopkChunk));
-  w.hist = off;
-  off = align_up(off + size_t(T) * (2048 + 2048 + 1024) * 4);
-  w.counts = off;
-  off = align_up(off + size_t(T) * w.topk_nchunks * 2 * 4);
+  w.topk = off;
+  off = align_up(off + topk_scratch_layout(T, w.topk_nchunks).total);
   w.ld = (b->max_ctx_len + 3) / 4 * 4;
   w.scores = off;
   off = align_up(off + size_t(T) * size_t(w.ld) * 4);
@@ -109,7 +106,7 @@ Ws plan_ws(const dsa_kv_layout* l, const dsa_batch* b, int topk) {
   w.tps = static_cast<int>(cdiv(ntiles, nsplit));
   w.nsplit = static_cast<int>(cdiv(ntiles, w.tps));
   w.part_o = off;
-  if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * kVDim * 4);
+  if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * kVDim * 2);
   w.part_ml = off;
   if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * 8);
   w.total = off;
@@ -224,7 +221,7 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return DSA_ERR_CUDA;
   const int G = (T == b->num_reqs) ? 1 : 8;
   uint32_t* status = at<uint32_t>(ws, wl.status);
-  cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, wl.plan_hdr), 0, wl.hist - wl.plan_hdr, st);
+  cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, wl.plan_hdr), 0, wl.groups + size_t(T) * sizeof(ScoreGroup) - wl.plan_hdr, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   BatchView bv = batch_view(b);
   e = launch_plan_groups(bv, G, at<ScoreGroup>(ws, wl.groups), at<PlanHeader>(ws, wl.plan_hdr), status, st);
@@ -249,12 +246,8 @@ dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* sco
   p.scores = scores;
   p.ld = ld;
   p.k = topk;
-  p.chunk = kTopkChunk;
-  p.hist1 = at<uint32_t>(ws, wl.hist);
-  p.hist2 = p.hist1 + size_t(b->num_tokens) * 2048;
-  p.hist3 = p.hist2 + size_t(b->num_tokens) * 2048;
-  p.counts = at<uint32_t>(ws, wl.counts);
-  p.nchunks = wl.topk_nchunks;
+  topk_bind_scratch(p, at<uint8_t>(ws, wl.topk), topk_scratch_layout(b->num_tokens, wl.topk_nchunks),
+                    wl.topk_nchunks);
   p.idx = idx;
   p.phys = phys;
   int lg = 0;
@@ -281,7 +274,7 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   p.nsplit = wl.nsplit;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  p.part_o = at<float>(ws, wl.part_o);
+  p.part_o = at<__half>(ws, wl.part_o);
   p.part_ml = at<float2>(ws, wl.part_ml);
   p.status = at<uint32_t>(ws, wl.status);
   return cuda_status(launch_sparse_mla(qmap, p, st));

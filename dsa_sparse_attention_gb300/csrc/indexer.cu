@@ -125,14 +125,18 @@ template <int G>
 struct ScorerCfg {
   static constexpr int STAGES = (G == 1) ? 8 : 6;
   static constexpr int ACC_COLS = 32 * G;
-  static constexpr int TMEM_COLS = 2 * ACC_COLS;          // 64 or 512 (powers of two)
-  static constexpr int KEY_BYTES = kKeyTile * kIdxDim;    // 16 KB
+  static constexpr int NACC = (G == 1) ? 4 : 2;            // TMEM accumulators (even: set = tile parity)
+  static constexpr int TMEM_COLS = NACC * ACC_COLS;        // 128 or 512 (powers of two)
+  static constexpr int KEY_BYTES = kKeyTile * kIdxDim;     // 16 KB
   static constexpr int SCALE_BYTES = kKeyTile * 4;
   static constexpr int Q_BYTES = G * kIdxHeads * kIdxDim;
+  static constexpr int W_BYTES = G * kIdxHeads * 4;
   static constexpr int OFF_Q = STAGES * KEY_BYTES;
   static constexpr int OFF_SCALES = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_BARS = OFF_SCALES + STAGES * SCALE_BYTES;
-  static constexpr int N_BARS = 2 * STAGES + 9;
+  static constexpr int OFF_W = OFF_SCALES + STAGES * SCALE_BYTES;   // 2 x [G][32] fp32
+  static constexpr int OFF_POS = OFF_W + 2 * W_BYTES;                // 2 x [G] int
+  static constexpr int OFF_BARS = OFF_POS + 2 * G * 4 + 64;
+  static constexpr int N_BARS = 2 * STAGES + 2 * NACC + 5;
   static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr int THREADS = 320;
@@ -143,15 +147,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-// Wait ignoring the CTA abort flag, for draining copies/MMAs in flight before exit.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(addr, parity)) {
-    if (globaltimer() - t0 > 200000000ull) break;   // 0.2 s
-  }
-}
-
 __device__ __forceinline__ int find_group(const ScoreGroup* groups, int ng, int tile) {
   int lo = 0, hi = ng - 1;
   while (lo < hi) {
@@ -160,6 +155,31 @@ __device__ __forceinline__ int find_group(const ScoreGroup* groups, int ng, int 
   }
   return lo;
 }
+
+// Walks a CTA's tile range, tracking the group each tile belongs to.
+struct GroupCursor {
+  const ScoreGroup* groups;
+  int ng, total, g, next_begin, count;
+  ScoreGroup grp;
+  __device__ void init(const ScoreGroup* gs, int n, int tot, int tile) {
+    groups = gs;
+    ng = n;
+    total = tot;
+    g = find_group(gs, n, tile);
+    grp = gs[g];
+    next_begin = g + 1 < n ? gs[g + 1].tile_begin : tot;
+    count = 0;
+  }
+  // advance to tile i (called for consecutive i); returns true on a group change
+  __device__ bool advance(int i) {
+    if (i != next_begin) return false;
+    ++g;
+    grp = groups[g];
+    next_begin = g + 1 < ng ? groups[g + 1].tile_begin : total;
+    ++count;
+    return true;
+  }
+};
 
 template <int G>
 __global__ void __launch_bounds__(320, 1)
@@ -172,12 +192,14 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* tfull = bars + 2 * C::STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* qfull = tempty + 2;
+  uint64_t* tempty = tfull + C::NACC;
+  uint64_t* qfull = tempty + C::NACC;
   uint64_t* qempty = qfull + 2;
   uint64_t* drain = qempty + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  float* wsm = reinterpret_cast<float*>(smem + C::OFF_W);
+  int* possm = reinterpret_cast<int*>(smem + C::OFF_POS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int total = p.hdr->total_tiles;
@@ -188,13 +210,15 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 8);
+      mbar_init(&empty[s], 1 + 4);
+    }
+    for (int a = 0; a < C::NACC; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 8);
       mbar_init(&qfull[i], 1);
-      mbar_init(&qempty[i], 1);
+      mbar_init(&qempty[i], 1 + 8);
     }
     mbar_init(drain, 1);
     *abortf = 0;
@@ -211,140 +235,172 @@ __global__ void __launch_bounds__(320, 1)
   const int nbox = kKeyTile / box;
 
   if (tile_lo < tile_hi) {
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       // ------------------------------------------------------------ producer
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&qmap);
-      int g = find_group(p.groups, ng, tile_lo);
-      ScoreGroup grp = p.groups[g];
-      int next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
-      int gcount = 0;
+      // The whole warp walks the tiles; lane j resolves the block-table rows of
+      // tile (base + j) for each batch of 32 tiles, lane 0 issues the copies.
+      if (lane == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&qmap);
+      }
+      GroupCursor cur;
+      cur.init(p.groups, ng, total, tile_lo);
       int issued = 0;
       bool ok = true;
-      for (int i = tile_lo; i < tile_hi && ok; ++i) {
-        if (i == next_begin) {
-          ++g;
-          grp = p.groups[g];
-          next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
-          ++gcount;
-        }
-        if (i == tile_lo || i == grp.tile_begin) {
-          const int qb = gcount & 1;
-          if (gcount >= 2 && !(ok = mbar_wait(&qempty[qb], ((gcount - 2) >> 1) & 1, ab))) break;
-          mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * kIdxHeads * kIdxDim);
-          for (int j = 0; j < grp.n; ++j)
-            tma_load_2d(smem + C::OFF_Q + qb * C::Q_BYTES + j * kIdxHeads * kIdxDim, &qmap, &qfull[qb], 0,
-                        (grp.t0 + j) * kIdxHeads);
-        }
-        const int it = i - tile_lo;
-        const int s = it % C::STAGES;
-        if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
-        const int64_t key0 = static_cast<int64_t>(i - grp.tile_begin) * kKeyTile;
-        int rows[kKeyTile / 16];
+      int my_rows[kKeyTile / 16];
+      for (int base = tile_lo; base < tile_hi && ok; base += 32) {
+        // lane j: rows of tile base + j
+        {
+          const int i = base + lane;
 #pragma unroll
-        for (int bx = 0; bx < kKeyTile / 16; ++bx) rows[bx] = -1;
-        uint32_t bytes = 0;
-        for (int bx = 0; bx < nbox; ++bx) {
-          const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
-          if (k0 >= grp.L) break;
-          const int row = p.b.bt[static_cast<int64_t>(grp.req) * p.b.bt_stride + (k0 >> p.pool.log2_bs)];
-          if (row < 0 || row >= p.pool.num_rows) {
-            atomicOr(p.status, DEV_BAD_BLOCK);
-            continue;
+          for (int bx = 0; bx < kKeyTile / 16; ++bx) my_rows[bx] = -1;
+          if (i < tile_hi) {
+            const int g = find_group(p.groups, ng, i);
+            const ScoreGroup gg = p.groups[g];
+            const int64_t key0 = static_cast<int64_t>(i - gg.tile_begin) * kKeyTile;
+            const int32_t* btrow = p.b.bt + static_cast<int64_t>(gg.req) * p.b.bt_stride;
+#pragma unroll
+            for (int bx = 0; bx < kKeyTile / 16; ++bx) {
+              if (bx >= nbox) break;
+              const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
+              if (k0 >= gg.L) break;
+              const int row = btrow[k0 >> p.pool.log2_bs];
+              if (row < 0 || row >= p.pool.num_rows) {
+                atomicOr(p.status, DEV_BAD_BLOCK);
+                continue;
+              }
+              my_rows[bx] = row;
+            }
           }
-          rows[bx] = row;
-          bytes += static_cast<uint32_t>(box) * (kIdxDim + 4);
         }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        for (int bx = 0; bx < nbox; ++bx) {
-          if (rows[bx] < 0) continue;
-          const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
-          const int slot0 = static_cast<int>(k0 & (bs - 1));
-          tma_load_3d(smem + s * C::KEY_BYTES + bx * box * kIdxDim, &kmap, &full[s], 0, slot0, rows[bx]);
-          const uint8_t* src = p.pool.pool + static_cast<int64_t>(rows[bx]) * p.pool.row_stride + p.pool.idx_off +
-                               static_cast<int64_t>(bs) * kIdxDim + static_cast<int64_t>(slot0) * 4;
-          bulk_load(smem + C::OFF_SCALES + s * C::SCALE_BYTES + bx * box * 4, src, box * 4, &full[s]);
+        const int nb = min(32, tile_hi - base);
+        for (int jj = 0; jj < nb; ++jj) {
+          const int i = base + jj;
+          int rows[kKeyTile / 16];
+#pragma unroll
+          for (int bx = 0; bx < kKeyTile / 16; ++bx) rows[bx] = __shfl_sync(0xffffffffu, my_rows[bx], jj);
+          const bool changed = cur.advance(i);
+          const ScoreGroup& grp = cur.grp;
+          if (i == tile_lo || changed) {
+            const int qb = cur.count & 1;
+            if (cur.count >= 2 && !(ok = mbar_wait(&qempty[qb], ((cur.count - 2) >> 1) & 1, ab))) break;
+            if (lane == 0) {
+              for (int j = 0; j < grp.n; ++j) {
+                int req, pos;
+                load_token(p.b, grp.t0 + j, p.status, req, pos);
+                possm[qb * G + j] = pos;
+              }
+              mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * (kIdxHeads * kIdxDim + kIdxHeads * 4));
+              for (int j = 0; j < grp.n; ++j)
+                tma_load_2d(smem + C::OFF_Q + qb * C::Q_BYTES + j * kIdxHeads * kIdxDim, &qmap, &qfull[qb], 0,
+                            (grp.t0 + j) * kIdxHeads);
+              bulk_load(wsm + qb * G * kIdxHeads, p.w + static_cast<int64_t>(grp.t0) * kIdxHeads,
+                        static_cast<uint32_t>(grp.n) * kIdxHeads * 4, &qfull[qb]);
+            }
+            __syncwarp();
+          }
+          const int it = i - tile_lo;
+          const int s = it % C::STAGES;
+          if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
+          if (lane == 0) {
+            const int64_t key0 = static_cast<int64_t>(i - grp.tile_begin) * kKeyTile;
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int bx = 0; bx < kKeyTile / 16; ++bx)
+              if (rows[bx] >= 0) bytes += static_cast<uint32_t>(box) * (kIdxDim + 4);
+            mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+            for (int bx = 0; bx < kKeyTile / 16; ++bx) {
+              if (rows[bx] < 0) continue;
+              const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
+              const int slot0 = static_cast<int>(k0 & (bs - 1));
+              tma_load_3d(smem + s * C::KEY_BYTES + bx * box * kIdxDim, &kmap, &full[s], 0, slot0, rows[bx]);
+              const uint8_t* src = p.pool.pool + static_cast<int64_t>(rows[bx]) * p.pool.row_stride +
+                                   p.pool.idx_off + static_cast<int64_t>(bs) * kIdxDim +
+                                   static_cast<int64_t>(slot0) * 4;
+              bulk_load(smem + C::OFF_SCALES + s * C::SCALE_BYTES + bx * box * 4, src, box * 4, &full[s]);
+            }
+          }
+          __syncwarp();
+          ++issued;
         }
-        ++issued;
       }
-      if (!ok) {   // drain the copies still in flight before the CTA exits
+      if (!ok && lane == 0) {   // drain the copies still in flight before the CTA exits
         for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it)
           drain_wait(&full[it % C::STAGES], (it / C::STAGES) & 1);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
-      int g = find_group(p.groups, ng, tile_lo);
-      ScoreGroup grp = p.groups[g];
-      int next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
-      int gcount = 0;
-      uint32_t idesc = make_idesc(0, 0, false, false, kKeyTile, grp.n * kIdxHeads);
-      bool ok = mbar_wait(&qfull[0], 0, ab);
-      for (int i = tile_lo; i < tile_hi && ok; ++i) {
-        if (i == next_begin) {
-          ++g;
-          grp = p.groups[g];
-          next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
-          ++gcount;
-          idesc = make_idesc(0, 0, false, false, kKeyTile, grp.n * kIdxHeads);
-          if (!(ok = mbar_wait(&qfull[gcount & 1], (gcount >> 1) & 1, ab))) break;
-        }
-        const int it = i - tile_lo;
-        const int s = it % C::STAGES;
-        const int acc = it & 1;
-        if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
-        if (it >= 2 && !(ok = mbar_wait(&tempty[acc], ((it >> 1) - 1) & 1, ab))) break;
-        tc_fence_after();
-        const uint32_t d = tmem + acc * C::ACC_COLS;
-        const uint32_t a0 = smem_u32(smem + s * C::KEY_BYTES);
-        const uint32_t b0 = smem_u32(smem + C::OFF_Q + (gcount & 1) * C::Q_BYTES);
+      if (lane == 0) {
+        GroupCursor cur;
+        cur.init(p.groups, ng, total, tile_lo);
+        uint32_t idesc = make_idesc(0, 0, false, false, kKeyTile, cur.grp.n * kIdxHeads);
+        bool ok = mbar_wait(&qfull[0], 0, ab);
+        for (int i = tile_lo; i < tile_hi && ok; ++i) {
+          if (cur.advance(i)) {
+            idesc = make_idesc(0, 0, false, false, kKeyTile, cur.grp.n * kIdxHeads);
+            if (!(ok = mbar_wait(&qfull[cur.count & 1], (cur.count >> 1) & 1, ab))) break;
+          }
+          const int it = i - tile_lo;
+          const int s = it % C::STAGES;
+          const int acc = it % C::NACC;
+          if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
+          if (it >= C::NACC && !(ok = mbar_wait(&tempty[acc], ((it / C::NACC) - 1) & 1, ab))) break;
+          tc_fence_after();
+          const uint32_t d = tmem + acc * C::ACC_COLS;
+          const uint32_t a0 = smem_u32(smem + s * C::KEY_BYTES);
+          const uint32_t b0 = smem_u32(smem + C::OFF_Q + (cur.count & 1) * C::Q_BYTES);
 #pragma unroll
-        for (int k = 0; k < kIdxDim / 32; ++k)
-          mma_f8f6f4(d, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
-                     k > 0 ? 1u : 0u);
-        tc_commit(&empty[s]);
-        tc_commit(&tfull[acc]);
-        if (i + 1 == next_begin || i + 1 == tile_hi) tc_commit(&qempty[gcount & 1]);
+          for (int k = 0; k < kIdxDim / 32; ++k)
+            mma_f8f6f4(d, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
+                       k > 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+          tc_commit(&tfull[acc]);
+          if (i + 1 == cur.next_begin || i + 1 == tile_hi) tc_commit(&qempty[cur.count & 1]);
+        }
+        if (!ok) {
+          tc_commit(drain);
+          drain_wait(drain, 0);
+        }
       }
-      if (!ok) {
-        tc_commit(drain);
-        drain_wait(drain, 0);
-      }
-    } else if (warp >= 2) {
+    } else {
       // ------------------------------------------------------------ epilogue
+      // Two sets of four warps take alternate tiles; in a set, warp w reads TMEM
+      // lanes 32*(w%4).. (one key per thread) and reduces all the group's tokens.
       const int e = warp - 2;
       const int quarter = warp & 3;
-      const int half = e >> 2;
-      int g = find_group(p.groups, ng, tile_lo);
-      ScoreGroup grp = p.groups[g];
-      int next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
-      for (int i = tile_lo; i < tile_hi; ++i) {
-        if (i == next_begin) {
-          ++g;
-          grp = p.groups[g];
-          next_begin = g + 1 < ng ? p.groups[g + 1].tile_begin : total;
+      const int set = e >> 2;
+      GroupCursor cur;
+      cur.init(p.groups, ng, total, tile_lo);
+      bool ok = mbar_wait(&qfull[0], 0, ab);
+      for (int i = tile_lo; i < tile_hi && ok; ++i) {
+        if (cur.advance(i)) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qempty[(cur.count - 1) & 1]);   // done with the previous group
+          if (!(ok = mbar_wait(&qfull[cur.count & 1], (cur.count >> 1) & 1, ab))) break;
         }
         const int it = i - tile_lo;
+        if ((it & 1) != set) continue;
         const int s = it % C::STAGES;
-        const int acc = it & 1;
-        if (!mbar_wait(&tfull[acc], (it >> 1) & 1, ab)) break;
-        if (!mbar_wait(&full[s], (it / C::STAGES) & 1, ab)) break;
+        const int acc = it % C::NACC;
+        if (!(ok = mbar_wait(&tfull[acc], (it / C::NACC) & 1, ab))) break;
+        if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
         tc_fence_after();
+        const ScoreGroup& grp = cur.grp;
+        const int qb = cur.count & 1;
         const int kloc = quarter * 32 + lane;
         const int key = (i - grp.tile_begin) * kKeyTile + kloc;
         const float scale = reinterpret_cast<const float*>(smem + C::OFF_SCALES + s * C::SCALE_BYTES)[kloc];
-        for (int j = half; j < grp.n; j += 2) {
+        for (int j = 0; j < grp.n; ++j) {
           uint32_t r[32];
           DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + j * kIdxHeads + (static_cast<uint32_t>(quarter * 32) << 16), r);
           tmem_wait_ld();
-          const int t = grp.t0 + j;
-          int req, pos;
-          load_token(p.b, t, p.status, req, pos);
-          const float4* wv = reinterpret_cast<const float4*>(p.w + static_cast<int64_t>(t) * kIdxHeads);
+          const float4* wv = reinterpret_cast<const float4*>(wsm + (qb * G + j) * kIdxHeads);
           float sum = 0.f;
           if (scale >= 0.f) {
 #pragma unroll
             for (int h4 = 0; h4 < 8; ++h4) {
-              const float4 w4 = __ldg(wv + h4);
+              const float4 w4 = wv[h4];
               sum = fmaf(w4.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), sum);
               sum = fmaf(w4.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), sum);
               sum = fmaf(w4.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), sum);
@@ -353,14 +409,15 @@ __global__ void __launch_bounds__(320, 1)
           } else {   // ReLU(c * x) = c * min(x, 0) for c < 0
 #pragma unroll
             for (int h4 = 0; h4 < 8; ++h4) {
-              const float4 w4 = __ldg(wv + h4);
+              const float4 w4 = wv[h4];
               sum = fmaf(w4.x, fminf(__uint_as_float(r[4 * h4 + 0]), 0.f), sum);
               sum = fmaf(w4.y, fminf(__uint_as_float(r[4 * h4 + 1]), 0.f), sum);
               sum = fmaf(w4.z, fminf(__uint_as_float(r[4 * h4 + 2]), 0.f), sum);
               sum = fmaf(w4.w, fminf(__uint_as_float(r[4 * h4 + 3]), 0.f), sum);
             }
           }
-          if (key <= pos) p.scores[static_cast<int64_t>(t) * p.ld + key] = scale * sum;
+          const int pos = possm[qb * G + j];
+          if (key <= pos) p.scores[static_cast<int64_t>(grp.t0 + j) * p.ld + key] = scale * sum;
         }
         tc_fence_before();
         __syncwarp();
@@ -369,6 +426,8 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive(&empty[s]);
         }
       }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&qempty[cur.count & 1]);
     }
   }
   tc_fence_before();

@@ -36,42 +36,37 @@ namespace mla {
 constexpr int RAW_STRIDE = 592;                   // 576 + 16: conflict-free row reads
 constexpr int OFF_RAW = 0;
 constexpr int RAW_BYTES = kSelTile * RAW_STRIDE;  // 75,776
-constexpr int OFF_Q = 76800;                      // 2 x [96 x 128 B]
-constexpr int Q_SLOT = kMlaHeads * 128;
-constexpr int OFF_C = OFF_Q + 2 * Q_SLOT;         // 2 x [128 x 128 B]
-constexpr int C_SLOT = kSelTile * 128;
-constexpr int OFF_P = OFF_C + 2 * C_SLOT;         // P^T: 2 head atoms x 16 token groups x 1 KB
+constexpr int QSLOTS = 3;
+constexpr int OFF_Q = 76800;                      // QSLOTS x [96 x 128 B] (1024-aligned slots)
+constexpr int Q_SLOT = kMlaHeads * 128;           // 12 KB
+constexpr int RSLOTS = 3;
+constexpr int OFF_RING = OFF_Q + QSLOTS * Q_SLOT; // RSLOTS x 16 KB: C chunks (QK) then V half-blocks (PV)
+constexpr int RING_SLOT = 16384;
+constexpr int OFF_P = OFF_RING + RSLOTS * RING_SLOT;   // P^T: 2 head atoms x 16 token groups x 1 KB
 constexpr int P_BYTES = 2 * 16 * 1024;
-constexpr int OFF_V = OFF_P + P_BYTES;            // 2 x [128 dims x 64 tokens] f16
-constexpr int V_SLOT = 2 * 8 * 1024;
-constexpr int OFF_RED = OFF_V + 2 * V_SLOT;       // 4 x 96 floats
-constexpr int OFF_MUSE = OFF_RED + 4 * 96 * 4;    // 96 floats
+constexpr int OFF_RED = OFF_P + P_BYTES;          // 4 x 96 floats
+constexpr int OFF_RED2 = OFF_RED + 4 * 96 * 4;    // 4 x 96 floats
+constexpr int OFF_MUSE = OFF_RED2 + 4 * 96 * 4;   // 96 floats
 constexpr int OFF_ALPHA = OFF_MUSE + 96 * 4;      // 96 floats
 constexpr int OFF_LFIN = OFF_ALPHA + 96 * 4;      // 96 floats
-constexpr int OFF_RED2 = OFF_LFIN + 96 * 4;       // 4 x 96 floats
-constexpr int OFF_BARS = OFF_RED2 + 4 * 96 * 4;
-constexpr int N_BARS = 16;
+constexpr int OFF_ROWOK = OFF_LFIN + 96 * 4;      // 128 bytes: selected row present in the raw tile
+constexpr int OFF_BARS = OFF_ROWOK + 128;
+constexpr int N_BARS = 24;
 constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;                      // producer, MMA, 4 converter warps, 4 softmax warps
 constexpr int TMEM_COLS = 512;
 constexpr int S_COL = 0;
 constexpr int O_COL = 128;
+constexpr int FILLS = kLatDim / 64 + 8;           // ring fills per tile: 9 C chunks + 8 V half-blocks
 constexpr float TAU = 8.0f;                       // log2 headroom before the running max moves
-static_assert(OFF_Q % 1024 == 0 && OFF_C % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0, "align");
+static_assert(OFF_Q % 1024 == 0 && OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "align");
 static_assert(OFF_Q >= RAW_BYTES, "raw");
 static_assert(SMEM_BYTES <= 232448, "smem");
 }  // namespace mla
 
 __device__ __forceinline__ uint8_t* align1024_mla(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
-__device__ __forceinline__ void drain_wait_mla(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(addr, parity))
-    if (globaltimer() - t0 > 200000000ull) break;
 }
 
 // 16 e4m3 bytes -> 16 bf16 values (exact), packed as 8 x bf16x2.
@@ -134,25 +129,25 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
   uint64_t* raw_full = bars + 0;
   uint64_t* raw_empty = bars + 1;
-  uint64_t* q_full = bars + 2;    // [2]
-  uint64_t* q_empty = bars + 4;   // [2]
-  uint64_t* c_full = bars + 6;    // [2]
-  uint64_t* c_empty = bars + 8;   // [2]
-  uint64_t* v_full = bars + 10;   // [2]
-  uint64_t* v_empty = bars + 12;  // [2]
-  uint64_t* s_full = bars + 14;
-  uint64_t* misc_bar = bars + 15;
-  __shared__ __align__(8) uint64_t s_free, p_full, o_done, drain;
+  uint64_t* q_full = bars + 2;      // [QSLOTS]
+  uint64_t* q_empty = bars + 6;     // [QSLOTS]
+  uint64_t* ring_full = bars + 10;  // [RSLOTS]
+  uint64_t* ring_empty = bars + 14; // [RSLOTS]
+  uint64_t* s_full = bars + 18;
+  uint64_t* s_free = bars + 19;
+  uint64_t* p_full = bars + 20;
+  uint64_t* o_done = bars + 21;
+  uint64_t* drain = bars + 22;
   __shared__ int n_valid_sh;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + OFF_MISC + 8);
+  int* rescale_sh = reinterpret_cast<int*>(smem + OFF_MISC + 16);
   float* red = reinterpret_cast<float*>(smem + OFF_RED);
+  float* red2 = reinterpret_cast<float*>(smem + OFF_RED2);
   float* m_use = reinterpret_cast<float*>(smem + OFF_MUSE);
   float* alpha_sh = reinterpret_cast<float*>(smem + OFF_ALPHA);
   float* l_fin = reinterpret_cast<float*>(smem + OFF_LFIN);
-  float* red2 = reinterpret_cast<float*>(smem + OFF_RED2);
-  int* rescale_sh = reinterpret_cast<int*>(smem + OFF_MISC + 16);
-  (void)misc_bar;
+  uint8_t* rowok = smem + OFF_ROWOK;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.y;
@@ -164,19 +159,19 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(raw_full, 1);
     mbar_init(raw_empty, 4);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < QSLOTS; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
-      mbar_init(&c_full[i], 4);
-      mbar_init(&c_empty[i], 1);
-      mbar_init(&v_full[i], 4);
-      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < RSLOTS; ++i) {
+      mbar_init(&ring_full[i], 4);
+      mbar_init(&ring_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(&s_free, 4);
-    mbar_init(&p_full, 4);
-    mbar_init(&o_done, 1);
-    mbar_init(&drain, 1);
+    mbar_init(s_free, 4);
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
     *abortf = 0;
     n_valid_sh = 0;
     fence_mbar_init();
@@ -224,7 +219,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         const int e = j * kSelTile + r;
         src[i] = nullptr;
         if (e < n_valid) {
-          int s = idx_row[e];
+          const int s = idx_row[e];
           if (s < 0 || s > pos) {
             atomicOr(p.status, DEV_BAD_BATCH);
           } else {
@@ -238,19 +233,22 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
             }
           }
         }
+        rowok[r] = src[i] != nullptr;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) nrow += __shfl_xor_sync(0xffffffffu, nrow, o);
+      __threadfence_block();
+      __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(raw_full, nrow * kLatDim);
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         if (src[i]) bulk_load(smem + OFF_RAW + (lane + 32 * i) * RAW_STRIDE, src[i], kLatDim, raw_full);
       ++issued_tiles;
-      // q in 9 chunks of 64 dims
+      // q in 9 chunks of 64 dims through the 4-slot ring
       for (int kc = 0; kc < kLatDim / 64 && ok; ++kc, ++qc) {
-        const int slot = qc & 1;
-        if (qc >= 2) ok = mbar_wait(&q_empty[slot], ((qc >> 1) - 1) & 1, ab);
+        const int slot = qc % QSLOTS;
+        if (qc >= QSLOTS) ok = mbar_wait(&q_empty[slot], ((qc / QSLOTS) - 1) & 1, ab);
         if (ok && lane == 0) {
           mbar_arrive_expect_tx(&q_full[slot], Q_SLOT);
           tma_load_2d(smem + OFF_Q + slot * Q_SLOT, &qmap, &q_full[slot], kc * 64, t * kMlaHeads);
@@ -258,135 +256,155 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         __syncwarp();
       }
     }
-    if (!ok && issued_tiles > 0) drain_wait_mla(raw_full, (issued_tiles - 1) & 1);
+    if (!ok && issued_tiles > 0) drain_wait(raw_full, (issued_tiles - 1) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(1, 1, false, false, 128, kMlaHeads);
       const uint32_t idesc_pv = make_idesc(0, 0, true, true, 128, kMlaHeads);
-      int cc = 0, vc = 0;
+      int fc = 0, qc = 0;
       bool ok = true;
       for (int j = j0; j < j1 && ok; ++j) {
         const int jt = j - j0;
-        if (jt > 0 && !(ok = mbar_wait(&s_free, (jt - 1) & 1, ab))) break;
-        for (int kc = 0; kc < kLatDim / 64; ++kc, ++cc) {
-          const int slot = cc & 1;
-          const uint32_t ph = (cc >> 1) & 1;
-          if (!(ok = mbar_wait(&c_full[slot], ph, ab))) break;
-          if (!(ok = mbar_wait(&q_full[slot], ph, ab))) break;
+        if (jt > 0 && !(ok = mbar_wait(s_free, (jt - 1) & 1, ab))) break;
+        for (int kc = 0; kc < kLatDim / 64; ++kc, ++fc, ++qc) {
+          const int slot = fc % RSLOTS;
+          const int qs = qc % QSLOTS;
+          if (!(ok = mbar_wait(&ring_full[slot], (fc / RSLOTS) & 1, ab))) break;
+          if (!(ok = mbar_wait(&q_full[qs], (qc / QSLOTS) & 1, ab))) break;
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + OFF_C + slot * C_SLOT);
-          const uint32_t b0 = smem_u32(smem + OFF_Q + slot * Q_SLOT);
+          const uint32_t a0 = smem_u32(smem + OFF_RING + slot * RING_SLOT);
+          const uint32_t b0 = smem_u32(smem + OFF_Q + qs * Q_SLOT);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f16(tmem + S_COL, make_sdesc_sw128(a0 + 32 * kk, 16, 1024), make_sdesc_sw128(b0 + 32 * kk, 16, 1024),
                     idesc_qk, (kc | kk) ? 1u : 0u);
-          tc_commit(&c_empty[slot]);
-          tc_commit(&q_empty[slot]);
+          tc_commit(&ring_empty[slot]);
+          tc_commit(&q_empty[qs]);
         }
         if (!ok) break;
         tc_commit(s_full);
-        if (!(ok = mbar_wait(&p_full, jt & 1, ab))) break;
+        if (!(ok = mbar_wait(p_full, jt & 1, ab))) break;
         tc_fence_after();
         for (int v = 0; v < 4 && ok; ++v) {
-          for (int kh = 0; kh < 2; ++kh, ++vc) {
-            const int slot = vc & 1;
-            if (!(ok = mbar_wait(&v_full[slot], (vc >> 1) & 1, ab))) break;
+          for (int kh = 0; kh < 2; ++kh, ++fc) {
+            const int slot = fc % RSLOTS;
+            if (!(ok = mbar_wait(&ring_full[slot], (fc / RSLOTS) & 1, ab))) break;
             tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + OFF_V + slot * V_SLOT);
+            const uint32_t a0 = smem_u32(smem + OFF_RING + slot * RING_SLOT);
             const uint32_t b0 = smem_u32(smem + OFF_P);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_f16(tmem + O_COL + 96 * v, make_sdesc_sw128(a0 + k * 2048, 8192, 1024),
                       make_sdesc_sw128(b0 + (kh * 8 + k * 2) * 1024, 16384, 1024), idesc_pv,
                       (jt > 0 || kh > 0 || k > 0) ? 1u : 0u);
-            tc_commit(&v_empty[slot]);
+            tc_commit(&ring_empty[slot]);
           }
         }
         if (!ok) break;
-        tc_commit(&o_done);
+        tc_commit(o_done);
       }
       if (!ok) {
-        tc_commit(&drain);
-        drain_wait_mla(&drain, 0);
+        tc_commit(drain);
+        drain_wait(drain, 0);
       }
     }
-  } else {
-    // ------------------------------------------------------ math warps (2..5)
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;          // token lane within the tile
-    const int mt = threadIdx.x - 64;            // 0..127
-    float m_run[3] = {-INFINITY, -INFINITY, -INFINITY};   // per head (lane + 32 i), log2 units
-    float l_run[3] = {0.f, 0.f, 0.f};                      // warp 2 only: running sums
-    float alpha_r[3] = {1.f, 1.f, 1.f};
-    int cc = 0, vc = 0;
+  } else if (warp < 6) {
+    // ----------------------------------------------------- converters (2..5)
+    const int ct = threadIdx.x - 64;            // 0..127
+    int fc = 0;
     bool ok = true;
     for (int j = j0; j < j1 && ok; ++j) {
       const int jt = j - j0;
       if (!(ok = mbar_wait(raw_full, jt & 1, ab))) break;
       const uint8_t* raw = smem + OFF_RAW;
-      // validity of this thread's token row (the producer skipped invalid rows)
-      bool valid = false;
+      // C chunks (bf16, K-major, 128-byte swizzle): thread ct converts row ct
       {
-        const int e = j * kSelTile + r;
-        if (e < n_valid) {
-          const int s = idx_row[e];
-          if (s >= 0 && s <= pos) {
-            const int row = p.b.bt[static_cast<int64_t>(req) * p.b.bt_stride + (s >> p.pool.log2_bs)];
-            valid = row >= 0 && row < p.pool.num_rows;
-          }
-        }
-      }
-      // ---- C chunks (bf16, K-major, 128-byte swizzle): thread r writes row r
-      for (int kc = 0; kc < kLatDim / 64; ++kc, ++cc) {
-        const int slot = cc & 1;
-        if (cc >= 2 && !(ok = mbar_wait(&c_empty[slot], ((cc >> 1) - 1) & 1, ab))) break;
-        uint8_t* dst = smem + OFF_C + slot * C_SLOT + (r >> 3) * 1024;
+        const bool valid = rowok[ct] != 0;
+        for (int kc = 0; kc < kLatDim / 64; ++kc, ++fc) {
+          const int slot = fc % RSLOTS;
+          if (fc >= RSLOTS && !(ok = mbar_wait(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
+          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (ct >> 3) * 1024;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t o[8];
-          if (valid) {
-            const uint4 in = *reinterpret_cast<const uint4*>(raw + r * RAW_STRIDE + kc * 64 + q4 * 16);
-            e4m3x16_to_bf16(in, o);
-          } else {
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t o[8];
+            if (valid) {
+              const uint4 in = *reinterpret_cast<const uint4*>(raw + ct * RAW_STRIDE + kc * 64 + q4 * 16);
+              e4m3x16_to_bf16(in, o);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = 0;
+              for (int i = 0; i < 8; ++i) o[i] = 0;
+            }
+            sts128(dst + sw128_off(ct & 7, 2 * q4), o);
+            sts128(dst + sw128_off(ct & 7, 2 * q4 + 1), o + 4);
           }
-          sts128(dst + sw128_off(r & 7, 2 * q4), o);
-          sts128(dst + sw128_off(r & 7, 2 * q4 + 1), o + 4);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ring_full[slot]);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c_full[slot]);
       }
       if (!ok) break;
-      // ---- softmax over the tile's tokens (TMEM lanes) for each head (columns)
-      if (!(ok = mbar_wait(s_full, jt & 1, ab))) break;
-      tc_fence_after();
-      float x[kMlaHeads];
-      {
-        uint32_t rr[32];
+      // V half-blocks (fp16, MN-major): block v = dims [128v, +128), half kh = tokens [64kh, +64)
+      for (int v = 0; v < 4 && ok; ++v) {
+        for (int kh = 0; kh < 2; ++kh, ++fc) {
+          const int slot = fc % RSLOTS;
+          if (fc >= RSLOTS && !(ok = mbar_wait(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
+          const int tl = ct >> 1;            // token within the half (0..63)
+          const int d2 = ct & 1;             // which 64-dim atom of the block
+          const int row = kh * 64 + tl;
+          const bool rv = rowok[row] != 0;
+          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + d2 * 8192 + (tl >> 3) * 1024;
 #pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          DSA_TMEM_LD32(tmem + S_COL + 32 * c + (static_cast<uint32_t>(quarter * 32) << 16), rr);
-          tmem_wait_ld();
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t o[8];
+            if (rv) {
+              const uint4 in = *reinterpret_cast<const uint4*>(raw + row * RAW_STRIDE + v * 128 + d2 * 64 + q4 * 16);
+              e4m3x16_to_f16(in, o);
+            } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[32 * c + i] = valid ? __uint_as_float(rr[i]) * p.scale_log2 : -INFINITY;
+              for (int i = 0; i < 8; ++i) o[i] = 0;
+            }
+            sts128(dst + sw128_off(tl & 7, 2 * q4), o);
+            sts128(dst + sw128_off(tl & 7, 2 * q4 + 1), o + 4);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ring_full[slot]);
         }
       }
-      tc_fence_before();
+      if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free);
+      if (lane == 0) mbar_arrive(raw_empty);
+    }
+  } else {
+    // ------------------------------------------------ softmax warps (6..9)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;          // token lane within the tile
+    const int mt = threadIdx.x - 192;           // 0..127
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float m_run[3] = {-INFINITY, -INFINITY, -INFINITY};   // per head (lane + 32 i), log2 units
+    float l_run[3] = {0.f, 0.f, 0.f};                      // warp 6 only: running sums
+    float alpha_r[3] = {1.f, 1.f, 1.f};
+    bool ok = true;
+    for (int j = j0; j < j1 && ok; ++j) {
+      const int jt = j - j0;
+      if (!(ok = mbar_wait(s_full, jt & 1, ab))) break;
+      if (!(ok = mbar_wait(raw_full, jt & 1, ab))) break;   // rowok of this tile
+      tc_fence_after();
+      const bool valid = rowok[r] != 0;
       // tile maxima per head: warp butterfly, then the 4 warps through shared memory
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
+        uint32_t rr[32];
+        DSA_TMEM_LD32(tmem + S_COL + 32 * c + lane_off, rr);
+        tmem_wait_ld();
         float tmp[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tmp[i] = x[32 * c + i];
+        for (int i = 0; i < 32; ++i) tmp[i] = valid ? __uint_as_float(rr[i]) * p.scale_log2 : -INFINITY;
         red[quarter * kMlaHeads + 32 * c + lane] = warp_transpose_reduce32<true>(tmp);
       }
       named_bar_sync(1, 128);
-      if (warp == 2) {
+      if (warp == 6) {
         bool moved = false;
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
@@ -407,14 +425,14 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       named_bar_sync(1, 128);
       const bool any_rescale = *reinterpret_cast<volatile int*>(rescale_sh) != 0;
       // PV of the previous tile must be done before P is overwritten or O rescaled
-      if (jt > 0 && !(ok = mbar_wait(&o_done, (jt - 1) & 1, ab))) break;
+      if (jt > 0 && !(ok = mbar_wait(o_done, (jt - 1) & 1, ab))) break;
       if (any_rescale) {
         tc_fence_after();
         for (int v = 0; v < 4; ++v) {
 #pragma unroll
           for (int c = 0; c < 3; ++c) {
             uint32_t rr[32];
-            const uint32_t ta = tmem + O_COL + 96 * v + 32 * c + (static_cast<uint32_t>(quarter * 32) << 16);
+            const uint32_t ta = tmem + O_COL + 96 * v + 32 * c + lane_off;
             DSA_TMEM_LD32(ta, rr);
             tmem_wait_ld();
 #pragma unroll
@@ -423,16 +441,19 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           }
         }
         tmem_wait_st();
-        tc_fence_before();
       }
       // P^T row r (fp16), MN-major: heads contiguous in 16-byte chunks of 8; row sums per head
       {
         uint8_t* prow = smem + OFF_P + (r >> 3) * 1024;
 #pragma unroll
         for (int c = 0; c < 3; ++c) {
+          uint32_t rr[32];
+          DSA_TMEM_LD32(tmem + S_COL + 32 * c + lane_off, rr);
+          tmem_wait_ld();
           float pv[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pv[i] = valid ? exp2f(x[32 * c + i] - m_use[32 * c + i]) : 0.f;
+          for (int i = 0; i < 32; ++i)
+            pv[i] = valid ? exp2f(__uint_as_float(rr[i]) * p.scale_log2 - m_use[32 * c + i]) : 0.f;
 #pragma unroll
           for (int cc4 = 0; cc4 < 4; ++cc4) {
             uint32_t o[4];
@@ -448,10 +469,14 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         }
       }
       fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full);
+      if (lane == 0) {
+        mbar_arrive(s_free);
+        mbar_arrive(p_full);
+      }
       named_bar_sync(1, 128);
-      if (warp == 2) {
+      if (warp == 6) {
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           const int h = lane + 32 * i;
@@ -459,56 +484,16 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
                      red2[3 * kMlaHeads + h];
         }
       }
-      // ---- V blocks (fp16, MN-major): block v = dims [128v, 128v+128), half kh = tokens [64kh, 64kh+64)
-      for (int v = 0; v < 4 && ok; ++v) {
-        for (int kh = 0; kh < 2; ++kh, ++vc) {
-          const int slot = vc & 1;
-          if (vc >= 2 && !(ok = mbar_wait(&v_empty[slot], ((vc >> 1) - 1) & 1, ab))) break;
-          const int tl = mt >> 1;            // token within the half (0..63)
-          const int d2 = mt & 1;             // which 64-dim atom of the block
-          const int row = kh * 64 + tl;
-          bool rv = false;
-          {
-            const int e = j * kSelTile + row;
-            if (e < n_valid) {
-              const int s = idx_row[e];
-              if (s >= 0 && s <= pos) {
-                const int prow = p.b.bt[static_cast<int64_t>(req) * p.b.bt_stride + (s >> p.pool.log2_bs)];
-                rv = prow >= 0 && prow < p.pool.num_rows;
-              }
-            }
-          }
-          uint8_t* dst = smem + OFF_V + slot * V_SLOT + d2 * 8192 + (tl >> 3) * 1024;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t o[8];
-            if (rv) {
-              const uint4 in =
-                  *reinterpret_cast<const uint4*>(raw + row * RAW_STRIDE + v * 128 + d2 * 64 + q4 * 16);
-              e4m3x16_to_f16(in, o);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] = 0;
-            }
-            sts128(dst + sw128_off(tl & 7, 2 * q4), o);
-            sts128(dst + sw128_off(tl & 7, 2 * q4 + 1), o + 4);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&v_full[slot]);
-        }
-      }
-      if (!ok) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(raw_empty);
     }
-    // ---- epilogue: row sums across the 128 token lanes, then O / l or the partial
-    if (ok) ok = mbar_wait(&o_done, (j1 - j0 - 1) & 1, ab);
+    // ---- epilogue: O / l, or the normalised fp16 partial and (max, sum)
+    if (ok) ok = mbar_wait(o_done, (j1 - j0 - 1) & 1, ab);
     if (ok) {
       tc_fence_after();
-      if (warp == 2) {
+      if (warp == 6) {
 #pragma unroll
         for (int i = 0; i < 3; ++i) l_fin[lane + 32 * i] = l_run[i];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) alpha_sh[lane + 32 * i] = 1.f / l_run[i];   // reused: 1 / sum
       }
       named_bar_sync(1, 128);
       if (p.nsplit == 1) {
@@ -518,28 +503,31 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 3; ++c) {
             uint32_t rr[32];
-            DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + (static_cast<uint32_t>(quarter * 32) << 16), rr);
+            DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int h = 32 * c + i;
-              orow[h * kVDim + dim] = __float2bfloat16_rn(__uint_as_float(rr[i]) / l_fin[h]);
+              orow[h * kVDim + dim] = __float2bfloat16_rn(__uint_as_float(rr[i]) * alpha_sh[h]);
             }
           }
         }
         if (p.lse && mt < kMlaHeads)
           p.lse[static_cast<int64_t>(t) * kMlaHeads + mt] = (m_use[mt] + log2f(l_fin[mt])) * 0.69314718055994531f;
       } else {
-        float* po = p.part_o + ts * kMlaHeads * kVDim;
+        __half* po = p.part_o + ts * kMlaHeads * kVDim;
         for (int v = 0; v < 4; ++v) {
           const int dim = v * 128 + r;
 #pragma unroll
           for (int c = 0; c < 3; ++c) {
             uint32_t rr[32];
-            DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + (static_cast<uint32_t>(quarter * 32) << 16), rr);
+            DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) po[(32 * c + i) * kVDim + dim] = __uint_as_float(rr[i]);
+            for (int i = 0; i < 32; ++i) {
+              const int h = 32 * c + i;
+              po[h * kVDim + dim] = __float2half_rn(__uint_as_float(rr[i]) * alpha_sh[h]);
+            }
           }
         }
         if (mt < kMlaHeads) p.part_ml[ts * kMlaHeads + mt] = make_float2(m_use[mt], l_fin[mt]);
@@ -551,46 +539,63 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// Log-sum-exp combine of the split partials: grid (12, T), 256 threads = 8 heads x 32.
+// Log-sum-exp combine of the split partials (each partial normalised by its
+// own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m).
+// Grid (12, T), 256 threads = 8 heads x 32.
 __global__ void __launch_bounds__(256) mla_combine_kernel(MlaParams p) {
   const int t = blockIdx.y;
   const int h = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int64_t base = static_cast<int64_t>(t) * p.nsplit;
-  float M = -INFINITY;
-  for (int j = 0; j < p.nsplit; ++j) {
-    const float2 ml = p.part_ml[(base + j) * kMlaHeads + h];
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  // lane j holds split j's (max, sum); nsplit <= 16
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < p.nsplit) ml = p.part_ml[(base + lane) * kMlaHeads + h];
+  float M = ml.y > 0.f ? ml.x : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float wl_mine = ml.y > 0.f ? exp2f(ml.x - M) * ml.y : 0.f;
+  float L = wl_mine;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  // all splits' slices of this head in flight at once
+  uint4 u[16][2];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < p.nsplit) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.part_o + ((base + j) * kMlaHeads + h) * kVDim);
+      u[j][0] = __ldcg(src + lane);
+      u[j][1] = __ldcg(src + lane + 32);
+    }
   }
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  float L = 0.f;
-  for (int j = 0; j < p.nsplit; ++j) {
-    const float2 ml = p.part_ml[(base + j) * kMlaHeads + h];
-    if (!(ml.y > 0.f)) continue;
-    const float wgt = exp2f(ml.x - M);
-    L += wgt * ml.y;
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + ((base + j) * kMlaHeads + h) * kVDim);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = __ldcg(src + lane + 32 * q);
-      acc[4 * q + 0] = fmaf(wgt, v.x, acc[4 * q + 0]);
-      acc[4 * q + 1] = fmaf(wgt, v.y, acc[4 * q + 1]);
-      acc[4 * q + 2] = fmaf(wgt, v.z, acc[4 * q + 2]);
-      acc[4 * q + 3] = fmaf(wgt, v.w, acc[4 * q + 3]);
+  for (int j = 0; j < 16; ++j) {
+    const float wj = __shfl_sync(0xffffffffu, wl_mine, j);
+    if (j >= p.nsplit || wj == 0.f) continue;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t w4[4] = {u[j][q].x, u[j][q].y, u[j][q].z, u[j][q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+        acc[8 * q + 2 * e] = fmaf(wj, f.x, acc[8 * q + 2 * e]);
+        acc[8 * q + 2 * e + 1] = fmaf(wj, f.y, acc[8 * q + 2 * e + 1]);
+      }
     }
   }
   const float inv = 1.f / L;
   __nv_bfloat16* orow = p.out + (static_cast<int64_t>(t) * kMlaHeads + h) * kVDim;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * q + 0] * inv, acc[4 * q + 1] * inv);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&a);
-    u.y = *reinterpret_cast<const uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(orow + 4 * (lane + 32 * q)) = u;
+  for (int q = 0; q < 2; ++q) {
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * q + 2 * e] * inv, acc[8 * q + 2 * e + 1] * inv);
+      w4[e] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(orow + 8 * (lane + 32 * q)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
   }
   if (p.lse && lane == 0) p.lse[static_cast<int64_t>(t) * kMlaHeads + h] = (M + log2f(L)) * 0.69314718055994531f;
 }

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -23,14 +24,20 @@ struct TopkParams {
   const float* scores;
   int64_t ld;
   int k;
-  int chunk;          // scores per CTA
-  uint32_t* hist1;    // [T, 2048]
-  uint32_t* hist2;    // [T, 2048]
-  uint32_t* hist3;    // [T, 1024]
-  uint32_t* counts;   // [T, nchunks, 2] (greater, equal)
-  int nchunks;
-  int32_t* idx;       // [T, k]
-  int32_t* phys;      // [T, k] or null
+  int chunk;            // scores per CTA (4096)
+  int nchunks;          // chunks per row at max_ctx_len
+  uint32_t* hist;       // [T, 2048]  top-digit histogram                 (zeroed)
+  uint32_t* done;       // [T, 2]     per-pass CTA tickets                 (zeroed)
+  uint32_t* cand_count; // [T]        candidates appended                  (zeroed)
+  uint32_t* taken;      // [T, nchunks] candidates taken per chunk         (zeroed)
+  uint32_t* thr;        // [T, 4]     digit b1, count above b1, key T, position cut
+  uint32_t* gt;         // [T, nchunks] keys above digit b1 per chunk
+  uint2* cands;         // [T, cap]   (key, position) in digit b1
+  int cap;
+  void* zero_begin;     // the zeroed fields are one contiguous region
+  size_t zero_bytes;
+  int32_t* idx;         // [T, k]
+  int32_t* phys;        // [T, k] or null
   int log2_bs;
   uint32_t* status;
 };
@@ -45,10 +52,58 @@ struct MlaParams {
   int nsplit;
   __nv_bfloat16* out;      // [T, 96, 512]       (nsplit == 1)
   float* lse;              // [T, 96] or null    (nsplit == 1)
-  float* part_o;           // [T, nsplit, 96, 512] (nsplit > 1)
+  __half* part_o;          // [T, nsplit, 96, 512] (nsplit > 1), each normalised by its own sum
   float2* part_ml;         // [T, nsplit, 96]      (nsplit > 1): (max in log2 units, sum)
   uint32_t* status;
 };
+
+constexpr int kTopkChunk = 4096;   // scores per CTA in the top-k passes
+constexpr int kTopkCap = 4096;     // candidates per row kept for the exact resolution
+
+// Byte offsets of the top-k scratch inside a region (256-byte aligned segments);
+// [hist .. zero_end) must be zeroed before the passes (launch_topk does it).
+struct TopkScratch {
+  size_t hist, done, cand_count, taken, zero_end, thr, gt, cands, total;
+};
+
+inline TopkScratch topk_scratch_layout(int64_t T, int nchunks) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  TopkScratch L;
+  size_t off = 0;
+  L.hist = off;
+  off += size_t(T) * 2048 * 4;
+  L.done = off;
+  off += size_t(T) * 2 * 4;
+  L.cand_count = off;
+  off += size_t(T) * 4;
+  L.taken = off;
+  off += size_t(T) * nchunks * 4;
+  L.zero_end = off;
+  off = up(off);
+  L.thr = off;
+  off = up(off + size_t(T) * 4 * 4);
+  L.gt = off;
+  off = up(off + size_t(T) * nchunks * 4);
+  L.cands = off;
+  off = up(off + size_t(T) * kTopkCap * 8);
+  L.total = off;
+  return L;
+}
+
+inline void topk_bind_scratch(TopkParams& p, uint8_t* base, const TopkScratch& L, int nchunks) {
+  p.chunk = kTopkChunk;
+  p.nchunks = nchunks;
+  p.hist = reinterpret_cast<uint32_t*>(base + L.hist);
+  p.done = reinterpret_cast<uint32_t*>(base + L.done);
+  p.cand_count = reinterpret_cast<uint32_t*>(base + L.cand_count);
+  p.taken = reinterpret_cast<uint32_t*>(base + L.taken);
+  p.thr = reinterpret_cast<uint32_t*>(base + L.thr);
+  p.gt = reinterpret_cast<uint32_t*>(base + L.gt);
+  p.cands = reinterpret_cast<uint2*>(base + L.cands);
+  p.cap = kTopkCap;
+  p.zero_begin = base + L.hist;
+  p.zero_bytes = L.zero_end - L.hist;
+}
 
 cudaError_t launch_plan_groups(const BatchView& b, int G, ScoreGroup* groups, PlanHeader* hdr, uint32_t* status,
                                cudaStream_t st);

@@ -13,18 +13,14 @@ enum : uint32_t {
   DEV_BAD_BATCH = 4u,    // q_req / q_pos / ctx_len / idx outside their ranges
 };
 
-// Upper bound of any single wait inside a kernel (ns).  A healthy pipeline
-// waits microseconds; reaching this means a logic error, not a slow GPU.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Upper bound of any single wait inside a kernel, in SM clock cycles (about
+// 2 s at 2 GHz).  A healthy pipeline waits microseconds; reaching this means a
+// logic error, not a slow GPU.  The SM cycle counter is used because it is cheap
+// to read; the global nanosecond timer costs far more per read.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -71,18 +67,27 @@ struct Abort {
 static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort ab) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(addr, parity)) return true;
-    if ((it & 31u) == 0u) {
+    if ((it & 15u) == 0u) {
       if (*reinterpret_cast<volatile int*>(ab.flag)) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (clock64() - t0 > kWaitLimitCycles) {
         *reinterpret_cast<volatile int*>(ab.flag) = 1;
         atomicOr(ab.status, DEV_TIMEOUT);
         return false;
       }
     }
   }
+}
+
+// Wait ignoring the CTA abort flag, for draining copies/MMAs in flight before an
+// early exit; gives up after about 0.2 s.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(addr, parity))
+    if (clock64() - t0 > 400000000ll) break;
 }
 
 // --------------------------------------------------------------------- fences

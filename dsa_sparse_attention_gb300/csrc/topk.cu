@@ -2,96 +2,108 @@
 //
 // vLLM K3.1 Pro day-0 post, "Sparse Attention in K3.1 Pro": the indexer keeps
 // the top 2,048 tokens and attention runs exactly over them; "An exact top-k
-// merge with 10x less traffic" selects the global top-2048 with a radix select;
-// "Zero-mismatch RL on day 0" asks for a top-k whose result does not depend on
-// the batch.  Here:
-//  * each score maps to an order-preserving 32-bit key; the k-th largest key is
-//    found digit by digit (11 + 11 + 10 bits) from per-query histograms that
-//    every chunk of the row contributes to (one CTA per chunk of 4096 scores, so
-//    a single 1M-token query still spreads over hundreds of CTAs);
-//  * equal keys are taken lowest position first: with the threshold key T and
-//    r = k - #{key > T}, the selection is {key > T} plus the first r positions
-//    with key == T;
-//  * the output is written in ascending position order by an ordered compaction
-//    (per-chunk counts, then prefix sums), so it is deterministic and identical
-//    whether the query runs alone or inside any batch.
+// merge with 10x less traffic" selects the global top-2048 with a radix select
+// over a small candidate set, falling back to a full resend when the candidates
+// do not suffice; "Zero-mismatch RL on day 0" asks for a top-k whose result does
+// not depend on the batch.  Here, per query row of n scores split into chunks
+// of 4096 (one CTA each, so a 1M-token row still spreads over 256 CTAs):
+//  1. hist:       11-bit histogram of the top digit of each score's order-
+//                 preserving key; the last CTA of the row finds the digit b1 that
+//                 holds the k-th largest key and the count above it.
+//  2. candidates: each chunk counts its keys above digit b1 and appends the keys
+//                 in digit b1 (the candidates) to a per-row list; the last CTA
+//                 of the row resolves the exact threshold key T among them, and
+//                 the position cut for keys equal to T (lowest positions first),
+//                 then counts per chunk how many candidates are taken.  If the
+//                 list overflows (heavy ties), that CTA redoes this step exactly
+//                 over the whole row.
+//  3. emit:       ordered compaction: chunk c writes its selected positions after
+//                 those of chunks < c, so the output is ascending, deterministic
+//                 and independent of the rest of the batch.
 #include "params.cuh"
 
 namespace dsa {
 
 constexpr int kTopkThreads = 256;
-constexpr int kBins1 = 2048, kBins2 = 2048, kBins3 = 1024;
+constexpr int kBins = 2048;
+constexpr int kPerThread = 16;                       // scores per thread per chunk
+static_assert(kTopkThreads * kPerThread == 4096, "chunk");
+static_assert(kTopkCap <= 4096, "the resolving CTA stages the candidate list in its 4096-entry buffer");
 
+// Order of the 16 scores a thread owns in its chunk: [c0 + 16*tid, +16).
+__device__ __forceinline__ void load16(const float* row, int s0, int c1, uint32_t (&u)[kPerThread]) {
+  if (s0 + kPerThread <= c1) {
+    const float4* p4 = reinterpret_cast<const float4*>(row + s0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = __ldcg(p4 + q);
+      u[4 * q + 0] = score_key(v.x);
+      u[4 * q + 1] = score_key(v.y);
+      u[4 * q + 2] = score_key(v.z);
+      u[4 * q + 3] = score_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) u[i] = (s0 + i < c1) ? score_key(__ldcg(row + s0 + i)) : 0u;
+  }
+}
 
-// Finds, in a histogram whose bins are ordered by key, the bin b* holding the
-// kk-th largest element (counting from the top) and the count strictly above it.
-__device__ void find_threshold(const uint32_t* hist, int nbins, uint32_t kk, int* out_bin, uint32_t* out_above,
-                               uint32_t* sh) {
-  const int per = nbins / kTopkThreads;
-  const int hi = nbins - threadIdx.x * per;   // this thread: bins [hi - per, hi), scanned downwards
-  uint32_t local = 0;
-  for (int b = hi - 1; b >= hi - per; --b) local += __ldcg(hist + b);
-  // exclusive scan of `local` in thread order (= descending bin order)
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t v = local;
+// Block-wide exclusive scan of one uint32 per thread; also returns the total.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t x = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += x;
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  if (lane == 31) sh[warp] = v;
+  if (lane == 31) sh[warp] = x;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t run = 0;
-    for (int w = 0; w < kTopkThreads / 32; ++w) {
-      uint32_t t = sh[w];
-      sh[w] = run;
-      run += t;
+  if (warp == 0) {
+    uint32_t w = lane < nw ? sh[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
     }
+    sh[lane] = w;   // inclusive per warp
   }
   __syncthreads();
-  const uint32_t excl = sh[warp] + v - local;
+  total = sh[nw - 1];
+  const uint32_t excl = (warp > 0 ? sh[warp - 1] : 0u) + x - v;
   __syncthreads();
+  return excl;
+}
+
+// In a histogram of `nbins` bins ordered by key, the bin holding the kk-th
+// largest element (1-based) and the number of elements in higher bins.
+// `hist` may be shared or global memory.  Uses sh[0..40].
+__device__ void find_bin(const uint32_t* hist, int nbins, uint32_t kk, int& bin, uint32_t& above, uint32_t* sh) {
+  const int per = nbins / blockDim.x;
+  const int hi = nbins - static_cast<int>(threadIdx.x) * per;
+  uint32_t local = 0;
+  for (int b = hi - 1; b >= hi - per; --b) local += hist[b];
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(local, sh, total);
   if (excl < kk && excl + local >= kk) {
     uint32_t cum = excl;
     for (int b = hi - 1; b >= hi - per; --b) {
-      const uint32_t h = __ldcg(hist + b);
+      const uint32_t h = hist[b];
       if (cum + h >= kk) {
-        sh[8] = static_cast<uint32_t>(b);
-        sh[9] = cum;
+        sh[33] = static_cast<uint32_t>(b);
+        sh[34] = cum;
         break;
       }
       cum += h;
     }
   }
   __syncthreads();
-  *out_bin = static_cast<int>(sh[8]);
-  *out_above = sh[9];
+  bin = static_cast<int>(sh[33]);
+  above = sh[34];
   __syncthreads();
 }
 
-struct Threshold {
-  uint32_t key;     // the k-th largest key
-  uint32_t above;   // elements with key > threshold
-};
-
-__device__ Threshold compute_threshold(const TopkParams& p, int t, int levels, uint32_t* sh, int* b1o = nullptr,
-                                       int* b2o = nullptr) {
-  int b1, b2 = 0, b3 = 0;
-  uint32_t a1, a2 = 0, a3 = 0;
-  const uint32_t k = static_cast<uint32_t>(p.k);
-  find_threshold(p.hist1 + static_cast<int64_t>(t) * kBins1, kBins1, k, &b1, &a1, sh);
-  if (levels >= 2) find_threshold(p.hist2 + static_cast<int64_t>(t) * kBins2, kBins2, k - a1, &b2, &a2, sh);
-  if (levels >= 3) find_threshold(p.hist3 + static_cast<int64_t>(t) * kBins3, kBins3, k - a1 - a2, &b3, &a3, sh);
-  if (b1o) *b1o = b1;
-  if (b2o) *b2o = b2;
-  Threshold th;
-  th.key = (static_cast<uint32_t>(b1) << 21) | (static_cast<uint32_t>(b2) << 10) | static_cast<uint32_t>(b3);
-  th.above = a1 + a2 + a3;
-  return th;
-}
-
-__device__ __forceinline__ bool chunk_range(const TopkParams& p, int t, int& c0, int& c1, int& n) {
+__device__ __forceinline__ bool row_range(const TopkParams& p, int t, int& c0, int& c1, int& n) {
   int req, pos;
   load_token(p.b, t, p.status, req, pos);
   n = pos + 1;
@@ -100,80 +112,213 @@ __device__ __forceinline__ bool chunk_range(const TopkParams& p, int t, int& c0,
   return c0 < n;
 }
 
-// Pass `level` (1..3): histogram of the next digit among the elements whose
-// higher digits equal the current prefix.
-template <int LEVEL>
+// The last CTA (by ticket) of row t to finish a pass; call with every thread.
+__device__ __forceinline__ bool last_of_row(uint32_t* counter, int nchunks_row, uint32_t* sh) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) sh[40] = atomicAdd(counter, 1u);
+  __syncthreads();
+  const bool last = sh[40] == static_cast<uint32_t>(nchunks_row - 1);
+  if (last) __threadfence();
+  return last;
+}
+
+// ------------------------------------------------------------------- pass 1
+
 __global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(TopkParams p) {
-  __shared__ uint32_t h[kBins1];
-  __shared__ uint32_t sh[16];
+  __shared__ uint32_t h[kBins];
+  __shared__ uint32_t sh[48];
   const int t = blockIdx.y;
   int c0, c1, n;
-  if (!chunk_range(p, t, c0, c1, n) || n <= p.k) return;
-  uint32_t prefix = 0;
-  if (LEVEL >= 2) {
-    int b1, b2;
-    compute_threshold(p, t, LEVEL - 1, sh, &b1, &b2);
-    prefix = LEVEL == 2 ? static_cast<uint32_t>(b1) : ((static_cast<uint32_t>(b1) << 11) | static_cast<uint32_t>(b2));
-  }
-  constexpr int nb = LEVEL == 3 ? kBins3 : kBins1;
-  for (int i = threadIdx.x; i < nb; i += kTopkThreads) h[i] = 0;
+  if (!row_range(p, t, c0, c1, n) || n <= p.k) return;
+  for (int i = threadIdx.x; i < kBins; i += kTopkThreads) h[i] = 0;
   __syncthreads();
   const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
-  for (int s = c0 + threadIdx.x; s < c1; s += kTopkThreads) {
-    const uint32_t u = score_key(__ldg(row + s));
-    if (LEVEL == 1) {
-      atomicAdd(&h[u >> 21], 1u);
-    } else if (LEVEL == 2) {
-      if ((u >> 21) == prefix) atomicAdd(&h[(u >> 10) & 2047u], 1u);
-    } else {
-      if ((u >> 10) == prefix) atomicAdd(&h[u & 1023u], 1u);
+  uint32_t u[kPerThread];
+  const int s0 = c0 + threadIdx.x * kPerThread;
+  load16(row, s0, c1, u);
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i)
+    if (s0 + i < c1) atomicAdd(&h[u[i] >> 21], 1u);
+  __syncthreads();
+  uint32_t* gh = p.hist + static_cast<int64_t>(t) * kBins;
+  for (int i = threadIdx.x; i < kBins; i += kTopkThreads)
+    if (h[i]) atomicAdd(gh + i, h[i]);
+  const int nch = static_cast<int>(cdiv(n, p.chunk));
+  if (!last_of_row(p.done + 2 * t, nch, sh)) return;
+  for (int i = threadIdx.x; i < kBins; i += kTopkThreads) h[i] = __ldcg(gh + i);
+  __syncthreads();
+  int b1;
+  uint32_t above;
+  find_bin(h, kBins, static_cast<uint32_t>(p.k), b1, above, sh);
+  if (threadIdx.x == 0) {
+    p.thr[4 * t + 0] = static_cast<uint32_t>(b1);
+    p.thr[4 * t + 1] = above;
+  }
+}
+
+// ------------------------------------------------------------------- pass 2
+
+// Exact resolution of the threshold among keys with top digit b1, by one CTA.
+// Inputs either the candidate list (smem-resident) or, on overflow, the row.
+struct Resolve {
+  uint32_t T;        // threshold key
+  int32_t cut;       // keys == T are taken at positions <= cut
+};
+
+// Returns the kk-th largest value (1-based) of the 21-bit low parts of the
+// elements produced by `gen(i, key, idx, valid)` for i < count, and the number
+// of elements strictly above it.  Two digit passes: 11 + 10 bits.
+template <typename Gen>
+__device__ void select_low21(Gen gen, int count, uint32_t kk, uint32_t& value, uint32_t& above, uint32_t* h,
+                             uint32_t* sh) {
+  // pass A: bits 20..10
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < count; i += blockDim.x) {
+    uint32_t key;
+    int32_t idx;
+    if (gen(i, key, idx)) atomicAdd(&h[(key >> 10) & 2047u], 1u);
+  }
+  __syncthreads();
+  int bA;
+  uint32_t aA;
+  find_bin(h, kBins, kk, bA, aA, sh);
+  // pass B: bits 9..0 among digit bA
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < count; i += blockDim.x) {
+    uint32_t key;
+    int32_t idx;
+    if (gen(i, key, idx) && ((key >> 10) & 2047u) == static_cast<uint32_t>(bA)) atomicAdd(&h[key & 1023u], 1u);
+  }
+  __syncthreads();
+  int bB;
+  uint32_t aB;
+  find_bin(h, 1024, kk - aA, bB, aB, sh);
+  value = (static_cast<uint32_t>(bA) << 10) | static_cast<uint32_t>(bB);
+  above = aA + aB;
+}
+
+// The m-th smallest position (1-based) among elements with key == T.
+template <typename Gen>
+__device__ int32_t select_cut(Gen gen, int count, uint32_t T, uint32_t m, uint32_t* h, uint32_t* sh) {
+  // positions < 2^30: three 10-bit digits, smallest first = largest of (2^30-1-pos)
+  uint32_t prefix = 0, got = 0;
+  for (int level = 0; level < 3; ++level) {
+    const int shift = 20 - 10 * level;
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < count; i += blockDim.x) {
+      uint32_t key;
+      int32_t idx;
+      if (gen(i, key, idx) && key == T) {
+        const uint32_t v = 0x3FFFFFFFu - static_cast<uint32_t>(idx);
+        if (level == 0 || (v >> (shift + 10)) == prefix) atomicAdd(&h[(v >> shift) & 1023u], 1u);
+      }
+    }
+    __syncthreads();
+    int b;
+    uint32_t a;
+    find_bin(h, 1024, m - got, b, a, sh);
+    prefix = (prefix << 10) | static_cast<uint32_t>(b);
+    got += a;
+  }
+  return static_cast<int32_t>(0x3FFFFFFFu - prefix);
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParams p) {
+  __shared__ uint32_t h[kBins];
+  __shared__ uint32_t sh[48];
+  __shared__ uint32_t lcount, lbase;
+  __shared__ uint2 lc[4096];       // this chunk's candidates (key, position)
+  const int t = blockIdx.y;
+  int c0, c1, n;
+  if (!row_range(p, t, c0, c1, n) || n <= p.k) return;
+  const uint32_t b1 = p.thr[4 * t + 0];
+  const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
+  if (threadIdx.x == 0) lcount = 0;
+  __syncthreads();
+  uint32_t u[kPerThread];
+  const int s0 = c0 + threadIdx.x * kPerThread;
+  load16(row, s0, c1, u);
+  uint32_t gt = 0;
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    if (s0 + i >= c1) continue;
+    const uint32_t d = u[i] >> 21;
+    gt += d > b1;
+    if (d == b1) {
+      const uint32_t slot = atomicAdd(&lcount, 1u);
+      lc[slot] = make_uint2(u[i], static_cast<uint32_t>(s0 + i));
     }
   }
-  __syncthreads();
-  uint32_t* gh = (LEVEL == 1 ? p.hist1 : LEVEL == 2 ? p.hist2 : p.hist3) + static_cast<int64_t>(t) * nb;
-  for (int i = threadIdx.x; i < nb; i += kTopkThreads)
-    if (h[i]) atomicAdd(gh + i, h[i]);
-}
-
-// Per chunk: how many keys are above the threshold and how many equal it.
-__global__ void __launch_bounds__(kTopkThreads) topk_count_kernel(TopkParams p) {
-  __shared__ uint32_t sh[16];
-  __shared__ uint32_t red[2];
-  const int t = blockIdx.y;
-  int c0, c1, n;
-  if (!chunk_range(p, t, c0, c1, n) || n <= p.k) return;
-  const Threshold th = compute_threshold(p, t, 3, sh);
-  if (threadIdx.x == 0) { red[0] = 0; red[1] = 0; }
-  __syncthreads();
-  const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
-  uint32_t gt = 0, eq = 0;
-  for (int s = c0 + threadIdx.x; s < c1; s += kTopkThreads) {
-    const uint32_t u = score_key(__ldg(row + s));
-    gt += u > th.key;
-    eq += u == th.key;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    eq += __shfl_xor_sync(0xffffffffu, eq, o);
-  }
-  if ((threadIdx.x & 31) == 0) {
-    atomicAdd(&red[0], gt);
-    atomicAdd(&red[1], eq);
-  }
-  __syncthreads();
+  uint32_t total;
+  block_excl_scan(gt, sh, total);
   if (threadIdx.x == 0) {
-    uint32_t* c = p.counts + (static_cast<int64_t>(t) * p.nchunks + blockIdx.x) * 2;
-    c[0] = red[0];
-    c[1] = red[1];
+    p.gt[static_cast<int64_t>(t) * p.nchunks + blockIdx.x] = total;
+    lbase = atomicAdd(p.cand_count + t, lcount);
+  }
+  __syncthreads();
+  uint2* cand = p.cands + static_cast<int64_t>(t) * p.cap;
+  for (uint32_t i = threadIdx.x; i < lcount; i += kTopkThreads)
+    if (lbase + i < static_cast<uint32_t>(p.cap)) cand[lbase + i] = lc[i];
+  const int nch = static_cast<int>(cdiv(n, p.chunk));
+  if (!last_of_row(p.done + 2 * t + 1, nch, sh)) return;
+
+  // ---- last CTA of the row: exact threshold and position cut
+  const uint32_t r = static_cast<uint32_t>(p.k) - p.thr[4 * t + 1];   // to take from digit b1
+  const uint32_t count = __ldcg(p.cand_count + t);
+  uint32_t Tlow, aboveT;
+  int32_t cut;
+  uint32_t* taken = p.taken + static_cast<int64_t>(t) * p.nchunks;
+  if (count <= static_cast<uint32_t>(p.cap)) {
+    // the whole candidate list fits this CTA's staging buffer (cap == 4096)
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < count; i += kTopkThreads) lc[i] = __ldcg(cand + i);
+    __syncthreads();
+    auto gen = [&](int i, uint32_t& key, int32_t& idx) {
+      const uint2 c = lc[i];
+      key = c.x & 0x1FFFFFu;
+      idx = static_cast<int32_t>(c.y);
+      return true;
+    };
+    select_low21(gen, static_cast<int>(count), r, Tlow, aboveT, h, sh);
+    cut = select_cut(gen, static_cast<int>(count), Tlow, r - aboveT, h, sh);
+    for (uint32_t i = threadIdx.x; i < count; i += kTopkThreads) {
+      const uint2 c = lc[i];
+      const uint32_t lo = c.x & 0x1FFFFFu;
+      if (lo > Tlow || (lo == Tlow && static_cast<int32_t>(c.y) <= cut))
+        atomicAdd(taken + c.y / static_cast<uint32_t>(p.chunk), 1u);
+    }
+  } else {
+    // heavy ties: redo the resolution over the whole row in this CTA
+    auto gen = [&](int i, uint32_t& key, int32_t& idx) {
+      const uint32_t k = score_key(__ldcg(row + i));
+      key = k & 0x1FFFFFu;
+      idx = i;
+      return (k >> 21) == b1;
+    };
+    select_low21(gen, n, r, Tlow, aboveT, h, sh);
+    cut = select_cut(gen, n, Tlow, r - aboveT, h, sh);
+    for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+      uint32_t key;
+      int32_t idx;
+      if (gen(i, key, idx) && (key > Tlow || (key == Tlow && idx <= cut)))
+        atomicAdd(taken + i / p.chunk, 1u);
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.thr[4 * t + 2] = (b1 << 21) | Tlow;
+    p.thr[4 * t + 3] = static_cast<uint32_t>(cut);
   }
 }
 
-// Ordered compaction: chunk c writes its selected positions after those of chunks < c.
+// ------------------------------------------------------------------- pass 3
+
 __global__ void __launch_bounds__(kTopkThreads) topk_emit_kernel(TopkParams p) {
-  __shared__ uint32_t sh[16];
-  __shared__ uint32_t wsel[kTopkThreads / 32], weq[kTopkThreads / 32];
-  __shared__ uint32_t base_sel, base_eq;
+  __shared__ uint32_t sh[48];
+  __shared__ uint32_t base_sh;
   const int t = blockIdx.y;
   int req, pos;
   load_token(p.b, t, p.status, req, pos);
@@ -198,74 +343,52 @@ __global__ void __launch_bounds__(kTopkThreads) topk_emit_kernel(TopkParams p) {
     return;
   }
   if (c0 >= n) return;
-  const Threshold th = compute_threshold(p, t, 3, sh);
-  const uint32_t r = static_cast<uint32_t>(p.k) - th.above;   // keys equal to T to take
-  if (threadIdx.x == 0) {
-    // positions selected by earlier chunks, and keys == T they hold
-    const uint32_t* cnt = p.counts + static_cast<int64_t>(t) * p.nchunks * 2;
-    uint32_t sel = 0, eqb = 0;
-    for (int c = 0; c < static_cast<int>(blockIdx.x); ++c) {
-      const uint32_t g = __ldcg(cnt + 2 * c), e = __ldcg(cnt + 2 * c + 1);
-      const uint32_t take = eqb >= r ? 0u : (r - eqb < e ? r - eqb : e);
-      sel += g + take;
-      eqb += e;
-    }
-    base_sel = sel;
-    base_eq = eqb;
+  const uint32_t T = __ldcg(p.thr + 4 * t + 2);
+  const int32_t cut = static_cast<int32_t>(__ldcg(p.thr + 4 * t + 3));
+  // positions selected by earlier chunks
+  {
+    uint32_t part = 0;
+    const uint32_t* gt = p.gt + static_cast<int64_t>(t) * p.nchunks;
+    const uint32_t* tk = p.taken + static_cast<int64_t>(t) * p.nchunks;
+    for (int c = threadIdx.x; c < static_cast<int>(blockIdx.x); c += kTopkThreads) part += __ldcg(gt + c) + __ldcg(tk + c);
+    uint32_t total;
+    block_excl_scan(part, sh, total);
+    if (threadIdx.x == 0) base_sh = total;
+    __syncthreads();
   }
-  __syncthreads();
-  uint32_t run_sel = base_sel, run_eq = base_eq;
   const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int s0 = c0; s0 < c1; s0 += kTopkThreads) {
-    const int s = s0 + threadIdx.x;
-    uint32_t u = 0;
-    const bool in = s < c1;
-    if (in) u = score_key(__ldg(row + s));
-    const bool is_gt = in && u > th.key;
-    const bool is_eq = in && u == th.key;
-    // rank of this element among keys == T (in position order)
-    const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
-    if (lane == 0) weq[warp] = __popc(beq);
-    __syncthreads();
-    uint32_t eq_before = run_eq;
-    uint32_t eq_total = 0;
-    for (int w = 0; w < kTopkThreads / 32; ++w) {
-      if (w < warp) eq_before += weq[w];
-      eq_total += weq[w];
+  uint32_t u[kPerThread];
+  const int s0 = c0 + threadIdx.x * kPerThread;
+  load16(row, s0, c1, u);
+  uint32_t mine = 0, flags = 0;
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    const int s = s0 + i;
+    const bool take = s < c1 && (u[i] > T || (u[i] == T && s <= cut));
+    flags |= static_cast<uint32_t>(take) << i;
+    mine += take;
+  }
+  uint32_t total;
+  uint32_t o = base_sh + block_excl_scan(mine, sh, total);
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    if (!((flags >> i) & 1u)) continue;
+    const int s = s0 + i;
+    if (o < static_cast<uint32_t>(p.k)) {
+      out[o] = s;
+      if (phys) phys[o] = (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask);
     }
-    eq_before += __popc(beq & ((1u << lane) - 1u));
-    const bool take = is_gt || (is_eq && eq_before < r);
-    const uint32_t bsel = __ballot_sync(0xffffffffu, take);
-    if (lane == 0) wsel[warp] = __popc(bsel);
-    __syncthreads();
-    uint32_t pos_out = run_sel;
-    uint32_t sel_total = 0;
-    for (int w = 0; w < kTopkThreads / 32; ++w) {
-      if (w < warp) pos_out += wsel[w];
-      sel_total += wsel[w];
-    }
-    pos_out += __popc(bsel & ((1u << lane) - 1u));
-    if (take && pos_out < static_cast<uint32_t>(p.k)) {
-      out[pos_out] = s;
-      if (phys) phys[pos_out] = (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask);
-    }
-    run_sel += sel_total;
-    run_eq += eq_total;
-    __syncthreads();
+    ++o;
   }
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st) {
-  dim3 grid(p.nchunks, p.b.T);
   if (p.b.T == 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(p.hist1, 0,
-                                  static_cast<size_t>(p.b.T) * (kBins1 + kBins2 + kBins3) * sizeof(uint32_t), st);
+  const dim3 grid(p.nchunks, p.b.T);
+  cudaError_t e = cudaMemsetAsync(p.zero_begin, 0, p.zero_bytes, st);
   if (e != cudaSuccess) return e;
-  topk_hist_kernel<1><<<grid, kTopkThreads, 0, st>>>(p);
-  topk_hist_kernel<2><<<grid, kTopkThreads, 0, st>>>(p);
-  topk_hist_kernel<3><<<grid, kTopkThreads, 0, st>>>(p);
-  topk_count_kernel<<<grid, kTopkThreads, 0, st>>>(p);
+  topk_hist_kernel<<<grid, kTopkThreads, 0, st>>>(p);
+  topk_candidates_kernel<<<grid, kTopkThreads, 0, st>>>(p);
   topk_emit_kernel<<<grid, kTopkThreads, 0, st>>>(p);
   return cudaGetLastError();
 }

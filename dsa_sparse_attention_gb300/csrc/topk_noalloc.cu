@@ -25,7 +25,6 @@
 namespace {
 
 constexpr size_t kNoAllocBytes = DSA_NOALLOC_SCRATCH_BYTES;
-constexpr int kChunk = 4096;      // scores per CTA, as in dsa_topk
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocBytes];
@@ -45,8 +44,6 @@ void* scratch_address() {
   }
   return g_scratch_ptr[dev];
 }
-
-size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
@@ -72,12 +69,10 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_kv_layout* layout, const dsa_ba
   if (!batch->q_req || !batch->q_pos || !scores || !idx || (reinterpret_cast<uintptr_t>(scores) & 15))
     return DSA_ERR_INVALID_ARG;
 
-  // scratch: status word, three histogram levels per query, per-chunk counts
-  const int nchunks = static_cast<int>((batch->max_ctx_len + kChunk - 1) / kChunk);
-  const size_t off_hist = 256;
-  const size_t off_counts = up256(off_hist + size_t(T) * (2048 + 2048 + 1024) * 4);
-  const size_t need = up256(off_counts + size_t(T) * nchunks * 2 * 4);
-  if (need > kNoAllocBytes) return DSA_ERR_WORKSPACE;   // batch too large for the fixed scratch
+  // scratch: the status word, then the top-k histograms, tickets, counts and candidates
+  const int nchunks = static_cast<int>((batch->max_ctx_len + kTopkChunk - 1) / kTopkChunk);
+  const TopkScratch L = topk_scratch_layout(T, nchunks);
+  if (256 + L.total > kNoAllocBytes) return DSA_ERR_WORKSPACE;   // batch too large for the fixed scratch
 
   uint8_t* base = static_cast<uint8_t*>(scratch_address());
   if (!base) return DSA_ERR_CUDA;
@@ -94,12 +89,7 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_kv_layout* layout, const dsa_ba
   p.scores = scores;
   p.ld = ld_scores;
   p.k = topk;
-  p.chunk = kChunk;
-  p.hist1 = reinterpret_cast<uint32_t*>(base + off_hist);
-  p.hist2 = p.hist1 + size_t(T) * 2048;
-  p.hist3 = p.hist2 + size_t(T) * 2048;
-  p.counts = reinterpret_cast<uint32_t*>(base + off_counts);
-  p.nchunks = nchunks;
+  topk_bind_scratch(p, base + 256, L, nchunks);
   p.idx = idx;
   p.phys = phys_slots;
   p.log2_bs = log2_bs;

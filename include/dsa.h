@@ -209,11 +209,12 @@ dsa_status dsa_layer_step(const dsa_kv_layout *layout, const dsa_batch *batch,
  * The pages describe no such call; it exists only for those callers.
  *
  * Same arguments, results and guarantees as dsa_topk, minus the workspace: the
- * scratch (256 B + T x 20 KiB of histograms + T x ceil(max_ctx_len / 4096) x 8 B
- * of counts) lives in a fixed DSA_NOALLOC_SCRATCH_BYTES array of device memory
- * inside the library, which every GPU that loads the library holds until the
- * process exits.  Batches that need more return DSA_ERR_WORKSPACE (for example
- * T <= 128 fits at a 1M-token context).  The call allocates nothing.
+ * scratch (about T x (40 KiB + 8 B x ceil(max_ctx_len / 4096)) for histograms,
+ * candidate lists and per-chunk counts) lives in a fixed DSA_NOALLOC_SCRATCH_BYTES
+ * array of device memory inside the library, which every GPU that loads the
+ * library holds until the process exits.  Batches that need more return
+ * DSA_ERR_WORKSPACE (T <= 96 query tokens fit at any context up to 1M tokens).
+ * The call allocates nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress with that device current); make that first call
  *    before any stream capture.
