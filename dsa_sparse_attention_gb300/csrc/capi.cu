@@ -53,7 +53,6 @@ dsa_status check_layout(const dsa_kv_layout* l, bool need_pool = true) {
   if (!is_pow2(l->block_size) || l->block_size < 16 || l->block_size > 256) return DSA_ERR_UNSUPPORTED;
   if (l->idx_fmt != DSA_IDX_FP8 && l->idx_fmt != DSA_IDX_MXFP4) return DSA_ERR_INVALID_ARG;
   if (l->lat_fmt != DSA_LAT_FP8 && l->lat_fmt != DSA_LAT_NVFP4) return DSA_ERR_INVALID_ARG;
-  if (l->idx_fmt != DSA_IDX_FP8 || l->lat_fmt != DSA_LAT_FP8) return DSA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(l->pool) & 15) || (l->row_stride_bytes & 15) || (l->idx_page_offset & 15) ||
       (l->lat_page_offset & 15))
     return DSA_ERR_INVALID_ARG;
@@ -128,18 +127,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over the index-key value bytes of every page: {128 B, block slots, rows}.
+// 3-D map over the index-key value bytes of every page: {value bytes per key,
+// block slots, rows}.  FP8 keys (128 B) land 128-byte swizzled, ready for the
+// MMA; packed MXFP4 keys (64 B) land row-major for the converter warps.
 bool make_key_map(CUtensorMap* m, const dsa_kv_layout* l) {
   auto enc = encode_fn();
   if (!enc) return false;
+  const bool mx = l->idx_fmt == DSA_IDX_MXFP4;
+  const cuuint64_t vb = mx ? 64 : 128;
   const int box_rows = l->block_size < kKeyTile ? l->block_size : kKeyTile;
-  cuuint64_t dims[3] = {128, cuuint64_t(l->block_size), cuuint64_t(l->num_rows)};
-  cuuint64_t strides[2] = {128, cuuint64_t(l->row_stride_bytes)};
-  cuuint32_t box[3] = {128, cuuint32_t(box_rows), 1};
+  cuuint64_t dims[3] = {vb, cuuint64_t(l->block_size), cuuint64_t(l->num_rows)};
+  cuuint64_t strides[2] = {vb, cuuint64_t(l->row_stride_bytes)};
+  cuuint32_t box[3] = {cuuint32_t(vb), cuuint32_t(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(l->pool)) + l->idx_page_offset;
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             mx ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -219,7 +222,7 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   if (T == 0) return DSA_OK;
   CUtensorMap kmap, qmap;
   if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return DSA_ERR_CUDA;
-  const int G = (T == b->num_reqs) ? 1 : 8;
+  const int G = indexer_group_size(l->idx_fmt, T == b->num_reqs);
   uint32_t* status = at<uint32_t>(ws, wl.status);
   cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, wl.plan_hdr), 0, wl.groups + size_t(T) * sizeof(ScoreGroup) - wl.plan_hdr, st);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
@@ -235,7 +238,7 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   p.hdr = at<PlanHeader>(ws, wl.plan_hdr);
   p.groups = at<ScoreGroup>(ws, wl.groups);
   p.status = status;
-  return cuda_status(launch_indexer_fp8(kmap, qmap, p, G, num_sms(), st));
+  return cuda_status(launch_indexer(kmap, qmap, p, G, num_sms(), st));
 }
 
 dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* scores, int64_t ld, int topk,

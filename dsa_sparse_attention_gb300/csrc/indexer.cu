@@ -121,27 +121,48 @@ __global__ void __launch_bounds__(1024) plan_groups_kernel(PlanParams p) {
 // ------------------------------------------------------------------- scorer
 
 
-template <int G>
+// Shared-memory / TMEM plan of the scorer.  IDXF = DSA_IDX_FP8 (0) or
+// DSA_IDX_MXFP4 (1); G = max tokens per group (N = 32 G).  MXFP4 keys arrive
+// packed (64 B/key) and converter warps expand them to e4m3 (exact); each
+// 32-dim scale block gets its own accumulator so the E8M0 scales are applied
+// exactly in the epilogue.
+template <int IDXF, int G>
 struct ScorerCfg {
-  static constexpr int STAGES = (G == 1) ? 8 : 6;
-  static constexpr int ACC_COLS = 32 * G;
-  static constexpr int NACC = (G == 1) ? 4 : 2;            // TMEM accumulators (even: set = tile parity)
-  static constexpr int TMEM_COLS = NACC * ACC_COLS;        // 128 or 512 (powers of two)
-  static constexpr int KEY_BYTES = kKeyTile * kIdxDim;     // 16 KB
+  static constexpr bool MX = IDXF == 1;
+  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 8 : 6);
+  static constexpr int NBLK = MX ? 4 : 1;                   // accumulators per tile (scale blocks)
+  static constexpr int ACC_COLS = 32 * G * NBLK;
+  static constexpr int NACC = (G == 1 && !MX) ? 4 : 2;      // TMEM accumulators (even: set = tile parity)
+  static constexpr int TMEM_COLS = NACC * ACC_COLS;         // 128 / 256 / 512 (powers of two)
+  static constexpr int KEY_BYTES = kKeyTile * kIdxDim;      // 16 KB of e4m3 (MMA operand)
+  static constexpr int PACK_BYTES = MX ? kKeyTile * 64 : 0; // 8 KB of packed e2m1 per stage
   static constexpr int SCALE_BYTES = kKeyTile * 4;
   static constexpr int Q_BYTES = G * kIdxHeads * kIdxDim;
   static constexpr int W_BYTES = G * kIdxHeads * 4;
   static constexpr int OFF_Q = STAGES * KEY_BYTES;
-  static constexpr int OFF_SCALES = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_PACK = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_SCALES = OFF_PACK + STAGES * PACK_BYTES;
   static constexpr int OFF_W = OFF_SCALES + STAGES * SCALE_BYTES;   // 2 x [G][32] fp32
   static constexpr int OFF_POS = OFF_W + 2 * W_BYTES;                // 2 x [G] int
   static constexpr int OFF_BARS = OFF_POS + 2 * G * 4 + 64;
-  static constexpr int N_BARS = 2 * STAGES + 2 * NACC + 5;
+  static constexpr int N_BARS = 3 * STAGES + 2 * NACC + 5;
   static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
-  static constexpr int THREADS = 320;
+  static constexpr int CONV_WARPS = MX ? 8 : 0;
+  static constexpr int THREADS = 320 + 32 * CONV_WARPS;
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
+  static_assert(SMEM_BYTES <= 232448, "smem");
 };
+
+// 4 e2m1 codes (low 16 bits of w, element 0 in the lowest nibble) -> 4 e4m3 bytes.
+// Magnitudes {0,.5,1,1.5,2,3,4,6} map to e4m3 codes {00,30,38,3C,40,44,48,4C}
+// through a byte permute; the sign bit moves from nibble bit 3 to byte bit 7.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t w) {
+  uint32_t mag;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(mag) : "r"(0x3C383000u), "r"(0x4C484440u), "r"(w & 0x7777u));
+  const uint32_t sg = ((w & 0x8u) << 4) | ((w & 0x80u) << 8) | ((w & 0x800u) << 12) | ((w & 0x8000u) << 16);
+  return mag | sg;
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -181,11 +202,11 @@ struct GroupCursor {
   }
 };
 
-template <int G>
-__global__ void __launch_bounds__(320, 1)
-    indexer_fp8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                       IndexerParams p) {
-  using C = ScorerCfg<G>;
+template <int IDXF, int G>
+__global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                   IndexerParams p) {
+  using C = ScorerCfg<IDXF, G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
@@ -196,6 +217,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* qfull = tempty + C::NACC;
   uint64_t* qempty = qfull + 2;
   uint64_t* drain = qempty + 2;
+  uint64_t* cvt = drain + 1;                  // [STAGES] MXFP4: converted keys ready
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
   float* wsm = reinterpret_cast<float*>(smem + C::OFF_W);
@@ -221,6 +243,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&qempty[i], 1 + 8);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&cvt[s], C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
     *abortf = 0;
     fence_mbar_init();
   }
@@ -304,20 +327,22 @@ __global__ void __launch_bounds__(320, 1)
           if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
           if (lane == 0) {
             const int64_t key0 = static_cast<int64_t>(i - grp.tile_begin) * kKeyTile;
+            constexpr int VB = C::MX ? kIdxDim / 2 : kIdxDim;   // value bytes per key in the page
             uint32_t bytes = 0;
 #pragma unroll
             for (int bx = 0; bx < kKeyTile / 16; ++bx)
-              if (rows[bx] >= 0) bytes += static_cast<uint32_t>(box) * (kIdxDim + 4);
+              if (rows[bx] >= 0) bytes += static_cast<uint32_t>(box) * (VB + 4);
             mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
             for (int bx = 0; bx < kKeyTile / 16; ++bx) {
               if (rows[bx] < 0) continue;
               const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
               const int slot0 = static_cast<int>(k0 & (bs - 1));
-              tma_load_3d(smem + s * C::KEY_BYTES + bx * box * kIdxDim, &kmap, &full[s], 0, slot0, rows[bx]);
+              uint8_t* vdst = C::MX ? smem + C::OFF_PACK + s * C::PACK_BYTES + bx * box * VB
+                                    : smem + s * C::KEY_BYTES + bx * box * kIdxDim;
+              tma_load_3d(vdst, &kmap, &full[s], 0, slot0, rows[bx]);
               const uint8_t* src = p.pool.pool + static_cast<int64_t>(rows[bx]) * p.pool.row_stride +
-                                   p.pool.idx_off + static_cast<int64_t>(bs) * kIdxDim +
-                                   static_cast<int64_t>(slot0) * 4;
+                                   p.pool.idx_off + static_cast<int64_t>(bs) * VB + static_cast<int64_t>(slot0) * 4;
               bulk_load(smem + C::OFF_SCALES + s * C::SCALE_BYTES + bx * box * 4, src, box * 4, &full[s]);
             }
           }
@@ -344,16 +369,20 @@ __global__ void __launch_bounds__(320, 1)
           const int it = i - tile_lo;
           const int s = it % C::STAGES;
           const int acc = it % C::NACC;
-          if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
+          if (!(ok = mbar_wait(C::MX ? &cvt[s] : &full[s], (it / C::STAGES) & 1, ab))) break;
           if (it >= C::NACC && !(ok = mbar_wait(&tempty[acc], ((it / C::NACC) - 1) & 1, ab))) break;
           tc_fence_after();
           const uint32_t d = tmem + acc * C::ACC_COLS;
           const uint32_t a0 = smem_u32(smem + s * C::KEY_BYTES);
           const uint32_t b0 = smem_u32(smem + C::OFF_Q + (cur.count & 1) * C::Q_BYTES);
 #pragma unroll
-          for (int k = 0; k < kIdxDim / 32; ++k)
-            mma_f8f6f4(d, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
-                       k > 0 ? 1u : 0u);
+          for (int k = 0; k < kIdxDim / 32; ++k) {
+            // FP8: one accumulator over K = 128.  MXFP4: block k (dims 32k..32k+31) alone
+            // into accumulator k, scaled by its E8M0 exponent in the epilogue.
+            const uint32_t dk = C::MX ? d + k * (32 * G) : d;
+            mma_f8f6f4(dk, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
+                       C::MX ? 0u : (k > 0 ? 1u : 0u));
+          }
           tc_commit(&empty[s]);
           tc_commit(&tfull[acc]);
           if (i + 1 == cur.next_begin || i + 1 == tile_hi) tc_commit(&qempty[cur.count & 1]);
@@ -362,6 +391,31 @@ __global__ void __launch_bounds__(320, 1)
           tc_commit(drain);
           drain_wait(drain, 0);
         }
+      }
+    } else if (C::MX && warp >= 10) {
+      // ------------------------------------------------- converters (MXFP4)
+      // Thread pair per key: packed e2m1 (64 B, row-major) -> e4m3 K-major,
+      // 128-byte swizzle, as the TMA would have laid out FP8 keys.
+      const int ct = threadIdx.x - 320;       // 0..255
+      const int row = ct >> 1, hf = ct & 1;
+      bool ok = true;
+      for (int i = tile_lo; i < tile_hi && ok; ++i) {
+        const int it = i - tile_lo;
+        const int s = it % C::STAGES;
+        if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
+        const uint8_t* src = smem + C::OFF_PACK + s * C::PACK_BYTES + row * 64 + hf * 32;
+        uint8_t* dst = smem + s * C::KEY_BYTES + (row >> 3) * 1024;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(src + 8 * c4);   // 16 codes = dims 16c .. 16c+15
+          const int c = hf * 4 + c4;
+          const uint4 o = make_uint4(e2m1x4_to_e4m3x4(w.x), e2m1x4_to_e4m3x4(w.x >> 16), e2m1x4_to_e4m3x4(w.y),
+                                     e2m1x4_to_e4m3x4(w.y >> 16));
+          *reinterpret_cast<uint4*>(dst + sw128_off(row & 7, c)) = o;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cvt[s]);
       }
     } else {
       // ------------------------------------------------------------ epilogue
@@ -390,11 +444,37 @@ __global__ void __launch_bounds__(320, 1)
         const int qb = cur.count & 1;
         const int kloc = quarter * 32 + lane;
         const int key = (i - grp.tile_begin) * kKeyTile + kloc;
-        const float scale = reinterpret_cast<const float*>(smem + C::OFF_SCALES + s * C::SCALE_BYTES)[kloc];
+        float scale = 1.f;
+        float bsc[4] = {1.f, 1.f, 1.f, 1.f};
+        if (C::MX) {
+          const uint32_t e8 = reinterpret_cast<const uint32_t*>(smem + C::OFF_SCALES + s * C::SCALE_BYTES)[kloc];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t e = (e8 >> (8 * b)) & 0xFFu;   // 2^(e-127); e = 0 is 2^-127, e = 255 NaN
+            bsc[b] = __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : e << 23));
+          }
+        } else {
+          scale = reinterpret_cast<const float*>(smem + C::OFF_SCALES + s * C::SCALE_BYTES)[kloc];
+        }
         for (int j = 0; j < grp.n; ++j) {
           uint32_t r[32];
           DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + j * kIdxHeads + (static_cast<uint32_t>(quarter * 32) << 16), r);
           tmem_wait_ld();
+          if (C::MX) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bsc[0]);
+#pragma unroll
+            for (int b = 1; b < 4; ++b) {
+              uint32_t rb[32];
+              DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + b * (32 * G) + j * kIdxHeads +
+                                (static_cast<uint32_t>(quarter * 32) << 16),
+                            rb);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                r[i] = __float_as_uint(fmaf(__uint_as_float(rb[i]), bsc[b], __uint_as_float(r[i])));
+            }
+          }
           const float4* wv = reinterpret_cast<const float4*>(wsm + (qb * G + j) * kIdxHeads);
           float sum = 0.f;
           if (scale >= 0.f) {
@@ -444,25 +524,34 @@ cudaError_t launch_plan_groups(const BatchView& b, int G, ScoreGroup* groups, Pl
   return cudaGetLastError();
 }
 
-template <int G>
+template <int IDXF, int G>
 static cudaError_t launch_scorer_g(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p,
                                    int grid, cudaStream_t st) {
-  using C = ScorerCfg<G>;
+  using C = ScorerCfg<IDXF, G>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(indexer_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(indexer_kernel<IDXF, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  indexer_fp8_kernel<G><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(kmap, qmap, p);
+  indexer_kernel<IDXF, G><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(kmap, qmap, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_indexer_fp8(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,
-                               int grid, cudaStream_t st) {
-  if (G == 1) return launch_scorer_g<1>(kmap, qmap, p, grid, st);
-  return launch_scorer_g<8>(kmap, qmap, p, grid, st);
+int indexer_group_size(int idx_fmt, bool one_token_per_request) {
+  if (one_token_per_request) return 1;
+  return idx_fmt == 1 ? 2 : 8;
+}
+
+cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,
+                           int grid, cudaStream_t st) {
+  if (p.pool.idx_fmt == 1) {
+    if (G == 1) return launch_scorer_g<1, 1>(kmap, qmap, p, grid, st);
+    return launch_scorer_g<1, 2>(kmap, qmap, p, grid, st);
+  }
+  if (G == 1) return launch_scorer_g<0, 1>(kmap, qmap, p, grid, st);
+  return launch_scorer_g<0, 8>(kmap, qmap, p, grid, st);
 }
 
 }  // namespace dsa

@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "params.cuh"
@@ -33,7 +34,7 @@ namespace dsa {
 
 
 namespace mla {
-constexpr int RAW_STRIDE = 592;                   // 576 + 16: conflict-free row reads
+constexpr int RAW_STRIDE = 592;                   // FP8 rows 576 + 16 (NVFP4 rows 352 + 16): conflict-free reads
 constexpr int OFF_RAW = 0;
 constexpr int RAW_BYTES = kSelTile * RAW_STRIDE;  // 75,776
 constexpr int QSLOTS = 3;
@@ -54,7 +55,9 @@ constexpr int OFF_BARS = OFF_ROWOK + 128;
 constexpr int N_BARS = 24;
 constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
-constexpr int THREADS = 320;                      // producer, MMA, 4 converter warps, 4 softmax warps
+constexpr int THREADS = 448;                      // producer, MMA, 8 converter warps, 4 softmax warps
+constexpr int CONV_WARPS = 8;
+constexpr int SOFT_WARP0 = 2 + CONV_WARPS;        // first softmax warp
 constexpr int TMEM_COLS = 512;
 constexpr int S_COL = 0;
 constexpr int O_COL = 128;
@@ -97,6 +100,32 @@ __device__ __forceinline__ void e4m3x16_to_f16(const uint4 in, uint32_t (&o)[8])
   }
 }
 
+// 16 NVFP4 values (8 packed bytes, element 2i in the low nibble of byte i) with
+// their e4m3 block scale -> 16 fp16 values.  e2m1 x e4m3 has at most 6
+// significant bits and lies in [2^-10, 2688]: exact in fp16 (and in bf16).
+__device__ __forceinline__ void nvfp4x16_to_f16(const uint2 in, uint32_t scale_code, uint32_t (&o)[8]) {
+  const __half sc = __half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(scale_code), __NV_E4M3));
+  const __half2 sc2 = __half2(sc, sc);
+  const uint32_t w[2] = {in.x, in.y};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>((w[i >> 2] >> (8 * (i & 3))) & 0xFFu),
+                                                     __NV_E2M1);
+    const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&r), sc2);
+    o[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
+__device__ __forceinline__ void nvfp4x16_to_bf16(const uint2 in, uint32_t scale_code, uint32_t (&o)[8]) {
+  nvfp4x16_to_f16(in, scale_code, o);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&o[i]));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    o[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+}
+
 // Butterfly "transpose" reductions over a warp: on entry every lane holds 32
 // values (one per head j); on exit lane l holds the reduction over all 32 lanes
 // of head l.  31 shuffles per 32 heads.  `v` is destroyed.
@@ -121,9 +150,13 @@ __device__ __forceinline__ void sts128(uint8_t* p, const uint32_t* v) {
   *reinterpret_cast<uint4*>(p) = make_uint4(v[0], v[1], v[2], v[3]);
 }
 
+template <int LATF>
 __global__ void __launch_bounds__(mla::THREADS, 1)
-    sparse_mla_fp8_kernel(const __grid_constant__ CUtensorMap qmap, MlaParams p) {
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap qmap, MlaParams p) {
   using namespace mla;
+  constexpr bool NV = LATF == 1;
+  constexpr int ROWB = NV ? 352 : kLatDim;             // bytes per latent record
+  constexpr int RSTR = NV ? 368 : RAW_STRIDE;          // staging stride of a raw row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024_mla(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
@@ -138,7 +171,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   uint64_t* p_full = bars + 20;
   uint64_t* o_done = bars + 21;
   uint64_t* drain = bars + 22;
-  __shared__ int n_valid_sh;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   int* rescale_sh = reinterpret_cast<int*>(smem + OFF_MISC + 16);
@@ -152,19 +184,24 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.y;
   const int split = blockIdx.x;
-  int req, pos;
-  load_token(p.b, t, p.status, req, pos);
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.topk;
-
+  // Tiles of this split that hold selected entries (valid entries come first, so
+  // a tile is used iff its first entry is valid); every thread reads the same few
+  // words, in parallel with the set-up below.
+  const int ntiles_max = static_cast<int>(cdiv(p.topk, kSelTile));
+  const int j0 = split * p.tps;
+  int j1 = j0;
+  for (int j = j0; j < min(ntiles_max, j0 + p.tps); ++j)
+    if (__ldg(idx_row + j * kSelTile) >= 0) j1 = j + 1;
   if (threadIdx.x == 0) {
     mbar_init(raw_full, 1);
-    mbar_init(raw_empty, 4);
+    mbar_init(raw_empty, CONV_WARPS);
     for (int i = 0; i < QSLOTS; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
     for (int i = 0; i < RSLOTS; ++i) {
-      mbar_init(&ring_full[i], 4);
+      mbar_init(&ring_full[i], CONV_WARPS);
       mbar_init(&ring_empty[i], 1);
     }
     mbar_init(s_full, 1);
@@ -173,17 +210,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abortf = 0;
-    n_valid_sh = 0;
     fence_mbar_init();
-  }
-  __syncthreads();
-  // number of valid (non-negative) selected entries; they come first
-  {
-    int cnt = 0;
-    for (int i = threadIdx.x; i < p.topk; i += blockDim.x) cnt += idx_row[i] >= 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0 && cnt) atomicAdd(&n_valid_sh, cnt);
   }
   if (warp == 1) tmem_alloc(tslot, TMEM_COLS);
   tc_fence_before();
@@ -191,10 +218,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const Abort ab{abortf, p.status};
-  const int n_valid = n_valid_sh;
-  const int n_tiles = static_cast<int>(cdiv(n_valid, kSelTile));
-  const int j0 = split * p.tps;
-  const int j1 = min(n_tiles, j0 + p.tps);
   const int64_t ts = static_cast<int64_t>(t) * p.nsplit + split;
 
   if (j0 >= j1) {
@@ -203,6 +226,13 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   } else if (warp == 0) {
     // --------------------------------------------------------------- producer
     if (lane == 0) prefetch_tensormap(&qmap);
+    int req = __ldg(p.b.q_req + t);
+    const int pos = __ldg(p.b.q_pos + t);
+    if (req < 0 || req >= p.b.B) {
+      if (lane == 0) atomicOr(p.status, DEV_BAD_BATCH);
+      req = req < 0 ? 0 : p.b.B - 1;
+    }
+    const int64_t s_lim = static_cast<int64_t>(p.b.bt_stride) << p.pool.log2_bs;   // positions the table covers
     const int32_t* btrow = p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride;
     const int bsm = p.pool.bs - 1;
     int qc = 0;
@@ -218,9 +248,9 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         const int r = lane + 32 * i;
         const int e = j * kSelTile + r;
         src[i] = nullptr;
-        if (e < n_valid) {
-          const int s = idx_row[e];
-          if (s < 0 || s > pos) {
+        const int s = e < p.topk ? __ldg(idx_row + e) : -1;
+        if (s >= 0) {
+          if (s > pos || s >= s_lim) {
             atomicOr(p.status, DEV_BAD_BATCH);
           } else {
             const int row = btrow[s >> p.pool.log2_bs];
@@ -228,7 +258,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
               atomicOr(p.status, DEV_BAD_BLOCK);
             } else {
               src[i] = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.lat_off +
-                       static_cast<int64_t>(s & bsm) * kLatDim;
+                       static_cast<int64_t>(s & bsm) * ROWB;
               ++nrow;
             }
           }
@@ -239,11 +269,11 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       for (int o = 16; o > 0; o >>= 1) nrow += __shfl_xor_sync(0xffffffffu, nrow, o);
       __threadfence_block();
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(raw_full, nrow * kLatDim);
+      if (lane == 0) mbar_arrive_expect_tx(raw_full, nrow * ROWB);
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (src[i]) bulk_load(smem + OFF_RAW + (lane + 32 * i) * RAW_STRIDE, src[i], kLatDim, raw_full);
+        if (src[i]) bulk_load(smem + OFF_RAW + (lane + 32 * i) * RSTR, src[i], ROWB, raw_full);
       ++issued_tiles;
       // q in 9 chunks of 64 dims through the 4-slot ring
       for (int kc = 0; kc < kLatDim / 64 && ok; ++kc, ++qc) {
@@ -309,34 +339,41 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         drain_wait(drain, 0);
       }
     }
-  } else if (warp < 6) {
-    // ----------------------------------------------------- converters (2..5)
-    const int ct = threadIdx.x - 64;            // 0..127
+  } else if (warp < SOFT_WARP0) {
+    // ----------------------------------------------------- converters (2..9)
+    const int ct = threadIdx.x - 64;            // 0..255
     int fc = 0;
     bool ok = true;
     for (int j = j0; j < j1 && ok; ++j) {
       const int jt = j - j0;
       if (!(ok = mbar_wait(raw_full, jt & 1, ab))) break;
       const uint8_t* raw = smem + OFF_RAW;
-      // C chunks (bf16, K-major, 128-byte swizzle): thread ct converts row ct
+      // C chunks (bf16, K-major, 128-byte swizzle): threads 2r, 2r+1 convert row r
       {
-        const bool valid = rowok[ct] != 0;
+        const int row = ct >> 1, hf = ct & 1;
+        const bool valid = rowok[row] != 0;
         for (int kc = 0; kc < kLatDim / 64; ++kc, ++fc) {
           const int slot = fc % RSLOTS;
           if (fc >= RSLOTS && !(ok = mbar_wait(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
-          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (ct >> 3) * 1024;
+          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (row >> 3) * 1024;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int q4 = 2 * hf + q2;          // dims 64 kc + 16 q4 .. +16
             uint32_t o[8];
             if (valid) {
-              const uint4 in = *reinterpret_cast<const uint4*>(raw + ct * RAW_STRIDE + kc * 64 + q4 * 16);
-              e4m3x16_to_bf16(in, o);
+              if (NV) {
+                const uint2 in = *reinterpret_cast<const uint2*>(raw + row * RSTR + kc * 32 + q4 * 8);
+                nvfp4x16_to_bf16(in, raw[row * RSTR + 288 + kc * 4 + q4], o);
+              } else {
+                const uint4 in = *reinterpret_cast<const uint4*>(raw + row * RSTR + kc * 64 + q4 * 16);
+                e4m3x16_to_bf16(in, o);
+              }
             } else {
 #pragma unroll
               for (int i = 0; i < 8; ++i) o[i] = 0;
             }
-            sts128(dst + sw128_off(ct & 7, 2 * q4), o);
-            sts128(dst + sw128_off(ct & 7, 2 * q4 + 1), o + 4);
+            sts128(dst + sw128_off(row & 7, 2 * q4), o);
+            sts128(dst + sw128_off(row & 7, 2 * q4 + 1), o + 4);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -344,22 +381,30 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         }
       }
       if (!ok) break;
-      // V half-blocks (fp16, MN-major): block v = dims [128v, +128), half kh = tokens [64kh, +64)
+      // V half-blocks (fp16, MN-major): block v = dims [128v, +128), half kh = tokens [64kh, +64);
+      // thread -> (token tl, 32-dim quarter dq)
       for (int v = 0; v < 4 && ok; ++v) {
         for (int kh = 0; kh < 2; ++kh, ++fc) {
           const int slot = fc % RSLOTS;
           if (fc >= RSLOTS && !(ok = mbar_wait(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
-          const int tl = ct >> 1;            // token within the half (0..63)
-          const int d2 = ct & 1;             // which 64-dim atom of the block
+          const int tl = ct >> 2;            // token within the half (0..63)
+          const int dq = ct & 3;             // 32-dim quarter of the block
           const int row = kh * 64 + tl;
           const bool rv = rowok[row] != 0;
-          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + d2 * 8192 + (tl >> 3) * 1024;
+          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (dq >> 1) * 8192 + (tl >> 3) * 1024;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int q4 = 2 * (dq & 1) + q2;  // 16-dim piece within the 64-dim atom
             uint32_t o[8];
             if (rv) {
-              const uint4 in = *reinterpret_cast<const uint4*>(raw + row * RAW_STRIDE + v * 128 + d2 * 64 + q4 * 16);
-              e4m3x16_to_f16(in, o);
+              const int d0 = v * 128 + (dq >> 1) * 64 + q4 * 16;   // first of 16 dims
+              if (NV) {
+                const uint2 in = *reinterpret_cast<const uint2*>(raw + row * RSTR + d0 / 2);
+                nvfp4x16_to_f16(in, raw[row * RSTR + 288 + d0 / 16], o);
+              } else {
+                const uint4 in = *reinterpret_cast<const uint4*>(raw + row * RSTR + d0);
+                e4m3x16_to_f16(in, o);
+              }
             } else {
 #pragma unroll
               for (int i = 0; i < 8; ++i) o[i] = 0;
@@ -377,13 +422,13 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       if (lane == 0) mbar_arrive(raw_empty);
     }
   } else {
-    // ------------------------------------------------ softmax warps (6..9)
+    // ---------------------------------------------- softmax warps (10..13)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;          // token lane within the tile
-    const int mt = threadIdx.x - 192;           // 0..127
+    const int mt = threadIdx.x - 32 * SOFT_WARP0;   // 0..127
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float m_run[3] = {-INFINITY, -INFINITY, -INFINITY};   // per head (lane + 32 i), log2 units
-    float l_run[3] = {0.f, 0.f, 0.f};                      // warp 6 only: running sums
+    float l_run[3] = {0.f, 0.f, 0.f};                      // first softmax warp only: running sums
     float alpha_r[3] = {1.f, 1.f, 1.f};
     bool ok = true;
     for (int j = j0; j < j1 && ok; ++j) {
@@ -404,7 +449,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         red[quarter * kMlaHeads + 32 * c + lane] = warp_transpose_reduce32<true>(tmp);
       }
       named_bar_sync(1, 128);
-      if (warp == 6) {
+      if (warp == SOFT_WARP0) {
         bool moved = false;
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
@@ -476,7 +521,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         mbar_arrive(p_full);
       }
       named_bar_sync(1, 128);
-      if (warp == 6) {
+      if (warp == SOFT_WARP0) {
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           const int h = lane + 32 * i;
@@ -489,48 +534,52 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     if (ok) ok = mbar_wait(o_done, (j1 - j0 - 1) & 1, ab);
     if (ok) {
       tc_fence_after();
-      if (warp == 6) {
+      if (warp == SOFT_WARP0) {
 #pragma unroll
         for (int i = 0; i < 3; ++i) l_fin[lane + 32 * i] = l_run[i];
 #pragma unroll
         for (int i = 0; i < 3; ++i) alpha_sh[lane + 32 * i] = 1.f / l_run[i];   // reused: 1 / sum
       }
       named_bar_sync(1, 128);
-      if (p.nsplit == 1) {
-        __nv_bfloat16* orow = p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim;
-        for (int v = 0; v < 4; ++v) {
-          const int dim = v * 128 + r;
+      // per 128-dim block: TMEM (thread = dim) -> smem [head][dim] -> 16-byte global stores
+      uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_RAW);   // raw tile is free now
+      const bool final_out = p.nsplit == 1;
+      uint16_t* gbase = final_out ? reinterpret_cast<uint16_t*>(p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim)
+                                  : reinterpret_cast<uint16_t*>(p.part_o + ts * kMlaHeads * kVDim);
+      for (int v = 0; v < 4; ++v) {
 #pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            uint32_t rr[32];
-            DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
-            tmem_wait_ld();
+        for (int c = 0; c < 3; ++c) {
+          uint32_t rr[32];
+          DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int h = 32 * c + i;
-              orow[h * kVDim + dim] = __float2bfloat16_rn(__uint_as_float(rr[i]) * alpha_sh[h]);
+          for (int i = 0; i < 32; ++i) {
+            const int h = 32 * c + i;
+            const float val = __uint_as_float(rr[i]) * alpha_sh[h];
+            uint16_t bits;
+            if (final_out) {
+              const __nv_bfloat16 b = __float2bfloat16_rn(val);
+              bits = *reinterpret_cast<const uint16_t*>(&b);
+            } else {
+              const __half hv = __float2half_rn(val);
+              bits = *reinterpret_cast<const uint16_t*>(&hv);
             }
+            stage[h * 128 + r] = bits;
           }
         }
+        named_bar_sync(1, 128);
+        for (int i = mt; i < kMlaHeads * 16; i += 128) {
+          const int h = i >> 4, g = i & 15;
+          *reinterpret_cast<uint4*>(gbase + h * kVDim + v * 128 + g * 8) =
+              *reinterpret_cast<const uint4*>(stage + h * 128 + g * 8);
+        }
+        named_bar_sync(1, 128);
+      }
+      if (final_out) {
         if (p.lse && mt < kMlaHeads)
           p.lse[static_cast<int64_t>(t) * kMlaHeads + mt] = (m_use[mt] + log2f(l_fin[mt])) * 0.69314718055994531f;
-      } else {
-        __half* po = p.part_o + ts * kMlaHeads * kVDim;
-        for (int v = 0; v < 4; ++v) {
-          const int dim = v * 128 + r;
-#pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            uint32_t rr[32];
-            DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int h = 32 * c + i;
-              po[h * kVDim + dim] = __float2half_rn(__uint_as_float(rr[i]) * alpha_sh[h]);
-            }
-          }
-        }
-        if (mt < kMlaHeads) p.part_ml[ts * kMlaHeads + mt] = make_float2(m_use[mt], l_fin[mt]);
+      } else if (mt < kMlaHeads) {
+        p.part_ml[ts * kMlaHeads + mt] = make_float2(m_use[mt], l_fin[mt]);
       }
     }
   }
@@ -600,16 +649,23 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(MlaParams p) {
   if (p.lse && lane == 0) p.lse[static_cast<int64_t>(t) * kMlaHeads + h] = (M + log2f(L)) * 0.69314718055994531f;
 }
 
-cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st) {
-  if (p.b.T == 0) return cudaSuccess;
+template <int LATF>
+static cudaError_t launch_mla_fmt(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
-        cudaFuncSetAttribute(sparse_mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM_BYTES);
+        cudaFuncSetAttribute(sparse_mla_kernel<LATF>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  sparse_mla_fp8_kernel<<<dim3(p.nsplit, p.b.T), mla::THREADS, mla::SMEM_BYTES, st>>>(qmap, p);
+  sparse_mla_kernel<LATF><<<dim3(p.nsplit, p.b.T), mla::THREADS, mla::SMEM_BYTES, st>>>(qmap, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st) {
+  if (p.b.T == 0) return cudaSuccess;
+  cudaError_t e = p.pool.lat_fmt == 1 ? launch_mla_fmt<1>(qmap, p, st) : launch_mla_fmt<0>(qmap, p, st);
+  if (e != cudaSuccess) return e;
   if (p.nsplit > 1) mla_combine_kernel<<<dim3(kMlaHeads / 8, p.b.T), 256, 0, st>>>(p);
   return cudaGetLastError();
 }

@@ -107,8 +107,9 @@ inline void topk_bind_scratch(TopkParams& p, uint8_t* base, const TopkScratch& L
 
 cudaError_t launch_plan_groups(const BatchView& b, int G, ScoreGroup* groups, PlanHeader* hdr, uint32_t* status,
                                cudaStream_t st);
-cudaError_t launch_indexer_fp8(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,
-                               int grid, cudaStream_t st);
+cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,
+                           int grid, cudaStream_t st);
+int indexer_group_size(int idx_fmt, bool one_token_per_request);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st);
 cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st);
 

@@ -36,8 +36,9 @@ class OracleCache:
         self._scores = {}
 
     def keys(self, b, n):
-        if b not in self._keys or self._keys[b].shape[0] < n:
-            self._keys[b] = O.gather_index_keys(self.lay, self.wl.block_table[b], int(self.wl.ctx_lens[b]))
+        # one request's keys at a time (contexts of the large workloads are big)
+        if b not in self._keys:
+            self._keys = {b: O.gather_index_keys(self.lay, self.wl.block_table[b], int(self.wl.ctx_lens[b]))}
         return self._keys[b][:n]
 
     def scores(self, t):

@@ -181,3 +181,50 @@ def test_full_cfg1_decode_b8_64k():
     wl = W.config(1)
     r = _run_all(wl, check_split=False)
     print(r)
+
+
+@pytest.mark.slow
+def test_full_cfg2_mtp_b32x6_sampled():
+    # 32 requests x 6 speculative query tokens, contexts log-uniform in [16K, 256K];
+    # oracle on every request's first and last query token.
+    wl = W.config(2)
+    toks = sorted(set(int(np.nonzero(wl.q_req == b)[0][i]) for b in range(wl.num_reqs) for i in (0, -1)))
+    r = _run_all(wl, tokens=toks, check_split=False)
+    print(r)
+
+
+@pytest.mark.slow
+def test_full_cfg4_prefill_8192_on_131072_sampled():
+    # 8192 new queries on a 131,072-token cache; oracle on 64 seeded positions
+    # including the first two and the last.
+    wl = W.config(4)
+    rng = np.random.default_rng(4)
+    toks = sorted(set([0, 1, 8191] + list(rng.choice(8192, 61, replace=False))))
+    r = _run_all(wl, tokens=toks, check_split=False)
+    print(r)
+
+
+# ------------------------------------------------- MXFP4 keys / NVFP4 latents
+
+def test_mxfp4_keys_fp8_latents():
+    wl = W.make_workload([5000, 700, 2049], 1, seed=41, idx_fmt=W.IDX_MXFP4, permute=True, pool_rows=200)
+    _run_all(wl)
+
+
+def test_fp8_keys_nvfp4_latents():
+    wl = W.make_workload([5000, 700, 2049], 1, seed=42, lat_fmt=W.LAT_NVFP4, permute=True, pool_rows=200)
+    _run_all(wl)
+
+
+def test_mxfp4_nvfp4_mtp_groups():
+    wl = W.make_workload([3000, 4100], 6, seed=43, idx_fmt=W.IDX_MXFP4, lat_fmt=W.LAT_NVFP4, permute=True,
+                         pool_rows=200)
+    _run_all(wl)
+
+
+@pytest.mark.slow
+def test_full_cfg3_decode_1m_mxfp4_nvfp4():
+    # one request, 1,048,576-token context, MXFP4 index keys and NVFP4 latents
+    wl = W.config(3)
+    r = _run_all(wl, check_split=False)
+    print(r)
