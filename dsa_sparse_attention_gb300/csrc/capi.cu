@@ -27,7 +27,7 @@ struct Ws {
   size_t topk = 0;
   size_t scores = 0;
   int64_t ld = 0;
-  size_t idx = 0;
+  size_t idx = 0, phys = 0;
   size_t part_o = 0, part_ml = 0;
   int nsplit = 1, tps = 16;
   int topk_nchunks = 1;
@@ -92,6 +92,8 @@ Ws plan_ws(const dsa_kv_layout* l, const dsa_batch* b, int topk) {
   w.scores = off;
   off = align_up(off + size_t(T) * size_t(w.ld) * 4);
   w.idx = off;
+  off = align_up(off + size_t(T) * size_t(topk > 0 ? topk : 1) * 4);
+  w.phys = off;
   off = align_up(off + size_t(T) * size_t(topk > 0 ? topk : 1) * 4);
   // MLA split: enough CTAs to cover the GPU about twice
   const int ntiles = static_cast<int>(cdiv(topk > 0 ? topk : 1, kSelTile));
@@ -223,12 +225,16 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   CUtensorMap kmap, qmap;
   if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return DSA_ERR_CUDA;
   const int G = indexer_group_size(l->idx_fmt, T == b->num_reqs);
+  const bool direct = G == 1 && T <= 256;
   uint32_t* status = at<uint32_t>(ws, wl.status);
-  cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, wl.plan_hdr), 0, wl.groups + size_t(T) * sizeof(ScoreGroup) - wl.plan_hdr, st);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
   BatchView bv = batch_view(b);
-  e = launch_plan_groups(bv, G, at<ScoreGroup>(ws, wl.groups), at<PlanHeader>(ws, wl.plan_hdr), status, st);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (!direct) {
+    cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, wl.plan_hdr), 0,
+                                    wl.groups + size_t(T) * sizeof(ScoreGroup) - wl.plan_hdr, st);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    e = launch_plan_groups(bv, G, at<ScoreGroup>(ws, wl.groups), at<PlanHeader>(ws, wl.plan_hdr), status, st);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
   IndexerParams p;
   p.pool = pool_view(l);
   p.b = bv;
@@ -238,6 +244,7 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   p.hdr = at<PlanHeader>(ws, wl.plan_hdr);
   p.groups = at<ScoreGroup>(ws, wl.groups);
   p.status = status;
+  p.direct = direct ? 1 : 0;
   return cuda_status(launch_indexer(kmap, qmap, p, G, num_sms(), st));
 }
 
@@ -261,8 +268,9 @@ dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* sco
   return cuda_status(launch_topk(p, st));
 }
 
-dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, const int32_t* idx, int topk,
-                   float sm_scale, void* out, float* lse, void* ws, const Ws& wl, cudaStream_t st) {
+dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, const int32_t* idx,
+                   const int32_t* phys, int topk, float sm_scale, void* out, float* lse, void* ws, const Ws& wl,
+                   cudaStream_t st) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
   CUtensorMap qmap;
@@ -271,6 +279,7 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   p.pool = pool_view(l);
   p.b = batch_view(b);
   p.idx = idx;
+  p.phys = phys;
   p.topk = topk;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.tps = wl.tps;
@@ -350,7 +359,7 @@ dsa_status dsa_sparse_mla(const dsa_kv_layout* layout, const dsa_batch* batch, c
   if (batch->num_tokens > 0 && (!q || !idx || !out || !aligned16(q) || !aligned16(out))) return DSA_ERR_INVALID_ARG;
   const Ws wl = plan_ws(layout, batch, topk);
   if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
-  return run_mla(layout, batch, q, idx, topk, sm_scale, out, lse, workspace, wl, stream);
+  return run_mla(layout, batch, q, idx, nullptr, topk, sm_scale, out, lse, workspace, wl, stream);
 }
 
 dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
@@ -368,8 +377,10 @@ dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, c
   float* scores = at<float>(workspace, wl.scores);
   int32_t* idx = idx_out ? idx_out : at<int32_t>(workspace, wl.idx);
   if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream)) != DSA_OK) return s;
-  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, nullptr, workspace, wl, stream)) != DSA_OK) return s;
-  return run_mla(layout, batch, q, idx, topk, sm_scale, out, lse, workspace, wl, stream);
+  // the top-k also emits each selection's physical cache slot, which the attention gathers directly
+  int32_t* phys = at<int32_t>(workspace, wl.phys);
+  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream)) != DSA_OK) return s;
+  return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream);
 }
 
 dsa_status dsa_check(void* workspace, size_t workspace_bytes, dsa_stream_t stream) {

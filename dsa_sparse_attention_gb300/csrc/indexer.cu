@@ -121,6 +121,10 @@ __global__ void __launch_bounds__(1024) plan_groups_kernel(PlanParams p) {
 // ------------------------------------------------------------------- scorer
 
 
+// Decode batches of at most this many tokens, one per group, are planned inside
+// the scorer (no separate planning launch).
+constexpr int kDirectMaxT = 256;
+
 // Shared-memory / TMEM plan of the scorer.  IDXF = DSA_IDX_FP8 (0) or
 // DSA_IDX_MXFP4 (1); G = max tokens per group (N = 32 G).  MXFP4 keys arrive
 // packed (64 B/key) and converter warps expand them to e4m3 (exact); each
@@ -147,7 +151,8 @@ struct ScorerCfg {
   static constexpr int OFF_BARS = OFF_POS + 2 * G * 4 + 64;
   static constexpr int N_BARS = 3 * STAGES + 2 * NACC + 5;
   static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int OFF_PLAN = OFF_MISC + 64;            // direct mode: groups [kDirectMaxT] + total
+  static constexpr int SMEM_BYTES = OFF_PLAN + kDirectMaxT * 32 + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr int CONV_WARPS = MX ? 8 : 0;
   static constexpr int THREADS = 320 + 32 * CONV_WARPS;
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
@@ -224,8 +229,48 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   int* possm = reinterpret_cast<int*>(smem + C::OFF_POS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int total = p.hdr->total_tiles;
-  const int ng = p.hdr->n_groups;
+  // Plan: groups of tokens and their key-tile ranges.  In direct mode every token
+  // is its own group and the plan is built here from q_req / q_pos (one global
+  // round trip); otherwise plan_groups_kernel wrote it to the workspace.
+  __shared__ int scan_sh[32];
+  const ScoreGroup* groups;
+  int total, ng;
+  if (p.direct) {
+    ScoreGroup* sg = reinterpret_cast<ScoreGroup*>(smem + C::OFF_PLAN);
+    int* plan_total = reinterpret_cast<int*>(smem + C::OFF_PLAN + kDirectMaxT * 32);
+    const int T = p.b.T;
+    int req = 0, L = 0, tiles = 0;
+    if (static_cast<int>(threadIdx.x) < T) {
+      int r = __ldg(p.b.q_req + threadIdx.x);
+      int pos = __ldg(p.b.q_pos + threadIdx.x);
+      bool bad = false;
+      if (r < 0 || r >= p.b.B) { bad = true; r = r < 0 ? 0 : p.b.B - 1; }
+      if (pos < 0 || pos >= p.b.max_ctx) { bad = true; pos = pos < 0 ? 0 : p.b.max_ctx - 1; }
+      if (bad) atomicOr(p.status, DEV_BAD_BATCH);
+      req = r;
+      L = pos + 1;
+      tiles = static_cast<int>(cdiv(L, kKeyTile));
+    }
+    const int incl = block_inclusive_scan(tiles, scan_sh, OpAdd(), 0);
+    if (static_cast<int>(threadIdx.x) < T) {
+      ScoreGroup g;
+      g.t0 = threadIdx.x;
+      g.n = 1;
+      g.req = req;
+      g.L = L;
+      g.tile_begin = incl - tiles;
+      sg[threadIdx.x] = g;
+    }
+    if (threadIdx.x == blockDim.x - 1) *plan_total = incl;
+    __syncthreads();
+    groups = sg;
+    ng = T;
+    total = *plan_total;
+  } else {
+    groups = p.groups;
+    total = p.hdr->total_tiles;
+    ng = p.hdr->n_groups;
+  }
   const int tile_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
   const int tile_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
 
@@ -267,7 +312,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         prefetch_tensormap(&qmap);
       }
       GroupCursor cur;
-      cur.init(p.groups, ng, total, tile_lo);
+      cur.init(groups, ng, total, tile_lo);
       int issued = 0;
       bool ok = true;
       int my_rows[kKeyTile / 16];
@@ -278,8 +323,8 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
 #pragma unroll
           for (int bx = 0; bx < kKeyTile / 16; ++bx) my_rows[bx] = -1;
           if (i < tile_hi) {
-            const int g = find_group(p.groups, ng, i);
-            const ScoreGroup gg = p.groups[g];
+            const int g = find_group(groups, ng, i);
+            const ScoreGroup gg = groups[g];
             const int64_t key0 = static_cast<int64_t>(i - gg.tile_begin) * kKeyTile;
             const int32_t* btrow = p.b.bt + static_cast<int64_t>(gg.req) * p.b.bt_stride;
 #pragma unroll
@@ -310,7 +355,11 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
             if (lane == 0) {
               for (int j = 0; j < grp.n; ++j) {
                 int req, pos;
-                load_token(p.b, grp.t0 + j, p.status, req, pos);
+                if (p.direct) {
+                  pos = grp.L - 1;
+                } else {
+                  load_token(p.b, grp.t0 + j, p.status, req, pos);
+                }
                 possm[qb * G + j] = pos;
               }
               mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * (kIdxHeads * kIdxDim + kIdxHeads * 4));
@@ -358,7 +407,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
         GroupCursor cur;
-        cur.init(p.groups, ng, total, tile_lo);
+        cur.init(groups, ng, total, tile_lo);
         uint32_t idesc = make_idesc(0, 0, false, false, kKeyTile, cur.grp.n * kIdxHeads);
         bool ok = mbar_wait(&qfull[0], 0, ab);
         for (int i = tile_lo; i < tile_hi && ok; ++i) {
@@ -425,7 +474,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       const int quarter = warp & 3;
       const int set = e >> 2;
       GroupCursor cur;
-      cur.init(p.groups, ng, total, tile_lo);
+      cur.init(groups, ng, total, tile_lo);
       bool ok = mbar_wait(&qfull[0], 0, ab);
       for (int i = tile_lo; i < tile_hi && ok; ++i) {
         if (cur.advance(i)) {

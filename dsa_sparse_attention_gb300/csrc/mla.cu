@@ -146,6 +146,13 @@ __device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32]) {
   return v[0];
 }
 
+// 2^x on the multi-function unit (relative error about 2^-22; subnormal results flush to 0).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void sts128(uint8_t* p, const uint32_t* v) {
   *reinterpret_cast<uint4*>(p) = make_uint4(v[0], v[1], v[2], v[3]);
 }
@@ -185,6 +192,8 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   const int t = blockIdx.y;
   const int split = blockIdx.x;
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.topk;
+  const int32_t* phys_row = p.phys ? p.phys + static_cast<int64_t>(t) * p.topk : nullptr;
+  const int32_t* sel_row = phys_row ? phys_row : idx_row;   // both use -1 padding
   // Tiles of this split that hold selected entries (valid entries come first, so
   // a tile is used iff its first entry is valid); every thread reads the same few
   // words, in parallel with the set-up below.
@@ -192,7 +201,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   const int j0 = split * p.tps;
   int j1 = j0;
   for (int j = j0; j < min(ntiles_max, j0 + p.tps); ++j)
-    if (__ldg(idx_row + j * kSelTile) >= 0) j1 = j + 1;
+    if (__ldg(sel_row + j * kSelTile) >= 0) j1 = j + 1;
   if (threadIdx.x == 0) {
     mbar_init(raw_full, 1);
     mbar_init(raw_empty, CONV_WARPS);
@@ -248,6 +257,22 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         const int r = lane + 32 * i;
         const int e = j * kSelTile + r;
         src[i] = nullptr;
+        if (phys_row) {
+          // physical slot from the top-k: no block-table lookup
+          const int ph = e < p.topk ? __ldg(phys_row + e) : -1;
+          const int row = ph >> p.pool.log2_bs;
+          if (ph >= 0) {
+            if (row >= p.pool.num_rows) {
+              atomicOr(p.status, DEV_BAD_BLOCK);
+            } else {
+              src[i] = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.lat_off +
+                       static_cast<int64_t>(ph & bsm) * ROWB;
+              ++nrow;
+            }
+          }
+          rowok[r] = src[i] != nullptr;
+          continue;
+        }
         const int s = e < p.topk ? __ldg(idx_row + e) : -1;
         if (s >= 0) {
           if (s > pos || s >= s_lim) {
@@ -498,7 +523,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           float pv[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            pv[i] = valid ? exp2f(__uint_as_float(rr[i]) * p.scale_log2 - m_use[32 * c + i]) : 0.f;
+            pv[i] = valid ? ex2_fast(__uint_as_float(rr[i]) * p.scale_log2 - m_use[32 * c + i]) : 0.f;
 #pragma unroll
           for (int cc4 = 0; cc4 < 4; ++cc4) {
             uint32_t o[4];
@@ -530,56 +555,62 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         }
       }
     }
-    // ---- epilogue: O / l, or the normalised fp16 partial and (max, sum)
-    if (ok) ok = mbar_wait(o_done, (j1 - j0 - 1) & 1, ab);
-    if (ok) {
-      tc_fence_after();
-      if (warp == SOFT_WARP0) {
+    // row sums (and their reciprocals) for the shared epilogue below
+    if (ok && warp == SOFT_WARP0) {
 #pragma unroll
-        for (int i = 0; i < 3; ++i) l_fin[lane + 32 * i] = l_run[i];
-#pragma unroll
-        for (int i = 0; i < 3; ++i) alpha_sh[lane + 32 * i] = 1.f / l_run[i];   // reused: 1 / sum
+      for (int i = 0; i < 3; ++i) {
+        l_fin[lane + 32 * i] = l_run[i];
+        alpha_sh[lane + 32 * i] = 1.f / l_run[i];   // reused: 1 / sum
       }
-      named_bar_sync(1, 128);
-      // per 128-dim block: TMEM (thread = dim) -> smem [head][dim] -> 16-byte global stores
-      uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_RAW);   // raw tile is free now
+    }
+  }
+  // ---- epilogue (all 12 math warps): O / l, or the normalised fp16 partial and
+  // (max, sum).  TMEM (thread = dim) -> shared [head][512 dims] -> 16-byte stores.
+  if (j0 < j1 && warp >= 2) {
+    const int mw = warp - 2;                        // 0..11
+    const int quarter = warp & 3;
+    const int which = mw >> 2;                      // 0..2: the three warps of this lane quarter
+    const int et = threadIdx.x - 64;                // 0..383
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    mbar_wait(o_done, (j1 - j0 - 1) & 1, ab);
+    named_bar_sync(2, 384);
+    // a failed wait sets the CTA abort flag before this barrier, so the test is uniform
+    if (!*reinterpret_cast<volatile int*>(abortf)) {
+      tc_fence_after();
+      uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_RAW);   // raw tile and q ring are free now
       const bool final_out = p.nsplit == 1;
+      for (int pc = which; pc < 12; pc += 3) {       // (block v, head chunk c) pairs
+        const int v = pc / 3, c = pc % 3;
+        uint32_t rr[32];
+        DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
+        tmem_wait_ld();
+        const int dim = v * 128 + quarter * 32 + lane;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int h = 32 * c + i;
+          const float val = __uint_as_float(rr[i]) * alpha_sh[h];
+          uint16_t bits;
+          if (final_out) {
+            const __nv_bfloat16 bv = __float2bfloat16_rn(val);
+            bits = *reinterpret_cast<const uint16_t*>(&bv);
+          } else {
+            const __half hv = __float2half_rn(val);
+            bits = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+          stage[h * kVDim + dim] = bits;
+        }
+      }
+      named_bar_sync(2, 384);
       uint16_t* gbase = final_out ? reinterpret_cast<uint16_t*>(p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim)
                                   : reinterpret_cast<uint16_t*>(p.part_o + ts * kMlaHeads * kVDim);
-      for (int v = 0; v < 4; ++v) {
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          uint32_t rr[32];
-          DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int h = 32 * c + i;
-            const float val = __uint_as_float(rr[i]) * alpha_sh[h];
-            uint16_t bits;
-            if (final_out) {
-              const __nv_bfloat16 b = __float2bfloat16_rn(val);
-              bits = *reinterpret_cast<const uint16_t*>(&b);
-            } else {
-              const __half hv = __float2half_rn(val);
-              bits = *reinterpret_cast<const uint16_t*>(&hv);
-            }
-            stage[h * 128 + r] = bits;
-          }
+      for (int i = et; i < kMlaHeads * kVDim / 8; i += 384)
+        *reinterpret_cast<uint4*>(gbase + 8 * i) = *reinterpret_cast<const uint4*>(stage + 8 * i);
+      if (et < kMlaHeads) {
+        if (final_out) {
+          if (p.lse) p.lse[static_cast<int64_t>(t) * kMlaHeads + et] = (m_use[et] + log2f(l_fin[et])) * 0.69314718055994531f;
+        } else {
+          p.part_ml[ts * kMlaHeads + et] = make_float2(m_use[et], l_fin[et]);
         }
-        named_bar_sync(1, 128);
-        for (int i = mt; i < kMlaHeads * 16; i += 128) {
-          const int h = i >> 4, g = i & 15;
-          *reinterpret_cast<uint4*>(gbase + h * kVDim + v * 128 + g * 8) =
-              *reinterpret_cast<const uint4*>(stage + h * 128 + g * 8);
-        }
-        named_bar_sync(1, 128);
-      }
-      if (final_out) {
-        if (p.lse && mt < kMlaHeads)
-          p.lse[static_cast<int64_t>(t) * kMlaHeads + mt] = (m_use[mt] + log2f(l_fin[mt])) * 0.69314718055994531f;
-      } else if (mt < kMlaHeads) {
-        p.part_ml[ts * kMlaHeads + mt] = make_float2(m_use[mt], l_fin[mt]);
       }
     }
   }

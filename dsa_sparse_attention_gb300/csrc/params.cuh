@@ -17,6 +17,7 @@ struct IndexerParams {
   const PlanHeader* hdr;
   const ScoreGroup* groups;
   uint32_t* status;
+  int direct;              // 1: one token per group, planned inside the scorer (hdr/groups unused)
 };
 
 struct TopkParams {
@@ -46,6 +47,7 @@ struct MlaParams {
   PoolView pool;
   BatchView b;
   const int32_t* idx;      // [T, topk]
+  const int32_t* phys;     // [T, topk] physical slots (row * bs + slot) of idx, or null
   int topk;
   float scale_log2;        // sm_scale * log2(e)
   int tps;                 // tiles per split
