@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(1024) plan_groups_kernel(PlanParams p) {
 // Decode batches of at most this many tokens, one per group, are planned inside
 // the scorer (no separate planning launch).
 constexpr int kDirectMaxT = 256;
+constexpr int kRowBatch = 64;      // tiles whose block-table rows the producer resolves at once
 
 // Shared-memory / TMEM plan of the scorer.  IDXF = DSA_IDX_FP8 (0) or
 // DSA_IDX_MXFP4 (1); G = max tokens per group (N = 32 G).  MXFP4 keys arrive
@@ -152,7 +153,8 @@ struct ScorerCfg {
   static constexpr int N_BARS = 3 * STAGES + 2 * NACC + 5;
   static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
   static constexpr int OFF_PLAN = OFF_MISC + 64;            // direct mode: groups [kDirectMaxT] + total
-  static constexpr int SMEM_BYTES = OFF_PLAN + kDirectMaxT * 32 + 64 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int OFF_ROWS = OFF_PLAN + kDirectMaxT * 32 + 64;   // producer: [kRowBatch][8] block ids
+  static constexpr int SMEM_BYTES = OFF_ROWS + kRowBatch * 8 * 4 + 1024;  // + slack for 1024-byte alignment
   static constexpr int CONV_WARPS = MX ? 8 : 0;
   static constexpr int THREADS = 320 + 32 * CONV_WARPS;
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
@@ -315,44 +317,56 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       cur.init(groups, ng, total, tile_lo);
       int issued = 0;
       bool ok = true;
-      int my_rows[kKeyTile / 16];
-      for (int base = tile_lo; base < tile_hi && ok; base += 32) {
-        // lane j: rows of tile base + j
-        {
-          const int i = base + lane;
-#pragma unroll
-          for (int bx = 0; bx < kKeyTile / 16; ++bx) my_rows[bx] = -1;
-          if (i < tile_hi) {
-            const int g = find_group(groups, ng, i);
-            const ScoreGroup gg = groups[g];
-            const int64_t key0 = static_cast<int64_t>(i - gg.tile_begin) * kKeyTile;
-            const int32_t* btrow = p.b.bt + static_cast<int64_t>(gg.req) * p.b.bt_stride;
-#pragma unroll
-            for (int bx = 0; bx < kKeyTile / 16; ++bx) {
-              if (bx >= nbox) break;
-              const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
-              if (k0 >= gg.L) break;
-              const int row = btrow[k0 >> p.pool.log2_bs];
-              if (row < 0 || row >= p.pool.num_rows) {
-                atomicOr(p.status, DEV_BAD_BLOCK);
-                continue;
-              }
-              my_rows[bx] = row;
-            }
-          }
-        }
-        const int nb = min(32, tile_hi - base);
-        for (int jj = 0; jj < nb; ++jj) {
+      int* rows_sm = reinterpret_cast<int*>(smem + C::OFF_ROWS);   // [kRowBatch][8] block ids
+      int gb = cur.g;                                               // group of tile `base`
+      for (int base = tile_lo; base < tile_hi && ok; base += kRowBatch) {
+        const int nb = min(kRowBatch, tile_hi - base);
+        // the warp resolves the block-table rows of tiles base .. base+nb-1, every
+        // load of a lane issued before any is used
+        for (int jj = lane; jj < kRowBatch; jj += 32) {
           const int i = base + jj;
-          int rows[kKeyTile / 16];
+          int idx[kKeyTile / 16];
+          int vals[kKeyTile / 16];
+          const int32_t* btrow = p.b.bt;
+          int L = 0;
+          int64_t key0 = 0;
+          int g = gb;
+          if (jj < nb) {
+            while (g + 1 < ng && groups[g + 1].tile_begin <= i) ++g;   // groups span many tiles
+            const ScoreGroup gg = groups[g];
+            key0 = static_cast<int64_t>(i - gg.tile_begin) * kKeyTile;
+            btrow = p.b.bt + static_cast<int64_t>(gg.req) * p.b.bt_stride;
+            L = gg.L;
+          }
 #pragma unroll
-          for (int bx = 0; bx < kKeyTile / 16; ++bx) rows[bx] = __shfl_sync(0xffffffffu, my_rows[bx], jj);
-          const bool changed = cur.advance(i);
-          const ScoreGroup& grp = cur.grp;
-          if (i == tile_lo || changed) {
-            const int qb = cur.count & 1;
-            if (cur.count >= 2 && !(ok = mbar_wait(&qempty[qb], ((cur.count - 2) >> 1) & 1, ab))) break;
-            if (lane == 0) {
+          for (int bx = 0; bx < kKeyTile / 16; ++bx) {
+            const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
+            idx[bx] = (jj < nb && bx < nbox && k0 < L) ? static_cast<int>(k0 >> p.pool.log2_bs) : -1;
+          }
+#pragma unroll
+          for (int bx = 0; bx < kKeyTile / 16; ++bx) vals[bx] = idx[bx] >= 0 ? __ldg(btrow + idx[bx]) : -1;
+#pragma unroll
+          for (int bx = 0; bx < kKeyTile / 16; ++bx) {
+            int row = vals[bx];
+            if (idx[bx] >= 0 && (row < 0 || row >= p.pool.num_rows)) {
+              atomicOr(p.status, DEV_BAD_BLOCK);
+              row = -1;
+            }
+            rows_sm[jj * 8 + bx] = idx[bx] >= 0 ? row : -1;
+          }
+          gb = max(gb, g);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gb = max(gb, __shfl_xor_sync(0xffffffffu, gb, o));
+        __syncwarp();
+        if (lane == 0) {
+          for (int jj = 0; jj < nb; ++jj) {
+            const int i = base + jj;
+            const bool changed = cur.advance(i);
+            const ScoreGroup& grp = cur.grp;
+            if (i == tile_lo || changed) {
+              const int qb = cur.count & 1;
+              if (cur.count >= 2 && !(ok = mbar_wait(&qempty[qb], ((cur.count - 2) >> 1) & 1, ab))) break;
               for (int j = 0; j < grp.n; ++j) {
                 int req, pos;
                 if (p.direct) {
@@ -369,35 +383,33 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
               bulk_load(wsm + qb * G * kIdxHeads, p.w + static_cast<int64_t>(grp.t0) * kIdxHeads,
                         static_cast<uint32_t>(grp.n) * kIdxHeads * 4, &qfull[qb]);
             }
-            __syncwarp();
-          }
-          const int it = i - tile_lo;
-          const int s = it % C::STAGES;
-          if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
-          if (lane == 0) {
+            const int it = i - tile_lo;
+            const int s = it % C::STAGES;
+            if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
+            const int* rows = rows_sm + jj * 8;
             const int64_t key0 = static_cast<int64_t>(i - grp.tile_begin) * kKeyTile;
             constexpr int VB = C::MX ? kIdxDim / 2 : kIdxDim;   // value bytes per key in the page
             uint32_t bytes = 0;
-#pragma unroll
-            for (int bx = 0; bx < kKeyTile / 16; ++bx)
+            for (int bx = 0; bx < nbox; ++bx)
               if (rows[bx] >= 0) bytes += static_cast<uint32_t>(box) * (VB + 4);
             mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-            for (int bx = 0; bx < kKeyTile / 16; ++bx) {
-              if (rows[bx] < 0) continue;
+            for (int bx = 0; bx < nbox; ++bx) {
+              const int row = rows[bx];
+              if (row < 0) continue;
               const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
               const int slot0 = static_cast<int>(k0 & (bs - 1));
               uint8_t* vdst = C::MX ? smem + C::OFF_PACK + s * C::PACK_BYTES + bx * box * VB
                                     : smem + s * C::KEY_BYTES + bx * box * kIdxDim;
-              tma_load_3d(vdst, &kmap, &full[s], 0, slot0, rows[bx]);
-              const uint8_t* src = p.pool.pool + static_cast<int64_t>(rows[bx]) * p.pool.row_stride +
-                                   p.pool.idx_off + static_cast<int64_t>(bs) * VB + static_cast<int64_t>(slot0) * 4;
+              tma_load_3d(vdst, &kmap, &full[s], 0, slot0, row);
+              const uint8_t* src = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.idx_off +
+                                   static_cast<int64_t>(bs) * VB + static_cast<int64_t>(slot0) * 4;
               bulk_load(smem + C::OFF_SCALES + s * C::SCALE_BYTES + bx * box * 4, src, box * 4, &full[s]);
             }
+            ++issued;
           }
-          __syncwarp();
-          ++issued;
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        __syncwarp();
       }
       if (!ok && lane == 0) {   // drain the copies still in flight before the CTA exits
         for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it)

@@ -252,38 +252,44 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       if (jt > 0 && !(ok = mbar_wait(raw_empty, (jt - 1) & 1, ab))) break;
       const uint8_t* src[4];
       uint32_t nrow = 0;
+      // every selected entry of this lane's four rows is loaded before any is used
+      int sel[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = j * kSelTile + lane + 32 * i;
+        sel[i] = e < p.topk ? __ldg(sel_row + e) : -1;
+      }
+      int rowid[4];
+      if (!phys_row) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int s = sel[i];
+          const bool in = s >= 0 && s <= pos && s < s_lim;
+          rowid[i] = in ? __ldg(btrow + (s >> p.pool.log2_bs)) : -1;
+          if (s >= 0 && !in) atomicOr(p.status, DEV_BAD_BATCH);
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = lane + 32 * i;
-        const int e = j * kSelTile + r;
         src[i] = nullptr;
-        if (phys_row) {
-          // physical slot from the top-k: no block-table lookup
-          const int ph = e < p.topk ? __ldg(phys_row + e) : -1;
-          const int row = ph >> p.pool.log2_bs;
-          if (ph >= 0) {
-            if (row >= p.pool.num_rows) {
-              atomicOr(p.status, DEV_BAD_BLOCK);
-            } else {
-              src[i] = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.lat_off +
-                       static_cast<int64_t>(ph & bsm) * ROWB;
-              ++nrow;
-            }
-          }
-          rowok[r] = src[i] != nullptr;
-          continue;
-        }
-        const int s = e < p.topk ? __ldg(idx_row + e) : -1;
-        if (s >= 0) {
-          if (s > pos || s >= s_lim) {
-            atomicOr(p.status, DEV_BAD_BATCH);
+        const int sv = sel[i];
+        if (sv >= 0) {
+          int row, slot;
+          if (phys_row) {
+            row = sv >> p.pool.log2_bs;   // physical slot from the top-k: no block-table lookup
+            slot = sv & bsm;
           } else {
-            const int row = btrow[s >> p.pool.log2_bs];
+            row = rowid[i];
+            slot = sv & bsm;
+          }
+          const bool present = phys_row || (sv <= pos && sv < s_lim);
+          if (present) {
             if (row < 0 || row >= p.pool.num_rows) {
               atomicOr(p.status, DEV_BAD_BLOCK);
             } else {
               src[i] = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.lat_off +
-                       static_cast<int64_t>(s & bsm) * ROWB;
+                       static_cast<int64_t>(slot) * ROWB;
               ++nrow;
             }
           }

@@ -31,9 +31,15 @@ class DeviceWorkload:
         self.lse = torch.empty(T, 96, dtype=torch.float32, device=device)
         self.idx = torch.empty(T, self.topk, dtype=torch.int32, device=device)
 
-    def layer_step(self, stream=None):
-        dsa_layer_step(self.layout, self.batch, self.q_idx, self.w, self.q, self.topk, self.wl.sm_scale, self.out,
-                       idx_out=self.idx, lse=self.lse, ws=self.ws, stream=stream)
+    def pool_copy_layout(self, pool):
+        """Layout over another device copy of the pool (same rows, other addresses)."""
+        wl = self.wl
+        return make_layout(pool, wl.num_rows, wl.row_stride, wl.idx_page_offset, wl.lat_page_offset, wl.block_size,
+                           wl.idx_fmt, wl.lat_fmt)
+
+    def layer_step(self, stream=None, layout=None):
+        dsa_layer_step(self.layout if layout is None else layout, self.batch, self.q_idx, self.w, self.q, self.topk,
+                       self.wl.sm_scale, self.out, idx_out=self.idx, lse=self.lse, ws=self.ws, stream=stream)
         return self.idx, self.out, self.lse
 
     def indexer_scores(self, stream=None):
