@@ -226,7 +226,9 @@ def main():
         graphs.append(g)
     torch.cuda.synchronize()
 
-    n_kernels_per_step = 6   # scorer, top-k (histogram, candidates, emit), mla, combine
+    # scorer, top-k (one cluster launch for rows up to 65,536 scores, else histogram,
+    # candidates and emit), attention, split combine
+    n_kernels_per_step = 1 + (1 if int(wl.ctx_lens.max()) <= 65536 else 3) + 1 + 1
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup) * len(graphs)):

@@ -248,8 +248,9 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   return cuda_status(launch_indexer(kmap, qmap, p, G, num_sms(), st));
 }
 
+// `chained`: the launch follows a kernel of this library on the stream (see launch_ex).
 dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* scores, int64_t ld, int topk,
-                    int32_t* idx, int32_t* phys, void* ws, const Ws& wl, cudaStream_t st) {
+                    int32_t* idx, int32_t* phys, void* ws, const Ws& wl, cudaStream_t st, bool chained) {
   if (b->num_tokens == 0) return DSA_OK;
   TopkParams p;
   p.b = batch_view(b);
@@ -265,12 +266,12 @@ dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* sco
     while ((1 << lg) < l->block_size) ++lg;
   p.log2_bs = lg;
   p.status = at<uint32_t>(ws, wl.status);
-  return cuda_status(launch_topk(p, st));
+  return cuda_status(launch_topk(p, st, chained));
 }
 
 dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, const int32_t* idx,
                    const int32_t* phys, int topk, float sm_scale, void* out, float* lse, void* ws, const Ws& wl,
-                   cudaStream_t st) {
+                   cudaStream_t st, bool chained) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
   CUtensorMap qmap;
@@ -289,7 +290,7 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   p.part_o = at<__half>(ws, wl.part_o);
   p.part_ml = at<float2>(ws, wl.part_ml);
   p.status = at<uint32_t>(ws, wl.status);
-  return cuda_status(launch_sparse_mla(qmap, p, st));
+  return cuda_status(launch_sparse_mla(qmap, p, st, chained));
 }
 
 }  // namespace
@@ -346,7 +347,7 @@ dsa_status dsa_topk(const dsa_kv_layout* layout, const dsa_batch* batch, const f
   dummy.block_size = 64;
   const Ws wl = plan_ws(layout ? layout : &dummy, batch, topk);
   if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
-  return run_topk(layout, batch, scores, ld_scores, topk, idx, phys_slots, workspace, wl, stream);
+  return run_topk(layout, batch, scores, ld_scores, topk, idx, phys_slots, workspace, wl, stream, false);
 }
 
 dsa_status dsa_sparse_mla(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q, const int32_t* idx,
@@ -359,7 +360,7 @@ dsa_status dsa_sparse_mla(const dsa_kv_layout* layout, const dsa_batch* batch, c
   if (batch->num_tokens > 0 && (!q || !idx || !out || !aligned16(q) || !aligned16(out))) return DSA_ERR_INVALID_ARG;
   const Ws wl = plan_ws(layout, batch, topk);
   if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
-  return run_mla(layout, batch, q, idx, nullptr, topk, sm_scale, out, lse, workspace, wl, stream);
+  return run_mla(layout, batch, q, idx, nullptr, topk, sm_scale, out, lse, workspace, wl, stream, false);
 }
 
 dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
@@ -379,8 +380,9 @@ dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, c
   if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream)) != DSA_OK) return s;
   // the top-k also emits each selection's physical cache slot, which the attention gathers directly
   int32_t* phys = at<int32_t>(workspace, wl.phys);
-  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream)) != DSA_OK) return s;
-  return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream);
+  // the top-k and the attention start while their predecessor drains (programmatic launch)
+  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream, true)) != DSA_OK) return s;
+  return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream, true);
 }
 
 dsa_status dsa_check(void* workspace, size_t workspace_bytes, dsa_stream_t stream) {

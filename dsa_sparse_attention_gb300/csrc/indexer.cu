@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   float* wsm = reinterpret_cast<float*>(smem + C::OFF_W);
   int* possm = reinterpret_cast<int*>(smem + C::OFF_POS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_launch();   // a chained top-k may be scheduled as this grid's CTAs retire
 
   // Plan: groups of tokens and their key-tile ranges.  In direct mode every token
   // is its own group and the plan is built here from q_req / q_pos (one global

@@ -194,14 +194,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.topk;
   const int32_t* phys_row = p.phys ? p.phys + static_cast<int64_t>(t) * p.topk : nullptr;
   const int32_t* sel_row = phys_row ? phys_row : idx_row;   // both use -1 padding
-  // Tiles of this split that hold selected entries (valid entries come first, so
-  // a tile is used iff its first entry is valid); every thread reads the same few
-  // words, in parallel with the set-up below.
-  const int ntiles_max = static_cast<int>(cdiv(p.topk, kSelTile));
-  const int j0 = split * p.tps;
-  int j1 = j0;
-  for (int j = j0; j < min(ntiles_max, j0 + p.tps); ++j)
-    if (__ldg(sel_row + j * kSelTile) >= 0) j1 = j + 1;
   if (threadIdx.x == 0) {
     mbar_init(raw_full, 1);
     mbar_init(raw_empty, CONV_WARPS);
@@ -222,6 +214,16 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, TMEM_COLS);
+  // The set-up above overlaps the end of the kernel that writes the selection.
+  grid_dep_wait();
+  grid_dep_launch();
+  // Tiles of this split that hold selected entries (valid entries come first, so
+  // a tile is used iff its first entry is valid); every thread reads the same few words.
+  const int ntiles_max = static_cast<int>(cdiv(p.topk, kSelTile));
+  const int j0 = split * p.tps;
+  int j1 = j0;
+  for (int j = j0; j < min(ntiles_max, j0 + p.tps); ++j)
+    if (__ldcg(sel_row + j * kSelTile) >= 0) j1 = j + 1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int e = j * kSelTile + lane + 32 * i;
-        sel[i] = e < p.topk ? __ldg(sel_row + e) : -1;
+        sel[i] = e < p.topk ? __ldcg(sel_row + e) : -1;
       }
       int rowid[4];
       if (!phys_row) {
@@ -629,6 +631,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
 // own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m).
 // Grid (12, T), 256 threads = 8 heads x 32.
 __global__ void __launch_bounds__(256) mla_combine_kernel(MlaParams p) {
+  grid_dep_wait();
   const int t = blockIdx.y;
   const int h = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -687,7 +690,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(MlaParams p) {
 }
 
 template <int LATF>
-static cudaError_t launch_mla_fmt(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st) {
+static cudaError_t launch_mla_fmt(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
@@ -695,16 +698,16 @@ static cudaError_t launch_mla_fmt(const CUtensorMap& qmap, const MlaParams& p, c
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  sparse_mla_kernel<LATF><<<dim3(p.nsplit, p.b.T), mla::THREADS, mla::SMEM_BYTES, st>>>(qmap, p);
-  return cudaGetLastError();
+  return launch_ex(sparse_mla_kernel<LATF>, dim3(p.nsplit, p.b.T), dim3(mla::THREADS), mla::SMEM_BYTES, st, chained,
+                   0u, qmap, p);
 }
 
-cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st) {
+cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained) {
   if (p.b.T == 0) return cudaSuccess;
-  cudaError_t e = p.pool.lat_fmt == 1 ? launch_mla_fmt<1>(qmap, p, st) : launch_mla_fmt<0>(qmap, p, st);
-  if (e != cudaSuccess) return e;
-  if (p.nsplit > 1) mla_combine_kernel<<<dim3(kMlaHeads / 8, p.b.T), 256, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaError_t e =
+      p.pool.lat_fmt == 1 ? launch_mla_fmt<1>(qmap, p, st, chained) : launch_mla_fmt<0>(qmap, p, st, chained);
+  if (e != cudaSuccess || p.nsplit == 1) return e;
+  return launch_ex(mla_combine_kernel, dim3(kMlaHeads / 8, p.b.T), dim3(256), 0, st, true, 0u, p);
 }
 
 }  // namespace dsa

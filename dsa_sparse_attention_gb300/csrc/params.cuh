@@ -107,12 +107,42 @@ inline void topk_bind_scratch(TopkParams& p, uint8_t* base, const TopkScratch& L
   p.zero_bytes = L.zero_end - L.hist;
 }
 
+// Launches `kern` on `st`; `chained` allows it to start before the previous
+// kernel on the stream ends (it then calls grid_dep_wait before it reads that
+// kernel's output), `cluster_x` > 0 groups its CTAs in clusters of that size.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             bool chained, unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  unsigned na = 0;
+  if (chained) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster_x > 0) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = cluster_x;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_plan_groups(const BatchView& b, int G, ScoreGroup* groups, PlanHeader* hdr, uint32_t* status,
                                cudaStream_t st);
 cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,
                            int grid, cudaStream_t st);
 int indexer_group_size(int idx_fmt, bool one_token_per_request);
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t st);
-cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained);
+cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained);
 
 }  // namespace dsa

@@ -20,6 +20,11 @@
 //  3. emit:       ordered compaction: chunk c writes its selected positions after
 //                 those of chunks < c, so the output is ascending, deterministic
 //                 and independent of the rest of the batch.
+// Rows of at most 65,536 scores take a one-launch path instead: a cluster of up
+// to eight CTAs per row keeps the row in registers (16 scores per thread) and
+// resolves all three digits (11 + 11 + 10 bits) of the threshold key, the
+// position cut and the output offsets through histograms read across the
+// cluster's shared memory; it needs no global scratch and no zeroing.
 #include "params.cuh"
 
 namespace dsa {
@@ -382,8 +387,168 @@ __global__ void __launch_bounds__(kTopkThreads) topk_emit_kernel(TopkParams p) {
   }
 }
 
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t st) {
+// ------------------------------------------------------- one-launch cluster path
+
+constexpr int kClThreads = 512;
+constexpr int kClSlice = kClThreads * kPerThread;   // 8192 scores per CTA
+constexpr int kClMaxCtas = 8;                       // portable cluster size
+constexpr int kClMaxRow = kClSlice * kClMaxCtas;    // 65,536
+
+// The bin of the merged (cluster-wide) histogram `hist` holding the kk-th
+// largest key, and the number of keys in higher bins.  Thread i owns bins
+// [2044 - 4i, 2048 - 4i), so thread order is descending bin order.
+__device__ void cluster_find(const uint32_t* hist, uint32_t csize, uint32_t kk, int& bin, uint32_t& above,
+                             uint32_t* sh) {
+  const int lo = kBins - 4 * (static_cast<int>(threadIdx.x) + 1);
+  const uint32_t a = smem_u32(hist + lo);
+  uint4 m = make_uint4(0, 0, 0, 0);
+  for (uint32_t r = 0; r < csize; ++r) {
+    const uint4 v = ld_cluster_v4(cluster_map(a, r));
+    m.x += v.x;
+    m.y += v.y;
+    m.z += v.z;
+    m.w += v.w;
+  }
+  const uint32_t local = m.x + m.y + m.z + m.w;
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(local, sh, total);
+  if (excl < kk && excl + local >= kk) {
+    // walk bins lo+3 .. lo
+    uint32_t cum = excl;
+    int b = lo + 3;
+    if (cum + m.w < kk) {
+      cum += m.w;
+      --b;
+      if (cum + m.z < kk) {
+        cum += m.z;
+        --b;
+        if (cum + m.y < kk) {
+          cum += m.y;
+          --b;
+        }
+      }
+    }
+    sh[33] = static_cast<uint32_t>(b);
+    sh[34] = cum;
+  }
+  __syncthreads();
+  bin = static_cast<int>(sh[33]);
+  above = sh[34];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) {
+  __shared__ __align__(16) uint32_t h[3][kBins];   // this CTA's histograms of digits 1, 2, 3
+  __shared__ uint32_t sh[48];
+  __shared__ uint32_t counts;                      // (keys above T) << 16 | (keys equal to T)
+  const int t = blockIdx.y;
+  const uint32_t rank = cluster_rank(), csize = cluster_size();
+  int req, pos;
+  load_token(p.b, t, p.status, req, pos);
+  const int n = pos + 1;
+  for (int i = threadIdx.x; i < 3 * kBins; i += kClThreads) h[0][i] = 0;
+  grid_dep_wait();
+  grid_dep_launch();
+  int32_t* out = p.idx + static_cast<int64_t>(t) * p.k;
+  int32_t* phys = p.phys ? p.phys + static_cast<int64_t>(t) * p.k : nullptr;
+  const int32_t* btrow = p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride;
+  const int bs_mask = (1 << p.log2_bs) - 1;
+
+  if (n <= p.k) {   // every position is selected, then -1 padding
+    for (int s = rank * kClThreads + threadIdx.x; s < p.k; s += csize * kClThreads) {
+      out[s] = s < n ? s : -1;
+      if (phys) phys[s] = s < n ? (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask) : -1;
+    }
+    return;   // uniform over the cluster: no CTA touches another's shared memory
+  }
+  // this CTA's slice of the row, a multiple of 4 scores long (<= 8192)
+  const int S = (static_cast<int>(cdiv(n, csize)) + 3) & ~3;
+  const int c0 = static_cast<int>(rank) * S;
+  const int c1 = min(n, c0 + S);
+  const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
+  const int s0 = c0 + threadIdx.x * kPerThread;
+  const int nv = max(0, min(kPerThread, c1 - s0));
+  uint32_t u[kPerThread];
+  load16(row, s0, s0 + nv, u);
+  __syncthreads();   // histograms zeroed
+
+  // digit 1: bits 31..21
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i)
+    if (i < nv) atomicAdd(&h[0][u[i] >> 21], 1u);
+  cluster_sync();
+  int b1, bA, bB;
+  uint32_t a1, a2, a3;
+  const uint32_t k = static_cast<uint32_t>(p.k);
+  cluster_find(h[0], csize, k, b1, a1, sh);
+  // digit 2: bits 20..10 of the keys in digit b1
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i)
+    if (i < nv && (u[i] >> 21) == static_cast<uint32_t>(b1)) atomicAdd(&h[1][(u[i] >> 10) & 2047u], 1u);
+  cluster_sync();
+  cluster_find(h[1], csize, k - a1, bA, a2, sh);
+  // digit 3: bits 9..0 of the keys in digits (b1, bA)
+  const uint32_t pre = (static_cast<uint32_t>(b1) << 11) | static_cast<uint32_t>(bA);
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i)
+    if (i < nv && (u[i] >> 10) == pre) atomicAdd(&h[2][u[i] & 1023u], 1u);
+  cluster_sync();
+  cluster_find(h[2], csize, k - a1 - a2, bB, a3, sh);
+  const uint32_t T = (pre << 10) | static_cast<uint32_t>(bB);
+  const uint32_t need_eq = k - a1 - a2 - a3;   // keys equal to T to take, lowest positions first
+
+  // per thread (above, equal) counts, scanned in position order; fits 16 + 16 bits
+  uint32_t gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    gt += i < nv && u[i] > T;
+    eq += i < nv && u[i] == T;
+  }
+  uint32_t tot;
+  const uint32_t excl = block_excl_scan((gt << 16) | eq, sh, tot);
+  if (threadIdx.x == 0) counts = tot;
+  cluster_sync();
+  // offsets of this CTA from the counts of the CTAs before it in the row
+  if (threadIdx.x == 0) {
+    uint32_t eq_before = 0, base = 0;
+    for (uint32_t r = 0; r < rank; ++r) {
+      const uint32_t c = ld_cluster_u32(cluster_map(smem_u32(&counts), r));
+      const uint32_t e = c & 0xFFFFu;
+      const uint32_t left = need_eq > eq_before ? need_eq - eq_before : 0u;
+      base += (c >> 16) + min(e, left);
+      eq_before += e;
+    }
+    const uint32_t left = need_eq > eq_before ? need_eq - eq_before : 0u;
+    sh[35] = base;
+    sh[36] = min(tot & 0xFFFFu, left);   // equal keys this CTA takes
+  }
+  cluster_arrive();   // no shared memory of another CTA is read after this point
+  __syncthreads();
+  const uint32_t take = sh[36];
+  uint32_t eq_rank = excl & 0xFFFFu;
+  uint32_t o = sh[35] + (excl >> 16) + min(eq_rank, take);
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    if (i >= nv) continue;
+    bool sel = u[i] > T;
+    if (u[i] == T) sel = eq_rank++ < take;
+    if (!sel) continue;
+    const int s = s0 + i;
+    if (o < k) {   // exactly k are selected; the guard only bounds the stores
+      out[o] = s;
+      if (phys) phys[o] = (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask);
+    }
+    ++o;
+  }
+  cluster_wait();   // keep this CTA's shared memory alive until every CTA has read it
+}
+
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained) {
   if (p.b.T == 0) return cudaSuccess;
+  if (p.b.max_ctx <= kClMaxRow) {
+    const unsigned csize = static_cast<unsigned>(cdiv(p.b.max_ctx, kClSlice));
+    return launch_ex(topk_cluster_kernel, dim3(csize, p.b.T), dim3(kClThreads), 0, st, chained, csize, p);
+  }
   const dim3 grid(p.nchunks, p.b.T);
   cudaError_t e = cudaMemsetAsync(p.zero_begin, 0, p.zero_bytes, st);
   if (e != cudaSuccess) return e;

@@ -94,5 +94,5 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_kv_layout* layout, const dsa_ba
   p.phys = phys_slots;
   p.log2_bs = log2_bs;
   p.status = reinterpret_cast<uint32_t*>(base);
-  return launch_topk(p, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_topk(p, stream, false) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

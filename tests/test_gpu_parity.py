@@ -101,6 +101,27 @@ def test_all_scores_tied_takes_lowest_positions():
     check_mla(OracleCache(wl), g, _np(out), _np(lse), [0, 1])
 
 
+@pytest.mark.parametrize("lens", [[65536, 9000, 3000, 1, 2048, 2049, 40000], [70000, 12345, 5]])
+def test_topk_heavy_ties_exact(lens):
+    # Scores with five distinct values (and both signs of zero): the threshold
+    # key is shared by thousands of positions spread over several CTAs of a row,
+    # so the lowest-position cut decides the selection, which must equal the
+    # oracle's exactly.  Rows up to 65,536 scores take the one-launch cluster
+    # path; the second case also runs the multi-pass path.
+    from oracle import dsa_oracle as O
+    wl = W.make_workload(lens, 1, seed=51, permute=True)
+    dw = _dev(wl)
+    rng = np.random.default_rng(51)
+    sc = rng.integers(-2, 3, size=(wl.num_tokens, dw.ld)).astype(np.float32)
+    sc[(sc == 0) & (rng.random(sc.shape) < 0.5)] = -0.0
+    idx = _np(dw.topk_of(torch.from_numpy(sc).cuda()))
+    for t in range(wl.num_tokens):
+        n = int(wl.q_pos[t]) + 1
+        ref = O.topk_select(sc[t, :n].astype(np.float64), dw.topk)
+        assert np.array_equal(idx[t, :ref.size], ref), f"token {t} (n={n})"
+        assert np.all(idx[t, ref.size:] == -1)
+
+
 def _embed(big, b, alone):
     """Give request b of `big` exactly the cache and queries of request 0 of `alone`."""
     nb = (int(alone.ctx_lens[0]) + 63) // 64
