@@ -61,6 +61,7 @@ def _load():
         "dsa_sparse_mla": (i32, [L, B, vp, vp, i32, f32, vp, vp, vp, sz, vp]),
         "dsa_layer_step": (i32, [L, B, vp, vp, vp, i32, f32, vp, vp, vp, vp, sz, vp]),
         "dsa_check": (i32, [vp, sz, vp]),
+        "dsa_last_cuda_error": (i32, [P(ctypes.c_char_p)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -94,8 +95,18 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def dsa_last_cuda_error():
+    """(code, name) of the CUDA error behind the last DSA_ERR_CUDA on this thread."""
+    name = ctypes.c_char_p()
+    code = library().dsa_last_cuda_error(ctypes.byref(name))
+    return int(code), name.value.decode()
+
+
 def _check(status, where):
     if status != DSA_OK:
+        if status == -3:   # DSA_ERR_CUDA
+            code, name = dsa_last_cuda_error()
+            where = f"{where} (CUDA error {code}: {name})"
         raise DSAError(status, where)
 
 

@@ -216,14 +216,30 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
-dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+// The CUDA error behind the last DSA_ERR_CUDA returned on this host thread.
+thread_local int32_t g_last_cuda = 0;
+thread_local const char* g_last_cuda_name = "no error";
+
+dsa_status cuda_fail(cudaError_t e) {
+  g_last_cuda = static_cast<int32_t>(e);
+  g_last_cuda_name = cudaGetErrorName(e);
+  return DSA_ERR_CUDA;
+}
+
+dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : cuda_fail(e); }
+
+dsa_status encode_fail() {
+  g_last_cuda = -1;
+  g_last_cuda_name = "TMA descriptor encoding failed";
+  return DSA_ERR_CUDA;
+}
 
 dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q_idx, const float* w, float* scores,
                        int64_t ld, void* ws, const Ws& wl, cudaStream_t st) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
   CUtensorMap kmap, qmap;
-  if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return DSA_ERR_CUDA;
+  if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return encode_fail();
   const int G = indexer_group_size(l->idx_fmt, T == b->num_reqs);
   const bool direct = G == 1 && T <= 256;
   uint32_t* status = at<uint32_t>(ws, wl.status);
@@ -231,9 +247,9 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   if (!direct) {
     cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, wl.plan_hdr), 0,
                                     wl.groups + size_t(T) * sizeof(ScoreGroup) - wl.plan_hdr, st);
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e);
     e = launch_plan_groups(bv, G, at<ScoreGroup>(ws, wl.groups), at<PlanHeader>(ws, wl.plan_hdr), status, st);
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e);
   }
   IndexerParams p;
   p.pool = pool_view(l);
@@ -275,7 +291,7 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
   CUtensorMap qmap;
-  if (!make_q_map(&qmap, q, T)) return DSA_ERR_CUDA;
+  if (!make_q_map(&qmap, q, T)) return encode_fail();
   MlaParams p;
   p.pool = pool_view(l);
   p.b = batch_view(b);
@@ -295,9 +311,18 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
 
 }  // namespace
 
+namespace dsa {
+dsa_status record_cuda_status(cudaError_t e) { return cuda_status(e); }
+}  // namespace dsa
+
 extern "C" {
 
 int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+int32_t dsa_last_cuda_error(const char** name) {
+  if (name) *name = g_last_cuda_name;
+  return g_last_cuda;
+}
 
 const char* dsa_status_string(dsa_status s) {
   switch (s) {
@@ -388,10 +413,11 @@ dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, c
 dsa_status dsa_check(void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   if (!workspace || workspace_bytes < kStatusBytes) return DSA_ERR_WORKSPACE;
   uint32_t word = 0;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
-  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
   if (word == 0) return DSA_OK;
-  if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return DSA_ERR_CUDA;
+  if ((e = cudaMemset(workspace, 0, sizeof(word))) != cudaSuccess) return cuda_fail(e);
   if (word & DEV_TIMEOUT) return DSA_ERR_TIMEOUT;
   return DSA_ERR_DEVICE_CHECK;
 }

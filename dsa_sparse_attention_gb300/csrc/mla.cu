@@ -17,11 +17,14 @@
 // and a 4-warp exchange; the running maximum is only moved when a tile exceeds
 // it by more than 2^8 (the output is unchanged: the final normalisation uses the
 // same maximum), so O^T is rescaled in TMEM only on those rare tiles.
-// Roles: warp 0 gathers the 128 selected latent rows of a tile with bulk copies
-// (page translation per row) and streams q in 64-dim chunks with TMA; warp 1
-// issues MMAs; warps 2..5 convert e4m3 -> bf16 (QK operand) and -> fp16 (PV
-// operand) into 128-byte-swizzled tiles, run the softmax (P in fp16), and write
-// the output (or the fp32 partial for the LSE combine).
+// Roles: warp 0 loads the whole query (96 x 576 bf16) into shared memory with
+// TMA before the kernel waits for the selection, so the load overlaps the
+// kernel before it; warp 1 issues MMAs; warps 2..9 each own 16 selected rows of
+// a tile: they translate each selection to its cache slot, load their half rows
+// straight into registers, and convert them e4m3 (or NVFP4) -> bf16 (QK
+// operand) and -> fp16 (PV operand) into 128-byte-swizzled tiles of a 4-slot
+// ring; warps 10..13 run the softmax (P in fp16); all 12 math warps write the
+// output (or the fp16 partial for the LSE combine).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -34,14 +37,11 @@ namespace dsa {
 
 
 namespace mla {
-constexpr int RAW_STRIDE = 592;                   // FP8 rows 576 + 16 (NVFP4 rows 352 + 16): conflict-free reads
-constexpr int OFF_RAW = 0;
-constexpr int RAW_BYTES = kSelTile * RAW_STRIDE;  // 75,776
-constexpr int QSLOTS = 3;
-constexpr int OFF_Q = 76800;                      // QSLOTS x [96 x 128 B] (1024-aligned slots)
-constexpr int Q_SLOT = kMlaHeads * 128;           // 12 KB
-constexpr int RSLOTS = 3;
-constexpr int OFF_RING = OFF_Q + QSLOTS * Q_SLOT; // RSLOTS x 16 KB: C chunks (QK) then V half-blocks (PV)
+constexpr int QCHUNKS = kLatDim / 64;             // 9 chunks of 64 dims
+constexpr int Q_SLOT = kMlaHeads * 128;           // 12 KB: [96 heads x 128 B], 128-byte swizzle
+constexpr int OFF_Q = 0;                          // the whole query; the output staging after the last MMA
+constexpr int RSLOTS = 4;
+constexpr int OFF_RING = QCHUNKS * Q_SLOT;        // RSLOTS x 16 KB: C chunks (QK) then V half-blocks (PV)
 constexpr int RING_SLOT = 16384;
 constexpr int OFF_P = OFF_RING + RSLOTS * RING_SLOT;   // P^T: 2 head atoms x 16 token groups x 1 KB
 constexpr int P_BYTES = 2 * 16 * 1024;
@@ -50,21 +50,22 @@ constexpr int OFF_RED2 = OFF_RED + 4 * 96 * 4;    // 4 x 96 floats
 constexpr int OFF_MUSE = OFF_RED2 + 4 * 96 * 4;   // 96 floats
 constexpr int OFF_ALPHA = OFF_MUSE + 96 * 4;      // 96 floats
 constexpr int OFF_LFIN = OFF_ALPHA + 96 * 4;      // 96 floats
-constexpr int OFF_ROWOK = OFF_LFIN + 96 * 4;      // 128 bytes: selected row present in the raw tile
-constexpr int OFF_BARS = OFF_ROWOK + 128;
+constexpr int OFF_ROWOK = OFF_LFIN + 96 * 4;      // 2 x 128 bytes: selected row present (by tile parity)
+constexpr int OFF_BARS = OFF_ROWOK + 256;
 constexpr int N_BARS = 24;
 constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
-constexpr int THREADS = 448;                      // producer, MMA, 8 converter warps, 4 softmax warps
+constexpr int THREADS = 448;                      // q loader, MMA, 8 converter warps, 4 softmax warps
+// 14 warps put 4 on two of the SM's four register-file quarters (16K registers
+// each): 128 registers per thread at most.
 constexpr int CONV_WARPS = 8;
 constexpr int SOFT_WARP0 = 2 + CONV_WARPS;        // first softmax warp
 constexpr int TMEM_COLS = 512;
 constexpr int S_COL = 0;
 constexpr int O_COL = 128;
-constexpr int FILLS = kLatDim / 64 + 8;           // ring fills per tile: 9 C chunks + 8 V half-blocks
 constexpr float TAU = 8.0f;                       // log2 headroom before the running max moves
-static_assert(OFF_Q % 1024 == 0 && OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "align");
-static_assert(OFF_Q >= RAW_BYTES, "raw");
+static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "align");
+static_assert(kMlaHeads * kVDim * 2 <= OFF_RING, "output staging fits the query region");
 static_assert(SMEM_BYTES <= 232448, "smem");
 }  // namespace mla
 
@@ -153,6 +154,11 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
+// An empty asm that "modifies" v: code using v cannot be moved above this point.
+__device__ __forceinline__ void pin_after_wait(uint4& v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+}
+
 __device__ __forceinline__ void sts128(uint8_t* p, const uint32_t* v) {
   *reinterpret_cast<uint4*>(p) = make_uint4(v[0], v[1], v[2], v[3]);
 }
@@ -163,21 +169,19 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   using namespace mla;
   constexpr bool NV = LATF == 1;
   constexpr int ROWB = NV ? 352 : kLatDim;             // bytes per latent record
-  constexpr int RSTR = NV ? 368 : RAW_STRIDE;          // staging stride of a raw row
+  constexpr int NRAW = NV ? QCHUNKS : 2 * QCHUNKS;     // 16-byte registers of a half row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024_mla(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
-  uint64_t* raw_full = bars + 0;
-  uint64_t* raw_empty = bars + 1;
-  uint64_t* q_full = bars + 2;      // [QSLOTS]
-  uint64_t* q_empty = bars + 6;     // [QSLOTS]
-  uint64_t* ring_full = bars + 10;  // [RSLOTS]
-  uint64_t* ring_empty = bars + 14; // [RSLOTS]
-  uint64_t* s_full = bars + 18;
-  uint64_t* s_free = bars + 19;
-  uint64_t* p_full = bars + 20;
-  uint64_t* o_done = bars + 21;
-  uint64_t* drain = bars + 22;
+  uint64_t* q_full = bars + 0;
+  uint64_t* rows_ready = bars + 1;
+  uint64_t* ring_full = bars + 2;   // [RSLOTS]
+  uint64_t* ring_empty = bars + 6;  // [RSLOTS]
+  uint64_t* s_full = bars + 10;
+  uint64_t* s_free = bars + 11;
+  uint64_t* p_full = bars + 12;
+  uint64_t* o_done = bars + 13;
+  uint64_t* drain = bars + 14;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   int* rescale_sh = reinterpret_cast<int*>(smem + OFF_MISC + 16);
@@ -195,12 +199,8 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   const int32_t* phys_row = p.phys ? p.phys + static_cast<int64_t>(t) * p.topk : nullptr;
   const int32_t* sel_row = phys_row ? phys_row : idx_row;   // both use -1 padding
   if (threadIdx.x == 0) {
-    mbar_init(raw_full, 1);
-    mbar_init(raw_empty, CONV_WARPS);
-    for (int i = 0; i < QSLOTS; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
-    }
+    mbar_init(q_full, 1);
+    mbar_init(rows_ready, CONV_WARPS);
     for (int i = 0; i < RSLOTS; ++i) {
       mbar_init(&ring_full[i], CONV_WARPS);
       mbar_init(&ring_empty[i], 1);
@@ -212,6 +212,11 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     mbar_init(drain, 1);
     *abortf = 0;
     fence_mbar_init();
+    // the query is an input of the call, not of the kernel before: load it now
+    prefetch_tensormap(&qmap);
+    mbar_arrive_expect_tx(q_full, QCHUNKS * Q_SLOT);
+    for (int kc = 0; kc < QCHUNKS; ++kc)
+      tma_load_2d(smem + OFF_Q + kc * Q_SLOT, &qmap, q_full, kc * 64, t * kMlaHeads);
   }
   if (warp == 1) tmem_alloc(tslot, TMEM_COLS);
   // The set-up above overlaps the end of the kernel that writes the selection.
@@ -234,116 +239,27 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   if (j0 >= j1) {
     // nothing selected for this split: an empty partial (weight 0 in the combine)
     if (p.nsplit > 1 && threadIdx.x < kMlaHeads) p.part_ml[ts * kMlaHeads + threadIdx.x] = make_float2(-INFINITY, 0.f);
-  } else if (warp == 0) {
-    // --------------------------------------------------------------- producer
-    if (lane == 0) prefetch_tensormap(&qmap);
-    int req = __ldg(p.b.q_req + t);
-    const int pos = __ldg(p.b.q_pos + t);
-    if (req < 0 || req >= p.b.B) {
-      if (lane == 0) atomicOr(p.status, DEV_BAD_BATCH);
-      req = req < 0 ? 0 : p.b.B - 1;
-    }
-    const int64_t s_lim = static_cast<int64_t>(p.b.bt_stride) << p.pool.log2_bs;   // positions the table covers
-    const int32_t* btrow = p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride;
-    const int bsm = p.pool.bs - 1;
-    int qc = 0;
-    bool ok = true;
-    int issued_tiles = 0;
-    for (int j = j0; j < j1 && ok; ++j) {
-      const int jt = j - j0;
-      if (jt > 0 && !(ok = mbar_wait(raw_empty, (jt - 1) & 1, ab))) break;
-      const uint8_t* src[4];
-      uint32_t nrow = 0;
-      // every selected entry of this lane's four rows is loaded before any is used
-      int sel[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e = j * kSelTile + lane + 32 * i;
-        sel[i] = e < p.topk ? __ldcg(sel_row + e) : -1;
-      }
-      int rowid[4];
-      if (!phys_row) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int s = sel[i];
-          const bool in = s >= 0 && s <= pos && s < s_lim;
-          rowid[i] = in ? __ldg(btrow + (s >> p.pool.log2_bs)) : -1;
-          if (s >= 0 && !in) atomicOr(p.status, DEV_BAD_BATCH);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane + 32 * i;
-        src[i] = nullptr;
-        const int sv = sel[i];
-        if (sv >= 0) {
-          int row, slot;
-          if (phys_row) {
-            row = sv >> p.pool.log2_bs;   // physical slot from the top-k: no block-table lookup
-            slot = sv & bsm;
-          } else {
-            row = rowid[i];
-            slot = sv & bsm;
-          }
-          const bool present = phys_row || (sv <= pos && sv < s_lim);
-          if (present) {
-            if (row < 0 || row >= p.pool.num_rows) {
-              atomicOr(p.status, DEV_BAD_BLOCK);
-            } else {
-              src[i] = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.lat_off +
-                       static_cast<int64_t>(slot) * ROWB;
-              ++nrow;
-            }
-          }
-        }
-        rowok[r] = src[i] != nullptr;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) nrow += __shfl_xor_sync(0xffffffffu, nrow, o);
-      __threadfence_block();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(raw_full, nrow * ROWB);
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (src[i]) bulk_load(smem + OFF_RAW + (lane + 32 * i) * RSTR, src[i], ROWB, raw_full);
-      ++issued_tiles;
-      // q in 9 chunks of 64 dims through the 4-slot ring
-      for (int kc = 0; kc < kLatDim / 64 && ok; ++kc, ++qc) {
-        const int slot = qc % QSLOTS;
-        if (qc >= QSLOTS) ok = mbar_wait(&q_empty[slot], ((qc / QSLOTS) - 1) & 1, ab);
-        if (ok && lane == 0) {
-          mbar_arrive_expect_tx(&q_full[slot], Q_SLOT);
-          tma_load_2d(smem + OFF_Q + slot * Q_SLOT, &qmap, &q_full[slot], kc * 64, t * kMlaHeads);
-        }
-        __syncwarp();
-      }
-    }
-    if (!ok && issued_tiles > 0) drain_wait(raw_full, (issued_tiles - 1) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(1, 1, false, false, 128, kMlaHeads);
       const uint32_t idesc_pv = make_idesc(0, 0, true, true, 128, kMlaHeads);
-      int fc = 0, qc = 0;
-      bool ok = true;
+      int fc = 0;
+      bool ok = mbar_wait(q_full, 0, ab);
       for (int j = j0; j < j1 && ok; ++j) {
         const int jt = j - j0;
         if (jt > 0 && !(ok = mbar_wait(s_free, (jt - 1) & 1, ab))) break;
-        for (int kc = 0; kc < kLatDim / 64; ++kc, ++fc, ++qc) {
+        for (int kc = 0; kc < QCHUNKS; ++kc, ++fc) {
           const int slot = fc % RSLOTS;
-          const int qs = qc % QSLOTS;
           if (!(ok = mbar_wait(&ring_full[slot], (fc / RSLOTS) & 1, ab))) break;
-          if (!(ok = mbar_wait(&q_full[qs], (qc / QSLOTS) & 1, ab))) break;
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + OFF_RING + slot * RING_SLOT);
-          const uint32_t b0 = smem_u32(smem + OFF_Q + qs * Q_SLOT);
+          const uint32_t b0 = smem_u32(smem + OFF_Q + kc * Q_SLOT);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f16(tmem + S_COL, make_sdesc_sw128(a0 + 32 * kk, 16, 1024), make_sdesc_sw128(b0 + 32 * kk, 16, 1024),
                     idesc_qk, (kc | kk) ? 1u : 0u);
           tc_commit(&ring_empty[slot]);
-          tc_commit(&q_empty[qs]);
         }
         if (!ok) break;
         tc_commit(s_full);
@@ -372,93 +288,134 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         drain_wait(drain, 0);
       }
     }
-  } else if (warp < SOFT_WARP0) {
+  } else if (warp >= 2 && warp < SOFT_WARP0) {
     // ----------------------------------------------------- converters (2..9)
     const int ct = threadIdx.x - 64;            // 0..255
+    const int row = ct >> 1, hf = ct & 1;       // this thread's half row: dims [64 kc + 32 hf, +32) of each chunk kc
+    const int vg = (ct >> 5) >> 2;              // V half-block of this warp's rows: tokens [64 vg, +64)
+    const int tl = row & 63;
+    const int bsm = p.pool.bs - 1;
+    int pos = 0;
+    int64_t s_lim = 0;
+    const int32_t* btrow = nullptr;
+    if (!phys_row) {   // logical positions: translate through the block table
+      int req = __ldg(p.b.q_req + t);
+      pos = __ldg(p.b.q_pos + t);
+      if (req < 0 || req >= p.b.B) {
+        if (ct == 0) atomicOr(p.status, DEV_BAD_BATCH);
+        req = req < 0 ? 0 : p.b.B - 1;
+      }
+      s_lim = static_cast<int64_t>(p.b.bt_stride) << p.pool.log2_bs;   // positions the table covers
+      btrow = p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride;
+    }
     int fc = 0;
     bool ok = true;
     for (int j = j0; j < j1 && ok; ++j) {
       const int jt = j - j0;
-      if (!(ok = mbar_wait(raw_full, jt & 1, ab))) break;
-      const uint8_t* raw = smem + OFF_RAW;
-      // C chunks (bf16, K-major, 128-byte swizzle): threads 2r, 2r+1 convert row r
-      {
-        const int row = ct >> 1, hf = ct & 1;
-        const bool valid = rowok[row] != 0;
-        for (int kc = 0; kc < kLatDim / 64; ++kc, ++fc) {
-          const int slot = fc % RSLOTS;
-          if (fc >= RSLOTS && !(ok = mbar_wait(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
-          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (row >> 3) * 1024;
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const int q4 = 2 * hf + q2;          // dims 64 kc + 16 q4 .. +16
-            uint32_t o[8];
-            if (valid) {
-              if (NV) {
-                const uint2 in = *reinterpret_cast<const uint2*>(raw + row * RSTR + kc * 32 + q4 * 8);
-                nvfp4x16_to_bf16(in, raw[row * RSTR + 288 + kc * 4 + q4], o);
-              } else {
-                const uint4 in = *reinterpret_cast<const uint4*>(raw + row * RSTR + kc * 64 + q4 * 16);
-                e4m3x16_to_bf16(in, o);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] = 0;
-            }
-            sts128(dst + sw128_off(row & 7, 2 * q4), o);
-            sts128(dst + sw128_off(row & 7, 2 * q4 + 1), o + 4);
+      // selected entry -> latent record
+      const int e = j * kSelTile + row;
+      const int sv = e < p.topk ? __ldcg(sel_row + e) : -1;
+      const uint8_t* src = nullptr;
+      if (sv >= 0) {
+        int prow = -1;
+        bool present = true;
+        if (phys_row) {
+          prow = sv >> p.pool.log2_bs;   // physical slot from the top-k: no block-table lookup
+        } else {
+          present = sv <= pos && sv < s_lim;
+          if (present)
+            prow = __ldg(btrow + (sv >> p.pool.log2_bs));
+          else if (hf == 0)
+            atomicOr(p.status, DEV_BAD_BATCH);
+        }
+        if (present) {
+          if (prow < 0 || prow >= p.pool.num_rows) {
+            if (hf == 0) atomicOr(p.status, DEV_BAD_BLOCK);
+          } else {
+            src = p.pool.pool + static_cast<int64_t>(prow) * p.pool.row_stride + p.pool.lat_off +
+                  static_cast<int64_t>(sv & bsm) * ROWB;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ring_full[slot]);
         }
       }
-      if (!ok) break;
-      // V half-blocks (fp16, MN-major): block v = dims [128v, +128), half kh = tokens [64kh, +64);
-      // thread -> (token tl, 32-dim quarter dq)
-      for (int v = 0; v < 4 && ok; ++v) {
-        for (int kh = 0; kh < 2; ++kh, ++fc) {
-          const int slot = fc % RSLOTS;
-          if (fc >= RSLOTS && !(ok = mbar_wait(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
-          const int tl = ct >> 2;            // token within the half (0..63)
-          const int dq = ct & 3;             // 32-dim quarter of the block
-          const int row = kh * 64 + tl;
-          const bool rv = rowok[row] != 0;
-          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (dq >> 1) * 8192 + (tl >> 3) * 1024;
+      // the half row, all loads in flight at once (zeros for an absent row)
+      uint4 raw[NRAW];
+      uint32_t scl[NV ? QCHUNKS : 1];
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const int q4 = 2 * (dq & 1) + q2;  // 16-dim piece within the 64-dim atom
-            uint32_t o[8];
-            if (rv) {
-              const int d0 = v * 128 + (dq >> 1) * 64 + q4 * 16;   // first of 16 dims
-              if (NV) {
-                const uint2 in = *reinterpret_cast<const uint2*>(raw + row * RSTR + d0 / 2);
-                nvfp4x16_to_f16(in, raw[row * RSTR + 288 + d0 / 16], o);
-              } else {
-                const uint4 in = *reinterpret_cast<const uint4*>(raw + row * RSTR + d0);
-                e4m3x16_to_f16(in, o);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] = 0;
-            }
-            sts128(dst + sw128_off(tl & 7, 2 * q4), o);
-            sts128(dst + sw128_off(tl & 7, 2 * q4 + 1), o + 4);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ring_full[slot]);
-        }
+      for (int i = 0; i < NRAW; ++i) {
+        const int off = NV ? 32 * i + 16 * hf : 64 * (i >> 1) + 32 * hf + 16 * (i & 1);
+        raw[i] = src ? __ldg(reinterpret_cast<const uint4*>(src + off)) : make_uint4(0, 0, 0, 0);
       }
-      if (!ok) break;
+      if (NV) {
+#pragma unroll
+        for (int kc = 0; kc < QCHUNKS; ++kc)
+          scl[kc] = src ? __ldg(reinterpret_cast<const uint16_t*>(src + 288 + 4 * kc + 2 * hf)) : 0u;
+      }
+      if (hf == 0) rowok[(jt & 1) * kSelTile + row] = src != nullptr;
       __syncwarp();
-      if (lane == 0) mbar_arrive(raw_empty);
+      if (lane == 0) mbar_arrive(rows_ready);
+      // C chunks (bf16, K-major, 128-byte swizzle): 128 rows x 64 dims per ring slot
+#pragma unroll
+      for (int kc = 0; kc < QCHUNKS; ++kc, ++fc) {
+        const int slot = fc % RSLOTS;
+        if (fc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
+        uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (row >> 3) * 1024;
+        // keep the conversion after the wait: hoisted, all chunks' results would be live at once
+        pin_after_wait(raw[NV ? kc : 2 * kc]);
+        if (!NV) pin_after_wait(raw[2 * kc + 1]);
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int q4 = 2 * hf + q2;          // 16-dim piece of the chunk
+          uint32_t o[8];
+          if (NV)
+            nvfp4x16_to_bf16(q2 ? make_uint2(raw[kc].z, raw[kc].w) : make_uint2(raw[kc].x, raw[kc].y),
+                             (scl[kc] >> (8 * q2)) & 0xFFu, o);
+          else
+            e4m3x16_to_bf16(raw[2 * kc + q2], o);
+          sts128(dst + sw128_off(row & 7, 2 * q4), o);
+          sts128(dst + sw128_off(row & 7, 2 * q4 + 1), o + 4);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring_full[slot]);
+      }
+      if (!ok) break;
+      // V half-blocks (fp16, MN-major): block v = dims [128v, +128), half vg = tokens [64vg, +64).
+      // The warps of rows 0..63 fill the even ring fills, those of rows 64..127 the odd ones;
+      // four warps complete a fill, each arriving twice.
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int myfc = fc + 2 * v + vg;
+        const int slot = myfc % RSLOTS;
+        if (myfc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((myfc / RSLOTS) - 1) & 1, ab))) break;
+        uint8_t* base = smem + OFF_RING + slot * RING_SLOT + (tl >> 3) * 1024;
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {          // 64-dim atom a = chunk 2v + a
+          const int kc = 2 * v + a;
+          pin_after_wait(raw[NV ? kc : 2 * kc]);
+          if (!NV) pin_after_wait(raw[2 * kc + 1]);
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int q4 = 2 * hf + q2;        // 16-dim piece within the atom
+            uint32_t o[8];
+            if (NV)
+              nvfp4x16_to_f16(q2 ? make_uint2(raw[kc].z, raw[kc].w) : make_uint2(raw[kc].x, raw[kc].y),
+                              (scl[kc] >> (8 * q2)) & 0xFFu, o);
+            else
+              e4m3x16_to_f16(raw[2 * kc + q2], o);
+            sts128(base + a * 8192 + sw128_off(tl & 7, 2 * q4), o);
+            sts128(base + a * 8192 + sw128_off(tl & 7, 2 * q4 + 1), o + 4);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cnt(&ring_full[slot], 2);
+      }
+      fc += 8;
     }
-  } else {
+  } else if (warp >= SOFT_WARP0) {
     // ---------------------------------------------- softmax warps (10..13)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;          // token lane within the tile
-    const int mt = threadIdx.x - 32 * SOFT_WARP0;   // 0..127
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float m_run[3] = {-INFINITY, -INFINITY, -INFINITY};   // per head (lane + 32 i), log2 units
     float l_run[3] = {0.f, 0.f, 0.f};                      // first softmax warp only: running sums
@@ -467,9 +424,9 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     for (int j = j0; j < j1 && ok; ++j) {
       const int jt = j - j0;
       if (!(ok = mbar_wait(s_full, jt & 1, ab))) break;
-      if (!(ok = mbar_wait(raw_full, jt & 1, ab))) break;   // rowok of this tile
+      if (!(ok = mbar_wait(rows_ready, jt & 1, ab))) break;   // rowok of this tile
       tc_fence_after();
-      const bool valid = rowok[r] != 0;
+      const bool valid = rowok[(jt & 1) * kSelTile + r] != 0;
       // tile maxima per head: warp butterfly, then the 4 warps through shared memory
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
@@ -506,8 +463,9 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       if (jt > 0 && !(ok = mbar_wait(o_done, (jt - 1) & 1, ab))) break;
       if (any_rescale) {
         tc_fence_after();
+#pragma unroll 1
         for (int v = 0; v < 4; ++v) {
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < 3; ++c) {
             uint32_t rr[32];
             const uint32_t ta = tmem + O_COL + 96 * v + 32 * c + lane_off;
@@ -585,7 +543,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     // a failed wait sets the CTA abort flag before this barrier, so the test is uniform
     if (!*reinterpret_cast<volatile int*>(abortf)) {
       tc_fence_after();
-      uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_RAW);   // raw tile and q ring are free now
+      uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_Q);   // the query is no longer read
       const bool final_out = p.nsplit == 1;
       for (int pc = which; pc < 12; pc += 3) {       // (block v, head chunk c) pairs
         const int v = pc / 3, c = pc % 3;
@@ -622,6 +580,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       }
     }
   }
+  if (threadIdx.x == 0) drain_wait(q_full, 0);   // no copy into shared memory outlives the CTA
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);

@@ -57,6 +57,13 @@ __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
                : "memory");
   return v;
 }
+// Atomic add into the shared memory of a CTA of the cluster (no return value).
+__device__ __forceinline__ void red_cluster_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -88,6 +95,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// Arrive counting `cnt` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t cnt) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+               "r"(cnt)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
                    smem_u32(bar)),
@@ -112,9 +126,10 @@ struct Abort {
 };
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
-// false) when another role of the CTA already gave up, or after kWaitLimitNs,
-// in which case it records DEV_TIMEOUT.  Never traps.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort ab) {
+// false) when another role of the CTA already gave up, or after
+// kWaitLimitCycles, in which case it records DEV_TIMEOUT.  Never traps.
+// Inlined form, for loops that keep many registers live (a call would spill them).
+__device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity, Abort ab) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const long long t0 = clock64();
@@ -129,6 +144,10 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Ab
       }
     }
   }
+}
+
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort ab) {
+  return mbar_wait_inline(bar, parity, ab);
 }
 
 // Wait ignoring the CTA abort flag, for draining copies/MMAs in flight before an

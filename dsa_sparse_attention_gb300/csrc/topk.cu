@@ -23,8 +23,10 @@
 // Rows of at most 65,536 scores take a one-launch path instead: a cluster of up
 // to eight CTAs per row keeps the row in registers (16 scores per thread) and
 // resolves all three digits (11 + 11 + 10 bits) of the threshold key, the
-// position cut and the output offsets through histograms read across the
-// cluster's shared memory; it needs no global scratch and no zeroing.
+// position cut and the output offsets; each CTA adds the non-empty bins of its
+// histograms into every CTA's copy of the merged histogram through distributed
+// shared memory, so each digit costs one cluster barrier.  It needs no global
+// scratch and no zeroing.
 #include "params.cuh"
 
 namespace dsa {
@@ -394,59 +396,31 @@ constexpr int kClSlice = kClThreads * kPerThread;   // 8192 scores per CTA
 constexpr int kClMaxCtas = 8;                       // portable cluster size
 constexpr int kClMaxRow = kClSlice * kClMaxCtas;    // 65,536
 
-// The bin of the merged (cluster-wide) histogram `hist` holding the kk-th
-// largest key, and the number of keys in higher bins.  Thread i owns bins
-// [2044 - 4i, 2048 - 4i), so thread order is descending bin order.
-__device__ void cluster_find(const uint32_t* hist, uint32_t csize, uint32_t kk, int& bin, uint32_t& above,
-                             uint32_t* sh) {
-  const int lo = kBins - 4 * (static_cast<int>(threadIdx.x) + 1);
-  const uint32_t a = smem_u32(hist + lo);
-  uint4 m = make_uint4(0, 0, 0, 0);
-  for (uint32_t r = 0; r < csize; ++r) {
-    const uint4 v = ld_cluster_v4(cluster_map(a, r));
-    m.x += v.x;
-    m.y += v.y;
-    m.z += v.z;
-    m.w += v.w;
+// Adds this CTA's histogram `hl` into the merged histogram `hm` of every CTA of
+// the cluster (only its non-empty bins travel).
+__device__ __forceinline__ void push_hist(const uint32_t* hl, uint32_t* hm, uint32_t csize) {
+  for (int b = threadIdx.x; b < kBins; b += blockDim.x) {
+    const uint32_t c = hl[b];
+    if (c == 0) continue;
+    const uint32_t a = smem_u32(hm + b);
+    for (uint32_t r = 0; r < csize; ++r) red_cluster_add(cluster_map(a, r), c);
   }
-  const uint32_t local = m.x + m.y + m.z + m.w;
-  uint32_t total;
-  const uint32_t excl = block_excl_scan(local, sh, total);
-  if (excl < kk && excl + local >= kk) {
-    // walk bins lo+3 .. lo
-    uint32_t cum = excl;
-    int b = lo + 3;
-    if (cum + m.w < kk) {
-      cum += m.w;
-      --b;
-      if (cum + m.z < kk) {
-        cum += m.z;
-        --b;
-        if (cum + m.y < kk) {
-          cum += m.y;
-          --b;
-        }
-      }
-    }
-    sh[33] = static_cast<uint32_t>(b);
-    sh[34] = cum;
-  }
-  __syncthreads();
-  bin = static_cast<int>(sh[33]);
-  above = sh[34];
-  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) {
-  __shared__ __align__(16) uint32_t h[3][kBins];   // this CTA's histograms of digits 1, 2, 3
+  __shared__ __align__(16) uint32_t hl[3][kBins];   // this CTA's histograms of digits 1, 2, 3
+  __shared__ __align__(16) uint32_t hm[3][kBins];   // the same summed over the cluster
   __shared__ uint32_t sh[48];
-  __shared__ uint32_t counts;                      // (keys above T) << 16 | (keys equal to T)
+  __shared__ uint32_t counts[kClMaxCtas];           // per CTA: (keys above T) << 16 | (keys equal to T)
   const int t = blockIdx.y;
   const uint32_t rank = cluster_rank(), csize = cluster_size();
   int req, pos;
   load_token(p.b, t, p.status, req, pos);
   const int n = pos + 1;
-  for (int i = threadIdx.x; i < 3 * kBins; i += kClThreads) h[0][i] = 0;
+  for (int i = threadIdx.x; i < 3 * kBins; i += kClThreads) {
+    hl[0][i] = 0;
+    hm[0][i] = 0;
+  }
   grid_dep_wait();
   grid_dep_launch();
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.k;
@@ -471,29 +445,44 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   uint32_t u[kPerThread];
   load16(row, s0, s0 + nv, u);
   __syncthreads();   // histograms zeroed
+  const bool multi = csize > 1;
+  if (multi) cluster_arrive();   // ... in every CTA before any CTA adds into them
 
   // digit 1: bits 31..21
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i)
-    if (i < nv) atomicAdd(&h[0][u[i] >> 21], 1u);
-  cluster_sync();
+    if (i < nv) atomicAdd(&hl[0][u[i] >> 21], 1u);
+  __syncthreads();
+  if (multi) {
+    cluster_wait();
+    push_hist(hl[0], hm[0], csize);
+    cluster_sync();
+  }
   int b1, bA, bB;
   uint32_t a1, a2, a3;
   const uint32_t k = static_cast<uint32_t>(p.k);
-  cluster_find(h[0], csize, k, b1, a1, sh);
+  find_bin(multi ? hm[0] : hl[0], kBins, k, b1, a1, sh);
   // digit 2: bits 20..10 of the keys in digit b1
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i)
-    if (i < nv && (u[i] >> 21) == static_cast<uint32_t>(b1)) atomicAdd(&h[1][(u[i] >> 10) & 2047u], 1u);
-  cluster_sync();
-  cluster_find(h[1], csize, k - a1, bA, a2, sh);
+    if (i < nv && (u[i] >> 21) == static_cast<uint32_t>(b1)) atomicAdd(&hl[1][(u[i] >> 10) & 2047u], 1u);
+  __syncthreads();
+  if (multi) {
+    push_hist(hl[1], hm[1], csize);
+    cluster_sync();
+  }
+  find_bin(multi ? hm[1] : hl[1], kBins, k - a1, bA, a2, sh);
   // digit 3: bits 9..0 of the keys in digits (b1, bA)
   const uint32_t pre = (static_cast<uint32_t>(b1) << 11) | static_cast<uint32_t>(bA);
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i)
-    if (i < nv && (u[i] >> 10) == pre) atomicAdd(&h[2][u[i] & 1023u], 1u);
-  cluster_sync();
-  cluster_find(h[2], csize, k - a1 - a2, bB, a3, sh);
+    if (i < nv && (u[i] >> 10) == pre) atomicAdd(&hl[2][u[i] & 1023u], 1u);
+  __syncthreads();
+  if (multi) {
+    push_hist(hl[2], hm[2], csize);
+    cluster_sync();
+  }
+  find_bin(multi ? hm[2] : hl[2], 1024, k - a1 - a2, bB, a3, sh);
   const uint32_t T = (pre << 10) | static_cast<uint32_t>(bB);
   const uint32_t need_eq = k - a1 - a2 - a3;   // keys equal to T to take, lowest positions first
 
@@ -506,27 +495,21 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   }
   uint32_t tot;
   const uint32_t excl = block_excl_scan((gt << 16) | eq, sh, tot);
-  if (threadIdx.x == 0) counts = tot;
-  cluster_sync();
+  if (threadIdx.x < csize) st_cluster_u32(cluster_map(smem_u32(&counts[rank]), threadIdx.x), tot);
+  if (multi) cluster_sync();   // the last access to another CTA's shared memory is before this
+  else __syncthreads();
   // offsets of this CTA from the counts of the CTAs before it in the row
-  if (threadIdx.x == 0) {
-    uint32_t eq_before = 0, base = 0;
-    for (uint32_t r = 0; r < rank; ++r) {
-      const uint32_t c = ld_cluster_u32(cluster_map(smem_u32(&counts), r));
-      const uint32_t e = c & 0xFFFFu;
-      const uint32_t left = need_eq > eq_before ? need_eq - eq_before : 0u;
-      base += (c >> 16) + min(e, left);
-      eq_before += e;
-    }
+  uint32_t eq_before = 0, base = 0;
+  for (uint32_t r = 0; r < rank; ++r) {
+    const uint32_t c = counts[r];
+    const uint32_t e = c & 0xFFFFu;
     const uint32_t left = need_eq > eq_before ? need_eq - eq_before : 0u;
-    sh[35] = base;
-    sh[36] = min(tot & 0xFFFFu, left);   // equal keys this CTA takes
+    base += (c >> 16) + min(e, left);
+    eq_before += e;
   }
-  cluster_arrive();   // no shared memory of another CTA is read after this point
-  __syncthreads();
-  const uint32_t take = sh[36];
+  const uint32_t take = min(tot & 0xFFFFu, need_eq > eq_before ? need_eq - eq_before : 0u);   // equal keys taken here
   uint32_t eq_rank = excl & 0xFFFFu;
-  uint32_t o = sh[35] + (excl >> 16) + min(eq_rank, take);
+  uint32_t o = base + (excl >> 16) + min(eq_rank, take);
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i) {
     if (i >= nv) continue;
@@ -540,7 +523,6 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
     }
     ++o;
   }
-  cluster_wait();   // keep this CTA's shared memory alive until every CTA has read it
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained) {

@@ -22,6 +22,10 @@
 #include "../../include/dsa.h"
 #include "params.cuh"
 
+namespace dsa {
+dsa_status record_cuda_status(cudaError_t e);   // capi.cu: DSA_OK, or DSA_ERR_CUDA with the error recorded
+}
+
 namespace {
 
 constexpr size_t kNoAllocBytes = DSA_NOALLOC_SCRATCH_BYTES;
@@ -75,7 +79,7 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_kv_layout* layout, const dsa_ba
   if (256 + L.total > kNoAllocBytes) return DSA_ERR_WORKSPACE;   // batch too large for the fixed scratch
 
   uint8_t* base = static_cast<uint8_t*>(scratch_address());
-  if (!base) return DSA_ERR_CUDA;
+  if (!base) return record_cuda_status(cudaErrorInvalidSymbol);
 
   TopkParams p;
   p.b.T = T;
@@ -94,5 +98,5 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_kv_layout* layout, const dsa_ba
   p.phys = phys_slots;
   p.log2_bs = log2_bs;
   p.status = reinterpret_cast<uint32_t*>(base);
-  return launch_topk(p, stream, false) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return record_cuda_status(launch_topk(p, stream, false));
 }

@@ -129,6 +129,15 @@ int32_t dsa_abi_version(void);
 const char *dsa_status_string(dsa_status status);
 
 /*
+ * The CUDA error behind the last DSA_ERR_CUDA that a call returned on the
+ * calling host thread: the cudaError_t value of the failing runtime call (0 if
+ * none yet), or -1 when encoding a TMA tensor map failed.  If `name` is not
+ * NULL it receives the error's name (static storage).  Later successful calls
+ * do not clear it.
+ */
+int32_t dsa_last_cuda_error(const char **name);
+
+/*
  * Bytes of device workspace the calls below need for this layout/batch/topk
  * (the maximum over all calls; 256-byte aligned).  0 on invalid arguments.
  * The first 256 bytes hold the status word, which persists across calls until

@@ -31,6 +31,7 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
     assert dsa.dsa_abi_version() == 1
     assert dsa.dsa_status_string(-6) == "DSA_ERR_DEVICE_CHECK"
+    assert dsa.dsa_last_cuda_error() == (0, "no error")
 
 
 def _layout(**kw):
