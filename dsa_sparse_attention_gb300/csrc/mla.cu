@@ -14,7 +14,8 @@
 //   O^T[dim, head]  += V^T[dim, token] . P^T[token, head]     M=128 (x4 dim blocks), N=96, K=128 (f16 x f16)
 // TMEM: S^T in columns [0, 96), O^T blocks at 128 + 96 v (v = 0..3): 480 of 512.
 // Softmax runs across TMEM lanes (tokens): per-head maxima with redux.sync.max.f32
-// and a 4-warp exchange; the running maximum is only moved when a tile exceeds
+// and a 4-warp exchange; per-head sums of P come from the tensor core (P^T
+// against a block of ones, into the S columns once P is written); the running maximum is only moved when a tile exceeds
 // it by more than 2^8 (the output is unchanged: the final normalisation uses the
 // same maximum), so O^T is rescaled in TMEM only on those rare tiles.
 // Roles: warp 0 loads the whole query (96 x 576 bf16) into shared memory with
@@ -45,9 +46,9 @@ constexpr int OFF_RING = QCHUNKS * Q_SLOT;        // RSLOTS x 16 KB: C chunks (Q
 constexpr int RING_SLOT = 16384;
 constexpr int OFF_P = OFF_RING + RSLOTS * RING_SLOT;   // P^T: 2 head atoms x 16 token groups x 1 KB
 constexpr int P_BYTES = 2 * 16 * 1024;
-constexpr int OFF_RED = OFF_P + P_BYTES;          // 4 x 96 floats
-constexpr int OFF_RED2 = OFF_RED + 4 * 96 * 4;    // 4 x 96 floats
-constexpr int OFF_MUSE = OFF_RED2 + 4 * 96 * 4;   // 96 floats
+constexpr int OFF_ONES = OFF_P + P_BYTES;         // one 8-row atom of fp16 ones (all rows of the sum operand)
+constexpr int OFF_RED = OFF_ONES + 1024;          // 4 x 96 floats
+constexpr int OFF_MUSE = OFF_RED + 4 * 96 * 4;    // 96 floats
 constexpr int OFF_ALPHA = OFF_MUSE + 96 * 4;      // 96 floats
 constexpr int OFF_LFIN = OFF_ALPHA + 96 * 4;      // 96 floats
 constexpr int OFF_ROWOK = OFF_LFIN + 96 * 4;      // 2 x 128 bytes: selected row present (by tile parity)
@@ -64,8 +65,8 @@ constexpr int TMEM_COLS = 512;
 constexpr int S_COL = 0;
 constexpr int O_COL = 128;
 constexpr float TAU = 8.0f;                       // log2 headroom before the running max moves
-static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "align");
-static_assert(kMlaHeads * kVDim * 2 <= OFF_RING, "output staging fits the query region");
+static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0 && OFF_ONES % 1024 == 0, "align");
+static_assert(kMlaHeads * kVDim * 2 <= OFF_RING && kVDim * 208 <= OFF_RING, "output staging fits the query region");
 static_assert(SMEM_BYTES <= 232448, "smem");
 }  // namespace mla
 
@@ -127,26 +128,6 @@ __device__ __forceinline__ void nvfp4x16_to_bf16(const uint2 in, uint32_t scale_
   }
 }
 
-// Butterfly "transpose" reductions over a warp: on entry every lane holds 32
-// values (one per head j); on exit lane l holds the reduction over all 32 lanes
-// of head l.  31 shuffles per 32 heads.  `v` is destroyed.
-template <bool MAX>
-__device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
-#pragma unroll
-    for (int j = 0; j < half; ++j) {
-      const float send = upper ? v[j] : v[j + half];
-      const float keep = upper ? v[j + half] : v[j];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, half);
-      v[j] = MAX ? fmaxf(keep, recv) : keep + recv;
-    }
-  }
-  return v[0];
-}
-
 // 2^x on the multi-function unit (relative error about 2^-22; subnormal results flush to 0).
 __device__ __forceinline__ float ex2_fast(float x) {
   float y;
@@ -154,9 +135,45 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
-// An empty asm that "modifies" v: code using v cannot be moved above this point.
-__device__ __forceinline__ void pin_after_wait(uint4& v) {
-  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+// One 64-dim chunk of a converter thread's half row: dims [64 kc + 32 hf, +32).
+// FP8: 32 bytes in a, b.  NVFP4: 16 bytes of packed values in a, the two e4m3
+// block scales in the low bytes of s.  An absent row reads as zeros.
+struct LatPiece {
+  uint4 a, b;
+  uint32_t s;
+};
+
+template <bool NV>
+__device__ __forceinline__ LatPiece load_piece(const uint8_t* src, int kc, int hf) {
+  LatPiece r;
+  r.a = r.b = make_uint4(0, 0, 0, 0);
+  r.s = 0;
+  if (src) {
+    if (NV) {
+      r.a = __ldg(reinterpret_cast<const uint4*>(src + 32 * kc + 16 * hf));
+      r.s = __ldg(reinterpret_cast<const uint16_t*>(src + 288 + 4 * kc + 2 * hf));
+    } else {
+      r.a = __ldg(reinterpret_cast<const uint4*>(src + 64 * kc + 32 * hf));
+      r.b = __ldg(reinterpret_cast<const uint4*>(src + 64 * kc + 32 * hf + 16));
+    }
+  }
+  return r;
+}
+
+// 16 values (piece q2 of the chunk) -> 8 packed bf16x2 / f16x2 words.
+template <bool NV>
+__device__ __forceinline__ void piece_to_bf16(const LatPiece& c, int q2, uint32_t (&o)[8]) {
+  if (NV)
+    nvfp4x16_to_bf16(q2 ? make_uint2(c.a.z, c.a.w) : make_uint2(c.a.x, c.a.y), (c.s >> (8 * q2)) & 0xFFu, o);
+  else
+    e4m3x16_to_bf16(q2 ? c.b : c.a, o);
+}
+template <bool NV>
+__device__ __forceinline__ void piece_to_f16(const LatPiece& c, int q2, uint32_t (&o)[8]) {
+  if (NV)
+    nvfp4x16_to_f16(q2 ? make_uint2(c.a.z, c.a.w) : make_uint2(c.a.x, c.a.y), (c.s >> (8 * q2)) & 0xFFu, o);
+  else
+    e4m3x16_to_f16(q2 ? c.b : c.a, o);
 }
 
 __device__ __forceinline__ void sts128(uint8_t* p, const uint32_t* v) {
@@ -169,7 +186,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   using namespace mla;
   constexpr bool NV = LATF == 1;
   constexpr int ROWB = NV ? 352 : kLatDim;             // bytes per latent record
-  constexpr int NRAW = NV ? QCHUNKS : 2 * QCHUNKS;     // 16-byte registers of a half row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024_mla(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
@@ -182,11 +198,11 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   uint64_t* p_full = bars + 12;
   uint64_t* o_done = bars + 13;
   uint64_t* drain = bars + 14;
+  uint64_t* sum_done = bars + 15;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   int* rescale_sh = reinterpret_cast<int*>(smem + OFF_MISC + 16);
   float* red = reinterpret_cast<float*>(smem + OFF_RED);
-  float* red2 = reinterpret_cast<float*>(smem + OFF_RED2);
   float* m_use = reinterpret_cast<float*>(smem + OFF_MUSE);
   float* alpha_sh = reinterpret_cast<float*>(smem + OFF_ALPHA);
   float* l_fin = reinterpret_cast<float*>(smem + OFF_LFIN);
@@ -210,14 +226,18 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(sum_done, 1);
     *abortf = 0;
     fence_mbar_init();
     // the query is an input of the call, not of the kernel before: load it now
     prefetch_tensormap(&qmap);
     mbar_arrive_expect_tx(q_full, QCHUNKS * Q_SLOT);
+    #pragma unroll 1
     for (int kc = 0; kc < QCHUNKS; ++kc)
       tma_load_2d(smem + OFF_Q + kc * Q_SLOT, &qmap, q_full, kc * 64, t * kMlaHeads);
   }
+  for (int i = threadIdx.x; i < 256; i += THREADS) reinterpret_cast<uint32_t*>(smem + OFF_ONES)[i] = 0x3C003C00u;
+  fence_proxy_async_smem();   // the ones are read by the tensor core
   if (warp == 1) tmem_alloc(tslot, TMEM_COLS);
   // The set-up above overlaps the end of the kernel that writes the selection.
   grid_dep_wait();
@@ -244,11 +264,13 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(1, 1, false, false, 128, kMlaHeads);
       const uint32_t idesc_pv = make_idesc(0, 0, true, true, 128, kMlaHeads);
+      const uint32_t idesc_sum = make_idesc(0, 0, false, true, 128, kMlaHeads);
       int fc = 0;
       bool ok = mbar_wait(q_full, 0, ab);
       for (int j = j0; j < j1 && ok; ++j) {
         const int jt = j - j0;
         if (jt > 0 && !(ok = mbar_wait(s_free, (jt - 1) & 1, ab))) break;
+        #pragma unroll 1
         for (int kc = 0; kc < QCHUNKS; ++kc, ++fc) {
           const int slot = fc % RSLOTS;
           if (!(ok = mbar_wait(&ring_full[slot], (fc / RSLOTS) & 1, ab))) break;
@@ -265,6 +287,20 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         tc_commit(s_full);
         if (!(ok = mbar_wait(p_full, jt & 1, ab))) break;
         tc_fence_after();
+        // per-head sums of P: ones[128 x 128] . P^T into the S columns (every lane gets the sums);
+        // the ones operand is one atom repeated (8-row-group stride 0, same 32-byte K step)
+        {
+          const uint32_t o0 = smem_u32(smem + OFF_ONES);
+          const uint32_t b0 = smem_u32(smem + OFF_P);
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f16(tmem + S_COL, make_sdesc_sw128(o0 + 32 * k, 16, 0),
+                      make_sdesc_sw128(b0 + (kh * 8 + k * 2) * 1024, 16384, 1024), idesc_sum, (kh | k) ? 1u : 0u);
+          tc_commit(sum_done);
+        }
+        #pragma unroll 1
         for (int v = 0; v < 4 && ok; ++v) {
           for (int kh = 0; kh < 2; ++kh, ++fc) {
             const int slot = fc % RSLOTS;
@@ -337,79 +373,83 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           }
         }
       }
-      // the half row, all loads in flight at once (zeros for an absent row)
-      uint4 raw[NRAW];
-      uint32_t scl[NV ? QCHUNKS : 1];
-#pragma unroll
-      for (int i = 0; i < NRAW; ++i) {
-        const int off = NV ? 32 * i + 16 * hf : 64 * (i >> 1) + 32 * hf + 16 * (i & 1);
-        raw[i] = src ? __ldg(reinterpret_cast<const uint4*>(src + off)) : make_uint4(0, 0, 0, 0);
-      }
-      if (NV) {
-#pragma unroll
-        for (int kc = 0; kc < QCHUNKS; ++kc)
-          scl[kc] = src ? __ldg(reinterpret_cast<const uint16_t*>(src + 288 + 4 * kc + 2 * hf)) : 0u;
-      }
+      // Chunks are loaded through a short register pipeline inside rolled loops: the
+      // code runs once per tile, and unrolled it would be fetched cold every time.
+      // Pull this half row into L2 first so the chunk loads that follow all hit it.
+      if (src) bulk_prefetch_l2(src + hf * (ROWB / 2), ROWB / 2);
       if (hf == 0) rowok[(jt & 1) * kSelTile + row] = src != nullptr;
       __syncwarp();
       if (lane == 0) mbar_arrive(rows_ready);
-      // C chunks (bf16, K-major, 128-byte swizzle): 128 rows x 64 dims per ring slot
+      // C chunks (bf16, K-major, 128-byte swizzle): 128 rows x 64 dims per ring slot.
+      // Four chunks in flight; a slot is reloaded right after its chunk is used (a
+      // register copy of a load still in flight would wait for it).
+      LatPiece cb[4];
 #pragma unroll
-      for (int kc = 0; kc < QCHUNKS; ++kc, ++fc) {
-        const int slot = fc % RSLOTS;
-        if (fc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
-        uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (row >> 3) * 1024;
-        // keep the conversion after the wait: hoisted, all chunks' results would be live at once
-        pin_after_wait(raw[NV ? kc : 2 * kc]);
-        if (!NV) pin_after_wait(raw[2 * kc + 1]);
+      for (int u = 0; u < 4; ++u) cb[u] = load_piece<NV>(src, u, hf);
+#pragma unroll 1
+      for (int kb = 0; kb < QCHUNKS && ok; kb += 4) {
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          const int q4 = 2 * hf + q2;          // 16-dim piece of the chunk
-          uint32_t o[8];
-          if (NV)
-            nvfp4x16_to_bf16(q2 ? make_uint2(raw[kc].z, raw[kc].w) : make_uint2(raw[kc].x, raw[kc].y),
-                             (scl[kc] >> (8 * q2)) & 0xFFu, o);
-          else
-            e4m3x16_to_bf16(raw[2 * kc + q2], o);
-          sts128(dst + sw128_off(row & 7, 2 * q4), o);
-          sts128(dst + sw128_off(row & 7, 2 * q4 + 1), o + 4);
+        for (int u = 0; u < 4; ++u) {
+          const int kc = kb + u;
+          if (kc >= QCHUNKS) break;
+          const int slot = fc % RSLOTS;
+          if (fc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((fc / RSLOTS) - 1) & 1, ab))) break;
+          uint8_t* dst = smem + OFF_RING + slot * RING_SLOT + (row >> 3) * 1024;
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int q4 = 2 * hf + q2;          // 16-dim piece of the chunk
+            uint32_t o[8];
+            piece_to_bf16<NV>(cb[u], q2, o);
+            sts128(dst + sw128_off(row & 7, 2 * q4), o);
+            sts128(dst + sw128_off(row & 7, 2 * q4 + 1), o + 4);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ring_full[slot]);
+          ++fc;
+          if (kc + 4 < QCHUNKS) cb[u] = load_piece<NV>(src, kc + 4, hf);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ring_full[slot]);
       }
       if (!ok) break;
       // V half-blocks (fp16, MN-major): block v = dims [128v, +128), half vg = tokens [64vg, +64).
       // The warps of rows 0..63 fill the even ring fills, those of rows 64..127 the odd ones;
-      // four warps complete a fill, each arriving twice.
+      // four warps complete a fill, each arriving twice.  Two blocks' chunks in flight.
+      LatPiece vbuf[2][2];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int myfc = fc + 2 * v + vg;
-        const int slot = myfc % RSLOTS;
-        if (myfc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((myfc / RSLOTS) - 1) & 1, ab))) break;
-        uint8_t* base = smem + OFF_RING + slot * RING_SLOT + (tl >> 3) * 1024;
+      for (int u = 0; u < 2; ++u) {
+        vbuf[u][0] = load_piece<NV>(src, 2 * u, hf);
+        vbuf[u][1] = load_piece<NV>(src, 2 * u + 1, hf);
+      }
+#pragma unroll 1
+      for (int vb2 = 0; vb2 < 4 && ok; vb2 += 2) {
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {          // 64-dim atom a = chunk 2v + a
-          const int kc = 2 * v + a;
-          pin_after_wait(raw[NV ? kc : 2 * kc]);
-          if (!NV) pin_after_wait(raw[2 * kc + 1]);
+        for (int u = 0; u < 2; ++u) {
+          const int v = vb2 + u;
+          const int myfc = fc + 2 * v + vg;
+          const int slot = myfc % RSLOTS;
+          if (myfc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((myfc / RSLOTS) - 1) & 1, ab))) break;
+          uint8_t* base = smem + OFF_RING + slot * RING_SLOT + (tl >> 3) * 1024;
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const int q4 = 2 * hf + q2;        // 16-dim piece within the atom
-            uint32_t o[8];
-            if (NV)
-              nvfp4x16_to_f16(q2 ? make_uint2(raw[kc].z, raw[kc].w) : make_uint2(raw[kc].x, raw[kc].y),
-                              (scl[kc] >> (8 * q2)) & 0xFFu, o);
-            else
-              e4m3x16_to_f16(raw[2 * kc + q2], o);
-            sts128(base + a * 8192 + sw128_off(tl & 7, 2 * q4), o);
-            sts128(base + a * 8192 + sw128_off(tl & 7, 2 * q4 + 1), o + 4);
+          for (int a = 0; a < 2; ++a) {          // 64-dim atom a = chunk 2v + a
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const int q4 = 2 * hf + q2;        // 16-dim piece within the atom
+              uint32_t o[8];
+              piece_to_f16<NV>(vbuf[u][a], q2, o);
+              sts128(base + a * 8192 + sw128_off(tl & 7, 2 * q4), o);
+              sts128(base + a * 8192 + sw128_off(tl & 7, 2 * q4 + 1), o + 4);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cnt(&ring_full[slot], 2);
+          if (v + 2 < 4) {
+            vbuf[u][0] = load_piece<NV>(src, 2 * v + 4, hf);
+            vbuf[u][1] = load_piece<NV>(src, 2 * v + 5, hf);
           }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cnt(&ring_full[slot], 2);
       }
+      if (!ok) break;
       fc += 8;
     }
   } else if (warp >= SOFT_WARP0) {
@@ -427,16 +467,19 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       if (!(ok = mbar_wait(rows_ready, jt & 1, ab))) break;   // rowok of this tile
       tc_fence_after();
       const bool valid = rowok[(jt & 1) * kSelTile + r] != 0;
-      // tile maxima per head: warp butterfly, then the 4 warps through shared memory
-#pragma unroll
+      // tile maxima per head: one warp reduction per head, then the 4 warps through shared memory
+#pragma unroll 1
       for (int c = 0; c < 3; ++c) {
         uint32_t rr[32];
         DSA_TMEM_LD32(tmem + S_COL + 32 * c + lane_off, rr);
         tmem_wait_ld();
-        float tmp[32];
+        float mine = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tmp[i] = valid ? __uint_as_float(rr[i]) * p.scale_log2 : -INFINITY;
-        red[quarter * kMlaHeads + 32 * c + lane] = warp_transpose_reduce32<true>(tmp);
+        for (int i = 0; i < 32; ++i) {
+          const float m = warp_max_f32(valid ? __uint_as_float(rr[i]) * p.scale_log2 : -INFINITY);
+          if (lane == i) mine = m;
+        }
+        red[quarter * kMlaHeads + 32 * c + lane] = mine;
       }
       named_bar_sync(1, 128);
       if (warp == SOFT_WARP0) {
@@ -481,7 +524,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       // P^T row r (fp16), MN-major: heads contiguous in 16-byte chunks of 8; row sums per head
       {
         uint8_t* prow = smem + OFF_P + (r >> 3) * 1024;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 3; ++c) {
           uint32_t rr[32];
           DSA_TMEM_LD32(tmem + S_COL + 32 * c + lane_off, rr);
@@ -501,24 +544,36 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
             const int chunk = 4 * c + cc4;
             sts128(prow + (chunk >> 3) * 16384 + sw128_off(r & 7, chunk & 7), o);
           }
-          red2[quarter * kMlaHeads + 32 * c + lane] = warp_transpose_reduce32<false>(pv);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(s_free);
         mbar_arrive(p_full);
+        if (warp != SOFT_WARP0) mbar_arrive(s_free);
       }
-      named_bar_sync(1, 128);
       if (warp == SOFT_WARP0) {
+        // this tile's per-head sums, from the S columns; then S may be overwritten
+        if (!(ok = mbar_wait(sum_done, jt & 1, ab))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          const int h = lane + 32 * i;
-          l_run[i] = l_run[i] * alpha_r[i] + red2[h] + red2[kMlaHeads + h] + red2[2 * kMlaHeads + h] +
-                     red2[3 * kMlaHeads + h];
+        for (int c = 0; c < 3; ++c) {
+          float ls = 0.f;
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            uint32_t rr[8];
+            DSA_TMEM_LD8(tmem + S_COL + 32 * c + 8 * q + lane_off, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (lane == 8 * q + i) ls = __uint_as_float(rr[i]);
+          }
+          l_run[c] = l_run[c] * alpha_r[c] + ls;
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
       }
     }
     // row sums (and their reciprocals) for the shared epilogue below
@@ -543,40 +598,60 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     // a failed wait sets the CTA abort flag before this barrier, so the test is uniform
     if (!*reinterpret_cast<volatile int*>(abortf)) {
       tc_fence_after();
-      uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_Q);   // the query is no longer read
-      const bool final_out = p.nsplit == 1;
-      for (int pc = which; pc < 12; pc += 3) {       // (block v, head chunk c) pairs
-        const int v = pc / 3, c = pc % 3;
-        uint32_t rr[32];
-        DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
-        tmem_wait_ld();
-        const int dim = v * 128 + quarter * 32 + lane;
+      if (p.nsplit == 1) {
+        // final output [head][512 dims] in bf16: through shared memory for 16-byte stores
+        uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_Q);   // the query is no longer read
+#pragma unroll 1
+        for (int pc = which; pc < 12; pc += 3) {       // (block v, head chunk c) pairs
+          const int v = pc / 3, c = pc % 3;
+          uint32_t rr[32];
+          DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
+          tmem_wait_ld();
+          const int dim = v * 128 + quarter * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int h = 32 * c + i;
-          const float val = __uint_as_float(rr[i]) * alpha_sh[h];
-          uint16_t bits;
-          if (final_out) {
-            const __nv_bfloat16 bv = __float2bfloat16_rn(val);
-            bits = *reinterpret_cast<const uint16_t*>(&bv);
-          } else {
-            const __half hv = __float2half_rn(val);
-            bits = *reinterpret_cast<const uint16_t*>(&hv);
+          for (int i = 0; i < 32; ++i) {
+            const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(rr[i]) * alpha_sh[32 * c + i]);
+            stage[(32 * c + i) * kVDim + dim] = *reinterpret_cast<const uint16_t*>(&bv);
           }
-          stage[h * kVDim + dim] = bits;
         }
-      }
-      named_bar_sync(2, 384);
-      uint16_t* gbase = final_out ? reinterpret_cast<uint16_t*>(p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim)
-                                  : reinterpret_cast<uint16_t*>(p.part_o + ts * kMlaHeads * kVDim);
-      for (int i = et; i < kMlaHeads * kVDim / 8; i += 384)
-        *reinterpret_cast<uint4*>(gbase + 8 * i) = *reinterpret_cast<const uint4*>(stage + 8 * i);
-      if (et < kMlaHeads) {
-        if (final_out) {
-          if (p.lse) p.lse[static_cast<int64_t>(t) * kMlaHeads + et] = (m_use[et] + log2f(l_fin[et])) * 0.69314718055994531f;
-        } else {
-          p.part_ml[ts * kMlaHeads + et] = make_float2(m_use[et], l_fin[et]);
+        named_bar_sync(2, 384);
+        uint16_t* gbase = reinterpret_cast<uint16_t*>(p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim);
+        for (int i = et; i < kMlaHeads * kVDim / 8; i += 384)
+          *reinterpret_cast<uint4*>(gbase + 8 * i) = *reinterpret_cast<const uint4*>(stage + 8 * i);
+        if (et < kMlaHeads && p.lse)
+          p.lse[static_cast<int64_t>(t) * kMlaHeads + et] = (m_use[et] + log2f(l_fin[et])) * 0.69314718055994531f;
+      } else {
+        // normalised fp16 partial, dim-major [512 dims][96 heads]: each thread owns a dim and
+        // packs pairs of heads; rows are staged at a 208-byte pitch (conflict-free 16-byte
+        // stores), then copied out with coalesced 16-byte stores
+        constexpr int PITCH = 208;
+        uint8_t* stg = smem + OFF_Q;   // the query is no longer read
+#pragma unroll 1
+        for (int pc = which; pc < 12; pc += 3) {
+          const int v = pc / 3, c = pc % 3;
+          uint32_t rr[32];
+          DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
+          tmem_wait_ld();
+          uint8_t* row = stg + (v * 128 + quarter * 32 + lane) * PITCH + 64 * c;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 8 * q + 2 * e;
+              const __half2 hv = __floats2half2_rn(__uint_as_float(rr[i]) * alpha_sh[32 * c + i],
+                                                   __uint_as_float(rr[i + 1]) * alpha_sh[32 * c + i + 1]);
+              w4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            sts128(row + 16 * q, w4);
+          }
         }
+        named_bar_sync(2, 384);
+        uint4* gdst = reinterpret_cast<uint4*>(p.part_o + ts * kVDim * kMlaHeads);
+#pragma unroll 4
+        for (int i = et; i < kVDim * (kMlaHeads / 8); i += 384)
+          gdst[i] = *reinterpret_cast<const uint4*>(stg + (i / 12) * PITCH + (i % 12) * 16);
+        if (et < kMlaHeads) p.part_ml[ts * kMlaHeads + et] = make_float2(m_use[et], l_fin[et]);
       }
     }
   }
@@ -588,64 +663,79 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
 
 // Log-sum-exp combine of the split partials (each partial normalised by its
 // own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m).
-// Grid (12, T), 256 threads = 8 heads x 32.
-__global__ void __launch_bounds__(256) mla_combine_kernel(MlaParams p) {
+// Grid (512 / 32 dims, T), 384 threads: thread = (dim of the block's 32, group of 8
+// heads); every split's 16 bytes are loaded at once.  Splits with nothing
+// selected (sum 0) are skipped, never read.  The [96 heads x 32 dims] result is
+// staged in shared memory for row stores.
+constexpr int kCombDims = 32;
+constexpr int kCombThreads = kCombDims * (kMlaHeads / 8);
+constexpr int kMaxSplits = kMaxTopk / kSelTile;
+__global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) {
+  __shared__ float2 mls[kMaxSplits][kMlaHeads];  // (max, sum) per split and head
+  __shared__ float wgt[kMaxSplits][kMlaHeads];   // normalised weight per split and head
+  __shared__ __align__(16) __nv_bfloat16 tile[kMlaHeads][kCombDims];
+  __shared__ int used[kMaxSplits];
   grid_dep_wait();
   const int t = blockIdx.y;
-  const int h = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   const int64_t base = static_cast<int64_t>(t) * p.nsplit;
-  // lane j holds split j's (max, sum); nsplit <= 16
-  float2 ml = make_float2(-INFINITY, 0.f);
-  if (lane < p.nsplit) ml = p.part_ml[(base + lane) * kMlaHeads + h];
-  float M = ml.y > 0.f ? ml.x : -INFINITY;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float wl_mine = ml.y > 0.f ? exp2f(ml.x - M) * ml.y : 0.f;
-  float L = wl_mine;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  // all splits' slices of this head in flight at once
-  uint4 u[16][2];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (j < p.nsplit) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.part_o + ((base + j) * kMlaHeads + h) * kVDim);
-      u[j][0] = __ldcg(src + lane);
-      u[j][1] = __ldcg(src + lane + 32);
+  // weights: (max, sum) of every split staged in shared memory, then four threads per
+  // head (splits q, q + 4, ...) reduce with two shuffle steps
+  for (int i = threadIdx.x; i < p.nsplit * kMlaHeads; i += kCombThreads)
+    mls[i / kMlaHeads][i % kMlaHeads] = __ldcg(p.part_ml + base * kMlaHeads + i);
+  __syncthreads();
+  {
+    const int h = threadIdx.x >> 2, q = threadIdx.x & 3;
+    float M = -INFINITY;
+    for (int j = q; j < p.nsplit; j += 4)
+      if (mls[j][h].y > 0.f) M = fmaxf(M, mls[j][h].x);
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+    float L = 0.f;
+    for (int j = q; j < p.nsplit; j += 4) {
+      const float w = mls[j][h].y > 0.f ? exp2f(mls[j][h].x - M) * mls[j][h].y : 0.f;
+      wgt[j][h] = w;
+      L += w;
     }
-  }
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float wj = __shfl_sync(0xffffffffu, wl_mine, j);
-    if (j >= p.nsplit || wj == 0.f) continue;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint32_t w4[4] = {u[j][q].x, u[j][q].y, u[j][q].z, u[j][q].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-        acc[8 * q + 2 * e] = fmaf(wj, f.x, acc[8 * q + 2 * e]);
-        acc[8 * q + 2 * e + 1] = fmaf(wj, f.y, acc[8 * q + 2 * e + 1]);
-      }
+    L += __shfl_xor_sync(0xffffffffu, L, 1);
+    L += __shfl_xor_sync(0xffffffffu, L, 2);
+    const float inv = 1.f / L;
+    for (int j = q; j < p.nsplit; j += 4) {
+      wgt[j][h] *= inv;
+      if (h == 0) used[j] = mls[j][0].y > 0.f;   // a split is empty for all heads or for none
     }
+    if (q == 0 && p.lse && blockIdx.x == 0)
+      p.lse[static_cast<int64_t>(t) * kMlaHeads + h] = (M + log2f(L)) * 0.69314718055994531f;
   }
-  const float inv = 1.f / L;
-  __nv_bfloat16* orow = p.out + (static_cast<int64_t>(t) * kMlaHeads + h) * kVDim;
+  __syncthreads();
+  const int g = threadIdx.x % (kMlaHeads / 8);            // heads [8g, 8g + 8)
+  const int dl = threadIdx.x / (kMlaHeads / 8);           // dim within the block
+  const int d = blockIdx.x * kCombDims + dl;
+  uint4 u[kMaxSplits];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    uint32_t w4[4];
+  for (int j = 0; j < kMaxSplits; ++j)
+    if (j < p.nsplit && used[j])
+      u[j] = __ldcg(reinterpret_cast<const uint4*>(p.part_o + ((base + j) * kVDim + d) * kMlaHeads + 8 * g));
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxSplits; ++j) {
+    if (j >= p.nsplit || !used[j]) continue;
+    const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * q + 2 * e] * inv, acc[8 * q + 2 * e + 1] * inv);
-      w4[e] = *reinterpret_cast<const uint32_t*>(&b);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+      acc[2 * e] = fmaf(wgt[j][8 * g + 2 * e], f.x, acc[2 * e]);
+      acc[2 * e + 1] = fmaf(wgt[j][8 * g + 2 * e + 1], f.y, acc[2 * e + 1]);
     }
-    *reinterpret_cast<uint4*>(orow + 8 * (lane + 32 * q)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
   }
-  if (p.lse && lane == 0) p.lse[static_cast<int64_t>(t) * kMlaHeads + h] = (M + log2f(L)) * 0.69314718055994531f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tile[8 * g + i][dl] = __float2bfloat16_rn(acc[i]);
+  __syncthreads();
+  // 96 rows of 32 dims (64 bytes): 4 x 16-byte stores per row
+  __nv_bfloat16* o = p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim + blockIdx.x * kCombDims;
+  const int h = threadIdx.x >> 2, q = threadIdx.x & 3;
+  *reinterpret_cast<uint4*>(o + h * kVDim + 8 * q) = *reinterpret_cast<const uint4*>(&tile[h][8 * q]);
 }
 
 template <int LATF>
@@ -666,7 +756,7 @@ cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaS
   cudaError_t e =
       p.pool.lat_fmt == 1 ? launch_mla_fmt<1>(qmap, p, st, chained) : launch_mla_fmt<0>(qmap, p, st, chained);
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  return launch_ex(mla_combine_kernel, dim3(kMlaHeads / 8, p.b.T), dim3(256), 0, st, true, 0u, p);
+  return launch_ex(mla_combine_kernel, dim3(kVDim / kCombDims, p.b.T), dim3(kCombThreads), 0, st, true, 0u, p);
 }
 
 }  // namespace dsa

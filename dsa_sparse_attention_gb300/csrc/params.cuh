@@ -54,7 +54,7 @@ struct MlaParams {
   int nsplit;
   __nv_bfloat16* out;      // [T, 96, 512]       (nsplit == 1)
   float* lse;              // [T, 96] or null    (nsplit == 1)
-  __half* part_o;          // [T, nsplit, 96, 512] (nsplit > 1), each normalised by its own sum
+  __half* part_o;          // [T, nsplit, 512, 96] (nsplit > 1), dim-major, each normalised by its own sum
   float2* part_ml;         // [T, nsplit, 96]      (nsplit > 1): (max in log2 units, sum)
   uint32_t* status;
 };

@@ -110,6 +110,11 @@ __device__ void find_bin(const uint32_t* hist, int nbins, uint32_t kk, int& bin,
   __syncthreads();
 }
 
+// Physical slot (row * block_size + slot) of position s.
+__device__ __forceinline__ int32_t emit_phys(const TopkParams& p, const int32_t* btrow, int s, int bs_mask) {
+  return (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask);
+}
+
 __device__ __forceinline__ bool row_range(const TopkParams& p, int t, int& c0, int& c1, int& n) {
   int req, pos;
   load_token(p.b, t, p.status, req, pos);
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_emit_kernel(TopkParams p) {
   if (n <= p.k) {   // every position is selected; chunk 0 also writes the -1 tail
     for (int s = c0 + threadIdx.x; s < c1; s += kTopkThreads) {
       out[s] = s;
-      if (phys) phys[s] = (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask);
+      if (phys) phys[s] = emit_phys(p, btrow, s, bs_mask);
     }
     if (blockIdx.x == 0)
       for (int s = n + threadIdx.x; s < p.k; s += kTopkThreads) {
@@ -383,7 +388,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_emit_kernel(TopkParams p) {
     const int s = s0 + i;
     if (o < static_cast<uint32_t>(p.k)) {
       out[o] = s;
-      if (phys) phys[o] = (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask);
+      if (phys) phys[o] = emit_phys(p, btrow, s, bs_mask);
     }
     ++o;
   }
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   if (n <= p.k) {   // every position is selected, then -1 padding
     for (int s = rank * kClThreads + threadIdx.x; s < p.k; s += csize * kClThreads) {
       out[s] = s < n ? s : -1;
-      if (phys) phys[s] = s < n ? (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask) : -1;
+      if (phys) phys[s] = s < n ? emit_phys(p, btrow, s, bs_mask) : -1;
     }
     return;   // uniform over the cluster: no CTA touches another's shared memory
   }
@@ -519,7 +524,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
     const int s = s0 + i;
     if (o < k) {   // exactly k are selected; the guard only bounds the stores
       out[o] = s;
-      if (phys) phys[o] = (btrow[s >> p.log2_bs] << p.log2_bs) | (s & bs_mask);
+      if (phys) phys[o] = emit_phys(p, btrow, s, bs_mask);
     }
     ++o;
   }
