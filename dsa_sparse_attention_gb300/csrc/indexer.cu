@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(1024) plan_groups_kernel(PlanParams p) {
 // Decode batches of at most this many tokens, one per group, are planned inside
 // the scorer (no separate planning launch).
 constexpr int kDirectMaxT = 256;
-constexpr int kRowBatch = 64;      // tiles whose block-table rows the producer resolves at once
+constexpr int kRowBatch = 32;      // tiles whose block-table rows a producer warp resolves at once (one per lane)
 
 // Shared-memory / TMEM plan of the scorer.  IDXF = DSA_IDX_FP8 (0) or
 // DSA_IDX_MXFP4 (1); G = max tokens per group (N = 32 G).  MXFP4 keys arrive
@@ -134,10 +134,16 @@ constexpr int kRowBatch = 64;      // tiles whose block-table rows the producer 
 template <int IDXF, int G>
 struct ScorerCfg {
   static constexpr bool MX = IDXF == 1;
-  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 8 : 6);
+  // Key stages are freed as soon as their MMA completes; the per-key scales the
+  // epilogue reads live in a separate, longer ring of SSLOTS slots.
+  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 12 : 8);
+  static constexpr int SSLOTS = STAGES + 4;
   static constexpr int NBLK = MX ? 4 : 1;                   // accumulators per tile (scale blocks)
   static constexpr int ACC_COLS = 32 * G * NBLK;
   static constexpr int NACC = (G == 1 && !MX) ? 4 : 2;      // TMEM accumulators (even: set = tile parity)
+  // MMA issue costs the issuing thread a few hundred cycles per tile, so NMMA
+  // warps take tiles in turn (each with its own accumulators).
+  static constexpr int NMMA = 2;
   static constexpr int TMEM_COLS = NACC * ACC_COLS;         // 128 / 256 / 512 (powers of two)
   static constexpr int KEY_BYTES = kKeyTile * kIdxDim;      // 16 KB of e4m3 (MMA operand)
   static constexpr int PACK_BYTES = MX ? kKeyTile * 64 : 0; // 8 KB of packed e2m1 per stage
@@ -147,16 +153,23 @@ struct ScorerCfg {
   static constexpr int OFF_Q = STAGES * KEY_BYTES;
   static constexpr int OFF_PACK = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_SCALES = OFF_PACK + STAGES * PACK_BYTES;
-  static constexpr int OFF_W = OFF_SCALES + STAGES * SCALE_BYTES;   // 2 x [G][32] fp32
+  static constexpr int OFF_W = OFF_SCALES + SSLOTS * SCALE_BYTES;   // 2 x [G][32] fp32
   static constexpr int OFF_POS = OFF_W + 2 * W_BYTES;                // 2 x [G] int
   static constexpr int OFF_BARS = OFF_POS + 2 * G * 4 + 64;
-  static constexpr int N_BARS = 3 * STAGES + 2 * NACC + 5;
+  static constexpr int N_BARS = 3 * STAGES + 2 * NACC + 4 + NMMA + 2 * SSLOTS;
   static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
   static constexpr int OFF_PLAN = OFF_MISC + 64;            // direct mode: groups [kDirectMaxT] + total
-  static constexpr int OFF_ROWS = OFF_PLAN + kDirectMaxT * 32 + 64;   // producer: [kRowBatch][8] block ids
-  static constexpr int SMEM_BYTES = OFF_ROWS + kRowBatch * 8 * 4 + 1024;  // + slack for 1024-byte alignment
+  // Copies are issued by NPROD producer warps taking tiles in turn: one thread
+  // issues a bulk or tensor copy in about 150 cycles, several warps in parallel
+  // several times faster.
+  static constexpr int NPROD = MX ? 2 : 4;   // MXFP4: the converter warps leave fewer registers
+  static constexpr int OFF_ROWS = OFF_PLAN + kDirectMaxT * 32 + 64;   // producers: [NPROD][kRowBatch][8] block ids
+  static constexpr int SMEM_BYTES = OFF_ROWS + NPROD * kRowBatch * 8 * 4 + 1024;  // + slack for alignment
   static constexpr int CONV_WARPS = MX ? 8 : 0;
-  static constexpr int THREADS = 320 + 32 * CONV_WARPS;
+  static constexpr int PROD_WARP0 = 10 + CONV_WARPS;     // producer warps: 0 and PROD_WARP0 ..
+  static constexpr int MMA_WARP1 = PROD_WARP0 + NPROD - 1;   // MMA warps: 1 and MMA_WARP1 ..
+  static constexpr int THREADS = 320 + 32 * CONV_WARPS + 32 * (NPROD - 1) + 32 * (NMMA - 1);
+  static_assert(NACC % NMMA == 0, "accumulators per MMA warp");
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
   static_assert(SMEM_BYTES <= 232448, "smem");
 };
@@ -223,8 +236,10 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   uint64_t* tempty = tfull + C::NACC;
   uint64_t* qfull = tempty + C::NACC;
   uint64_t* qempty = qfull + 2;
-  uint64_t* drain = qempty + 2;
-  uint64_t* cvt = drain + 1;                  // [STAGES] MXFP4: converted keys ready
+  uint64_t* drain = qempty + 2;               // [NMMA]
+  uint64_t* cvt = drain + C::NMMA;            // [STAGES] MXFP4: converted keys ready
+  uint64_t* sfull = cvt + C::STAGES;          // [SSLOTS] scales landed
+  uint64_t* sempty = sfull + C::SSLOTS;       // [SSLOTS] scales read by the epilogue
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
   float* wsm = reinterpret_cast<float*>(smem + C::OFF_W);
@@ -280,7 +295,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4);
+      mbar_init(&empty[s], 1);   // the MMA's commit (MXFP4: the converters finished before it)
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
@@ -288,10 +303,14 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
-      mbar_init(&qempty[i], 1 + 8);
+      mbar_init(&qempty[i], C::NMMA + 8);   // every MMA warp's commit, every epilogue warp
     }
-    mbar_init(drain, 1);
+    for (int m = 0; m < C::NMMA; ++m) mbar_init(&drain[m], 1);
     for (int s = 0; s < C::STAGES; ++s) mbar_init(&cvt[s], C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
+    for (int s = 0; s < C::SSLOTS; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 4);   // the epilogue warps of the tile's set
+    }
     *abortf = 0;
     fence_mbar_init();
   }
@@ -306,26 +325,29 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   const int nbox = kKeyTile / box;
 
   if (tile_lo < tile_hi) {
-    if (warp == 0) {
-      // ------------------------------------------------------------ producer
-      // The whole warp walks the tiles; lane j resolves the block-table rows of
-      // tile (base + j) for each batch of 32 tiles, lane 0 issues the copies.
-      if (lane == 0) {
+    if (warp == 0 || (warp >= C::PROD_WARP0 && warp < C::MMA_WARP1)) {
+      // ------------------------------------------------------------ producers
+      // Producer pid takes tiles tile_lo + pid + NPROD m.  Its warp resolves the
+      // block-table rows of a batch of its tiles (every load of a lane issued
+      // before any is used); lane 0 walks the group cursor over all tiles, loads
+      // the queries of each group whose first tile it owns, and issues its tiles' copies.
+      const int pid = warp == 0 ? 0 : 1 + warp - C::PROD_WARP0;
+      if (lane == 0 && pid == 0) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&qmap);
       }
       GroupCursor cur;
       cur.init(groups, ng, total, tile_lo);
-      int issued = 0;
+      int walked = tile_lo;                                          // tile the cursor is at
+      int issued = 0;                                                // this producer's tiles issued
       bool ok = true;
-      int* rows_sm = reinterpret_cast<int*>(smem + C::OFF_ROWS);   // [kRowBatch][8] block ids
-      int gb = cur.g;                                               // group of tile `base`
-      for (int base = tile_lo; base < tile_hi && ok; base += kRowBatch) {
-        const int nb = min(kRowBatch, tile_hi - base);
-        // the warp resolves the block-table rows of tiles base .. base+nb-1, every
-        // load of a lane issued before any is used
+      int* rows_sm = reinterpret_cast<int*>(smem + C::OFF_ROWS) + pid * kRowBatch * 8;   // [kRowBatch][8]
+      const int n_mine = tile_hi - tile_lo > pid ? (tile_hi - tile_lo - pid + C::NPROD - 1) / C::NPROD : 0;
+      int gb = cur.g;                                                // group of the batch's first tile
+      for (int mb = 0; mb < n_mine && ok; mb += kRowBatch) {
+        const int nb = min(kRowBatch, n_mine - mb);
         for (int jj = lane; jj < kRowBatch; jj += 32) {
-          const int i = base + jj;
+          const int i = tile_lo + pid + (mb + jj) * C::NPROD;
           int idx[kKeyTile / 16];
           int vals[kKeyTile / 16];
           const int32_t* btrow = p.b.bt;
@@ -362,10 +384,10 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           for (int jj = 0; jj < nb; ++jj) {
-            const int i = base + jj;
-            const bool changed = cur.advance(i);
+            const int i = tile_lo + pid + (mb + jj) * C::NPROD;
+            while (walked < i) cur.advance(++walked);
             const ScoreGroup& grp = cur.grp;
-            if (i == tile_lo || changed) {
+            if (i == tile_lo || i == grp.tile_begin) {   // this producer loads the group's queries
               const int qb = cur.count & 1;
               if (cur.count >= 2 && !(ok = mbar_wait(&qempty[qb], ((cur.count - 2) >> 1) & 1, ab))) break;
               for (int j = 0; j < grp.n; ++j) {
@@ -386,14 +408,17 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
             }
             const int it = i - tile_lo;
             const int s = it % C::STAGES;
+            const int ss = it % C::SSLOTS;
             if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
+            if (it >= C::SSLOTS && !(ok = mbar_wait(&sempty[ss], ((it / C::SSLOTS) - 1) & 1, ab))) break;
             const int* rows = rows_sm + jj * 8;
             const int64_t key0 = static_cast<int64_t>(i - grp.tile_begin) * kKeyTile;
             constexpr int VB = C::MX ? kIdxDim / 2 : kIdxDim;   // value bytes per key in the page
-            uint32_t bytes = 0;
+            uint32_t nkeys = 0;
             for (int bx = 0; bx < nbox; ++bx)
-              if (rows[bx] >= 0) bytes += static_cast<uint32_t>(box) * (VB + 4);
-            mbar_arrive_expect_tx(&full[s], bytes);
+              if (rows[bx] >= 0) nkeys += static_cast<uint32_t>(box);
+            mbar_arrive_expect_tx(&full[s], nkeys * VB);
+            mbar_arrive_expect_tx(&sfull[ss], nkeys * 4);
             for (int bx = 0; bx < nbox; ++bx) {
               const int row = rows[bx];
               if (row < 0) continue;
@@ -404,7 +429,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
               tma_load_3d(vdst, &kmap, &full[s], 0, slot0, row);
               const uint8_t* src = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.idx_off +
                                    static_cast<int64_t>(bs) * VB + static_cast<int64_t>(slot0) * 4;
-              bulk_load(smem + C::OFF_SCALES + s * C::SCALE_BYTES + bx * box * 4, src, box * 4, &full[s]);
+              bulk_load(smem + C::OFF_SCALES + ss * C::SCALE_BYTES + bx * box * 4, src, box * 4, &sfull[ss]);
             }
             ++issued;
           }
@@ -412,12 +437,18 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         __syncwarp();
       }
-      if (!ok && lane == 0) {   // drain the copies still in flight before the CTA exits
-        for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it)
+      if (!ok && lane == 0) {   // drain this producer's copies still in flight before the CTA exits
+        for (int m = issued - 1; m >= 0 && m >= issued - C::STAGES; --m) {
+          const int it = pid + m * C::NPROD;
           drain_wait(&full[it % C::STAGES], (it / C::STAGES) & 1);
+          drain_wait(&sfull[it % C::SSLOTS], (it / C::SSLOTS) & 1);
+        }
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp >= C::MMA_WARP1) {
+      // ---------------------------------------------------------- MMA issuers
+      // MMA warp mid takes tiles tile_lo + mid + NMMA m; every MMA warp walks the
+      // cursor over all tiles and commits the query buffer of each group it passes.
+      const int mid = warp == 1 ? 0 : 1 + warp - C::MMA_WARP1;
       if (lane == 0) {
         GroupCursor cur;
         cur.init(groups, ng, total, tile_lo);
@@ -429,32 +460,34 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
             if (!(ok = mbar_wait(&qfull[cur.count & 1], (cur.count >> 1) & 1, ab))) break;
           }
           const int it = i - tile_lo;
-          const int s = it % C::STAGES;
-          const int acc = it % C::NACC;
-          if (!(ok = mbar_wait(C::MX ? &cvt[s] : &full[s], (it / C::STAGES) & 1, ab))) break;
-          if (it >= C::NACC && !(ok = mbar_wait(&tempty[acc], ((it / C::NACC) - 1) & 1, ab))) break;
-          tc_fence_after();
-          const uint32_t d = tmem + acc * C::ACC_COLS;
-          const uint32_t a0 = smem_u32(smem + s * C::KEY_BYTES);
-          const uint32_t b0 = smem_u32(smem + C::OFF_Q + (cur.count & 1) * C::Q_BYTES);
+          if (it % C::NMMA == mid) {
+            const int s = it % C::STAGES;
+            const int acc = it % C::NACC;
+            if (!(ok = mbar_wait_inline(C::MX ? &cvt[s] : &full[s], (it / C::STAGES) & 1, ab))) break;
+            if (it >= C::NACC && !(ok = mbar_wait_inline(&tempty[acc], ((it / C::NACC) - 1) & 1, ab))) break;
+            tc_fence_after();
+            const uint32_t d = tmem + acc * C::ACC_COLS;
+            const uint32_t a0 = smem_u32(smem + s * C::KEY_BYTES);
+            const uint32_t b0 = smem_u32(smem + C::OFF_Q + (cur.count & 1) * C::Q_BYTES);
 #pragma unroll
-          for (int k = 0; k < kIdxDim / 32; ++k) {
-            // FP8: one accumulator over K = 128.  MXFP4: block k (dims 32k..32k+31) alone
-            // into accumulator k, scaled by its E8M0 exponent in the epilogue.
-            const uint32_t dk = C::MX ? d + k * (32 * G) : d;
-            mma_f8f6f4(dk, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
-                       C::MX ? 0u : (k > 0 ? 1u : 0u));
+            for (int k = 0; k < kIdxDim / 32; ++k) {
+              // FP8: one accumulator over K = 128.  MXFP4: block k (dims 32k..32k+31) alone
+              // into accumulator k, scaled by its E8M0 exponent in the epilogue.
+              const uint32_t dk = C::MX ? d + k * (32 * G) : d;
+              mma_f8f6f4(dk, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
+                         C::MX ? 0u : (k > 0 ? 1u : 0u));
+            }
+            tc_commit(&empty[s]);
+            tc_commit(&tfull[acc]);
           }
-          tc_commit(&empty[s]);
-          tc_commit(&tfull[acc]);
           if (i + 1 == cur.next_begin || i + 1 == tile_hi) tc_commit(&qempty[cur.count & 1]);
         }
         if (!ok) {
-          tc_commit(drain);
-          drain_wait(drain, 0);
+          tc_commit(&drain[mid]);
+          drain_wait(&drain[mid], 0);
         }
       }
-    } else if (C::MX && warp >= 10) {
+    } else if (C::MX && warp >= 10 && warp < C::PROD_WARP0) {
       // ------------------------------------------------- converters (MXFP4)
       // Thread pair per key: packed e2m1 (64 B, row-major) -> e4m3 K-major,
       // 128-byte swizzle, as the TMA would have laid out FP8 keys.
@@ -497,10 +530,10 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         }
         const int it = i - tile_lo;
         if ((it & 1) != set) continue;
-        const int s = it % C::STAGES;
+        const int ss = it % C::SSLOTS;
         const int acc = it % C::NACC;
         if (!(ok = mbar_wait(&tfull[acc], (it / C::NACC) & 1, ab))) break;
-        if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
+        if (!(ok = mbar_wait(&sfull[ss], (it / C::SSLOTS) & 1, ab))) break;
         tc_fence_after();
         const ScoreGroup& grp = cur.grp;
         const int qb = cur.count & 1;
@@ -509,14 +542,14 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         float scale = 1.f;
         float bsc[4] = {1.f, 1.f, 1.f, 1.f};
         if (C::MX) {
-          const uint32_t e8 = reinterpret_cast<const uint32_t*>(smem + C::OFF_SCALES + s * C::SCALE_BYTES)[kloc];
+          const uint32_t e8 = reinterpret_cast<const uint32_t*>(smem + C::OFF_SCALES + ss * C::SCALE_BYTES)[kloc];
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
             const uint32_t e = (e8 >> (8 * b)) & 0xFFu;   // 2^(e-127); e = 0 is 2^-127, e = 255 NaN
             bsc[b] = __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : e << 23));
           }
         } else {
-          scale = reinterpret_cast<const float*>(smem + C::OFF_SCALES + s * C::SCALE_BYTES)[kloc];
+          scale = reinterpret_cast<const float*>(smem + C::OFF_SCALES + ss * C::SCALE_BYTES)[kloc];
         }
         for (int j = 0; j < grp.n; ++j) {
           uint32_t r[32];
@@ -565,7 +598,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&tempty[acc]);
-          mbar_arrive(&empty[s]);
+          mbar_arrive(&sempty[ss]);
         }
       }
       __syncwarp();
