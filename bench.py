@@ -33,6 +33,27 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+SCORER_PROFILE = os.path.join(ROOT, "profiles", "indexer_scorer_decode_b8_64k.md")
+SCORER_SOURCES = ["indexer.cu", "ptx.cuh", "common.cuh", "params.cuh"]
+
+
+def scorer_traffic():
+    """DRAM bytes per scorer launch from the committed ncu summary, if the scorer
+    sources are unchanged since the capture (else None)."""
+    import hashlib
+    try:
+        text = open(SCORER_PROFILE).read()
+        want = text.split("scorer_sources_sha256:")[1].split()[0]
+        nbytes = int(text.split("dram_bytes_per_launch:")[1].split()[0])
+    except (OSError, IndexError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for f in SCORER_SOURCES:
+        with open(os.path.join(ROOT, "dsa_sparse_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest() == want else None
+
+
 L2_FLUSH_BYTES = 256 << 20
 N_POOL_COPIES = 4
 WORKLOAD = "decode b8 x 65536 ctx, FP8 keys+latents, 1 GiB packed pool, permuted block table, top-2048"
@@ -354,7 +375,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "indexer scorer (indexer_kernel, one launch per dsa_indexer_score)",
                          "achieved": sc_gbs, "peak": peak, "unit": "GB/s", "frac": sc_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth (burst)",
-                         "traffic": None, "launch_ms": sc_ms},
+                         "traffic": scorer_traffic(), "launch_ms": sc_ms},
             "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": n_kernels_per_step * args.steps,
             "breakdown_ms": breakdown,
