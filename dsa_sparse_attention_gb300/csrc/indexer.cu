@@ -245,6 +245,31 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   float* wsm = reinterpret_cast<float*>(smem + C::OFF_W);
   int* possm = reinterpret_cast<int*>(smem + C::OFF_POS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);   // the MMA's commit (MXFP4: the converters finished before it)
+    }
+    for (int a = 0; a < C::NACC; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], C::NMMA + 8);   // every MMA warp's commit, every epilogue warp
+    }
+    for (int m = 0; m < C::NMMA; ++m) mbar_init(&drain[m], 1);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&cvt[s], C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
+    for (int s = 0; s < C::SSLOTS; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 4);   // the epilogue warps of the tile's set
+    }
+    *abortf = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
+  // Everything above touches only this CTA; the inputs may come from the kernel before.
+  grid_dep_wait();
   grid_dep_launch();   // a chained top-k may be scheduled as this grid's CTAs retire
 
   // Plan: groups of tokens and their key-tile ranges.  In direct mode every token
@@ -292,29 +317,6 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   const int tile_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
   const int tile_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);   // the MMA's commit (MXFP4: the converters finished before it)
-    }
-    for (int a = 0; a < C::NACC; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&qfull[i], 1);
-      mbar_init(&qempty[i], C::NMMA + 8);   // every MMA warp's commit, every epilogue warp
-    }
-    for (int m = 0; m < C::NMMA; ++m) mbar_init(&drain[m], 1);
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(&cvt[s], C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
-    for (int s = 0; s < C::SSLOTS; ++s) {
-      mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], 4);   // the epilogue warps of the tile's set
-    }
-    *abortf = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -630,8 +632,8 @@ static cudaError_t launch_scorer_g(const CUtensorMap& kmap, const CUtensorMap& q
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  indexer_kernel<IDXF, G><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(kmap, qmap, p);
-  return cudaGetLastError();
+  // chained: the set-up above the kernel's wait overlaps the end of the kernel before it
+  return launch_ex(indexer_kernel<IDXF, G>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, true, 0u, kmap, qmap, p);
 }
 
 int indexer_group_size(int idx_fmt, bool one_token_per_request) {

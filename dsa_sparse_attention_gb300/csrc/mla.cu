@@ -676,6 +676,7 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
   __shared__ __align__(16) __nv_bfloat16 tile[kMlaHeads][kCombDims];
   __shared__ int used[kMaxSplits];
   grid_dep_wait();
+  grid_dep_launch();   // the next chained kernel (the next layer step's scorer) may be scheduled
   const int t = blockIdx.y;
   const int64_t base = static_cast<int64_t>(t) * p.nsplit;
   // weights: (max, sum) of every split staged in shared memory, then four threads per
