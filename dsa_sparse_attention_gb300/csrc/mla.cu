@@ -67,6 +67,7 @@ constexpr int O_COL = 128;
 constexpr float TAU = 8.0f;                       // log2 headroom before the running max moves
 static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0 && OFF_ONES % 1024 == 0, "align");
 static_assert(kMlaHeads * kVDim * 2 <= OFF_RING && kVDim * 208 <= OFF_RING, "output staging fits the query region");
+static_assert(4 * RING_SLOT <= OFF_RING, "four V half-blocks fit the query region");
 static_assert(SMEM_BYTES <= 232448, "smem");
 }  // namespace mla
 
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   uint64_t* o_done = bars + 13;
   uint64_t* drain = bars + 14;
   uint64_t* sum_done = bars + 15;
+  uint64_t* vfull = bars + 16;      // [4] last tile: V half-blocks 4..7, staged in the query region
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   int* rescale_sh = reinterpret_cast<int*>(smem + OFF_MISC + 16);
@@ -227,6 +229,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(sum_done, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&vfull[i], CONV_WARPS);
     *abortf = 0;
     fence_mbar_init();
     // the query is an input of the call, not of the kernel before: load it now
@@ -265,22 +268,29 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       const uint32_t idesc_qk = make_idesc(1, 1, false, false, 128, kMlaHeads);
       const uint32_t idesc_pv = make_idesc(0, 0, true, true, 128, kMlaHeads);
       const uint32_t idesc_sum = make_idesc(0, 0, false, true, 128, kMlaHeads);
+      // Descriptors of the first slot of each operand, built once; a byte offset X
+      // moves the start-address field (16-byte units, no carry below 256 KB) by X >> 4.
+      const uint64_t d_c = make_sdesc_sw128(smem_u32(smem + OFF_RING), 16, 1024);      // C chunk, K-major
+      const uint64_t d_q = make_sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);         // q chunk, K-major
+      const uint64_t d_vr = make_sdesc_sw128(smem_u32(smem + OFF_RING), 8192, 1024);   // V^T in the ring, MN-major
+      const uint64_t d_vq = make_sdesc_sw128(smem_u32(smem + OFF_Q), 8192, 1024);      // V^T in the query region
+      const uint64_t d_p = make_sdesc_sw128(smem_u32(smem + OFF_P), 16384, 1024);      // P^T, MN-major
+      const uint64_t d_one = make_sdesc_sw128(smem_u32(smem + OFF_ONES), 16, 0);       // the ones atom, repeated
+      constexpr uint64_t kSlot = RING_SLOT >> 4;
       int fc = 0;
       bool ok = mbar_wait(q_full, 0, ab);
       for (int j = j0; j < j1 && ok; ++j) {
         const int jt = j - j0;
         if (jt > 0 && !(ok = mbar_wait(s_free, (jt - 1) & 1, ab))) break;
-        #pragma unroll 1
+#pragma unroll 1
         for (int kc = 0; kc < QCHUNKS; ++kc, ++fc) {
           const int slot = fc % RSLOTS;
-          if (!(ok = mbar_wait(&ring_full[slot], (fc / RSLOTS) & 1, ab))) break;
+          if (!(ok = mbar_wait_inline(&ring_full[slot], (fc / RSLOTS) & 1, ab))) break;
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + OFF_RING + slot * RING_SLOT);
-          const uint32_t b0 = smem_u32(smem + OFF_Q + kc * Q_SLOT);
+          const uint64_t a = d_c + slot * kSlot;
+          const uint64_t b = d_q + kc * (Q_SLOT >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tmem + S_COL, make_sdesc_sw128(a0 + 32 * kk, 16, 1024), make_sdesc_sw128(b0 + 32 * kk, 16, 1024),
-                    idesc_qk, (kc | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) mma_f16(tmem + S_COL, a + 2 * kk, b + 2 * kk, idesc_qk, (kc | kk) ? 1u : 0u);
           tc_commit(&ring_empty[slot]);
         }
         if (!ok) break;
@@ -289,31 +299,38 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         tc_fence_after();
         // per-head sums of P: ones[128 x 128] . P^T into the S columns (every lane gets the sums);
         // the ones operand is one atom repeated (8-row-group stride 0, same 32-byte K step)
-        {
-          const uint32_t o0 = smem_u32(smem + OFF_ONES);
-          const uint32_t b0 = smem_u32(smem + OFF_P);
 #pragma unroll
-          for (int kh = 0; kh < 2; ++kh)
+        for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f16(tmem + S_COL, make_sdesc_sw128(o0 + 32 * k, 16, 0),
-                      make_sdesc_sw128(b0 + (kh * 8 + k * 2) * 1024, 16384, 1024), idesc_sum, (kh | k) ? 1u : 0u);
-          tc_commit(sum_done);
-        }
-        #pragma unroll 1
+          for (int k = 0; k < 4; ++k)
+            mma_f16(tmem + S_COL, d_one + 2 * k, d_p + (kh * 8 + k * 2) * 64, idesc_sum, (kh | k) ? 1u : 0u);
+        tc_commit(sum_done);
+        // PV; on the CTA's last tile, half-blocks 4..7 come from the query region (free
+        // once QK is done) instead of the ring, so none of them waits for a ring slot
+        const bool last = j == j1 - 1;
+#pragma unroll 1
         for (int v = 0; v < 4 && ok; ++v) {
-          for (int kh = 0; kh < 2; ++kh, ++fc) {
-            const int slot = fc % RSLOTS;
-            if (!(ok = mbar_wait(&ring_full[slot], (fc / RSLOTS) & 1, ab))) break;
+#pragma unroll 1
+          for (int kh = 0; kh < 2; ++kh) {
+            const int f = 2 * v + kh;
+            const bool in_q = last && f >= 4;
+            uint64_t a;
+            if (in_q) {
+              if (!(ok = mbar_wait_inline(&vfull[f - 4], 0, ab))) break;
+              a = d_vq + (f - 4) * kSlot;
+            } else {
+              if (!(ok = mbar_wait_inline(&ring_full[fc % RSLOTS], (fc / RSLOTS) & 1, ab))) break;
+              a = d_vr + (fc % RSLOTS) * kSlot;
+            }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + OFF_RING + slot * RING_SLOT);
-            const uint32_t b0 = smem_u32(smem + OFF_P);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f16(tmem + O_COL + 96 * v, make_sdesc_sw128(a0 + k * 2048, 8192, 1024),
-                      make_sdesc_sw128(b0 + (kh * 8 + k * 2) * 1024, 16384, 1024), idesc_pv,
+              mma_f16(tmem + O_COL + 96 * v, a + 128 * k, d_p + (kh * 8 + k * 2) * 64, idesc_pv,
                       (jt > 0 || kh > 0 || k > 0) ? 1u : 0u);
-            tc_commit(&ring_empty[slot]);
+            if (!in_q) {
+              tc_commit(&ring_empty[fc % RSLOTS]);
+              ++fc;
+            }
           }
         }
         if (!ok) break;
@@ -420,15 +437,25 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         vbuf[u][0] = load_piece<NV>(src, 2 * u, hf);
         vbuf[u][1] = load_piece<NV>(src, 2 * u + 1, hf);
       }
+      const bool last = j == j1 - 1;   // V half-blocks 4..7 go to the query region (see the MMA issuer)
 #pragma unroll 1
       for (int vb2 = 0; vb2 < 4 && ok; vb2 += 2) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int v = vb2 + u;
-          const int myfc = fc + 2 * v + vg;
-          const int slot = myfc % RSLOTS;
-          if (myfc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((myfc / RSLOTS) - 1) & 1, ab))) break;
-          uint8_t* base = smem + OFF_RING + slot * RING_SLOT + (tl >> 3) * 1024;
+          const int f = 2 * v + vg;
+          const bool in_q = last && f >= 4;
+          uint8_t* base;
+          int slot = 0;
+          if (in_q) {
+            if (!(ok = mbar_wait_inline(s_full, jt & 1, ab))) break;   // QK done: the query is no longer read
+            base = smem + OFF_Q + (f - 4) * RING_SLOT + (tl >> 3) * 1024;
+          } else {
+            const int myfc = fc + f;
+            slot = myfc % RSLOTS;
+            if (myfc >= RSLOTS && !(ok = mbar_wait_inline(&ring_empty[slot], ((myfc / RSLOTS) - 1) & 1, ab))) break;
+            base = smem + OFF_RING + slot * RING_SLOT + (tl >> 3) * 1024;
+          }
 #pragma unroll
           for (int a = 0; a < 2; ++a) {          // 64-dim atom a = chunk 2v + a
 #pragma unroll
@@ -442,7 +469,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cnt(&ring_full[slot], 2);
+          if (lane == 0) mbar_arrive_cnt(in_q ? &vfull[f - 4] : &ring_full[slot], 2);
           if (v + 2 < 4) {
             vbuf[u][0] = load_piece<NV>(src, 2 * v + 4, hf);
             vbuf[u][1] = load_piece<NV>(src, 2 * v + 5, hf);
@@ -450,7 +477,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         }
       }
       if (!ok) break;
-      fc += 8;
+      fc += last ? 4 : 8;
     }
   } else if (warp >= SOFT_WARP0) {
     // ---------------------------------------------- softmax warps (10..13)
