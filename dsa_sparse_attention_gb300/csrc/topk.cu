@@ -397,41 +397,105 @@ __global__ void __launch_bounds__(kTopkThreads) topk_emit_kernel(TopkParams p) {
 // ------------------------------------------------------- one-launch cluster path
 
 constexpr int kClThreads = 512;
+constexpr int kClWarps = kClThreads / 32;
 constexpr int kClSlice = kClThreads * kPerThread;   // 8192 scores per CTA
 constexpr int kClMaxCtas = 8;                       // portable cluster size
 constexpr int kClMaxRow = kClSlice * kClMaxCtas;    // 65,536
+constexpr int kClOwn = kBins / 2;                   // bins a CTA owns when the cluster has >= 2 CTAs
+static_assert(kClThreads * 4 == kBins, "one thread per four bins of the top digit");
 
-// Adds this CTA's histogram `hl` into the merged histogram `hm` of every CTA of
-// the cluster (only its non-empty bins travel).
-__device__ __forceinline__ void push_hist(const uint32_t* hl, uint32_t* hm, uint32_t csize) {
-  for (int b = threadIdx.x; b < kBins; b += blockDim.x) {
-    const uint32_t c = hl[b];
-    if (c == 0) continue;
-    const uint32_t a = smem_u32(hm + b);
-    for (uint32_t r = 0; r < csize; ++r) red_cluster_add(cluster_map(a, r), c);
+// Exclusive scan of one value per thread over the block with a single barrier;
+// `wsh` (kClWarps words) must not be in use by another scan until a later barrier.
+__device__ __forceinline__ uint32_t cl_excl_scan(uint32_t v, uint32_t* wsh, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
+  if (lane == 31) wsh[warp] = x;
+  __syncthreads();
+  const uint32_t wv = lane < kClWarps ? wsh[lane] : 0u;
+  total = __reduce_add_sync(0xffffffffu, wv);
+  return __reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) + x - v;
 }
 
+// Thread i holds bins 4i .. 4i+3 (ascending key order) of a histogram.  Finds the
+// bin holding the kk-th largest element (1 <= kk <= total) and the number of
+// elements in higher bins; two barriers.
+__device__ __forceinline__ void cl_find(uint4 c, uint32_t kk, uint32_t* wsh, uint32_t* res, int& bin,
+                                        uint32_t& above) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t s = c.x + c.y + c.z + c.w;
+  uint32_t x = s;   // becomes the sum over lanes >= this one (higher bins)
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  if (lane == 0) wsh[warp] = x;
+  __syncthreads();
+  const uint32_t wv = lane < kClWarps ? wsh[lane] : 0u;
+  uint32_t cum = __reduce_add_sync(0xffffffffu, lane > warp ? wv : 0u) + x - s;
+  if (cum < kk && cum + s >= kk) {
+    int b = 4 * static_cast<int>(threadIdx.x) + 3;
+    if (cum + c.w < kk) {
+      cum += c.w;
+      --b;
+      if (cum + c.z < kk) {
+        cum += c.z;
+        --b;
+        if (cum + c.y < kk) {
+          cum += c.y;
+          --b;
+        }
+      }
+    }
+    res[0] = static_cast<uint32_t>(b);
+    res[1] = cum;
+  }
+  __syncthreads();
+  bin = static_cast<int>(res[0]);
+  above = res[1];
+}
+
+// One CTA of a cluster of up to eight per query row; the row stays in registers
+// (16 scores per thread).  Each digit: local histogram, the non-empty bins added
+// into the CTA that owns them (a contiguous 1/csize of the bins) through
+// distributed shared memory, one cluster barrier, then every CTA reads the
+// merged histogram (four bins per thread) from the owners and finds the digit.
 __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) {
   __shared__ __align__(16) uint32_t hl[3][kBins];   // this CTA's histograms of digits 1, 2, 3
-  __shared__ __align__(16) uint32_t hm[3][kBins];   // the same summed over the cluster
-  __shared__ uint32_t sh[48];
+  __shared__ __align__(16) uint32_t hr[3][kClOwn];  // the bins this CTA owns, summed over the cluster
+  __shared__ uint32_t wsh[4][kClWarps];
+  __shared__ uint32_t res[2];
   __shared__ uint32_t counts[kClMaxCtas];           // per CTA: (keys above T) << 16 | (keys equal to T)
   const int t = blockIdx.y;
   const uint32_t rank = cluster_rank(), csize = cluster_size();
+  const bool multi = csize > 1;
+  // Inputs of the call (not of the kernel before): the row length and the
+  // block-table entry of this thread's 16 positions are read before the wait.
   int req, pos;
   load_token(p.b, t, p.status, req, pos);
   const int n = pos + 1;
-  for (int i = threadIdx.x; i < 3 * kBins; i += kClThreads) {
-    hl[0][i] = 0;
-    hm[0][i] = 0;
-  }
-  grid_dep_wait();
-  grid_dep_launch();
   int32_t* out = p.idx + static_cast<int64_t>(t) * p.k;
   int32_t* phys = p.phys ? p.phys + static_cast<int64_t>(t) * p.k : nullptr;
   const int32_t* btrow = p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride;
   const int bs_mask = (1 << p.log2_bs) - 1;
+  // this CTA's slice of the row, a multiple of 16 scores long (<= 8192)
+  const int S = (static_cast<int>(cdiv(n, csize)) + 15) & ~15;
+  const int c0 = static_cast<int>(rank) * S;
+  const int c1 = min(n, c0 + S);
+  const int s0 = c0 + threadIdx.x * kPerThread;
+  const int nv = max(0, min(kPerThread, c1 - s0));
+  // 16 consecutive positions from a multiple of 16 share one block when bs >= 16
+  const bool one_block = p.log2_bs >= 4;
+  const int32_t blk = (phys && one_block && nv > 0 && n > p.k) ? __ldcg(btrow + (s0 >> p.log2_bs)) : 0;
+  for (int i = threadIdx.x; i < 3 * kBins; i += kClThreads) hl[0][i] = 0;
+  for (int i = threadIdx.x; i < 3 * kClOwn; i += kClThreads) hr[0][i] = 0;
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (n <= p.k) {   // every position is selected, then -1 padding
     for (int s = rank * kClThreads + threadIdx.x; s < p.k; s += csize * kClThreads) {
@@ -440,56 +504,53 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
     }
     return;   // uniform over the cluster: no CTA touches another's shared memory
   }
-  // this CTA's slice of the row, a multiple of 4 scores long (<= 8192)
-  const int S = (static_cast<int>(cdiv(n, csize)) + 3) & ~3;
-  const int c0 = static_cast<int>(rank) * S;
-  const int c1 = min(n, c0 + S);
   const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
-  const int s0 = c0 + threadIdx.x * kPerThread;
-  const int nv = max(0, min(kPerThread, c1 - s0));
   uint32_t u[kPerThread];
   load16(row, s0, s0 + nv, u);
   __syncthreads();   // histograms zeroed
-  const bool multi = csize > 1;
   if (multi) cluster_arrive();   // ... in every CTA before any CTA adds into them
 
-  // digit 1: bits 31..21
+  // Digits: bits 31..21, 20..10, 9..0; a key takes part in digit d when its higher
+  // digits equal the ones found so far (pmask / pval).
+  uint32_t pmask = 0, pval = 0, kk = static_cast<uint32_t>(p.k);
+#pragma unroll 1
+  for (int d = 0; d < 3; ++d) {
+    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
+    const uint32_t nb = d == 2 ? 1024u : 2048u;
+    uint32_t* h = hl[d];
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i)
-    if (i < nv) atomicAdd(&hl[0][u[i] >> 21], 1u);
-  __syncthreads();
-  if (multi) {
-    cluster_wait();
-    push_hist(hl[0], hm[0], csize);
-    cluster_sync();
+    for (int i = 0; i < kPerThread; ++i)
+      if (i < nv && (u[i] & pmask) == pval) atomicAdd(&h[(u[i] >> shift) & (nb - 1)], 1u);
+    __syncthreads();
+    uint4 c = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t b0 = 4u * threadIdx.x;
+    if (multi) {
+      // owner slices: a multiple of four bins, so a thread's four bins have one owner
+      const uint32_t own = ((nb + csize - 1) / csize + 3u) & ~3u;
+      if (d == 0) cluster_wait();
+      for (uint32_t b = threadIdx.x; b < nb; b += kClThreads) {
+        const uint32_t v = h[b];
+        if (v == 0) continue;
+        const uint32_t o = b / own;
+        red_cluster_add(cluster_map(smem_u32(&hr[d][b - o * own]), o), v);
+      }
+      cluster_sync();
+      if (b0 < nb) {
+        const uint32_t o = b0 / own;
+        c = ld_cluster_v4(cluster_map(smem_u32(&hr[d][b0 - o * own]), o));
+      }
+    } else if (b0 < nb) {
+      c = *reinterpret_cast<const uint4*>(&h[b0]);
+    }
+    int bin;
+    uint32_t above;
+    cl_find(c, kk, wsh[d], res, bin, above);
+    pval |= static_cast<uint32_t>(bin) << shift;
+    pmask |= (nb - 1) << shift;
+    kk -= above;
   }
-  int b1, bA, bB;
-  uint32_t a1, a2, a3;
-  const uint32_t k = static_cast<uint32_t>(p.k);
-  find_bin(multi ? hm[0] : hl[0], kBins, k, b1, a1, sh);
-  // digit 2: bits 20..10 of the keys in digit b1
-#pragma unroll
-  for (int i = 0; i < kPerThread; ++i)
-    if (i < nv && (u[i] >> 21) == static_cast<uint32_t>(b1)) atomicAdd(&hl[1][(u[i] >> 10) & 2047u], 1u);
-  __syncthreads();
-  if (multi) {
-    push_hist(hl[1], hm[1], csize);
-    cluster_sync();
-  }
-  find_bin(multi ? hm[1] : hl[1], kBins, k - a1, bA, a2, sh);
-  // digit 3: bits 9..0 of the keys in digits (b1, bA)
-  const uint32_t pre = (static_cast<uint32_t>(b1) << 11) | static_cast<uint32_t>(bA);
-#pragma unroll
-  for (int i = 0; i < kPerThread; ++i)
-    if (i < nv && (u[i] >> 10) == pre) atomicAdd(&hl[2][u[i] & 1023u], 1u);
-  __syncthreads();
-  if (multi) {
-    push_hist(hl[2], hm[2], csize);
-    cluster_sync();
-  }
-  find_bin(multi ? hm[2] : hl[2], 1024, k - a1 - a2, bB, a3, sh);
-  const uint32_t T = (pre << 10) | static_cast<uint32_t>(bB);
-  const uint32_t need_eq = k - a1 - a2 - a3;   // keys equal to T to take, lowest positions first
+  const uint32_t T = pval;
+  const uint32_t need_eq = kk;   // keys equal to T to take, lowest positions first
 
   // per thread (above, equal) counts, scanned in position order; fits 16 + 16 bits
   uint32_t gt = 0, eq = 0;
@@ -499,32 +560,35 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
     eq += i < nv && u[i] == T;
   }
   uint32_t tot;
-  const uint32_t excl = block_excl_scan((gt << 16) | eq, sh, tot);
+  const uint32_t excl = cl_excl_scan((gt << 16) | eq, wsh[3], tot);
   if (threadIdx.x < csize) st_cluster_u32(cluster_map(smem_u32(&counts[rank]), threadIdx.x), tot);
   if (multi) cluster_sync();   // the last access to another CTA's shared memory is before this
   else __syncthreads();
   // offsets of this CTA from the counts of the CTAs before it in the row
   uint32_t eq_before = 0, base = 0;
   for (uint32_t r = 0; r < rank; ++r) {
-    const uint32_t c = counts[r];
-    const uint32_t e = c & 0xFFFFu;
+    const uint32_t cr = counts[r];
+    const uint32_t e = cr & 0xFFFFu;
     const uint32_t left = need_eq > eq_before ? need_eq - eq_before : 0u;
-    base += (c >> 16) + min(e, left);
+    base += (cr >> 16) + min(e, left);
     eq_before += e;
   }
   const uint32_t take = min(tot & 0xFFFFu, need_eq > eq_before ? need_eq - eq_before : 0u);   // equal keys taken here
   uint32_t eq_rank = excl & 0xFFFFu;
   uint32_t o = base + (excl >> 16) + min(eq_rank, take);
+  uint32_t flags = 0;
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i) {
-    if (i >= nv) continue;
-    bool sel = u[i] > T;
-    if (u[i] == T) sel = eq_rank++ < take;
-    if (!sel) continue;
-    const int s = s0 + i;
-    if (o < k) {   // exactly k are selected; the guard only bounds the stores
+    bool sel = i < nv && u[i] > T;
+    if (i < nv && u[i] == T) sel = eq_rank++ < take;
+    flags |= static_cast<uint32_t>(sel) << i;
+  }
+  while (flags) {
+    const int s = s0 + __ffs(flags) - 1;
+    flags &= flags - 1;
+    if (o < static_cast<uint32_t>(p.k)) {   // exactly k are selected; the guard only bounds the stores
       out[o] = s;
-      if (phys) phys[o] = emit_phys(p, btrow, s, bs_mask);
+      if (phys) phys[o] = one_block ? ((blk << p.log2_bs) | (s & bs_mask)) : emit_phys(p, btrow, s, bs_mask);
     }
     ++o;
   }
