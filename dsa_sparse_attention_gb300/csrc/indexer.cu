@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&qmap);
       }
+      const uint64_t stream_pol = l2_evict_first_policy();
       GroupCursor cur;
       cur.init(groups, ng, total, tile_lo);
       int walked = tile_lo;                                          // tile the cursor is at
@@ -428,10 +429,11 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
               const int slot0 = static_cast<int>(k0 & (bs - 1));
               uint8_t* vdst = C::MX ? smem + C::OFF_PACK + s * C::PACK_BYTES + bx * box * VB
                                     : smem + s * C::KEY_BYTES + bx * box * kIdxDim;
-              tma_load_3d(vdst, &kmap, &full[s], 0, slot0, row);
+              tma_load_3d_hint(vdst, &kmap, &full[s], 0, slot0, row, stream_pol);
               const uint8_t* src = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.idx_off +
                                    static_cast<int64_t>(bs) * VB + static_cast<int64_t>(slot0) * 4;
-              bulk_load(smem + C::OFF_SCALES + ss * C::SCALE_BYTES + bx * box * 4, src, box * 4, &sfull[ss]);
+              bulk_load_hint(smem + C::OFF_SCALES + ss * C::SCALE_BYTES + bx * box * 4, src, box * 4, &sfull[ss],
+                             stream_pol);
             }
             ++issued;
           }
