@@ -691,8 +691,8 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
 // Log-sum-exp combine of the split partials (each partial normalised by its
 // own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m).
 // Grid (512 / 32 dims, T), 384 threads: thread = (dim of the block's 32, group of 8
-// heads); every split's 16 bytes are loaded at once.  Splits with nothing
-// selected (sum 0) are skipped, never read.  The [96 heads x 32 dims] result is
+// heads); every split's 16 bytes are loaded at once, before the weights.  Splits
+// with nothing selected (sum 0) take no part in the sum.  The [96 heads x 32 dims] result is
 // staged in shared memory for row stores.
 constexpr int kCombDims = 32;
 constexpr int kCombThreads = kCombDims * (kMlaHeads / 8);
@@ -706,6 +706,15 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
   grid_dep_launch();   // the next chained kernel (the next layer step's scorer) may be scheduled
   const int t = blockIdx.y;
   const int64_t base = static_cast<int64_t>(t) * p.nsplit;
+  const int g = threadIdx.x % (kMlaHeads / 8);            // heads [8g, 8g + 8)
+  const int dl = threadIdx.x / (kMlaHeads / 8);           // dim within the block
+  const int d = blockIdx.x * kCombDims + dl;
+  // every split's 16 bytes are requested first, so their latency covers the weights
+  // below; an empty split's slot (in bounds, never written) is loaded but not used
+  uint4 u[kMaxSplits];
+#pragma unroll
+  for (int j = 0; j < kMaxSplits; ++j)
+    if (j < p.nsplit) u[j] = __ldcg(reinterpret_cast<const uint4*>(p.part_o + ((base + j) * kVDim + d) * kMlaHeads + 8 * g));
   // weights: (max, sum) of every split staged in shared memory, then four threads per
   // head (splits q, q + 4, ...) reduce with two shuffle steps
   for (int i = threadIdx.x; i < p.nsplit * kMlaHeads; i += kCombThreads)
@@ -735,14 +744,6 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
       p.lse[static_cast<int64_t>(t) * kMlaHeads + h] = (M + log2f(L)) * 0.69314718055994531f;
   }
   __syncthreads();
-  const int g = threadIdx.x % (kMlaHeads / 8);            // heads [8g, 8g + 8)
-  const int dl = threadIdx.x / (kMlaHeads / 8);           // dim within the block
-  const int d = blockIdx.x * kCombDims + dl;
-  uint4 u[kMaxSplits];
-#pragma unroll
-  for (int j = 0; j < kMaxSplits; ++j)
-    if (j < p.nsplit && used[j])
-      u[j] = __ldcg(reinterpret_cast<const uint4*>(p.part_o + ((base + j) * kVDim + d) * kMlaHeads + 8 * g));
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
