@@ -23,6 +23,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Ws {
   size_t status = 0;
+  size_t row_hist = 0;
   size_t plan_hdr = 0, groups = 0;
   size_t topk = 0;
   size_t scores = 0;
@@ -81,6 +82,10 @@ Ws plan_ws(const dsa_kv_layout* l, const dsa_batch* b, int topk) {
   size_t off = 0;
   w.status = off;
   off += kStatusBytes;
+  // top-digit histograms from the scorer to the top-k of a layer step; the top-k
+  // leaves them zeroed (a zeroed workspace starts them right; they are verified)
+  w.row_hist = off;
+  off = align_up(off + size_t(T > 0 ? T : 1) * 2048 * 4);
   w.plan_hdr = off;
   off = align_up(off + sizeof(PlanHeader));
   w.groups = off;
@@ -234,8 +239,9 @@ dsa_status encode_fail() {
   return DSA_ERR_CUDA;
 }
 
+// `row_hist`: the top-k hint histograms to add to, or null.
 dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q_idx, const float* w, float* scores,
-                       int64_t ld, void* ws, const Ws& wl, cudaStream_t st) {
+                       int64_t ld, void* ws, const Ws& wl, cudaStream_t st, uint32_t* row_hist = nullptr) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
   CUtensorMap kmap, qmap;
@@ -261,12 +267,15 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   p.groups = at<ScoreGroup>(ws, wl.groups);
   p.status = status;
   p.direct = direct ? 1 : 0;
+  p.row_hist = G == 1 ? row_hist : nullptr;
   return cuda_status(launch_indexer(kmap, qmap, p, G, num_sms(), st));
 }
 
 // `chained`: the launch follows a kernel of this library on the stream (see launch_ex).
+// `pre_hist`: histograms the scorer left for these scores, or null.
 dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* scores, int64_t ld, int topk,
-                    int32_t* idx, int32_t* phys, void* ws, const Ws& wl, cudaStream_t st, bool chained) {
+                    int32_t* idx, int32_t* phys, void* ws, const Ws& wl, cudaStream_t st, bool chained,
+                    uint32_t* pre_hist = nullptr) {
   if (b->num_tokens == 0) return DSA_OK;
   TopkParams p;
   p.b = batch_view(b);
@@ -282,6 +291,7 @@ dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* sco
     while ((1 << lg) < l->block_size) ++lg;
   p.log2_bs = lg;
   p.status = at<uint32_t>(ws, wl.status);
+  p.pre_hist = pre_hist;
   return cuda_status(launch_topk(p, st, chained));
 }
 
@@ -402,11 +412,14 @@ dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, c
   if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
   float* scores = at<float>(workspace, wl.scores);
   int32_t* idx = idx_out ? idx_out : at<int32_t>(workspace, wl.idx);
-  if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream)) != DSA_OK) return s;
+  // rows that the one-launch top-k takes start from the scorer's top-digit histograms
+  uint32_t* row_hist = batch->max_ctx_len <= kTopkClusterMaxRow ? at<uint32_t>(workspace, wl.row_hist) : nullptr;
+  if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream, row_hist)) != DSA_OK) return s;
   // the top-k also emits each selection's physical cache slot, which the attention gathers directly
   int32_t* phys = at<int32_t>(workspace, wl.phys);
   // the top-k and the attention start while their predecessor drains (programmatic launch)
-  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream, true)) != DSA_OK) return s;
+  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream, true, row_hist)) != DSA_OK)
+    return s;
   return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream, true);
 }
 

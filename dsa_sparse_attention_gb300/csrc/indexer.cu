@@ -17,6 +17,9 @@
 //    bulk copies; warp 1 issues the MMAs; warps 2..9 read the accumulators
 //    (thread = key) and reduce sum_h w * ReLU(acc) * scale into fp32 scores.
 // Page translation (row = block_table[req][s / bs]) happens in the producer.
+// Inside a layer step (one token per group) the epilogue also counts each
+// token's scores by the top 11 bits of their order-preserving key, the first
+// digit of the top-k's radix select, so the top-k starts from that histogram.
 #include <cuda.h>
 
 #include "params.cuh"
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(1024) plan_groups_kernel(PlanParams p) {
 // the scorer (no separate planning launch).
 constexpr int kDirectMaxT = 256;
 constexpr int kRowBatch = 32;      // tiles whose block-table rows a producer warp resolves at once (one per lane)
+constexpr int kHistBins = 2048;    // top-digit bins of the score histogram handed to the top-k
 
 // Shared-memory / TMEM plan of the scorer.  IDXF = DSA_IDX_FP8 (0) or
 // DSA_IDX_MXFP4 (1); G = max tokens per group (N = 32 G).  MXFP4 keys arrive
@@ -136,7 +140,7 @@ struct ScorerCfg {
   static constexpr bool MX = IDXF == 1;
   // Key stages are freed as soon as their MMA completes; the per-key scales the
   // epilogue reads live in a separate, longer ring of SSLOTS slots.
-  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 12 : 8);
+  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 11 : 8);
   static constexpr int SSLOTS = STAGES + 4;
   static constexpr int NBLK = MX ? 4 : 1;                   // accumulators per tile (scale blocks)
   static constexpr int ACC_COLS = 32 * G * NBLK;
@@ -164,7 +168,11 @@ struct ScorerCfg {
   // several times faster.
   static constexpr int NPROD = MX ? 2 : 4;   // MXFP4: the converter warps leave fewer registers
   static constexpr int OFF_ROWS = OFF_PLAN + kDirectMaxT * 32 + 64;   // producers: [NPROD][kRowBatch][8] block ids
-  static constexpr int SMEM_BYTES = OFF_ROWS + NPROD * kRowBatch * 8 * 4 + 1024;  // + slack for alignment
+  // One token per group: the epilogue counts the top 11 key bits of its first
+  // token's scores in shared memory (later tokens go straight to global memory).
+  static constexpr bool HIST = G == 1;
+  static constexpr int OFF_HIST = OFF_ROWS + NPROD * kRowBatch * 8 * 4;
+  static constexpr int SMEM_BYTES = OFF_HIST + (HIST ? kHistBins * 4 : 0) + 1024;  // + slack for alignment
   static constexpr int CONV_WARPS = MX ? 8 : 0;
   static constexpr int PROD_WARP0 = 10 + CONV_WARPS;     // producer warps: 0 and PROD_WARP0 ..
   static constexpr int MMA_WARP1 = PROD_WARP0 + NPROD - 1;   // MMA warps: 1 and MMA_WARP1 ..
@@ -317,6 +325,10 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   const int tile_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
   const int tile_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
 
+  uint32_t* hs = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
+  const bool hist_on = C::HIST && p.row_hist != nullptr;
+  if (hist_on)
+    for (int i = threadIdx.x; i < kHistBins; i += C::THREADS) hs[i] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -525,6 +537,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       const int set = e >> 2;
       GroupCursor cur;
       cur.init(groups, ng, total, tile_lo);
+      const int first_t = cur.grp.t0;
       bool ok = mbar_wait(&qfull[0], 0, ab);
       for (int i = tile_lo; i < tile_hi && ok; ++i) {
         if (cur.advance(i)) {
@@ -596,7 +609,15 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
             }
           }
           const int pos = possm[qb * G + j];
-          if (key <= pos) p.scores[static_cast<int64_t>(grp.t0 + j) * p.ld + key] = scale * sum;
+          if (key <= pos) {
+            const float v = scale * sum;
+            p.scores[static_cast<int64_t>(grp.t0 + j) * p.ld + key] = v;
+            if (hist_on) {
+              const uint32_t bin = score_key(v) >> 21;
+              if (cur.count == 0) atomicAdd(&hs[bin], 1u);
+              else atomicAdd(p.row_hist + static_cast<int64_t>(grp.t0 + j) * kHistBins + bin, 1u);
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -607,6 +628,15 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       }
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(&qempty[cur.count & 1]);
+      if (hist_on) {
+        // every epilogue warp leaves the loop (finished or aborted) and meets here
+        named_bar_sync(1, 256);
+        uint32_t* dst = p.row_hist + static_cast<int64_t>(first_t) * kHistBins;
+        for (int b = threadIdx.x - 64; b < kHistBins; b += 256) {
+          const uint32_t v = hs[b];
+          if (v) atomicAdd(dst + b, v);
+        }
+      }
     }
   }
   tc_fence_before();

@@ -18,6 +18,8 @@ struct IndexerParams {
   const ScoreGroup* groups;
   uint32_t* status;
   int direct;              // 1: one token per group, planned inside the scorer (hdr/groups unused)
+  uint32_t* row_hist;      // [T, 2048] or null: per-token counts of the scores' top 11 key bits are
+                           // added here (one token per group only); a hint for the top-k
 };
 
 struct TopkParams {
@@ -41,6 +43,8 @@ struct TopkParams {
   int32_t* phys;        // [T, k] or null
   int log2_bs;
   uint32_t* status;
+  uint32_t* pre_hist;   // [T, 2048] or null: top-digit counts left by the scorer (a hint, verified
+                        // before use); the cluster top-k zeroes each row after reading it
 };
 
 struct MlaParams {
@@ -60,6 +64,7 @@ struct MlaParams {
 };
 
 constexpr int kTopkChunk = 4096;   // scores per CTA in the top-k passes
+constexpr int kTopkClusterMaxRow = 65536;   // rows up to this long take the one-launch cluster top-k
 constexpr int kTopkCap = 4096;     // candidates per row kept for the exact resolution
 
 // Byte offsets of the top-k scratch inside a region (256-byte aligned segments);

@@ -402,11 +402,31 @@ constexpr int kClSlice = kClThreads * kPerThread;   // 8192 scores per CTA
 constexpr int kClMaxCtas = 8;                       // portable cluster size
 constexpr int kClMaxRow = kClSlice * kClMaxCtas;    // 65,536
 constexpr int kClOwn = kBins / 2;                   // bins a CTA owns when the cluster has >= 2 CTAs
+constexpr int kClCap = 4096;                        // candidates of a row gathered into every CTA
+constexpr int kClPer = kClCap / kClThreads;         // ... 8 per thread
 static_assert(kClThreads * 4 == kBins, "one thread per four bins of the top digit");
+static_assert(kClMaxRow == kTopkClusterMaxRow, "row limit of the cluster path");
 
-// Exclusive scan of one value per thread over the block with a single barrier;
-// `wsh` (kClWarps words) must not be in use by another scan until a later barrier.
-__device__ __forceinline__ uint32_t cl_excl_scan(uint32_t v, uint32_t* wsh, uint32_t& total) {
+struct ClShared {
+  // zeroed at the start (the first six arrays, contiguous)
+  uint32_t hl[kBins];             // this CTA's digit-1 histogram
+  uint32_t hr[kClOwn];            // the digit-1 bins this CTA owns, summed over the cluster
+  uint32_t h2[kBins];             // digit-2 histogram (of the row's candidates, or of this CTA's keys)
+  uint32_t h3[1024];              // digit-3 histogram
+  uint32_t hr2[kClOwn];           // owned digit-2 bins (many candidates)
+  uint32_t hr3[kClOwn / 2];       // owned digit-3 bins (many candidates)
+  uint32_t cl[kClCap];            // this CTA's candidate keys, in position order
+  uint32_t wsh[8][32];            // scratch of the scans and searches, one row per call site
+  uint32_t res[2];
+  uint32_t meta[kClMaxCtas];      // per CTA: (keys above digit b1) << 16 | (keys in digit b1)
+  uint32_t counts[kClMaxCtas];    // per CTA: (keys above T) << 16 | (keys equal to T)
+};
+constexpr int kClZeroWords = kBins + kClOwn + kBins + 1024 + kClOwn + kClOwn / 2;
+
+// Exclusive scan of one value per thread over the block with a single barrier:
+// (this thread's exclusive prefix, block total); `wsh` must not be in use by
+// another call until a later barrier.
+__device__ __noinline__ uint2 cl_excl_scan(uint32_t v, uint32_t* wsh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
@@ -417,15 +437,27 @@ __device__ __forceinline__ uint32_t cl_excl_scan(uint32_t v, uint32_t* wsh, uint
   if (lane == 31) wsh[warp] = x;
   __syncthreads();
   const uint32_t wv = lane < kClWarps ? wsh[lane] : 0u;
-  total = __reduce_add_sync(0xffffffffu, wv);
-  return __reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) + x - v;
+  return make_uint2(__reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) + x - v, __reduce_add_sync(0xffffffffu, wv));
+}
+
+// Block sums of two values per thread, one barrier; `wsh` as above (32 words).
+__device__ __forceinline__ uint2 cl_block_sum2(uint32_t x, uint32_t y, uint32_t* wsh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  x = __reduce_add_sync(0xffffffffu, x);
+  y = __reduce_add_sync(0xffffffffu, y);
+  if (lane == 0) {
+    wsh[warp] = x;
+    wsh[kClWarps + warp] = y;
+  }
+  __syncthreads();
+  return make_uint2(__reduce_add_sync(0xffffffffu, lane < kClWarps ? wsh[lane] : 0u),
+                    __reduce_add_sync(0xffffffffu, lane < kClWarps ? wsh[kClWarps + lane] : 0u));
 }
 
 // Thread i holds bins 4i .. 4i+3 (ascending key order) of a histogram.  Finds the
 // bin holding the kk-th largest element (1 <= kk <= total) and the number of
-// elements in higher bins; two barriers.
-__device__ __forceinline__ void cl_find(uint4 c, uint32_t kk, uint32_t* wsh, uint32_t* res, int& bin,
-                                        uint32_t& above) {
+// elements in higher bins, as (bin, above); two barriers.
+__device__ __noinline__ uint2 cl_find(uint4 c, uint32_t kk, uint32_t* wsh, uint32_t* res) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t s = c.x + c.y + c.z + c.w;
   uint32_t x = s;   // becomes the sum over lanes >= this one (higher bins)
@@ -456,22 +488,30 @@ __device__ __forceinline__ void cl_find(uint4 c, uint32_t kk, uint32_t* wsh, uin
     res[1] = cum;
   }
   __syncthreads();
-  bin = static_cast<int>(res[0]);
-  above = res[1];
+  return make_uint2(res[0], res[1]);
 }
 
 // One CTA of a cluster of up to eight per query row; the row stays in registers
-// (16 scores per thread).  Each digit: local histogram, the non-empty bins added
-// into the CTA that owns them (a contiguous 1/csize of the bins) through
-// distributed shared memory, one cluster barrier, then every CTA reads the
-// merged histogram (four bins per thread) from the owners and finds the digit.
+// (16 scores per thread).
+//  1. Digit 1 (the top 11 key bits): with PRE, the histogram the scorer left for
+//     the row; else each CTA's histogram, its non-empty bins added into the CTA
+//     owning them (a contiguous 1/csize of the bins) through distributed shared
+//     memory and read back four bins per thread.  The bin b1 holding the k-th key
+//     follows.
+//  2. Each CTA counts its keys above b1, lists its keys in b1 (the candidates) in
+//     position order and publishes both counts to every CTA.  The counts decide
+//     exactly whether b1 holds the k-th key; a hint that fails is replaced by the
+//     histogram of step 1 built from the scores.
+//  3. Up to kClCap candidates: every CTA gathers the row's candidates and resolves
+//     digits 2 and 3 (bits 20..10, 9..0) locally.  More (heavy ties): digits 2 and
+//     3 through the cluster as in step 1, over the keys in registers.
+//  4. Ordered output: keys above the threshold key T, then keys equal to T at the
+//     lowest positions, each CTA after the selections of the CTAs before it.
+template <bool PRE>
 __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) {
-  __shared__ __align__(16) uint32_t hl[3][kBins];   // this CTA's histograms of digits 1, 2, 3
-  __shared__ __align__(16) uint32_t hr[3][kClOwn];  // the bins this CTA owns, summed over the cluster
-  __shared__ uint32_t wsh[4][kClWarps];
-  __shared__ uint32_t res[2];
-  __shared__ uint32_t counts[kClMaxCtas];           // per CTA: (keys above T) << 16 | (keys equal to T)
+  __shared__ __align__(16) ClShared S;
   const int t = blockIdx.y;
+  const int tid = threadIdx.x;
   const uint32_t rank = cluster_rank(), csize = cluster_size();
   const bool multi = csize > 1;
   // Inputs of the call (not of the kernel before): the row length and the
@@ -484,96 +524,241 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   const int32_t* btrow = p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride;
   const int bs_mask = (1 << p.log2_bs) - 1;
   // this CTA's slice of the row, a multiple of 16 scores long (<= 8192)
-  const int S = (static_cast<int>(cdiv(n, csize)) + 15) & ~15;
-  const int c0 = static_cast<int>(rank) * S;
-  const int c1 = min(n, c0 + S);
-  const int s0 = c0 + threadIdx.x * kPerThread;
+  const int SL = (static_cast<int>(cdiv(n, csize)) + 15) & ~15;
+  const int c0 = static_cast<int>(rank) * SL;
+  const int c1 = min(n, c0 + SL);
+  const int s0 = c0 + tid * kPerThread;
   const int nv = max(0, min(kPerThread, c1 - s0));
   // 16 consecutive positions from a multiple of 16 share one block when bs >= 16
   const bool one_block = p.log2_bs >= 4;
   const int32_t blk = (phys && one_block && nv > 0 && n > p.k) ? __ldcg(btrow + (s0 >> p.log2_bs)) : 0;
-  for (int i = threadIdx.x; i < 3 * kBins; i += kClThreads) hl[0][i] = 0;
-  for (int i = threadIdx.x; i < 3 * kClOwn; i += kClThreads) hr[0][i] = 0;
+  for (int i = tid; i < kClZeroWords; i += kClThreads) S.hl[i] = 0;
   grid_dep_wait();
   grid_dep_launch();
+  uint4* gh = PRE ? reinterpret_cast<uint4*>(p.pre_hist + static_cast<int64_t>(t) * kBins) : nullptr;
 
   if (n <= p.k) {   // every position is selected, then -1 padding
-    for (int s = rank * kClThreads + threadIdx.x; s < p.k; s += csize * kClThreads) {
+    for (int s = rank * kClThreads + tid; s < p.k; s += csize * kClThreads) {
       out[s] = s < n ? s : -1;
       if (phys) phys[s] = s < n ? emit_phys(p, btrow, s, bs_mask) : -1;
     }
+    if (PRE && rank == 0) gh[tid] = make_uint4(0u, 0u, 0u, 0u);
     return;   // uniform over the cluster: no CTA touches another's shared memory
   }
   const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
+  uint4 c = make_uint4(0u, 0u, 0u, 0u);
+  if (PRE) c = __ldcg(gh + tid);
   uint32_t u[kPerThread];
   load16(row, s0, s0 + nv, u);
-  __syncthreads();   // histograms zeroed
+  __syncthreads();   // zeroed
+  bool pending = multi;
   if (multi) cluster_arrive();   // ... in every CTA before any CTA adds into them
+  const uint32_t k = static_cast<uint32_t>(p.k);
 
-  // Digits: bits 31..21, 20..10, 9..0; a key takes part in digit d when its higher
-  // digits equal the ones found so far (pmask / pval).
-  uint32_t pmask = 0, pval = 0, kk = static_cast<uint32_t>(p.k);
+  // ---- steps 1 and 2 (twice when a hint fails)
+  int b1 = 0;
+  uint32_t G = 0, Cc = 0;
+  bool exchange = !PRE;
 #pragma unroll 1
-  for (int d = 0; d < 3; ++d) {
-    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
-    const uint32_t nb = d == 2 ? 1024u : 2048u;
-    uint32_t* h = hl[d];
+  for (int round = 0; round < 2; ++round) {
+    if (exchange) {
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i)
+        if (i < nv) atomicAdd(&S.hl[u[i] >> 21], 1u);
+      __syncthreads();
+      if (multi) {
+        const uint32_t own = ((kBins + csize - 1) / csize + 3u) & ~3u;   // four-bin multiple: one owner per thread
+        if (pending) {
+          cluster_wait();
+          pending = false;
+        }
+        for (int b = tid; b < kBins; b += kClThreads) {
+          const uint32_t v = S.hl[b];
+          if (v == 0) continue;
+          const uint32_t o = static_cast<uint32_t>(b) / own;
+          red_cluster_add(cluster_map(smem_u32(&S.hr[b - o * own]), o), v);
+        }
+        cluster_sync();
+        const uint32_t b0 = 4u * tid, o = b0 / own;
+        c = ld_cluster_v4(cluster_map(smem_u32(&S.hr[b0 - o * own]), o));
+      } else {
+        c = *reinterpret_cast<const uint4*>(&S.hl[4 * tid]);
+      }
+    }
+    b1 = static_cast<int>(cl_find(c, k, S.wsh[0], S.res).x);
+    uint32_t gtm = 0, cm = 0;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      const uint32_t d = u[i] >> 21;
+      if (i < nv) {
+        gtm |= static_cast<uint32_t>(d > static_cast<uint32_t>(b1)) << i;
+        cm |= static_cast<uint32_t>(d == static_cast<uint32_t>(b1)) << i;
+      }
+    }
+    const uint2 sc = cl_excl_scan((static_cast<uint32_t>(__popc(gtm)) << 16) | __popc(cm), S.wsh[1]);
+    const uint32_t tot = sc.y;
+    uint32_t o = sc.x & 0xFFFFu;
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i)
-      if (i < nv && (u[i] & pmask) == pval) atomicAdd(&h[(u[i] >> shift) & (nb - 1)], 1u);
-    __syncthreads();
-    uint4 c = make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t b0 = 4u * threadIdx.x;
+      if ((cm >> i) & 1u) {
+        if (o < kClCap) S.cl[o] = u[i];
+        ++o;
+      }
+    if (tid < static_cast<int>(csize)) st_cluster_u32(cluster_map(smem_u32(&S.meta[rank]), tid), tot);
     if (multi) {
-      // owner slices: a multiple of four bins, so a thread's four bins have one owner
-      const uint32_t own = ((nb + csize - 1) / csize + 3u) & ~3u;
-      if (d == 0) cluster_wait();
-      for (uint32_t b = threadIdx.x; b < nb; b += kClThreads) {
-        const uint32_t v = h[b];
-        if (v == 0) continue;
-        const uint32_t o = b / own;
-        red_cluster_add(cluster_map(smem_u32(&hr[d][b - o * own]), o), v);
+      if (pending) {
+        cluster_wait();
+        pending = false;
       }
       cluster_sync();
-      if (b0 < nb) {
-        const uint32_t o = b0 / own;
-        c = ld_cluster_v4(cluster_map(smem_u32(&hr[d][b0 - o * own]), o));
-      }
-    } else if (b0 < nb) {
-      c = *reinterpret_cast<const uint4*>(&h[b0]);
+    } else {
+      __syncthreads();
     }
-    int bin;
-    uint32_t above;
-    cl_find(c, kk, wsh[d], res, bin, above);
-    pval |= static_cast<uint32_t>(bin) << shift;
-    pmask |= (nb - 1) << shift;
-    kk -= above;
+    if (PRE && round == 0 && rank == 0) gh[tid] = make_uint4(0u, 0u, 0u, 0u);   // every CTA has read it
+    G = 0;
+    Cc = 0;
+    for (uint32_t r = 0; r < csize; ++r) {
+      G += S.meta[r] >> 16;
+      Cc += S.meta[r] & 0xFFFFu;
+    }
+    if (!PRE || (G < k && k <= G + Cc)) break;   // uniform over the cluster
+    exchange = true;
   }
-  const uint32_t T = pval;
-  const uint32_t need_eq = kk;   // keys equal to T to take, lowest positions first
 
-  // per thread (above, equal) counts, scanned in position order; fits 16 + 16 bits
+  // ---- step 3: the threshold key T, the keys equal to T to take (need_eq), and
+  // this CTA's share: selections before it (base) and equal keys taken here (take)
+  uint32_t T, base, take;
+  const bool gathered = Cc <= static_cast<uint32_t>(kClCap);
+  if (gathered) {
+    // cum[r]: candidates of the CTAs before r (all ones past the cluster)
+    uint32_t cum[kClMaxCtas];
+    uint32_t lo = 0, G_lo = 0;
+    {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int r = 0; r < kClMaxCtas; ++r) {
+        cum[r] = r < static_cast<int>(csize) ? acc : 0xFFFFFFFFu;
+        if (r < static_cast<int>(csize)) {
+          const uint32_t m = S.meta[r];
+          if (static_cast<uint32_t>(r) < rank) G_lo += m >> 16;
+          if (static_cast<uint32_t>(r) == rank) lo = acc;
+          acc += m & 0xFFFFu;
+        }
+      }
+    }
+    const uint32_t hi = lo + (S.meta[rank] & 0xFFFFu);
+    uint32_t lv[kClPer];
+#pragma unroll
+    for (int m = 0; m < kClPer; ++m) {
+      const uint32_t g = static_cast<uint32_t>(tid + m * kClThreads);
+      lv[m] = 0;
+      if (g < Cc) {
+        uint32_t r = 0, br = 0;
+#pragma unroll
+        for (int q = 1; q < kClMaxCtas; ++q)
+          if (g >= cum[q]) {
+            r = static_cast<uint32_t>(q);
+            br = cum[q];
+          }
+        lv[m] = ld_cluster_u32(cluster_map(smem_u32(&S.cl[g - br]), r));
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < kClPer; ++m)
+      if (static_cast<uint32_t>(tid + m * kClThreads) < Cc) atomicAdd(&S.h2[(lv[m] >> 10) & 2047u], 1u);
+    __syncthreads();
+    if (multi) cluster_arrive();   // done with the other CTAs' shared memory (the wait is before the exit)
+    const uint2 fA = cl_find(*reinterpret_cast<const uint4*>(&S.h2[4 * tid]), k - G, S.wsh[2], S.res);
+    const uint32_t bA = fA.x, a2 = fA.y;
+#pragma unroll
+    for (int m = 0; m < kClPer; ++m)
+      if (static_cast<uint32_t>(tid + m * kClThreads) < Cc && ((lv[m] >> 10) & 2047u) == bA)
+        atomicAdd(&S.h3[lv[m] & 1023u], 1u);
+    __syncthreads();
+    const uint2 fB = cl_find(tid < 256 ? *reinterpret_cast<const uint4*>(&S.h3[4 * tid]) : make_uint4(0u, 0u, 0u, 0u),
+                             k - G - a2, S.wsh[3], S.res);
+    const uint32_t a3 = fB.y;
+    T = (static_cast<uint32_t>(b1) << 21) | (bA << 10) | fB.x;
+    const uint32_t need_eq = k - G - a2 - a3;
+    uint32_t x = 0, y = 0;   // candidates of earlier CTAs above | equal to T; this CTA's equal to T
+#pragma unroll
+    for (int m = 0; m < kClPer; ++m) {
+      const uint32_t g = static_cast<uint32_t>(tid + m * kClThreads);
+      if (g < lo) x += (static_cast<uint32_t>(lv[m] > T) << 16) | static_cast<uint32_t>(lv[m] == T);
+      else if (g < hi) y += lv[m] == T;
+    }
+    const uint2 xy = cl_block_sum2(x, y, S.wsh[4]);
+    const uint32_t eq_lo = min(xy.x & 0xFFFFu, need_eq);
+    base = G_lo + (xy.x >> 16) + eq_lo;
+    take = min(xy.y, need_eq - eq_lo);
+  } else {
+    // digits 2 and 3 through the cluster (owned bins in hr2 / hr3)
+    uint32_t pmask = 0xFFE00000u, pval = static_cast<uint32_t>(b1) << 21, kk = k - G;
+#pragma unroll 1
+    for (int d = 1; d < 3; ++d) {
+      const int shift = d == 1 ? 10 : 0;
+      const uint32_t nb = d == 1 ? 2048u : 1024u;
+      uint32_t* h = d == 1 ? S.h2 : S.h3;
+      uint32_t* hrr = d == 1 ? S.hr2 : S.hr3;
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i)
+        if (i < nv && (u[i] & pmask) == pval) atomicAdd(&h[(u[i] >> shift) & (nb - 1)], 1u);
+      __syncthreads();
+      uint4 cc = make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t b0 = 4u * tid;
+      if (multi) {
+        const uint32_t own = ((nb + csize - 1) / csize + 3u) & ~3u;
+        for (uint32_t b = tid; b < nb; b += kClThreads) {
+          const uint32_t v = h[b];
+          if (v == 0) continue;
+          const uint32_t o = b / own;
+          red_cluster_add(cluster_map(smem_u32(&hrr[b - o * own]), o), v);
+        }
+        cluster_sync();
+        if (b0 < nb) {
+          const uint32_t o = b0 / own;
+          cc = ld_cluster_v4(cluster_map(smem_u32(&hrr[b0 - o * own]), o));
+        }
+      } else if (b0 < nb) {
+        cc = *reinterpret_cast<const uint4*>(&h[b0]);
+      }
+      const uint2 f = cl_find(cc, kk, S.wsh[1 + d], S.res);
+      pval |= f.x << shift;
+      pmask |= (nb - 1) << shift;
+      kk -= f.y;
+    }
+    T = pval;
+    const uint32_t need_eq = kk;
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      gt += i < nv && u[i] > T;
+      eq += i < nv && u[i] == T;
+    }
+    const uint32_t tot = cl_excl_scan((gt << 16) | eq, S.wsh[4]).y;
+    if (tid < static_cast<int>(csize)) st_cluster_u32(cluster_map(smem_u32(&S.counts[rank]), tid), tot);
+    if (multi) cluster_sync();   // the last access to another CTA's shared memory is before this
+    else __syncthreads();
+    uint32_t eq_before = 0;
+    base = 0;
+    for (uint32_t r = 0; r < rank; ++r) {
+      const uint32_t cr = S.counts[r];
+      const uint32_t e = cr & 0xFFFFu;
+      const uint32_t left = need_eq > eq_before ? need_eq - eq_before : 0u;
+      base += (cr >> 16) + min(e, left);
+      eq_before += e;
+    }
+    take = min(tot & 0xFFFFu, need_eq > eq_before ? need_eq - eq_before : 0u);
+  }
+
+  // ---- step 4: this CTA's selections in position order
   uint32_t gt = 0, eq = 0;
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i) {
     gt += i < nv && u[i] > T;
     eq += i < nv && u[i] == T;
   }
-  uint32_t tot;
-  const uint32_t excl = cl_excl_scan((gt << 16) | eq, wsh[3], tot);
-  if (threadIdx.x < csize) st_cluster_u32(cluster_map(smem_u32(&counts[rank]), threadIdx.x), tot);
-  if (multi) cluster_sync();   // the last access to another CTA's shared memory is before this
-  else __syncthreads();
-  // offsets of this CTA from the counts of the CTAs before it in the row
-  uint32_t eq_before = 0, base = 0;
-  for (uint32_t r = 0; r < rank; ++r) {
-    const uint32_t cr = counts[r];
-    const uint32_t e = cr & 0xFFFFu;
-    const uint32_t left = need_eq > eq_before ? need_eq - eq_before : 0u;
-    base += (cr >> 16) + min(e, left);
-    eq_before += e;
-  }
-  const uint32_t take = min(tot & 0xFFFFu, need_eq > eq_before ? need_eq - eq_before : 0u);   // equal keys taken here
+  const uint32_t excl = cl_excl_scan((gt << 16) | eq, S.wsh[6]).x;
   uint32_t eq_rank = excl & 0xFFFFu;
   uint32_t o = base + (excl >> 16) + min(eq_rank, take);
   uint32_t flags = 0;
@@ -586,19 +771,22 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   while (flags) {
     const int s = s0 + __ffs(flags) - 1;
     flags &= flags - 1;
-    if (o < static_cast<uint32_t>(p.k)) {   // exactly k are selected; the guard only bounds the stores
+    if (o < k) {   // exactly k are selected; the guard only bounds the stores
       out[o] = s;
       if (phys) phys[o] = one_block ? ((blk << p.log2_bs) | (s & bs_mask)) : emit_phys(p, btrow, s, bs_mask);
     }
     ++o;
   }
+  if (gathered && multi) cluster_wait();   // no CTA leaves while another may still read its candidates
 }
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained) {
   if (p.b.T == 0) return cudaSuccess;
   if (p.b.max_ctx <= kClMaxRow) {
     const unsigned csize = static_cast<unsigned>(cdiv(p.b.max_ctx, kClSlice));
-    return launch_ex(topk_cluster_kernel, dim3(csize, p.b.T), dim3(kClThreads), 0, st, chained, csize, p);
+    if (p.pre_hist)
+      return launch_ex(topk_cluster_kernel<true>, dim3(csize, p.b.T), dim3(kClThreads), 0, st, chained, csize, p);
+    return launch_ex(topk_cluster_kernel<false>, dim3(csize, p.b.T), dim3(kClThreads), 0, st, chained, csize, p);
   }
   const dim3 grid(p.nchunks, p.b.T);
   cudaError_t e = cudaMemsetAsync(p.zero_begin, 0, p.zero_bytes, st);

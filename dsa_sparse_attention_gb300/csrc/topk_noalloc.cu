@@ -98,5 +98,6 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_kv_layout* layout, const dsa_ba
   p.phys = phys_slots;
   p.log2_bs = log2_bs;
   p.status = reinterpret_cast<uint32_t*>(base);
+  p.pre_hist = nullptr;
   return record_cuda_status(launch_topk(p, stream, false));
 }

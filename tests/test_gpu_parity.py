@@ -101,6 +101,27 @@ def test_all_scores_tied_takes_lowest_positions():
     check_mla(OracleCache(wl), g, _np(out), _np(lse), [0, 1])
 
 
+def test_layer_step_dirty_workspace_hint():
+    # Inside a layer step the top-k starts from top-digit histograms the scorer
+    # leaves in the workspace, and leaves them zeroed.  A workspace whose bytes
+    # past the status word hold garbage (here all ones) gives the top-k a wrong
+    # hint, which it must detect and replace; the next step starts clean.  All
+    # three steps must equal the separate calls exactly.
+    wl = W.make_workload([65536, 40000, 9000, 3000, 2049], 1, seed=23)
+    dw = _dev(wl)
+    ref_scores = dw.indexer_scores()
+    ref_idx = _np(dw.topk_of(ref_scores))
+    ref_out, ref_lse = (_np(x) for x in dw.sparse_mla_of(torch.from_numpy(ref_idx).cuda()))
+    for dirty in (True, False, True):
+        if dirty:
+            dw.ws[256:].fill_(255)
+        idx, out, lse = dw.layer_step()
+        torch.cuda.synchronize()
+        assert np.array_equal(_np(idx), ref_idx)
+        assert np.array_equal(_np(out), ref_out) and np.array_equal(_np(lse), ref_lse)
+    check_topk(OracleCache(wl), ref_idx, list(range(wl.num_tokens)), dw.topk)
+
+
 @pytest.mark.parametrize("lens", [[65536, 9000, 3000, 1, 2048, 2049, 40000], [70000, 12345, 5]])
 def test_topk_heavy_ties_exact(lens):
     # Scores with five distinct values (and both signs of zero): the threshold
