@@ -235,6 +235,7 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     pools = [dw.pool] + [dw.pool.clone() for _ in range(N_POOL_COPIES - 1)]
     layouts = [dw.layout] + [dw.pool_copy_layout(pl) for pl in pools[1:]]
+    torch.cuda.synchronize()   # the copies (current stream) are complete before the bench stream reads them
     with torch.cuda.stream(stream):
         for lay in layouts:
             dw.layer_step(stream, lay)  # eager warm-up (sets kernel attributes)

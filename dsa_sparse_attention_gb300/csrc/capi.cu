@@ -247,7 +247,7 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   CUtensorMap kmap, qmap;
   if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return encode_fail();
   const int G = indexer_group_size(l->idx_fmt, T == b->num_reqs);
-  const bool direct = G == 1 && T <= 256;
+  const bool direct = G == 1 && T <= kDirectMaxT;
   uint32_t* status = at<uint32_t>(ws, wl.status);
   BatchView bv = batch_view(b);
   if (!direct) {

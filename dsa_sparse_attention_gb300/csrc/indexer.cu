@@ -124,9 +124,6 @@ __global__ void __launch_bounds__(1024) plan_groups_kernel(PlanParams p) {
 // ------------------------------------------------------------------- scorer
 
 
-// Decode batches of at most this many tokens, one per group, are planned inside
-// the scorer (no separate planning launch).
-constexpr int kDirectMaxT = 256;
 constexpr int kRowBatch = 32;      // tiles whose block-table rows a producer warp resolves at once (one per lane)
 constexpr int kHistBins = 2048;    // top-digit bins of the score histogram handed to the top-k
 
@@ -140,7 +137,7 @@ struct ScorerCfg {
   static constexpr bool MX = IDXF == 1;
   // Key stages are freed as soon as their MMA completes; the per-key scales the
   // epilogue reads live in a separate, longer ring of SSLOTS slots.
-  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 11 : 8);
+  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 12 : 8);
   static constexpr int SSLOTS = STAGES + 4;
   static constexpr int NBLK = MX ? 4 : 1;                   // accumulators per tile (scale blocks)
   static constexpr int ACC_COLS = 32 * G * NBLK;
@@ -178,6 +175,13 @@ struct ScorerCfg {
   static constexpr int MMA_WARP1 = PROD_WARP0 + NPROD - 1;   // MMA warps: 1 and MMA_WARP1 ..
   static constexpr int THREADS = 320 + 32 * CONV_WARPS + 32 * (NPROD - 1) + 32 * (NMMA - 1);
   static_assert(NACC % NMMA == 0, "accumulators per MMA warp");
+  // Tile i uses stage i % STAGES, producer i % NPROD, MMA warp i % NMMA and scale
+  // slot i % SSLOTS.  Each ring's length is a multiple of the number of warps
+  // taking tiles in turn, so every slot has one producer and one consumer warp and
+  // their parity waits never run two phases apart.
+  static_assert(STAGES % NPROD == 0 && STAGES % NMMA == 0, "key stages per producer and MMA warp");
+  static_assert(SSLOTS % NPROD == 0 && SSLOTS % 2 == 0, "scale slots per producer and epilogue set");
+  static_assert(NACC % 2 == 0, "accumulators per epilogue set");
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
   static_assert(SMEM_BYTES <= 232448, "smem");
 };

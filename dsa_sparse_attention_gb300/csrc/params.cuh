@@ -65,6 +65,9 @@ struct MlaParams {
 
 constexpr int kTopkChunk = 4096;   // scores per CTA in the top-k passes
 constexpr int kTopkClusterMaxRow = 65536;   // rows up to this long take the one-launch cluster top-k
+// Decode batches of at most this many tokens, one per group, are planned inside
+// the scorer (no separate planning launch).
+constexpr int kDirectMaxT = 128;
 constexpr int kTopkCap = 4096;     // candidates per row kept for the exact resolution
 
 // Byte offsets of the top-k scratch inside a region (256-byte aligned segments);

@@ -604,16 +604,14 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
         if (o < kClCap) S.cl[o] = u[i];
         ++o;
       }
-    if (tid < static_cast<int>(csize)) st_cluster_u32(cluster_map(smem_u32(&S.meta[rank]), tid), tot);
-    if (multi) {
-      if (pending) {
-        cluster_wait();
-        pending = false;
-      }
-      cluster_sync();
-    } else {
-      __syncthreads();
+    // every CTA of the cluster has started (and zeroed) before any writes into it
+    if (pending) {
+      cluster_wait();
+      pending = false;
     }
+    if (tid < static_cast<int>(csize)) st_cluster_u32(cluster_map(smem_u32(&S.meta[rank]), tid), tot);
+    if (multi) cluster_sync();
+    else __syncthreads();
     if (PRE && round == 0 && rank == 0) gh[tid] = make_uint4(0u, 0u, 0u, 0u);   // every CTA has read it
     G = 0;
     Cc = 0;
