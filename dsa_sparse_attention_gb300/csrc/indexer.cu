@@ -347,8 +347,8 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       // ------------------------------------------------------------ producers
       // Producer pid takes tiles tile_lo + pid + NPROD m.  Its warp resolves the
       // block-table rows of a batch of its tiles (every load of a lane issued
-      // before any is used); lane 0 walks the group cursor over all tiles, loads
-      // the queries of each group whose first tile it owns, and issues its tiles' copies.
+      // before any is used); lane 0 walks the group cursor over all tiles and
+      // issues its tiles' copies.
       const int pid = warp == 0 ? 0 : 1 + warp - C::PROD_WARP0;
       if (lane == 0 && pid == 0) {
         prefetch_tensormap(&kmap);
@@ -357,6 +357,34 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       const uint64_t stream_pol = l2_evict_first_policy();
       GroupCursor cur;
       cur.init(groups, ng, total, tile_lo);
+      // Producer 0 alone loads the queries, in group order, each group's before
+      // the first tile of it that another producer may issue; its waits for a
+      // free query buffer therefore never run two phases apart.  A group's
+      // buffer is reused two groups later (released by the MMA warps' commits and
+      // the epilogue warps).
+      GroupCursor qc;
+      qc.init(groups, ng, total, tile_lo);
+      int q_loaded = 0;                                              // groups whose queries are requested
+      auto load_q = [&](const ScoreGroup& grp, int count) -> bool {
+        const int qb = count & 1;
+        if (count >= 2 && !mbar_wait(&qempty[qb], ((count - 2) >> 1) & 1, ab)) return false;
+        for (int j = 0; j < grp.n; ++j) {
+          int req, pos;
+          if (p.direct) {
+            pos = grp.L - 1;
+          } else {
+            load_token(p.b, grp.t0 + j, p.status, req, pos);
+          }
+          possm[qb * G + j] = pos;
+        }
+        mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * (kIdxHeads * kIdxDim + kIdxHeads * 4));
+        for (int j = 0; j < grp.n; ++j)
+          tma_load_2d(smem + C::OFF_Q + qb * C::Q_BYTES + j * kIdxHeads * kIdxDim, &qmap, &qfull[qb], 0,
+                      (grp.t0 + j) * kIdxHeads);
+        bulk_load(wsm + qb * G * kIdxHeads, p.w + static_cast<int64_t>(grp.t0) * kIdxHeads,
+                  static_cast<uint32_t>(grp.n) * kIdxHeads * 4, &qfull[qb]);
+        return true;
+      };
       int walked = tile_lo;                                          // tile the cursor is at
       int issued = 0;                                                // this producer's tiles issued
       bool ok = true;
@@ -406,24 +434,9 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
             const int i = tile_lo + pid + (mb + jj) * C::NPROD;
             while (walked < i) cur.advance(++walked);
             const ScoreGroup& grp = cur.grp;
-            if (i == tile_lo || i == grp.tile_begin) {   // this producer loads the group's queries
-              const int qb = cur.count & 1;
-              if (cur.count >= 2 && !(ok = mbar_wait(&qempty[qb], ((cur.count - 2) >> 1) & 1, ab))) break;
-              for (int j = 0; j < grp.n; ++j) {
-                int req, pos;
-                if (p.direct) {
-                  pos = grp.L - 1;
-                } else {
-                  load_token(p.b, grp.t0 + j, p.status, req, pos);
-                }
-                possm[qb * G + j] = pos;
-              }
-              mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * (kIdxHeads * kIdxDim + kIdxHeads * 4));
-              for (int j = 0; j < grp.n; ++j)
-                tma_load_2d(smem + C::OFF_Q + qb * C::Q_BYTES + j * kIdxHeads * kIdxDim, &qmap, &qfull[qb], 0,
-                            (grp.t0 + j) * kIdxHeads);
-              bulk_load(wsm + qb * G * kIdxHeads, p.w + static_cast<int64_t>(grp.t0) * kIdxHeads,
-                        static_cast<uint32_t>(grp.n) * kIdxHeads * 4, &qfull[qb]);
+            if (pid == 0 && q_loaded == 0) {
+              if (!(ok = load_q(qc.grp, 0))) break;
+              q_loaded = 1;
             }
             const int it = i - tile_lo;
             const int s = it % C::STAGES;
@@ -452,6 +465,14 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
                              stream_pol);
             }
             ++issued;
+            if (pid == 0) {   // the queries of the groups starting within the next NPROD tiles
+              const int ahead = min(i + C::NPROD, tile_hi - 1);
+              while (ok && qc.next_begin <= ahead) {
+                qc.advance(qc.next_begin);
+                if ((ok = load_q(qc.grp, qc.count))) q_loaded = qc.count + 1;
+              }
+              if (!ok) break;
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -463,6 +484,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
           drain_wait(&full[it % C::STAGES], (it / C::STAGES) & 1);
           drain_wait(&sfull[it % C::SSLOTS], (it / C::SSLOTS) & 1);
         }
+        for (int c = q_loaded > 2 ? q_loaded - 2 : 0; c < q_loaded; ++c) drain_wait(&qfull[c & 1], (c >> 1) & 1);
       }
     } else if (warp == 1 || warp >= C::MMA_WARP1) {
       // ---------------------------------------------------------- MMA issuers
