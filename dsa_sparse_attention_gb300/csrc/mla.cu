@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
   uint64_t* o_done = bars + 13;
   uint64_t* drain = bars + 14;
   uint64_t* sum_done = bars + 15;
-  uint64_t* vfull = bars + 16;      // [4] last tile: V half-blocks 4..7, staged in the query region
+  uint64_t* v_all = bars + 16;      // last tile: every V half-block is in shared memory (one arrival per converter warp)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   int* rescale_sh = reinterpret_cast<int*>(smem + OFF_MISC + 16);
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(sum_done, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&vfull[i], CONV_WARPS);
+    mbar_init(v_all, CONV_WARPS);
     *abortf = 0;
     fence_mbar_init();
     // the query is an input of the call, not of the kernel before: load it now
@@ -305,35 +305,46 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           for (int k = 0; k < 4; ++k)
             mma_f16(tmem + S_COL, d_one + 2 * k, d_p + (kh * 8 + k * 2) * 64, idesc_sum, (kh | k) ? 1u : 0u);
         tc_commit(sum_done);
-        // PV; on the CTA's last tile, half-blocks 4..7 come from the query region (free
-        // once QK is done) instead of the ring, so none of them waits for a ring slot
+        // PV.  On the CTA's last tile, half-blocks 0..3 sit in the next four ring slots
+        // and 4..7 in the query region (free once QK is done): one wait covers all
+        // eight and the 32 MMAs issue back to back (each wait, fence and commit costs
+        // the issuing thread about as much as an MMA).  Earlier tiles go through the
+        // ring, which the next tile's chunks reuse.
         const bool last = j == j1 - 1;
+        if (last) {
+          if (!(ok = mbar_wait_inline(v_all, 0, ab))) break;
+          tc_fence_after();
 #pragma unroll 1
-        for (int v = 0; v < 4 && ok; ++v) {
-#pragma unroll 1
-          for (int kh = 0; kh < 2; ++kh) {
-            const int f = 2 * v + kh;
-            const bool in_q = last && f >= 4;
-            uint64_t a;
-            if (in_q) {
-              if (!(ok = mbar_wait_inline(&vfull[f - 4], 0, ab))) break;
-              a = d_vq + (f - 4) * kSlot;
-            } else {
-              if (!(ok = mbar_wait_inline(&ring_full[fc % RSLOTS], (fc / RSLOTS) & 1, ab))) break;
-              a = d_vr + (fc % RSLOTS) * kSlot;
-            }
-            tc_fence_after();
+          for (int v = 0; v < 4; ++v) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f16(tmem + O_COL + 96 * v, a + 128 * k, d_p + (kh * 8 + k * 2) * 64, idesc_pv,
-                      (jt > 0 || kh > 0 || k > 0) ? 1u : 0u);
-            if (!in_q) {
+            for (int kh = 0; kh < 2; ++kh) {
+              const int f = 2 * v + kh;
+              const uint64_t a = f < 4 ? d_vr + ((fc + f) % RSLOTS) * kSlot : d_vq + (f - 4) * kSlot;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f16(tmem + O_COL + 96 * v, a + 128 * k, d_p + (kh * 8 + k * 2) * 64, idesc_pv,
+                        (jt > 0 || kh > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          fc += 4;   // the ring slots are not handed back: no chunk follows on this CTA
+        } else {
+#pragma unroll 1
+          for (int v = 0; v < 4 && ok; ++v) {
+#pragma unroll 1
+            for (int kh = 0; kh < 2; ++kh) {
+              if (!(ok = mbar_wait_inline(&ring_full[fc % RSLOTS], (fc / RSLOTS) & 1, ab))) break;
+              const uint64_t a = d_vr + (fc % RSLOTS) * kSlot;
+              tc_fence_after();
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f16(tmem + O_COL + 96 * v, a + 128 * k, d_p + (kh * 8 + k * 2) * 64, idesc_pv,
+                        (jt > 0 || kh > 0 || k > 0) ? 1u : 0u);
               tc_commit(&ring_empty[fc % RSLOTS]);
               ++fc;
             }
           }
+          if (!ok) break;
         }
-        if (!ok) break;
         tc_commit(o_done);
       }
       if (!ok) {
@@ -392,8 +403,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
       }
       // Chunks are loaded through a short register pipeline inside rolled loops: the
       // code runs once per tile, and unrolled it would be fetched cold every time.
-      // Pull this half row into L2 first so the chunk loads that follow all hit it.
-      if (src) bulk_prefetch_l2(src + hf * (ROWB / 2), ROWB / 2);
       if (hf == 0) rowok[(jt & 1) * kSelTile + row] = src != nullptr;
       __syncwarp();
       if (lane == 0) mbar_arrive(rows_ready);
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cnt(in_q ? &vfull[f - 4] : &ring_full[slot], 2);
+          if (lane == 0 && !last) mbar_arrive_cnt(&ring_full[slot], 2);
           if (v + 2 < 4) {
             vbuf[u][0] = load_piece<NV>(src, 2 * v + 4, hf);
             vbuf[u][1] = load_piece<NV>(src, 2 * v + 5, hf);
@@ -477,6 +486,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         }
       }
       if (!ok) break;
+      if (last && lane == 0) mbar_arrive(v_all);   // after this warp's four fills (each fenced above)
       fc += last ? 4 : 8;
     }
   } else if (warp >= SOFT_WARP0) {
