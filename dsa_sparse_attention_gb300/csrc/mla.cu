@@ -66,6 +66,7 @@ constexpr int S_COL = 0;
 constexpr int O_COL = 128;
 constexpr float TAU = 8.0f;                       // log2 headroom before the running max moves
 static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0 && OFF_ONES % 1024 == 0, "align");
+static_assert(OFF_MUSE % 16 == 0 && OFF_ALPHA % 16 == 0, "per-head vectors are read 16 bytes at a time");
 static_assert(kMlaHeads * kVDim * 2 <= OFF_RING && kVDim * 208 <= OFF_RING, "output staging fits the query region");
 static_assert(4 * RING_SLOT <= OFF_RING, "four V half-blocks fit the query region");
 static_assert(SMEM_BYTES <= 232448, "smem");
@@ -175,6 +176,18 @@ __device__ __forceinline__ void piece_to_f16(const LatPiece& c, int q2, uint32_t
     nvfp4x16_to_f16(q2 ? make_uint2(c.a.z, c.a.w) : make_uint2(c.a.x, c.a.y), (c.s >> (8 * q2)) & 0xFFu, o);
   else
     e4m3x16_to_f16(q2 ? c.b : c.a, o);
+}
+
+// 32 consecutive floats of shared memory (16-byte aligned) through 8 vector loads.
+__device__ __forceinline__ void lds_f32x32(const float* src, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 x = reinterpret_cast<const float4*>(src)[i];
+    v[4 * i] = x.x;
+    v[4 * i + 1] = x.y;
+    v[4 * i + 2] = x.z;
+    v[4 * i + 3] = x.w;
+  }
 }
 
 __device__ __forceinline__ void sts128(uint8_t* p, const uint32_t* v) {
@@ -567,9 +580,9 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           DSA_TMEM_LD32(tmem + S_COL + 32 * c + lane_off, rr);
           tmem_wait_ld();
           float pv[32];
+          lds_f32x32(m_use + 32 * c, pv);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            pv[i] = valid ? ex2_fast(__uint_as_float(rr[i]) * p.scale_log2 - m_use[32 * c + i]) : 0.f;
+          for (int i = 0; i < 32; ++i) pv[i] = valid ? ex2_fast(__uint_as_float(rr[i]) * p.scale_log2 - pv[i]) : 0.f;
 #pragma unroll
           for (int cc4 = 0; cc4 < 4; ++cc4) {
             uint32_t o[4];
@@ -645,9 +658,11 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
           tmem_wait_ld();
           const int dim = v * 128 + quarter * 32 + lane;
+          float al[32];
+          lds_f32x32(alpha_sh + 32 * c, al);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(rr[i]) * alpha_sh[32 * c + i]);
+            const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(rr[i]) * al[i]);
             stage[(32 * c + i) * kVDim + dim] = *reinterpret_cast<const uint16_t*>(&bv);
           }
         }
@@ -670,14 +685,15 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
           DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
           tmem_wait_ld();
           uint8_t* row = stg + (v * 128 + quarter * 32 + lane) * PITCH + 64 * c;
+          float al[32];
+          lds_f32x32(alpha_sh + 32 * c, al);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t w4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int i = 8 * q + 2 * e;
-              const __half2 hv = __floats2half2_rn(__uint_as_float(rr[i]) * alpha_sh[32 * c + i],
-                                                   __uint_as_float(rr[i + 1]) * alpha_sh[32 * c + i + 1]);
+              const __half2 hv = __floats2half2_rn(__uint_as_float(rr[i]) * al[i], __uint_as_float(rr[i + 1]) * al[i + 1]);
               w4[e] = *reinterpret_cast<const uint32_t*>(&hv);
             }
             sts128(row + 16 * q, w4);
@@ -709,7 +725,7 @@ constexpr int kCombThreads = kCombDims * (kMlaHeads / 8);
 constexpr int kMaxSplits = kMaxTopk / kSelTile;
 __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) {
   __shared__ float2 mls[kMaxSplits][kMlaHeads];  // (max, sum) per split and head
-  __shared__ float wgt[kMaxSplits][kMlaHeads];   // normalised weight per split and head
+  __shared__ __align__(16) float wgt[kMaxSplits][kMlaHeads];   // normalised weight per split and head
   __shared__ __align__(16) __nv_bfloat16 tile[kMlaHeads][kCombDims];
   __shared__ int used[kMaxSplits];
   grid_dep_wait();
@@ -761,11 +777,14 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
   for (int j = 0; j < kMaxSplits; ++j) {
     if (j >= p.nsplit || !used[j]) continue;
     const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+    const float4 wa = *reinterpret_cast<const float4*>(&wgt[j][8 * g]);       // this thread's 8 heads' weights
+    const float4 wb = *reinterpret_cast<const float4*>(&wgt[j][8 * g + 4]);
+    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-      acc[2 * e] = fmaf(wgt[j][8 * g + 2 * e], f.x, acc[2 * e]);
-      acc[2 * e + 1] = fmaf(wgt[j][8 * g + 2 * e + 1], f.y, acc[2 * e + 1]);
+      acc[2 * e] = fmaf(wv[2 * e], f.x, acc[2 * e]);
+      acc[2 * e + 1] = fmaf(wv[2 * e + 1], f.y, acc[2 * e + 1]);
     }
   }
 #pragma unroll
