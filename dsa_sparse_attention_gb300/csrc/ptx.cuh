@@ -39,6 +39,10 @@ __device__ __forceinline__ uint32_t cluster_size() {
 // arrive are visible to every CTA of the cluster after the wait.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Arrive without ordering this thread's earlier memory operations (a signal only).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   cluster_arrive();
   cluster_wait();

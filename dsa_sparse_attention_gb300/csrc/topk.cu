@@ -552,7 +552,13 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   load16(row, s0, s0 + nv, u);
   __syncthreads();   // zeroed
   bool pending = multi;
-  if (multi) cluster_arrive();   // ... in every CTA before any CTA adds into them
+  // Every CTA has started (and zeroed) before any CTA writes into it.  With the hint
+  // the first writes come after the publishing barrier, which orders the zeroing, so
+  // this arrival is only a signal.
+  if (multi) {
+    if (PRE) cluster_arrive_relaxed();
+    else cluster_arrive();
+  }
   const uint32_t k = static_cast<uint32_t>(p.k);
 
   // ---- steps 1 and 2 (twice when a hint fails)
@@ -665,7 +671,8 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
     for (int m = 0; m < kClPer; ++m)
       if (static_cast<uint32_t>(tid + m * kClThreads) < Cc) atomicAdd(&S.h2[(lv[m] >> 10) & 2047u], 1u);
     __syncthreads();
-    if (multi) cluster_arrive();   // done with the other CTAs' shared memory (the wait is before the exit)
+    // done with the other CTAs' shared memory (their loads consumed above; the wait is before the exit)
+    if (multi) cluster_arrive_relaxed();
     const uint2 fA = cl_find(*reinterpret_cast<const uint4*>(&S.h2[4 * tid]), k - G, S.wsh[2], S.res);
     const uint32_t bA = fA.x, a2 = fA.y;
 #pragma unroll
