@@ -168,7 +168,7 @@ struct ScorerCfg {
   // One token per group: the epilogue counts the top 11 key bits of its first
   // token's scores in shared memory (later tokens go straight to global memory).
   static constexpr bool HIST = G == 1;
-  static constexpr int OFF_HIST = OFF_ROWS + NPROD * kRowBatch * 8 * 4;
+  static constexpr int OFF_HIST = (OFF_ROWS + NPROD * kRowBatch * 8 * 4 + 15) & ~15;   // zeroed 16 bytes at a time
   static constexpr int SMEM_BYTES = OFF_HIST + (HIST ? kHistBins * 4 : 0) + 1024;  // + slack for alignment
   static constexpr int CONV_WARPS = MX ? 8 : 0;
   static constexpr int PROD_WARP0 = 10 + CONV_WARPS;     // producer warps: 0 and PROD_WARP0 ..
@@ -184,6 +184,8 @@ struct ScorerCfg {
   static_assert(NACC % 2 == 0, "accumulators per epilogue set");
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
   static_assert(SMEM_BYTES <= 232448, "smem");
+  static_assert(OFF_HIST % 16 == 0 && OFF_Q % 1024 == 0 && OFF_SCALES % 16 == 0 && OFF_W % 16 == 0 && OFF_BARS % 8 == 0,
+                "alignment of the shared-memory regions");
 };
 
 // 4 e2m1 codes (low 16 bits of w, element 0 in the lowest nibble) -> 4 e4m3 bytes.
@@ -285,58 +287,73 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   grid_dep_launch();   // a chained top-k may be scheduled as this grid's CTAs retire
 
   // Plan: groups of tokens and their key-tile ranges.  In direct mode every token
-  // is its own group and the plan is built here from q_req / q_pos (one global
-  // round trip); otherwise plan_groups_kernel wrote it to the workspace.
-  __shared__ int scan_sh[32];
-  const ScoreGroup* groups;
-  int total, ng;
-  if (p.direct) {
-    ScoreGroup* sg = reinterpret_cast<ScoreGroup*>(smem + C::OFF_PLAN);
-    int* plan_total = reinterpret_cast<int*>(smem + C::OFF_PLAN + kDirectMaxT * 32);
+  // is its own group and warp 0 builds the plan here from q_req / q_pos (one global
+  // round trip, a warp scan, no block barrier of its own); otherwise
+  // plan_groups_kernel wrote it to the workspace.
+  ScoreGroup* sg = reinterpret_cast<ScoreGroup*>(smem + C::OFF_PLAN);
+  int* plan_total = reinterpret_cast<int*>(smem + C::OFF_PLAN + kDirectMaxT * 32);
+  if (p.direct && warp == 0) {
+    constexpr int PER = kDirectMaxT / 32;
     const int T = p.b.T;
-    int req = 0, L = 0, tiles = 0;
-    if (static_cast<int>(threadIdx.x) < T) {
-      int r = __ldg(p.b.q_req + threadIdx.x);
-      int pos = __ldg(p.b.q_pos + threadIdx.x);
-      bool bad = false;
-      if (r < 0 || r >= p.b.B) { bad = true; r = r < 0 ? 0 : p.b.B - 1; }
-      if (pos < 0 || pos >= p.b.max_ctx) { bad = true; pos = pos < 0 ? 0 : p.b.max_ctx - 1; }
-      if (bad) atomicOr(p.status, DEV_BAD_BATCH);
-      req = r;
-      L = pos + 1;
-      tiles = static_cast<int>(cdiv(L, kKeyTile));
+    int rq[PER], ps[PER];
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {   // every load issued before any is used
+      const int t = lane + 32 * m;
+      rq[m] = t < T ? __ldg(p.b.q_req + t) : 0;
+      ps[m] = t < T ? __ldg(p.b.q_pos + t) : 0;
     }
-    const int incl = block_inclusive_scan(tiles, scan_sh, OpAdd(), 0);
-    if (static_cast<int>(threadIdx.x) < T) {
-      ScoreGroup g;
-      g.t0 = threadIdx.x;
-      g.n = 1;
-      g.req = req;
-      g.L = L;
-      g.tile_begin = incl - tiles;
-      sg[threadIdx.x] = g;
+    int carry = 0;
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      if (32 * m >= T) break;   // uniform: only the warps' worth of tokens present
+      const int t = lane + 32 * m;
+      int r = rq[m], pos = ps[m], tiles = 0;
+      if (t < T) {
+        bool bad = false;
+        if (r < 0 || r >= p.b.B) { bad = true; r = r < 0 ? 0 : p.b.B - 1; }
+        if (pos < 0 || pos >= p.b.max_ctx) { bad = true; pos = pos < 0 ? 0 : p.b.max_ctx - 1; }
+        if (bad) atomicOr(p.status, DEV_BAD_BATCH);
+        tiles = static_cast<int>(cdiv(pos + 1, kKeyTile));
+      }
+      int x = tiles;   // inclusive scan over the warp
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (t < T) {
+        ScoreGroup g;
+        g.t0 = t;
+        g.n = 1;
+        g.req = r;
+        g.L = pos + 1;
+        g.tile_begin = carry + x - tiles;
+        sg[t] = g;
+      }
+      carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (threadIdx.x == blockDim.x - 1) *plan_total = incl;
-    __syncthreads();
-    groups = sg;
-    ng = T;
-    total = *plan_total;
-  } else {
-    groups = p.groups;
-    total = p.hdr->total_tiles;
-    ng = p.hdr->n_groups;
+    if (lane == 0) *plan_total = carry;
   }
-  const int tile_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
-  const int tile_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
-
   uint32_t* hs = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
   const bool hist_on = C::HIST && p.row_hist != nullptr;
   if (hist_on)
-    for (int i = threadIdx.x; i < kHistBins; i += C::THREADS) hs[i] = 0;
+    for (int i = threadIdx.x; i < kHistBins / 4; i += C::THREADS) reinterpret_cast<uint4*>(hs)[i] = make_uint4(0, 0, 0, 0);
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();   // the plan, the histogram zeroing and the TMEM address are visible
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  const ScoreGroup* groups = p.direct ? sg : p.groups;
+  const int total = p.direct ? *plan_total : p.hdr->total_tiles;
+  const int ng = p.direct ? p.b.T : p.hdr->n_groups;
+  // this CTA's contiguous range of the global tile enumeration (32-bit products when they fit)
+  int tile_lo, tile_hi;
+  if (static_cast<uint64_t>(total) * gridDim.x < (1ull << 32)) {
+    tile_lo = static_cast<int>(blockIdx.x * static_cast<uint32_t>(total) / gridDim.x);
+    tile_hi = static_cast<int>((blockIdx.x + 1) * static_cast<uint32_t>(total) / gridDim.x);
+  } else {
+    tile_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
+    tile_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
+  }
   const Abort ab{abortf, p.status};
   const int bs = p.pool.bs;
   const int box = bs < kKeyTile ? bs : kKeyTile;   // keys per TMA box
