@@ -715,7 +715,8 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
 }
 
 // Log-sum-exp combine of the split partials (each partial normalised by its
-// own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m).
+// own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m);
+// one thread per head computes the weights.
 // Grid (512 / 32 dims, T), 384 threads: thread = (dim of the block's 32, group of 8
 // heads); every split's 16 bytes are loaded at once, before the weights.  Splits
 // with nothing selected (sum 0) take no part in the sum.  The [96 heads x 32 dims] result is
@@ -724,7 +725,6 @@ constexpr int kCombDims = 32;
 constexpr int kCombThreads = kCombDims * (kMlaHeads / 8);
 constexpr int kMaxSplits = kMaxTopk / kSelTile;
 __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) {
-  __shared__ float2 mls[kMaxSplits][kMlaHeads];  // (max, sum) per split and head
   __shared__ __align__(16) float wgt[kMaxSplits][kMlaHeads];   // normalised weight per split and head
   __shared__ __align__(16) __nv_bfloat16 tile[kMlaHeads][kCombDims];
   __shared__ int used[kMaxSplits];
@@ -741,32 +741,34 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
 #pragma unroll
   for (int j = 0; j < kMaxSplits; ++j)
     if (j < p.nsplit) u[j] = __ldcg(reinterpret_cast<const uint4*>(p.part_o + ((base + j) * kVDim + d) * kMlaHeads + 8 * g));
-  // weights: (max, sum) of every split staged in shared memory, then four threads per
-  // head (splits q, q + 4, ...) reduce with two shuffle steps
-  for (int i = threadIdx.x; i < p.nsplit * kMlaHeads; i += kCombThreads)
-    mls[i / kMlaHeads][i % kMlaHeads] = __ldcg(p.part_ml + base * kMlaHeads + i);
-  __syncthreads();
-  {
-    const int h = threadIdx.x >> 2, q = threadIdx.x & 3;
+  // weights: thread h < 96 owns head h; its (max, sum) of every split come straight
+  // from global memory, all loads in flight at once (alongside the partials above)
+  if (threadIdx.x < kMlaHeads) {
+    const int h = threadIdx.x;
+    float2 ml[kMaxSplits];
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j)
+      ml[j] = j < p.nsplit ? __ldcg(p.part_ml + (base + j) * kMlaHeads + h) : make_float2(-INFINITY, 0.f);
     float M = -INFINITY;
-    for (int j = q; j < p.nsplit; j += 4)
-      if (mls[j][h].y > 0.f) M = fmaxf(M, mls[j][h].x);
-    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j)
+      if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
+    float w[kMaxSplits];
     float L = 0.f;
-    for (int j = q; j < p.nsplit; j += 4) {
-      const float w = mls[j][h].y > 0.f ? exp2f(mls[j][h].x - M) * mls[j][h].y : 0.f;
-      wgt[j][h] = w;
-      L += w;
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j) {
+      w[j] = ml[j].y > 0.f ? exp2f(ml[j].x - M) * ml[j].y : 0.f;
+      L += w[j];
     }
-    L += __shfl_xor_sync(0xffffffffu, L, 1);
-    L += __shfl_xor_sync(0xffffffffu, L, 2);
     const float inv = 1.f / L;
-    for (int j = q; j < p.nsplit; j += 4) {
-      wgt[j][h] *= inv;
-      if (h == 0) used[j] = mls[j][0].y > 0.f;   // a split is empty for all heads or for none
-    }
-    if (q == 0 && p.lse && blockIdx.x == 0)
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j)
+      if (j < p.nsplit) wgt[j][h] = w[j] * inv;
+    if (h == 0)
+#pragma unroll
+      for (int j = 0; j < kMaxSplits; ++j)
+        if (j < p.nsplit) used[j] = ml[j].y > 0.f;   // a split is empty for all heads or for none
+    if (p.lse && blockIdx.x == 0)
       p.lse[static_cast<int64_t>(t) * kMlaHeads + h] = (M + log2f(L)) * 0.69314718055994531f;
   }
   __syncthreads();
