@@ -67,6 +67,17 @@ def test_ragged_multi_request_decode():
     _run_all(wl)
 
 
+def test_decode_batch_planned_by_kernel():
+    # 160 single-token requests: more than the scorer plans inside itself, so the
+    # planning kernel lays out the tiles; the layer step's histogram hand-off and the
+    # separate calls must agree, and sampled tokens match the oracle.
+    rng = np.random.default_rng(41)
+    lens = [int(x) for x in rng.integers(1, 4000, size=160)]
+    lens[:4] = [1, 2048, 2049, 3999]
+    wl = W.make_workload(lens, 1, seed=41, permute=True)
+    _run_all(wl, tokens=[0, 1, 2, 3, 50, 99, 159])
+
+
 def test_mtp_groups_of_six():
     wl = W.make_workload([3000, 5000, 9001], 6, seed=12, permute=True, pool_rows=300)
     _run_all(wl)
