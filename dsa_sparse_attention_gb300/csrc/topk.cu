@@ -426,7 +426,7 @@ constexpr int kClZeroWords = kBins + kClOwn + kBins + 1024 + kClOwn + kClOwn / 2
 // Exclusive scan of one value per thread over the block with a single barrier:
 // (this thread's exclusive prefix, block total); `wsh` must not be in use by
 // another call until a later barrier.
-__device__ __noinline__ uint2 cl_excl_scan(uint32_t v, uint32_t* wsh) {
+__device__ __forceinline__ uint2 cl_excl_scan(uint32_t v, uint32_t* wsh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
@@ -457,7 +457,7 @@ __device__ __forceinline__ uint2 cl_block_sum2(uint32_t x, uint32_t y, uint32_t*
 // Thread i holds bins 4i .. 4i+3 (ascending key order) of a histogram.  Finds the
 // bin holding the kk-th largest element (1 <= kk <= total) and the number of
 // elements in higher bins, as (bin, above); two barriers.
-__device__ __noinline__ uint2 cl_find(uint4 c, uint32_t kk, uint32_t* wsh, uint32_t* res) {
+__device__ __forceinline__ uint2 cl_find(uint4 c, uint32_t kk, uint32_t* wsh, uint32_t* res) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t s = c.x + c.y + c.z + c.w;
   uint32_t x = s;   // becomes the sum over lanes >= this one (higher bins)
