@@ -440,18 +440,28 @@ __device__ __forceinline__ uint2 cl_excl_scan(uint32_t v, uint32_t* wsh) {
   return make_uint2(__reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) + x - v, __reduce_add_sync(0xffffffffu, wv));
 }
 
-// Block sums of two values per thread, one barrier; `wsh` as above (32 words).
-__device__ __forceinline__ uint2 cl_block_sum2(uint32_t x, uint32_t y, uint32_t* wsh) {
+// Exclusive scan of v over the block and block sums of x and y, with one barrier;
+// `wa`, `wb`: two scratch rows (32 words each) not in use by another call until a
+// later barrier.  Returns the scan; x and y become the sums.
+__device__ __forceinline__ uint32_t cl_scan_sum2(uint32_t v, uint32_t& x, uint32_t& y, uint32_t* wa, uint32_t* wb) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  x = __reduce_add_sync(0xffffffffu, x);
-  y = __reduce_add_sync(0xffffffffu, y);
+  uint32_t s = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t z = __shfl_up_sync(0xffffffffu, s, o);
+    if (lane >= o) s += z;
+  }
+  const uint32_t xs = __reduce_add_sync(0xffffffffu, x), ys = __reduce_add_sync(0xffffffffu, y);
+  if (lane == 31) wa[warp] = s;
   if (lane == 0) {
-    wsh[warp] = x;
-    wsh[kClWarps + warp] = y;
+    wb[warp] = xs;
+    wb[kClWarps + warp] = ys;
   }
   __syncthreads();
-  return make_uint2(__reduce_add_sync(0xffffffffu, lane < kClWarps ? wsh[lane] : 0u),
-                    __reduce_add_sync(0xffffffffu, lane < kClWarps ? wsh[kClWarps + lane] : 0u));
+  const uint32_t wv = lane < kClWarps ? wa[lane] : 0u;
+  x = __reduce_add_sync(0xffffffffu, lane < kClWarps ? wb[lane] : 0u);
+  y = __reduce_add_sync(0xffffffffu, lane < kClWarps ? wb[kClWarps + lane] : 0u);
+  return __reduce_add_sync(0xffffffffu, lane < warp ? wv : 0u) + s - v;
 }
 
 // Thread i holds bins 4i .. 4i+3 (ascending key order) of a histogram.  Finds the
@@ -631,7 +641,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
 
   // ---- step 3: the threshold key T, the keys equal to T to take (need_eq), and
   // this CTA's share: selections before it (base) and equal keys taken here (take)
-  uint32_t T, base, take;
+  uint32_t T, base, take, excl;   // excl: this thread's (above T) << 16 | (equal to T) before it in the CTA
   const bool gathered = Cc <= static_cast<uint32_t>(kClCap);
   if (gathered) {
     // cum[r]: candidates of the CTAs before r (all ones past the cluster)
@@ -692,10 +702,18 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
       if (g < lo) x += (static_cast<uint32_t>(lv[m] > T) << 16) | static_cast<uint32_t>(lv[m] == T);
       else if (g < hi) y += lv[m] == T;
     }
-    const uint2 xy = cl_block_sum2(x, y, S.wsh[4]);
-    const uint32_t eq_lo = min(xy.x & 0xFFFFu, need_eq);
-    base = G_lo + (xy.x >> 16) + eq_lo;
-    take = min(xy.y, need_eq - eq_lo);
+    // this CTA's keys above / equal to T, scanned in position order, together with
+    // the sums of x and y (one barrier)
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      gt += i < nv && u[i] > T;
+      eq += i < nv && u[i] == T;
+    }
+    excl = cl_scan_sum2((gt << 16) | eq, x, y, S.wsh[4], S.wsh[5]);
+    const uint32_t eq_lo = min(x & 0xFFFFu, need_eq);
+    base = G_lo + (x >> 16) + eq_lo;
+    take = min(y, need_eq - eq_lo);
   } else {
     // digits 2 and 3 through the cluster (owned bins in hr2 / hr3)
     uint32_t pmask = 0xFFE00000u, pval = static_cast<uint32_t>(b1) << 21, kk = k - G;
@@ -740,7 +758,9 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
       gt += i < nv && u[i] > T;
       eq += i < nv && u[i] == T;
     }
-    const uint32_t tot = cl_excl_scan((gt << 16) | eq, S.wsh[4]).y;
+    const uint2 sc = cl_excl_scan((gt << 16) | eq, S.wsh[4]);
+    const uint32_t tot = sc.y;
+    excl = sc.x;
     if (tid < static_cast<int>(csize)) st_cluster_u32(cluster_map(smem_u32(&S.counts[rank]), tid), tot);
     if (multi) cluster_sync();   // the last access to another CTA's shared memory is before this
     else __syncthreads();
@@ -757,13 +777,6 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   }
 
   // ---- step 4: this CTA's selections in position order
-  uint32_t gt = 0, eq = 0;
-#pragma unroll
-  for (int i = 0; i < kPerThread; ++i) {
-    gt += i < nv && u[i] > T;
-    eq += i < nv && u[i] == T;
-  }
-  const uint32_t excl = cl_excl_scan((gt << 16) | eq, S.wsh[6]).x;
   uint32_t eq_rank = excl & 0xFFFFu;
   uint32_t o = base + (excl >> 16) + min(eq_rank, take);
   uint32_t flags = 0;
