@@ -678,25 +678,31 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
         // stores), then copied out with coalesced 16-byte stores
         constexpr int PITCH = 208;
         uint8_t* stg = smem + OFF_Q;   // the query is no longer read
+        // this warp's head chunk c = which for the four dim blocks, two blocks per TMEM wait
+        const int c = which;
+        float al[32];
+        lds_f32x32(alpha_sh + 32 * c, al);
 #pragma unroll 1
-        for (int pc = which; pc < 12; pc += 3) {
-          const int v = pc / 3, c = pc % 3;
-          uint32_t rr[32];
-          DSA_TMEM_LD32(tmem + O_COL + 96 * v + 32 * c + lane_off, rr);
+        for (int v2 = 0; v2 < 4; v2 += 2) {
+          uint32_t rr[2][32];
+          DSA_TMEM_LD32(tmem + O_COL + 96 * v2 + 32 * c + lane_off, rr[0]);
+          DSA_TMEM_LD32(tmem + O_COL + 96 * (v2 + 1) + 32 * c + lane_off, rr[1]);
           tmem_wait_ld();
-          uint8_t* row = stg + (v * 128 + quarter * 32 + lane) * PITCH + 64 * c;
-          float al[32];
-          lds_f32x32(alpha_sh + 32 * c, al);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w4[4];
+          for (int b = 0; b < 2; ++b) {
+            uint8_t* row = stg + ((v2 + b) * 128 + quarter * 32 + lane) * PITCH + 64 * c;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = 8 * q + 2 * e;
-              const __half2 hv = __floats2half2_rn(__uint_as_float(rr[i]) * al[i], __uint_as_float(rr[i + 1]) * al[i + 1]);
-              w4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 8 * q + 2 * e;
+                const __half2 hv =
+                    __floats2half2_rn(__uint_as_float(rr[b][i]) * al[i], __uint_as_float(rr[b][i + 1]) * al[i + 1]);
+                w4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+              sts128(row + 16 * q, w4);
             }
-            sts128(row + 16 * q, w4);
           }
         }
         named_bar_sync(2, 384);
