@@ -21,12 +21,15 @@
 //                 those of chunks < c, so the output is ascending, deterministic
 //                 and independent of the rest of the batch.
 // Rows of at most 65,536 scores take a one-launch path instead: a cluster of up
-// to eight CTAs per row keeps the row in registers (16 scores per thread) and
-// resolves all three digits (11 + 11 + 10 bits) of the threshold key, the
-// position cut and the output offsets; each CTA adds the non-empty bins of its
-// histograms into every CTA's copy of the merged histogram through distributed
-// shared memory, so each digit costs one cluster barrier.  It needs no global
-// scratch and no zeroing.
+// to eight CTAs per row keeps the row in registers (16 scores per thread).  The
+// top digit's histogram comes from the scorer (inside a layer step, verified by
+// exact counts) or is merged through distributed shared memory; each CTA then
+// lists its keys in the threshold digit, every CTA gathers the row's list and
+// resolves the remaining two digits (11 + 10 bits) and the position cut locally,
+// and each CTA writes its selections after those of the CTAs before it.  Heavy
+// ties (more than 4,096 keys in the threshold digit) resolve the two digits
+// through the cluster instead.  No global scratch (the hint histograms are left
+// zeroed for the next layer step).
 #include "params.cuh"
 
 namespace dsa {
