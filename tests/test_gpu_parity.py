@@ -112,20 +112,22 @@ def test_all_scores_tied_takes_lowest_positions():
     check_mla(OracleCache(wl), g, _np(out), _np(lse), [0, 1])
 
 
-def test_layer_step_all_scores_tied_long_rows():
+@pytest.mark.parametrize("lens", [[65536, 40000, 9000], [6000, 8000]])
+def test_layer_step_all_scores_tied_long_rows(lens):
     # w = 0: every score is 0, so the whole row shares the threshold key.  Inside a
     # layer step the top-k starts from the scorer's histogram (one full bin), finds more
-    # candidates than it gathers and resolves the cut through the cluster; the result is
-    # the lowest k positions of each row.
-    wl = W.make_workload([65536, 40000, 9000], 1, seed=29)
+    # candidates than it gathers and resolves the cut through the cluster (or, for rows
+    # of at most 8,192 scores, inside one CTA); the result is the lowest k positions.
+    wl = W.make_workload(lens, 1, seed=29)
     wl.w[:] = 0
     dw = _dev(wl)
+    toks = list(range(len(lens)))
     for _ in range(2):   # the second step starts from the histograms the first left zeroed
         idx, out, lse = dw.layer_step()
         g = _np(idx)
-        for t in range(3):
+        for t in toks:
             assert np.array_equal(g[t], np.arange(2048)), f"token {t}"
-    check_mla(OracleCache(wl), g, _np(out), _np(lse), [0, 1, 2])
+    check_mla(OracleCache(wl), g, _np(out), _np(lse), toks)
 
 
 def test_layer_step_dirty_workspace_hint():
