@@ -406,7 +406,7 @@ constexpr int kClMaxCtas = 8;                       // portable cluster size
 constexpr int kClMaxRow = kClSlice * kClMaxCtas;    // 65,536
 constexpr int kClOwn = kBins / 2;                   // bins a CTA owns when the cluster has >= 2 CTAs
 constexpr int kClCap = 4096;                        // candidates of a row gathered into every CTA
-constexpr int kClPer = kClCap / kClThreads;         // ... 8 per thread
+constexpr int kClPer4 = (kClCap / 4 + kClMaxCtas + kClThreads - 1) / kClThreads;   // 16-byte groups per thread (padded lists)
 static_assert(kClThreads * 4 == kBins, "one thread per four bins of the top digit");
 static_assert(kClMaxRow == kTopkClusterMaxRow, "row limit of the cluster path");
 
@@ -623,6 +623,13 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
         if (o < kClCap) S.cl[o] = u[i];
         ++o;
       }
+    // the list padded to a multiple of four keys (read back 16 bytes at a time) with
+    // keys outside digit b1, which every later pass skips
+    if (tid < 3) {
+      const uint32_t n_here = tot & 0xFFFFu, pad = n_here + static_cast<uint32_t>(tid);
+      if ((pad & ~3u) == (n_here & ~3u) && (n_here & 3u) != 0 && pad < static_cast<uint32_t>(kClCap))
+        S.cl[pad] = static_cast<uint32_t>(b1 ^ 1) << 21;
+    }
     // every CTA of the cluster has started (and zeroed) before any writes into it
     if (pending) {
       cluster_wait();
@@ -647,63 +654,76 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   uint32_t T, base, take, excl;   // excl: this thread's (above T) << 16 | (equal to T) before it in the CTA
   const bool gathered = Cc <= static_cast<uint32_t>(kClCap);
   if (gathered) {
-    // cum[r]: candidates of the CTAs before r (all ones past the cluster)
-    uint32_t cum[kClMaxCtas];
-    uint32_t lo = 0, G_lo = 0;
-    {
-      uint32_t acc = 0;
+    // cum4[r]: 16-byte groups of the padded lists of the CTAs before r (all ones past
+    // the cluster); lo4 / hi4: this CTA's groups
+    uint32_t cum4[kClMaxCtas];
+    uint32_t lo4 = 0, hi4 = 0, G_lo = 0, n4 = 0;
 #pragma unroll
-      for (int r = 0; r < kClMaxCtas; ++r) {
-        cum[r] = r < static_cast<int>(csize) ? acc : 0xFFFFFFFFu;
-        if (r < static_cast<int>(csize)) {
-          const uint32_t m = S.meta[r];
-          if (static_cast<uint32_t>(r) < rank) G_lo += m >> 16;
-          if (static_cast<uint32_t>(r) == rank) lo = acc;
-          acc += m & 0xFFFFu;
-        }
+    for (int r = 0; r < kClMaxCtas; ++r) {
+      cum4[r] = r < static_cast<int>(csize) ? n4 : 0xFFFFFFFFu;
+      if (r < static_cast<int>(csize)) {
+        const uint32_t m = S.meta[r];
+        if (static_cast<uint32_t>(r) < rank) G_lo += m >> 16;
+        if (static_cast<uint32_t>(r) == rank) lo4 = n4;
+        n4 += ((m & 0xFFFFu) + 3u) >> 2;
+        if (static_cast<uint32_t>(r) == rank) hi4 = n4;
       }
     }
-    const uint32_t hi = lo + (S.meta[rank] & 0xFFFFu);
-    uint32_t lv[kClPer];
+    const uint32_t in_b1 = static_cast<uint32_t>(b1);
+    uint4 lv[kClPer4];
 #pragma unroll
-    for (int m = 0; m < kClPer; ++m) {
-      const uint32_t g = static_cast<uint32_t>(tid + m * kClThreads);
-      lv[m] = 0;
-      if (g < Cc) {
+    for (int m = 0; m < kClPer4; ++m) {
+      const uint32_t g4 = static_cast<uint32_t>(tid + m * kClThreads);
+      lv[m] = make_uint4(0u, 0u, 0u, 0u);
+      if (g4 < n4) {
         uint32_t r = 0, br = 0;
 #pragma unroll
         for (int q = 1; q < kClMaxCtas; ++q)
-          if (g >= cum[q]) {
+          if (g4 >= cum4[q]) {
             r = static_cast<uint32_t>(q);
-            br = cum[q];
+            br = cum4[q];
           }
-        lv[m] = ld_cluster_u32(cluster_map(smem_u32(&S.cl[g - br]), r));
+        lv[m] = ld_cluster_v4(cluster_map(smem_u32(&S.cl[4 * (g4 - br)]), r));
       }
     }
 #pragma unroll
-    for (int m = 0; m < kClPer; ++m)
-      if (static_cast<uint32_t>(tid + m * kClThreads) < Cc) atomicAdd(&S.h2[(lv[m] >> 10) & 2047u], 1u);
+    for (int m = 0; m < kClPer4; ++m) {
+      const uint32_t kv[4] = {lv[m].x, lv[m].y, lv[m].z, lv[m].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (static_cast<uint32_t>(tid + m * kClThreads) < n4 && (kv[e] >> 21) == in_b1)
+          atomicAdd(&S.h2[(kv[e] >> 10) & 2047u], 1u);
+    }
     __syncthreads();
     // done with the other CTAs' shared memory (their loads consumed above; the wait is before the exit)
     if (multi) cluster_arrive_relaxed();
     const uint2 fA = cl_find(*reinterpret_cast<const uint4*>(&S.h2[4 * tid]), k - G, S.wsh[2], S.res);
     const uint32_t bA = fA.x, a2 = fA.y;
+    const uint32_t pre2 = (in_b1 << 11) | bA;
 #pragma unroll
-    for (int m = 0; m < kClPer; ++m)
-      if (static_cast<uint32_t>(tid + m * kClThreads) < Cc && ((lv[m] >> 10) & 2047u) == bA)
-        atomicAdd(&S.h3[lv[m] & 1023u], 1u);
+    for (int m = 0; m < kClPer4; ++m) {
+      const uint32_t kv[4] = {lv[m].x, lv[m].y, lv[m].z, lv[m].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (static_cast<uint32_t>(tid + m * kClThreads) < n4 && (kv[e] >> 10) == pre2) atomicAdd(&S.h3[kv[e] & 1023u], 1u);
+    }
     __syncthreads();
     const uint2 fB = cl_find(tid < 256 ? *reinterpret_cast<const uint4*>(&S.h3[4 * tid]) : make_uint4(0u, 0u, 0u, 0u),
                              k - G - a2, S.wsh[3], S.res);
     const uint32_t a3 = fB.y;
-    T = (static_cast<uint32_t>(b1) << 21) | (bA << 10) | fB.x;
+    T = (in_b1 << 21) | (bA << 10) | fB.x;
     const uint32_t need_eq = k - G - a2 - a3;
     uint32_t x = 0, y = 0;   // candidates of earlier CTAs above | equal to T; this CTA's equal to T
 #pragma unroll
-    for (int m = 0; m < kClPer; ++m) {
-      const uint32_t g = static_cast<uint32_t>(tid + m * kClThreads);
-      if (g < lo) x += (static_cast<uint32_t>(lv[m] > T) << 16) | static_cast<uint32_t>(lv[m] == T);
-      else if (g < hi) y += lv[m] == T;
+    for (int m = 0; m < kClPer4; ++m) {
+      const uint32_t g4 = static_cast<uint32_t>(tid + m * kClThreads);
+      const uint32_t kv[4] = {lv[m].x, lv[m].y, lv[m].z, lv[m].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((kv[e] >> 21) != in_b1) continue;   // padding
+        if (g4 < lo4) x += (static_cast<uint32_t>(kv[e] > T) << 16) | static_cast<uint32_t>(kv[e] == T);
+        else if (g4 < hi4) y += kv[e] == T;
+      }
     }
     // this CTA's keys above / equal to T, scanned in position order, together with
     // the sums of x and y (one barrier)
