@@ -468,8 +468,9 @@ __device__ __forceinline__ uint32_t cl_scan_sum2(uint32_t v, uint32_t& x, uint32
 }
 
 // Thread i holds bins 4i .. 4i+3 (ascending key order) of a histogram.  Finds the
-// bin holding the kk-th largest element (1 <= kk <= total) and the number of
-// elements in higher bins, as (bin, above); two barriers.
+// bin holding the kk-th largest element (kk >= 1) and the number of elements in
+// higher bins, as (bin, above); (~0u, 0) when the histogram holds fewer than kk.
+// Two barriers.
 __device__ __forceinline__ uint2 cl_find(uint4 c, uint32_t kk, uint32_t* wsh, uint32_t* res) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t s = c.x + c.y + c.z + c.w;
@@ -483,6 +484,7 @@ __device__ __forceinline__ uint2 cl_find(uint4 c, uint32_t kk, uint32_t* wsh, ui
   __syncthreads();
   const uint32_t wv = lane < kClWarps ? wsh[lane] : 0u;
   uint32_t cum = __reduce_add_sync(0xffffffffu, lane > warp ? wv : 0u) + x - s;
+  const uint32_t total = __reduce_add_sync(0xffffffffu, wv);
   if (cum < kk && cum + s >= kk) {
     int b = 4 * static_cast<int>(threadIdx.x) + 3;
     if (cum + c.w < kk) {
@@ -499,6 +501,10 @@ __device__ __forceinline__ uint2 cl_find(uint4 c, uint32_t kk, uint32_t* wsh, ui
     }
     res[0] = static_cast<uint32_t>(b);
     res[1] = cum;
+  } else if (threadIdx.x == 0 && total < kk) {
+    // fewer than kk elements (only a hint histogram can be short): no bin, ~0u
+    res[0] = 0xFFFFFFFFu;
+    res[1] = 0u;
   }
   __syncthreads();
   return make_uint2(res[0], res[1]);
