@@ -78,6 +78,19 @@ def dist_info():
     return rank, world, local
 
 
+def job_rate(ms_local, world, device="cpu"):
+    """Replicas: the job's step time is the slowest rank's; the job's rate is the
+    steps of all ranks over it.  Returns (ms, layer-steps/s)."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * 1000.0 / ms
+
+
 def algorithmic_bytes(wl, idx):
     """Bytes the method must move for one step: every index key of each context,
     the latents of the union of selected tokens per request, the query tensors
@@ -282,13 +295,7 @@ def main():
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * 1000.0 / ms
+    ms, value = job_rate(ev0.elapsed_time(ev1) / args.steps, world, device="cuda")
 
     # the same replay after a 256 MiB write flush of the L2 (reported for comparison)
     fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
