@@ -29,7 +29,7 @@ def _rank(rank, world, port, out):
 
 def test_job_rate_two_gloo_ranks():
     world, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
     for r in range(world):
         ms, value = out[r]
