@@ -39,21 +39,31 @@ SCORER_PROFILE = os.path.join(ROOT, "profiles", "indexer_scorer_decode_b8_64k.md
 SCORER_SOURCES = ["indexer.cu", "ptx.cuh", "common.cuh", "params.cuh"]
 
 
+def scorer_code_hash():
+    """sha256 of the scorer's sources with comments and blank space removed (a
+    comment edit does not change the kernel the counters were taken on)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in SCORER_SOURCES:
+        with open(os.path.join(ROOT, "dsa_sparse_attention_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip()).encode())
+    return h.hexdigest()
+
+
 def scorer_traffic():
     """DRAM bytes per scorer launch from the committed ncu summary, if the scorer
-    sources are unchanged since the capture (else None)."""
-    import hashlib
+    code is unchanged since the capture (else None)."""
     try:
         text = open(SCORER_PROFILE).read()
-        want = text.split("scorer_sources_sha256:")[1].split()[0]
+        want = text.split("scorer_code_sha256:")[1].split()[0]
         nbytes = int(text.split("dram_bytes_per_launch:")[1].split()[0])
     except (OSError, IndexError, ValueError):
         return None
-    h = hashlib.sha256()
-    for f in SCORER_SOURCES:
-        with open(os.path.join(ROOT, "dsa_sparse_attention_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return nbytes if h.hexdigest() == want else None
+    return nbytes if scorer_code_hash() == want else None
 
 
 L2_FLUSH_BYTES = 256 << 20

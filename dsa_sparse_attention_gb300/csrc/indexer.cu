@@ -12,10 +12,14 @@
 //    in TMEM.  A group's tokens share every key tile (one HBM read per key).
 //  * The grid is persistent; each CTA takes an equal contiguous range of the
 //    global key-tile enumeration (key-balanced across requests and groups).
-//  * Warp roles: warp 0 streams key pages with TMA (3-D map over the packed pool:
-//    128 B x block slots x rows, 128-byte swizzle) plus the per-token scales with
-//    bulk copies; warp 1 issues the MMAs; warps 2..9 read the accumulators
-//    (thread = key) and reduce sum_h w * ReLU(acc) * scale into fp32 scores.
+//  * Warp roles: producer warps take tiles in turn and stream key pages with TMA
+//    (3-D map over the packed pool: 128 B x block slots x rows, 128-byte swizzle,
+//    L2 evict-first) plus the per-token scales with bulk copies; producer 0 also
+//    loads each group's queries; two MMA warps take tiles in turn; warps 2..9,
+//    two sets of four taking alternate tiles, read the accumulators (thread = key)
+//    and reduce sum_h w * ReLU(acc) * scale into fp32 scores.  FP8 keys: producers
+//    0 and 10..12, MMA warps 1 and 13; MXFP4 keys: converter warps 10..17,
+//    producers 0 and 18, MMA warps 1 and 19.
 // Page translation (row = block_table[req][s / bs]) happens in the producer.
 // Inside a layer step (one token per group) the epilogue also counts each
 // token's scores by the top 11 bits of their order-preserving key, the first
