@@ -16,7 +16,8 @@
  * Conventions for every call:
  *  - Pointers documented "device" must point to device memory of the current
  *    CUDA device; the caller owns every buffer, including the workspace.  The
- *    library allocates no memory and keeps no state across calls.
+ *    library allocates no memory and keeps no state across calls (what a call
+ *    leaves in the workspace is a hint at most, see dsa_layer_step).
  *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; 0 = legacy
  *    default stream).  A return value of DSA_OK means the work was validated
  *    and enqueued; device-side findings (a block id outside the pool, a wait
@@ -205,6 +206,11 @@ dsa_status dsa_sparse_mla(const dsa_kv_layout *layout, const dsa_batch *batch, c
  * the intermediate scores and indices kept in the workspace.
  *  idx_out: device int32 [T, topk] or NULL — receives the selected positions
  *  other arguments as in the three calls above.
+ * The scorer also counts each token's scores by their top 11 key bits into the
+ * workspace, and the top-k starts its radix select from those counts and leaves
+ * them zeroed for the next step.  The counts are checked exactly before use:
+ * whatever the workspace held beforehand, the results are the same (a workspace
+ * that was not left zeroed only costs the top-k an extra pass).
  */
 dsa_status dsa_layer_step(const dsa_kv_layout *layout, const dsa_batch *batch,
                           const void *q_idx, const float *w, const void *q, int32_t topk,
