@@ -15,9 +15,10 @@ leave the L2 full of dirty lines whose write-back competes with the next step's
 reads; that variant is reported too, as `ms_per_step_after_l2_flush`.)  The
 timed steps replay a CUDA graph of four consecutive C-ABI layer-step calls (one
 per pool copy), as a multi-layer forward pass would capture them; one pair of
-CUDA events brackets all K steps.  `e2e` instead runs the plain C-ABI call each
-step with the step's query tensors copied from pinned host memory and the
-output copied back inside the timed region.
+CUDA events brackets all K steps.  `e2e` instead runs the host-buffer C-ABI call
+(dsa_layer_step_host) each step: the step's inputs are copied from page-locked
+host memory and the output is copied back inside the timed region, and the host
+waits for each step before issuing the next.
 
 `--impl reference` times the float64 CPU oracle on the same workload (the
 reference arm of this build; there is no other runnable implementation).
@@ -246,7 +247,7 @@ def main():
     from dsa_sparse_attention_gb300.build import build
     build()
     import dsa_sparse_attention_gb300 as dsa
-    from dsa_sparse_attention_gb300.harness import DeviceWorkload
+    from dsa_sparse_attention_gb300.harness import DeviceWorkload, HostStep
 
     def barrier():
         if world > 1:
@@ -374,32 +375,58 @@ def main():
     alg = algorithmic_bytes(wl, idx_np)
     step_tbs = alg / (ms / world * 1e-3) / 1e12 if world == 1 else alg / (ms * 1e-3) / 1e12
 
-    # end to end through the C ABI with host buffers
-    pin = {k: v.cpu().pin_memory() for k, v in
-           dict(q_idx=dw.q_idx, w=dw.w, q=dw.q, q_req=dw.q_req, q_pos=dw.q_pos, ctx=dw.ctx, bt=dw.bt).items()}
-    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = out_host.numel() * out_host.element_size()
-    dev = dict(q_idx=dw.q_idx, w=dw.w, q=dw.q, q_req=dw.q_req, q_pos=dw.q_pos, ctx=dw.ctx, bt=dw.bt)
-
-    def e2e_step(lay):
-        for k, v in pin.items():
-            dev[k].copy_(v, non_blocking=True)
-        dw.layer_step(stream, lay)
-        out_host.copy_(dw.out, non_blocking=True)
-
-    with torch.cuda.stream(stream):
+    # end to end through the C ABI with host buffers (dsa_layer_step_host): every step
+    # copies its inputs from page-locked host memory (packed back to back, so one
+    # copy), runs, and copies its output back; the host waits for each step, as a
+    # decode loop whose next input depends on this output does
+    def e2e_host_call():
+        hs = HostStep(dw, packed=True, with_lse=False, with_idx=False)
         for i in range(4):
-            e2e_step(layouts[i % len(layouts)])
-    torch.cuda.synchronize()
-    e2e_ms = []
-    with torch.cuda.stream(stream):
+            hs.step(stream, layouts[i % len(layouts)])
+        torch.cuda.synchronize()
+        ms_list = []
         for i in range(args.steps):
-            stream.synchronize()
             t0 = time.perf_counter()
-            e2e_step(layouts[i % len(layouts)])
+            hs.step(stream, layouts[i % len(layouts)])
             stream.synchronize()
-            e2e_ms.append((time.perf_counter() - t0) * 1000)
+            ms_list.append((time.perf_counter() - t0) * 1000)
+        return ms_list, hs.h2d_bytes, hs.d2h_bytes, ("dsa_layer_step_host per step: inputs from one page-locked "
+                                                     "buffer, output back, host waits for each step")
+
+    # the same with the copies issued from Python around the device-buffer call
+    def e2e_torch_copies():
+        pin = {k: v.cpu().pin_memory() for k, v in
+               dict(q_idx=dw.q_idx, w=dw.w, q=dw.q, q_req=dw.q_req, q_pos=dw.q_pos, ctx=dw.ctx, bt=dw.bt).items()}
+        out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+        dev = dict(q_idx=dw.q_idx, w=dw.w, q=dw.q, q_req=dw.q_req, q_pos=dw.q_pos, ctx=dw.ctx, bt=dw.bt)
+
+        def one(lay):
+            for k, v in pin.items():
+                dev[k].copy_(v, non_blocking=True)
+            dw.layer_step(stream, lay)
+            out_host.copy_(dw.out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(4):
+                one(layouts[i % len(layouts)])
+        torch.cuda.synchronize()
+        ms_list = []
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                t0 = time.perf_counter()
+                one(layouts[i % len(layouts)])
+                stream.synchronize()
+                ms_list.append((time.perf_counter() - t0) * 1000)
+        return (ms_list, sum(v.numel() * v.element_size() for v in pin.values()),
+                out_host.numel() * out_host.element_size(),
+                "torch copies from page-locked memory around dsa_layer_step, host waits for each step")
+
+    try:
+        e2e_ms, h2d, d2h, e2e_how = e2e_host_call()
+    except dsa.DSAError as err:
+        torch.cuda.synchronize()
+        e2e_ms, h2d, d2h, e2e_how = e2e_torch_copies()
+        e2e_how += f" (dsa_layer_step_host failed: {err})"
     e2e_value = world * 1000.0 / statistics.mean(e2e_ms)
     assert dsa.dsa_check(dw.ws, stream) == 0
 
@@ -427,7 +454,8 @@ def main():
                          "traffic": scorer_traffic(), "launch_ms": sc_ms,
                          "launch_ms_how": "mean over 8 scorer calls replayed from one CUDA graph (pool copies rotated)",
                          "launch_ms_eager": sc_ms_eager},
-            "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": e2e_how},
             "gpu_launches": n_kernels_per_step * args.steps,
             "breakdown_ms": breakdown,
             "clocks": clk, "wall_s_timed": t_wall,

@@ -8,7 +8,8 @@ raises ImportError if it is missing (build it with
 device memory and streams.
 
 Names mirror the C ABI: dsa_workspace_size, dsa_indexer_score, dsa_topk,
-dsa_sparse_mla, dsa_layer_step, dsa_check, dsa_status_string, dsa_abi_version.
+dsa_sparse_mla, dsa_layer_step, dsa_layer_step_host, dsa_check,
+dsa_status_string, dsa_abi_version.
 """
 import ctypes
 import os
@@ -22,6 +23,7 @@ DSA_IDX_FP8, DSA_IDX_MXFP4 = 0, 1
 DSA_LAT_FP8, DSA_LAT_NVFP4 = 0, 1
 DSA_MAX_TOPK = 2048
 DSA_BATCH_INVARIANT = 1
+DSA_HOST_PACKED = 1
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED", -3: "DSA_ERR_CUDA",
                 -4: "DSA_ERR_WORKSPACE", -5: "DSA_ERR_TIMEOUT", -6: "DSA_ERR_DEVICE_CHECK"}
 
@@ -45,6 +47,12 @@ class dsa_batch(ctypes.Structure):
                 ("bt_stride", ctypes.c_int32), ("flags", ctypes.c_int32), ("max_ctx_len", ctypes.c_int64)]
 
 
+class dsa_host_io(ctypes.Structure):
+    _fields_ = [("q_idx", ctypes.c_void_p), ("w", ctypes.c_void_p), ("q", ctypes.c_void_p), ("q_req", ctypes.c_void_p),
+                ("q_pos", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("flags", ctypes.c_int32)]
+
+
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"DSA CUDA library not built ({_LIB_PATH}); run dsa_sparse_attention_gb300.build.build()")
@@ -60,6 +68,7 @@ def _load():
         "dsa_topk": (i32, [L, B, vp, i64, i32, vp, vp, vp, sz, vp]),
         "dsa_sparse_mla": (i32, [L, B, vp, vp, i32, f32, vp, vp, vp, sz, vp]),
         "dsa_layer_step": (i32, [L, B, vp, vp, vp, i32, f32, vp, vp, vp, vp, sz, vp]),
+        "dsa_layer_step_host": (i32, [L, B, vp, vp, vp, i32, f32, vp, vp, vp, P(dsa_host_io), vp, sz, vp]),
         "dsa_check": (i32, [vp, sz, vp]),
         "dsa_last_cuda_error": (i32, [P(ctypes.c_char_p)]),
     }
@@ -164,6 +173,27 @@ def dsa_layer_step(layout, batch, q_idx, w, q, topk, sm_scale, out, idx_out=None
     _check(library().dsa_layer_step(ctypes.byref(layout), ctypes.byref(batch), _ptr(q_idx), _ptr(w), _ptr(q), int(topk),
                               float(sm_scale), _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                               _stream(stream)), "dsa_layer_step")
+
+
+def make_host_io(q_idx, w, q, q_req, q_pos, ctx_lens, block_table, out, lse=None, idx=None, packed=False):
+    """Host-buffer descriptor over CPU tensors (page-locked for asynchronous copies;
+    kept alive by the caller until the stream has passed the call).  packed: the
+    inputs, and their device buffers, lie back to back in one allocation each in
+    the order q, q_idx, w, q_req, q_pos, ctx_lens, block_table (DSA_HOST_PACKED)."""
+    for t in (q_idx, w, q, q_req, q_pos, ctx_lens, block_table, out, lse, idx):
+        if t is not None and t.is_cuda:
+            raise ValueError("dsa_host_io takes host tensors")
+    return dsa_host_io(*(_ptr(t) for t in (q_idx, w, q, q_req, q_pos, ctx_lens, block_table, out, lse, idx)),
+                       DSA_HOST_PACKED if packed else 0)
+
+
+def dsa_layer_step_host(layout, batch, q_idx, w, q, topk, sm_scale, out, host, idx_out=None, lse=None, ws=None,
+                        stream=None):
+    """dsa_layer_step with the inputs copied from, and the results copied to, the
+    host buffers of `host` (make_host_io) on the same stream."""
+    _check(library().dsa_layer_step_host(ctypes.byref(layout), ctypes.byref(batch), _ptr(q_idx), _ptr(w), _ptr(q),
+                                   int(topk), float(sm_scale), _ptr(idx_out), _ptr(out), _ptr(lse),
+                                   ctypes.byref(host), _ptr(ws), ws.numel(), _stream(stream)), "dsa_layer_step_host")
 
 
 def dsa_check(ws, stream=None):

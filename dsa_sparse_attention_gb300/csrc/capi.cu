@@ -319,6 +319,20 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   return cuda_status(launch_sparse_mla(qmap, p, st, chained));
 }
 
+// One host <-> device copy of dsa_layer_step_host.
+struct Copy {
+  void* dst;
+  const void* src;
+  size_t bytes;
+};
+
+dsa_status check_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
+                      const void* q, int32_t topk, float sm_scale, const void* out, void* workspace,
+                      size_t workspace_bytes, Ws& wl);
+dsa_status run_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
+                    const void* q, int32_t topk, float sm_scale, int32_t* idx_out, void* out, float* lse,
+                    void* workspace, const Ws& wl, dsa_stream_t stream);
+
 }  // namespace
 
 namespace dsa {
@@ -401,6 +415,71 @@ dsa_status dsa_sparse_mla(const dsa_kv_layout* layout, const dsa_batch* batch, c
 dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
                           const void* q, int32_t topk, float sm_scale, int32_t* idx_out, void* out, float* lse,
                           void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  Ws wl;
+  const dsa_status s = check_step(layout, batch, q_idx, w, q, topk, sm_scale, out, workspace, workspace_bytes, wl);
+  if (s != DSA_OK) return s;
+  return run_step(layout, batch, q_idx, w, q, topk, sm_scale, idx_out, out, lse, workspace, wl, stream);
+}
+
+dsa_status dsa_layer_step_host(const dsa_kv_layout* layout, const dsa_batch* batch, void* q_idx, float* w, void* q,
+                               int32_t topk, float sm_scale, int32_t* idx_out, void* out, float* lse,
+                               const dsa_host_io* host, void* workspace, size_t workspace_bytes,
+                               dsa_stream_t stream) {
+  Ws wl;
+  dsa_status s = check_step(layout, batch, q_idx, w, q, topk, sm_scale, out, workspace, workspace_bytes, wl);
+  if (s != DSA_OK) return s;
+  const int64_t T = batch->num_tokens, B = batch->num_reqs;
+  if (!host || !host->ctx_lens || !host->block_table) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (!host->q_idx || !host->w || !host->q || !host->q_req || !host->q_pos || !host->out))
+    return DSA_ERR_INVALID_ARG;
+  if ((host->lse && !lse) || (host->idx && !idx_out)) return DSA_ERR_INVALID_ARG;
+  if (host->flags & ~DSA_HOST_PACKED) return DSA_ERR_INVALID_ARG;
+  // in the order a packed layout follows
+  const Copy in[7] = {
+      {q, host->q, size_t(T) * kMlaHeads * kLatDim * 2},
+      {q_idx, host->q_idx, size_t(T) * kIdxHeads * kIdxDim},
+      {w, host->w, size_t(T) * kIdxHeads * 4},
+      {const_cast<int32_t*>(batch->q_req), host->q_req, size_t(T) * 4},
+      {const_cast<int32_t*>(batch->q_pos), host->q_pos, size_t(T) * 4},
+      {const_cast<int32_t*>(batch->ctx_lens), host->ctx_lens, size_t(B) * 4},
+      {const_cast<int32_t*>(batch->block_table), host->block_table, size_t(B) * batch->bt_stride * 4},
+  };
+  const bool packed = (host->flags & DSA_HOST_PACKED) && T > 0;
+  size_t total = in[0].bytes;
+  if (packed)
+    for (int i = 1; i < 7; ++i) {
+      if (static_cast<const uint8_t*>(in[i].src) != static_cast<const uint8_t*>(in[0].src) + total ||
+          static_cast<uint8_t*>(in[i].dst) != static_cast<uint8_t*>(in[0].dst) + total)
+        return DSA_ERR_INVALID_ARG;
+      total += in[i].bytes;
+    }
+  cudaError_t e = cudaSuccess;
+  if (packed) {
+    e = cudaMemcpyAsync(in[0].dst, in[0].src, total, cudaMemcpyHostToDevice, stream);
+  } else {
+    for (int i = 0; i < 7 && e == cudaSuccess; ++i)
+      if (in[i].bytes) e = cudaMemcpyAsync(in[i].dst, in[i].src, in[i].bytes, cudaMemcpyHostToDevice, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((s = run_step(layout, batch, q_idx, w, q, topk, sm_scale, idx_out, out, lse, workspace, wl, stream)) != DSA_OK)
+    return s;
+  const Copy back[3] = {
+      {host->out, out, size_t(T) * kMlaHeads * kVDim * 2},
+      {host->lse, lse, host->lse ? size_t(T) * kMlaHeads * 4 : 0},
+      {host->idx, idx_out, host->idx ? size_t(T) * size_t(topk) * 4 : 0},
+  };
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+    if (back[i].bytes) e = cudaMemcpyAsync(back[i].dst, back[i].src, back[i].bytes, cudaMemcpyDeviceToHost, stream);
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e);
+}
+
+}  // extern "C"
+
+namespace {
+
+dsa_status check_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
+                      const void* q, int32_t topk, float sm_scale, const void* out, void* workspace,
+                      size_t workspace_bytes, Ws& wl) {
   dsa_status s = check_layout(layout);
   if (s != DSA_OK) return s;
   if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
@@ -408,8 +487,14 @@ dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, c
   if (batch->num_tokens > 0 && (!q_idx || !w || !q || !out || !aligned16(q_idx) || !aligned16(w) ||
                                 !aligned16(q) || !aligned16(out)))
     return DSA_ERR_INVALID_ARG;
-  const Ws wl = plan_ws(layout, batch, topk);
-  if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
+  wl = plan_ws(layout, batch, topk);
+  return check_ws(workspace, workspace_bytes, wl);
+}
+
+dsa_status run_step(const dsa_kv_layout* layout, const dsa_batch* batch, const void* q_idx, const float* w,
+                    const void* q, int32_t topk, float sm_scale, int32_t* idx_out, void* out, float* lse,
+                    void* workspace, const Ws& wl, dsa_stream_t stream) {
+  dsa_status s;
   float* scores = at<float>(workspace, wl.scores);
   int32_t* idx = idx_out ? idx_out : at<int32_t>(workspace, wl.idx);
   // rows that the one-launch top-k takes start from the scorer's top-digit histograms
@@ -422,6 +507,10 @@ dsa_status dsa_layer_step(const dsa_kv_layout* layout, const dsa_batch* batch, c
     return s;
   return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream, true);
 }
+
+}  // namespace
+
+extern "C" {
 
 dsa_status dsa_check(void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   if (!workspace || workspace_bytes < kStatusBytes) return DSA_ERR_WORKSPACE;

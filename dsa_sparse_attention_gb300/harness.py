@@ -4,8 +4,8 @@ the computation happens here."""
 import numpy as np
 import torch
 
-from . import (alloc_workspace, dsa_indexer_score, dsa_layer_step, dsa_sparse_mla, dsa_topk, make_batch,
-               make_layout)
+from . import (alloc_workspace, dsa_indexer_score, dsa_layer_step, dsa_layer_step_host, dsa_sparse_mla, dsa_topk,
+               make_batch, make_host_io, make_layout)
 
 
 class DeviceWorkload:
@@ -59,3 +59,54 @@ class DeviceWorkload:
         dsa_sparse_mla(self.layout, self.batch, self.q, idx, self.topk, self.wl.sm_scale, out, lse, ws=self.ws,
                        stream=stream)
         return out, lse
+
+
+class HostStep:
+    """Page-locked host copies of a device workload's per-step inputs and outputs,
+    the device buffers dsa_layer_step_host copies them into, and that call.
+
+    packed=True lays the inputs out back to back, in the order DSA_HOST_PACKED
+    names, in one host buffer and one device buffer, and sets that flag (the call
+    moves them with one copy); packed=False gives every input its own allocation
+    on both sides and one copy each."""
+
+    def __init__(self, dw, packed=True, with_lse=True, with_idx=True):
+        self.dw = dw
+        src = [dw.q.view(torch.uint8), dw.q_idx, dw.w, dw.q_req, dw.q_pos, dw.ctx, dw.bt]
+        sizes = [t.numel() * t.element_size() for t in src]
+        if packed:
+            dev_all = torch.empty(sum(sizes), dtype=torch.uint8, device=dw.device)
+            host_all = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+            dev, host, off = [], [], 0
+            for t, n in zip(src, sizes):
+                dev.append(dev_all[off:off + n].view(t.dtype).view(t.shape))
+                host.append(host_all[off:off + n].view(t.dtype).view(t.shape))
+                off += n
+            self._keep = (dev_all, host_all)
+        else:
+            dev = [torch.empty_like(t) for t in src]
+            host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in src]
+        for h, t in zip(host, src):
+            h.copy_(t.cpu())
+        self.dev, self.host = dev, host
+        q, q_idx, w, q_req, q_pos, ctx, bt = dev
+        self.q, self.q_idx, self.w = q.view(torch.bfloat16), q_idx, w
+        self.batch = make_batch(q_req, q_pos, ctx, bt, dw.wl.max_ctx_len, dw.batch.flags)
+        T = dw.wl.num_tokens
+        self.out = torch.empty(T, 96, 512, dtype=torch.bfloat16, device=dw.device)
+        self.lse = torch.empty(T, 96, dtype=torch.float32, device=dw.device) if with_lse else None
+        self.idx = torch.empty(T, dw.topk, dtype=torch.int32, device=dw.device) if with_idx else None
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.lse_host = torch.empty(T, 96, dtype=torch.float32).pin_memory() if with_lse else None
+        self.idx_host = torch.empty(T, dw.topk, dtype=torch.int32).pin_memory() if with_idx else None
+        self.io = make_host_io(host[1], host[2], host[0], host[3], host[4], host[5], host[6], self.out_host,
+                               self.lse_host, self.idx_host, packed=packed)
+        self.h2d_bytes = sum(sizes)
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in (self.out_host, self.lse_host, self.idx_host)
+                             if t is not None)
+
+    def step(self, stream=None, layout=None):
+        dw = self.dw
+        dsa_layer_step_host(dw.layout if layout is None else layout, self.batch, self.q_idx, self.w, self.q, dw.topk,
+                            dw.wl.sm_scale, self.out, self.io, idx_out=self.idx, lse=self.lse, ws=dw.ws,
+                            stream=stream)

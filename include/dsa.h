@@ -218,6 +218,52 @@ dsa_status dsa_layer_step(const dsa_kv_layout *layout, const dsa_batch *batch,
                           void *workspace, size_t workspace_bytes, dsa_stream_t stream);
 
 /*
+ * The layer step for a caller whose per-step inputs and outputs live in host
+ * memory.  The pages describe the device-side step only; this call adds the
+ * transfers around it.  All of it is ordered on `stream`:
+ *  1. the host inputs are copied into the device buffers that the other arguments
+ *     and `batch` name (q_req, q_pos, ctx_lens and block_table are overwritten on
+ *     the device);
+ *  2. dsa_layer_step runs, with the same arguments and results;
+ *  3. out, and lse and idx where `host` asks for them, are copied back.
+ * Each array is copied on its own, unless host->flags holds DSA_HOST_PACKED.  With
+ * that flag, the caller promises that the inputs q, q_idx, w, q_req, q_pos,
+ * ctx_lens and block_table lie back to back in this order, in one host allocation
+ * and in one device allocation.  They then move as a single copy.  The call checks
+ * that each array starts where the one before it ends, on both sides, and returns
+ * DSA_ERR_INVALID_ARG where one does not.  Whether the arrays share an allocation
+ * cannot be checked: a copy must not span two allocations.  Host memory should be
+ * page-locked.  With pageable memory the results are the same, but the host waits
+ * for each copy.
+ * The call returns once everything is enqueued.  The host outputs hold the results
+ * only once the stream has passed them (cudaStreamSynchronize or an event).  Every
+ * argument is validated before anything is enqueued.
+ *  host: host pointers, each sized like its device counterpart.  ctx_lens and
+ *        block_table are always required.  q_idx, w, q, q_req, q_pos and out are
+ *        required when T > 0.  lse may be NULL, and is allowed only when the
+ *        device lse is given.  idx may be NULL, and is allowed only when idx_out
+ *        is given.  flags: 0 or DSA_HOST_PACKED.
+ */
+#define DSA_HOST_PACKED 1
+typedef struct {
+  const void *q_idx;          /* e4m3 [T, 32, 128] */
+  const float *w;             /* fp32 [T, 32] */
+  const void *q;              /* bf16 [T, 96, 576] */
+  const int32_t *q_req;       /* [T] */
+  const int32_t *q_pos;       /* [T] */
+  const int32_t *ctx_lens;    /* [B] */
+  const int32_t *block_table; /* [B, bt_stride] */
+  void *out;                  /* bf16 [T, 96, 512], written */
+  float *lse;                 /* fp32 [T, 96] or NULL, written */
+  int32_t *idx;               /* int32 [T, topk] or NULL, written */
+  int32_t flags;              /* DSA_HOST_* bits */
+} dsa_host_io;
+dsa_status dsa_layer_step_host(const dsa_kv_layout *layout, const dsa_batch *batch, void *q_idx, float *w,
+                               void *q, int32_t topk, float sm_scale, int32_t *idx_out, void *out,
+                               float *lse, const dsa_host_io *host, void *workspace,
+                               size_t workspace_bytes, dsa_stream_t stream);
+
+/*
  * dsa_topk without a workspace, for callers that cannot allocate device memory
  * (code running in a stream callback or host-function node, plugins whose host
  * framework owns all allocations, loops that forbid allocator use after start-up).

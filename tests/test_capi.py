@@ -76,3 +76,36 @@ def test_host_validation_errors(lib):
     assert L.dsa_layer_step(None, ctypes.byref(_batch()), 0, 0, 0, 2048, 1.0, None, 0, None, 0, 0, None) == -1
     assert L.dsa_topk(None, ctypes.byref(_batch()), 0x1000, 1000, 0, 0x2000, None, 0x100000, 1 << 30, None) == -1
     assert L.dsa_check(None, 0, None) == -4
+
+
+def _call_step_host(host, lse=None, idx=None):
+    L = dsa.library()
+    return L.dsa_layer_step_host(ctypes.byref(_layout()), ctypes.byref(_batch()), 0x70000, 0x80000, 0x60000, 2048,
+                                 1 / 24, idx, 0x90000, lse, host, 0x100000, 1 << 30, None)
+
+
+def test_host_step_validation_errors(lib):
+    full = dict(q_idx=0x1000, w=0x2000, q=0x3000, q_req=0x4000, q_pos=0x5000, ctx_lens=0x6000, block_table=0x7000,
+                out=0x8000)
+    assert _call_step_host(None) == -1                                          # no host descriptor
+    for missing in full:                                                        # each required host pointer
+        h = dsa.dsa_host_io(**{k: (0 if k == missing else v) for k, v in full.items()})
+        assert _call_step_host(ctypes.byref(h)) == -1, missing
+    h = dsa.dsa_host_io(**full, lse=0x9000)
+    assert _call_step_host(ctypes.byref(h)) == -1                               # host lse without device lse
+    h = dsa.dsa_host_io(**full, idx=0xa000)
+    assert _call_step_host(ctypes.byref(h)) == -1                               # host idx without idx_out
+    h = dsa.dsa_host_io(**full, flags=2)
+    assert _call_step_host(ctypes.byref(h)) == -1                               # unknown flag
+    h = dsa.dsa_host_io(**full, flags=dsa.DSA_HOST_PACKED)
+    assert _call_step_host(ctypes.byref(h)) == -1                               # packed, but not back to back
+    L = dsa.library()
+    h = dsa.dsa_host_io(**full)
+    assert L.dsa_layer_step_host(ctypes.byref(_layout()), ctypes.byref(_batch()), 0x70000, 0x80000, 0x60000, 2048,
+                                 1 / 24, None, 0x90000, None, ctypes.byref(h), 0x100000, 16, None) == -4
+    import torch
+    ts = [torch.zeros(4, dtype=torch.int32) for _ in range(8)]
+    h = dsa.make_host_io(*ts)
+    assert [h.q_idx, h.w, h.q, h.q_req, h.q_pos, h.ctx_lens, h.block_table, h.out] == [t.data_ptr() for t in ts]
+    assert h.lse is None and h.idx is None and h.flags == 0
+    assert dsa.make_host_io(*ts, packed=True).flags == dsa.DSA_HOST_PACKED

@@ -299,3 +299,29 @@ def test_full_cfg3_decode_1m_mxfp4_nvfp4():
     wl = W.config(3)
     r = _run_all(wl, check_split=False)
     print(r)
+
+
+@pytest.mark.parametrize("packed", [True, False])
+def test_layer_step_from_host_buffers(packed):
+    # the host-buffer call copies in, runs the same step and copies out: its host
+    # results equal the device call's bit for bit (inputs packed into one buffer
+    # each side, so they move as one copy, or each in its own allocation)
+    from dsa_sparse_attention_gb300 import dsa_check
+    from dsa_sparse_attention_gb300.harness import HostStep
+    lens = [5000, 1, 2049, 300]
+    wl = W.make_workload(lens, 1, seed=17, permute=True, pool_rows=120)
+    dw = _dev(wl)
+    idx, out, lse = (_np(x) for x in dw.layer_step())
+    hs = HostStep(dw, packed=packed)
+    for t in hs.dev:   # the step must read what the call copied in, not what was there
+        t.zero_()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    for _ in range(2):
+        hs.out_host.zero_()
+        hs.step(stream)
+        stream.synchronize()
+        assert np.array_equal(hs.idx_host.numpy(), idx)
+        assert np.array_equal(hs.out_host.float().numpy(), out)
+        assert np.array_equal(hs.lse_host.numpy(), lse)
+    assert dsa_check(dw.ws) == 0
