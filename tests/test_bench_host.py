@@ -1,0 +1,110 @@
+"""The benchmark's host-side logic, on the CPU: the algorithmic byte model behind
+`achieved` and `achieved_hbm_tbs_step`, the lookup of the scorer's captured DRAM
+traffic (keyed on the scorer's code), and the clock record that decides whether
+a run is kept."""
+import os
+import shutil
+import types
+
+import numpy as np
+
+import bench
+
+KEY_FP8, KEY_MXFP4, LAT_FP8, LAT_NVFP4 = 132, 68, 576, 352
+Q_AND_OUT = 4096 + 128 + 96 * 576 * 2 + 96 * 512 * 2   # q_idx, w, q, out per query token
+
+
+def _wl(ctx, q_req, idx_fmt=0, lat_fmt=0):
+    return types.SimpleNamespace(idx_fmt=idx_fmt, lat_fmt=lat_fmt, num_reqs=len(ctx),
+                                 ctx_lens=np.asarray(ctx, np.int32), q_req=np.asarray(q_req, np.int32),
+                                 num_tokens=len(q_req))
+
+
+def test_decode_b8_64k_step_bytes():
+    # one query per request, 2048 distinct selections each: L*132 + 2048*576 per
+    # query plus its q/out tensors (80.35 MB for the batch)
+    wl = _wl([65536] * 8, list(range(8)))
+    rng = np.random.default_rng(0)
+    idx = np.stack([np.sort(rng.choice(65536, 2048, replace=False)) for _ in range(8)]).astype(np.int32)
+    per_query = 65536 * KEY_FP8 + 2048 * LAT_FP8 + Q_AND_OUT
+    assert bench.algorithmic_bytes(wl, idx) == 8 * per_query == 80_348_160
+    assert bench.scorer_bytes(wl) == 8 * (65536 * KEY_FP8 + 4096 + 128) == 69_239_808
+
+
+def test_latents_counted_once_per_request_and_padding_skipped():
+    # two queries of request 0 share three selections; request 1 has a short
+    # context padded with -1; keys are read once per request
+    wl = _wl([100, 3], [0, 0, 1])
+    idx = np.array([[1, 2, 3, 4], [3, 4, 5, 6], [0, 1, 2, -1]], np.int32)
+    want = (100 + 3) * KEY_FP8 + (6 + 3) * LAT_FP8 + 3 * Q_AND_OUT
+    assert bench.algorithmic_bytes(wl, idx) == want
+
+
+def test_fp4_widths():
+    wl = _wl([1000], [0], idx_fmt=1, lat_fmt=1)
+    idx = np.arange(8, dtype=np.int32)[None]
+    assert bench.algorithmic_bytes(wl, idx) == 1000 * KEY_MXFP4 + 8 * LAT_NVFP4 + Q_AND_OUT
+    assert bench.scorer_bytes(wl) == 1000 * KEY_MXFP4 + 4096 + 128
+
+
+def _copy_sources(tmp_path):
+    src = os.path.join(bench.ROOT, "dsa_sparse_attention_gb300", "csrc")
+    dst = tmp_path / "dsa_sparse_attention_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for f in bench.SCORER_SOURCES:
+        shutil.copy(os.path.join(src, f), dst / f)
+    return dst
+
+
+def test_scorer_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    base = bench.scorer_code_hash()
+    dst = _copy_sources(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.scorer_code_hash() == base
+    f = dst / "indexer.cu"
+    f.write_text("// a new comment line\n/* and a block\n   comment */\n" + f.read_text() + "\n\n   \n")
+    assert bench.scorer_code_hash() == base
+    f.write_text(f.read_text() + "\nstatic int unused_symbol_for_the_test;\n")
+    assert bench.scorer_code_hash() != base
+
+
+def test_scorer_traffic_only_for_the_captured_code(tmp_path, monkeypatch):
+    prof = tmp_path / "scorer.md"
+    prof.write_text(f"scorer_code_sha256: {bench.scorer_code_hash()}\ndram_bytes_per_launch: 123456\n")
+    monkeypatch.setattr(bench, "SCORER_PROFILE", str(prof))
+    assert bench.scorer_traffic() == 123456
+    prof.write_text("scorer_code_sha256: " + "0" * 64 + "\ndram_bytes_per_launch: 123456\n")
+    assert bench.scorer_traffic() is None
+    monkeypatch.setattr(bench, "SCORER_PROFILE", str(tmp_path / "missing.md"))
+    assert bench.scorer_traffic() is None
+
+
+class _DoneProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _clock_record(tmp_path, lines):
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(lines) + "\n")
+    cs = bench.ClockSampler(0)
+    cs.path, cs.proc, cs.f = str(path), _DoneProc(), open(path, "a")
+    return cs.stop()
+
+
+def test_clock_record_median_max_and_reasons(tmp_path):
+    idle = "Not Active"
+    rec = _clock_record(tmp_path, [
+        f"0, 2070, 2070, 900.1, 0x0, {idle}, {idle}, {idle}, {idle}",
+        f"0, 1980, 2070, 1390.0, 0x4, {idle}, {idle}, {idle}, Active",
+        f"0, 2055, 2070, 1100.0, 0x0, {idle}, {idle}, {idle}, {idle}",
+        "0, [N/A], 2070, 0, 0x0, a, b, c, d",      # unreadable sample: skipped
+        "garbage",
+    ])
+    assert rec == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    rec = _clock_record(tmp_path, [f"0, 1500, 2070, 1000, 0x8, {idle}, Active, {idle}, {idle}"])
+    assert rec["reasons"] == ["hw_thermal_slowdown"]
+    assert _clock_record(tmp_path, ["nothing here"]) is None
