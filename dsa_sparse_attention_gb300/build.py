@@ -1,6 +1,7 @@
 """In-tree build of the CUDA library: every csrc/*.cu compiled for sm_103a and
 linked into ``_lib/libdsa_gb300.so`` (nvcc only, no cmake)."""
 import concurrent.futures as cf
+import fcntl
 import glob
 import os
 import shutil
@@ -37,11 +38,21 @@ def up_to_date():
 
 
 def build(force=False, verbose=False):
-    """Compile (in parallel) and link the library; returns its path."""
+    """Compile (in parallel) and link the library; returns its path.  Processes
+    that build at the same time take turns (a lock file in the build folder), and
+    a process that waited finds the library already fresh."""
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and up_to_date():
+            return LIB
+        return _build_locked(verbose)
+
+
+def _build_locked(verbose):
     exe = nvcc()
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
