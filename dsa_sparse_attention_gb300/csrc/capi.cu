@@ -35,13 +35,19 @@ struct Ws {
   size_t total = 0;
 };
 
+// SM count of the device current at the first call, for grid and split sizing.
+// Any value gives correct results.  The default attention split follows it, and
+// with it the rounding of the split combine; DSA_BATCH_INVARIANT fixes the split.
+// Thread-safe static initialisation.  When no device answers (workspace sizing on
+// a host without one) it is 152, a GB300's count.
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
+  static const int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 152;
+    return v;
+  }();
   return n;
 }
 
