@@ -201,9 +201,7 @@ def cpu_baseline(wl, budget_s=12.0):
 
 
 def run_reference(args, wl):
-    rank, world, _ = dist_info()
-    if rank != 0:
-        return
+    _, world, _ = dist_info()
     # K timed steps of the oracle, each a bounded sample: one query of the batch
     # (the per-step value is extrapolated to the 8-query step).
     from oracle import dsa_oracle as O
@@ -234,10 +232,11 @@ def main():
     args = parse()
     rank, world, local = dist_info()
     from dsa_sparse_attention_gb300 import workloads as W
-    wl = W.config(1, seed=0)
     if args.impl == "reference":
-        run_reference(args, wl)
+        if rank == 0:   # the other ranks exit without work
+            run_reference(args, W.config(1, seed=0))
         return
+    wl = W.config(1, seed=0)
 
     import torch
     torch.cuda.set_device(local)

@@ -1,7 +1,8 @@
 """The benchmark's host-side logic, on the CPU: the algorithmic byte model behind
 `achieved` and `achieved_hbm_tbs_step`, the lookup of the scorer's captured DRAM
-traffic (keyed on the scorer's code), and the clock record that decides whether
-a run is kept."""
+traffic (keyed on the scorer's code), the clock record that decides whether a
+run is kept, and the reference arm (the oracle timed on the host cores: its JSON
+line, and no work on ranks other than 0)."""
 import os
 import shutil
 import types
@@ -108,3 +109,30 @@ def test_clock_record_median_max_and_reasons(tmp_path):
     rec = _clock_record(tmp_path, [f"0, 1500, 2070, 1000, 0x8, {idle}, Active, {idle}, {idle}"])
     assert rec["reasons"] == ["hw_thermal_slowdown"]
     assert _clock_record(tmp_path, ["nothing here"]) is None
+
+
+def _run_bench(extra_env, *args):
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, **extra_env)
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), *args], capture_output=True, text=True,
+                       env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_line():
+    # the oracle timed as the reference arm: one JSON line with the contract's keys
+    (line,) = _run_bench({}, "--impl", "reference", "--steps", "1", "--warmup", "0")
+    assert line["impl"] == "reference" and line["unit"] == "layer-steps/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 1 and line["warmup"] == 0 and line["n_gpus"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "layer-steps/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["metric"].startswith("DSA decode layer-steps/s") and line["config"]["workload"] == bench.WORKLOAD
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    assert _run_bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--impl", "reference") == []
