@@ -1,5 +1,6 @@
 """The C-ABI library: it loads, exports every symbol include/dsa.h declares,
-and rejects invalid arguments on the host (no kernel is launched)."""
+rejects invalid arguments on the host (no kernel is launched), links into a
+plain C99 program, and the binding's structures have the C compiler's layout."""
 import ctypes
 import os
 import re
@@ -109,3 +110,63 @@ def test_host_step_validation_errors(lib):
     assert [h.q_idx, h.w, h.q, h.q_req, h.q_pos, h.ctx_lens, h.block_table, h.out] == [t.data_ptr() for t in ts]
     assert h.lse is None and h.idx is None and h.flags == 0
     assert dsa.make_host_io(*ts, packed=True).flags == dsa.DSA_HOST_PACKED
+
+
+C_PROBE = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "dsa.h"
+#define F(S, m) printf(#S " " #m " %zu %zu\n", offsetof(S, m), sizeof(((S *)0)->m))
+int main(void) {
+  printf("dsa_kv_layout size %zu\n", sizeof(dsa_kv_layout));
+  F(dsa_kv_layout, pool); F(dsa_kv_layout, num_rows); F(dsa_kv_layout, row_stride_bytes);
+  F(dsa_kv_layout, idx_page_offset); F(dsa_kv_layout, lat_page_offset); F(dsa_kv_layout, block_size);
+  F(dsa_kv_layout, idx_fmt); F(dsa_kv_layout, lat_fmt); F(dsa_kv_layout, reserved);
+  printf("dsa_batch size %zu\n", sizeof(dsa_batch));
+  F(dsa_batch, num_tokens); F(dsa_batch, num_reqs); F(dsa_batch, q_req); F(dsa_batch, q_pos);
+  F(dsa_batch, ctx_lens); F(dsa_batch, block_table); F(dsa_batch, bt_stride); F(dsa_batch, flags);
+  F(dsa_batch, max_ctx_len);
+  printf("dsa_host_io size %zu\n", sizeof(dsa_host_io));
+  F(dsa_host_io, q_idx); F(dsa_host_io, w); F(dsa_host_io, q); F(dsa_host_io, q_req); F(dsa_host_io, q_pos);
+  F(dsa_host_io, ctx_lens); F(dsa_host_io, block_table); F(dsa_host_io, out); F(dsa_host_io, lse);
+  F(dsa_host_io, idx); F(dsa_host_io, flags);
+  /* the library is usable from plain C: version, and a workspace size with no device */
+  dsa_kv_layout l = {(const void *)0x10000, 100, 45312, 0, 8448, 64, DSA_IDX_FP8, DSA_LAT_FP8, 0};
+  dsa_batch b = {2, 2, (const int32_t *)0x20000, (const int32_t *)0x30000, (const int32_t *)0x40000,
+                 (const int32_t *)0x50000, 16, 0, 1000};
+  printf("abi %d ws %zu\n", (int)dsa_abi_version(), dsa_workspace_size(&l, &b, 2048));
+  return 0;
+}
+"""
+
+
+def test_c_program_links_and_struct_layouts_match(lib, tmp_path):
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    from dsa_sparse_attention_gb300.build import LIB
+    src = tmp_path / "probe.c"
+    src.write_text(C_PROBE)
+    exe = tmp_path / "probe"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                    LIB, "-Wl,-rpath," + os.path.dirname(LIB)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    structs = {"dsa_kv_layout": dsa.dsa_kv_layout, "dsa_batch": dsa.dsa_batch, "dsa_host_io": dsa.dsa_host_io}
+    seen = set()
+    for line in out:
+        f = line.split()
+        if f[:1] == ["abi"]:
+            assert int(f[1]) == 1
+            assert int(f[3]) == dsa.dsa_workspace_size(_layout(), _batch(), 2048) > 0
+            seen.add("abi")
+        elif len(f) == 3 and f[1] == "size":
+            assert ctypes.sizeof(structs[f[0]]) == int(f[2]), line
+        elif len(f) == 4:
+            field = getattr(structs[f[0]], f[1])
+            assert (field.offset, field.size) == (int(f[2]), int(f[3])), line
+            seen.add((f[0], f[1]))
+    assert "abi" in seen
+    for name, st in structs.items():   # every ctypes field was compared
+        assert {(name, fn) for fn, _ in st._fields_} <= seen
