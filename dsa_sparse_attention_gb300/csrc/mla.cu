@@ -25,7 +25,9 @@
 // straight into registers, and convert them e4m3 (or NVFP4) -> bf16 (QK
 // operand) and -> fp16 (PV operand) into 128-byte-swizzled tiles of a 4-slot
 // ring; warps 10..13 run the softmax (P in fp16); all 12 math warps write the
-// output (or the fp16 partial for the LSE combine).
+// output (or the fp16 partial for the LSE combine).  On a CTA's last tile the
+// second half of V lands in the query region (free once QK has completed), so
+// all 32 PV MMAs issue after a single wait.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
