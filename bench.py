@@ -181,6 +181,45 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def load_bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s for a kernel timed alone (burst)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def call_rooflines(wl, idx, ms, hbm_gbs, bf16_tflops):
+    """Achieved rates of the three split calls from their graph-replayed times
+    (`ms`: name -> milliseconds per call) against the peaks.  Bytes are the
+    algorithmic bytes of each call:
+      indexer_score: every index key of each context, and each query's q_idx and w;
+      topk: the scores each query ranks (q_pos + 1 of them, 4 B each, written by the
+            scorer just before, so mostly read from L2) and its k output indices;
+      sparse_mla: each query's selected latents, its q and its output.
+    The attention's tensor work is 2 x 96 heads x (576 + 512) per selected token."""
+    key_b = 132 if wl.idx_fmt == 0 else 68
+    lat_b = 576 if wl.lat_fmt == 0 else 352
+    T = wl.num_tokens
+    n_sel = int(np.count_nonzero(idx >= 0))
+    b_score = scorer_bytes(wl)
+    b_topk = int(np.sum(wl.q_pos.astype(np.int64) + 1)) * 4 + T * idx.shape[1] * 4
+    b_mla = n_sel * lat_b + T * (96 * 576 * 2 + 96 * 512 * 2)
+    flops_mla = 2.0 * 96 * (576 + 512) * n_sel
+
+    def rate(nbytes, t_ms):
+        gbs = nbytes / (t_ms * 1e-3) / 1e9
+        return {"ms": t_ms, "bytes": nbytes, "gbs": gbs, "frac_hbm": gbs / hbm_gbs}
+
+    out = {"indexer_score": rate(b_score, ms["indexer_score"]), "topk": rate(b_topk, ms["topk"]),
+           "sparse_mla": rate(b_mla, ms["sparse_mla"])}
+    tf = flops_mla / (ms["sparse_mla"] * 1e-3) / 1e12
+    out["sparse_mla"].update({"flops": flops_mla, "tflops": tf, "frac_bf16": tf / bf16_tflops})
+    return out
+
+
 def cpu_baseline(wl, budget_s=12.0):
     """The float64 oracle, as it stands, on whole steps of the same workload."""
     from oracle import dsa_oracle as O
@@ -356,6 +395,7 @@ def main():
     sc_ms_eager = timed(score_call)
     sc_ms = graph_timed(score_call)
     peak, peak_kind = load_peaks()
+    bf16_peak, bf16_kind = load_bf16_peak()
     sc_gbs = scorer_bytes(wl) / (sc_ms * 1e-3) / 1e9
 
     idx_b = torch.empty_like(dw.idx)
@@ -457,6 +497,9 @@ def main():
                     "how": e2e_how},
             "gpu_launches": n_kernels_per_step * args.steps,
             "breakdown_ms": breakdown,
+            "call_rooflines": dict(call_rooflines(wl, idx_np, breakdown["graph_replayed"], peak, bf16_peak),
+                                   peaks=f"HBM {peak:.0f} GB/s ({peak_kind}), bf16 {bf16_peak:.0f} TFLOP/s "
+                                         f"({bf16_kind}, burst)"),
             "clocks": clk, "wall_s_timed": t_wall,
             "cpu_baseline": cpu,
         }

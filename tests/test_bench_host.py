@@ -136,3 +136,24 @@ def test_reference_arm_line():
 
 def test_reference_arm_other_ranks_exit_without_work():
     assert _run_bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--impl", "reference") == []
+
+
+def test_call_rooflines_decode_b8_64k():
+    # 8 queries at position 65,535, 2048 selections each; times of 1e-2 ms per call
+    wl = _wl([65536] * 8, list(range(8)))
+    wl.q_pos = np.full(8, 65535, np.int32)
+    idx = np.tile(np.arange(2048, dtype=np.int32), (8, 1))
+    r = bench.call_rooflines(wl, idx, {"indexer_score": 0.01, "topk": 0.01, "sparse_mla": 0.01}, 1000.0, 2000.0)
+    assert r["indexer_score"]["bytes"] == 69_239_808
+    assert r["topk"]["bytes"] == 8 * 65536 * 4 + 8 * 2048 * 4
+    assert r["sparse_mla"]["bytes"] == 8 * 2048 * LAT_FP8 + 8 * (96 * 576 * 2 + 96 * 512 * 2)
+    assert r["sparse_mla"]["flops"] == 2 * 96 * (576 + 512) * 8 * 2048          # 3.42 GFLOP
+    assert abs(r["sparse_mla"]["gbs"] - r["sparse_mla"]["bytes"] / 1e-5 / 1e9) < 1e-6
+    assert abs(r["sparse_mla"]["frac_hbm"] - r["sparse_mla"]["gbs"] / 1000.0) < 1e-12
+    assert abs(r["sparse_mla"]["tflops"] - r["sparse_mla"]["flops"] / 1e-5 / 1e12) < 1e-9
+    assert abs(r["sparse_mla"]["frac_bf16"] - r["sparse_mla"]["tflops"] / 2000.0) < 1e-12
+    # padding (-1) is not attended: half the selections give half the latent bytes and flops
+    idx[:, 1024:] = -1
+    r2 = bench.call_rooflines(wl, idx, {"indexer_score": 0.01, "topk": 0.01, "sparse_mla": 0.01}, 1000.0, 2000.0)
+    assert r2["sparse_mla"]["flops"] * 2 == r["sparse_mla"]["flops"]
+    assert r["sparse_mla"]["bytes"] - r2["sparse_mla"]["bytes"] == 8 * 1024 * LAT_FP8
