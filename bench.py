@@ -21,7 +21,7 @@ host memory and the output is copied back inside the timed region, and the host
 waits for each step before issuing the next.
 
 `--impl reference` times the float64 CPU oracle on the same workload (the
-reference arm of this build; there is no other runnable implementation).
+reference arm: the vLLM post describing the method ships no runnable code of it).
 """
 import argparse
 import json
@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -131,7 +132,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples; DSA_BENCH_CLOCKS_DIR keeps them where the caller wants them
+        out_dir = os.environ.get("DSA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"dsa_bench_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def start(self):
         try:

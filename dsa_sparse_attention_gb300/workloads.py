@@ -13,8 +13,8 @@ for three kinds of state" of the vLLM Kimi K3.1 Pro day-0 post):
   FP8 latent page : bs x 576 e4m3                                  (576 B/token)
   NVFP4 latent    : per token 288 packed e2m1, 36 e4m3 scales, 28 zero bytes (352 B)
 
-Value distributions (the workloads the pages describe, with the sizes of the
-five benchmark configurations): q_idx and FP8 index keys are N(0,1) clamped to
+Value distributions (the decode, MTP and prefill workloads of the vLLM post
+on Kimi K3.1 Pro, at the sizes of the five benchmark configurations): q_idx and FP8 index keys are N(0,1) clamped to
 [-8, 8] and rounded to e4m3; key scales U(0.5, 2); head weights N(0, 1/32);
 absorbed queries N(0,1) rounded to bf16; latents N(0,1) rounded to e4m3, or
 quantised to NVFP4 (e4m3 scale per 16 = amax/6); MXFP4 keys quantised with one

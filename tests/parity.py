@@ -1,8 +1,9 @@
 """Comparison of GPU results with the float64 oracle, with the tolerances of the
 parity bar:
 
-* indexer scores: |gpu - oracle| <= 1e-5 * max|oracle score| of the token (fp32
-  accumulation of exact e4m3 products; see the derivation in the design doc);
+* indexer scores: |gpu - oracle| <= 1e-5 * max|oracle score| of the token (the
+  e4m3 x e4m3 products are exact in fp32, so the error is that of the fp32 sum of
+  128 products and of the 32-head reduction, a few 1e-7 relative);
 * top-k: index sets bit-exact, except positions whose oracle score lies within
   1e-5 (relative) of the k-th oracle score; the GPU list must be ascending,
   unique, within 0..q_pos, of size min(k, q_pos + 1), then -1 padding;

@@ -1,8 +1,8 @@
 """Pins of the float64 oracle to facts fixed outside it.
 
-Each test checks the oracle against something the pages or mathematics fix:
-format tables (OCP definitions, cross-checked with torch's own casts), the
-pages' byte arithmetic, a hand-worked example with closed-form answers, brute
+Each test checks the oracle against something the vLLM post on Kimi K3.1 Pro
+or mathematics fix: format tables (OCP definitions, cross-checked with torch's
+own casts), the post's byte arithmetic (*KV cache footprint*), a hand-worked example with closed-form answers, brute
 force on tiny inputs, a library routine for the dense special case, and
 invariants.  None of them retypes the oracle's own formula.
 """
