@@ -85,6 +85,46 @@ def test_mxfp4_and_nvfp4_roundtrip_of_representable_vectors():
     assert not rec[0, 324:].any()        # 28 bytes of padding are zero
 
 
+def test_mxfp4_index_page_read_from_hand_written_bytes():
+    # Block of 16 tokens, token in slot 1 (so slot offsets matter): its 64 value
+    # bytes start at byte 64, its four E8M0 scales at 16 * 64 + 4.  Byte 0 = 0x21:
+    # elements 0, 1 = e2m1 codes 1, 2 = 0.5, 1.0; byte 16 = 0xF7: elements 32, 33 =
+    # codes 7, 15 = 6.0, -6.0.  Scales: block 0 = 127 (x1), block 1 = 129 (x4).
+    bs = 16
+    page = np.zeros(bs * 68, np.uint8)
+    page[64 + 0] = 0x21
+    page[64 + 16] = 0xF7
+    page[bs * 64 + 4 * 1 + 0] = 127
+    page[bs * 64 + 4 * 1 + 1] = 129
+    page[bs * 64 + 4 * 1 + 2] = 127
+    page[bs * 64 + 4 * 1 + 3] = 127
+    lay = O.Layout(page, bs * 68, 0, 0, bs, O.IDX_MXFP4, O.LAT_FP8)
+    keys = O.gather_index_keys(lay, np.array([0]), 2)
+    want = np.zeros(128)
+    want[[0, 1, 32, 33]] = [0.5, 1.0, 24.0, -24.0]
+    assert np.array_equal(keys[1], want)
+    assert not keys[0].any()                 # slot 0 is all zero codes
+
+
+def test_nvfp4_latent_record_read_from_hand_written_bytes():
+    # Token in slot 1 of a 16-token block: record at byte 352.  Byte 0 = 0x3A:
+    # elements 0, 1 = codes 0xA, 0x3 = -1.0, 1.5; element 16 (byte 8, low nibble)
+    # = code 0x7 = 6.0.  Scales (e4m3, per 16 values) at record byte 288: block 0 =
+    # 0x40 = 2.0, block 1 = 0x30 = 0.5.
+    bs = 16
+    page = np.zeros(bs * 352, np.uint8)
+    rec = 352
+    page[rec + 0] = 0x3A
+    page[rec + 8] = 0x07
+    page[rec + 288 + 0] = 0x40
+    page[rec + 288 + 1] = 0x30
+    lay = O.Layout(page, bs * 352, 0, 0, bs, O.IDX_FP8, O.LAT_NVFP4)
+    lat = O.gather_latents(lay, np.array([0]), np.array([1]))[0]
+    want = np.zeros(576)
+    want[[0, 1, 16]] = [-2.0, 3.0, 3.0]
+    assert np.array_equal(lat, want)
+
+
 # --------------------------------------------------------- byte arithmetic
 
 def test_per_token_widths():
