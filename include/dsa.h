@@ -219,8 +219,9 @@ dsa_status dsa_layer_step(const dsa_kv_layout *layout, const dsa_batch *batch,
 
 /*
  * The layer step for a caller whose per-step inputs and outputs live in host
- * memory.  The pages describe the device-side step only; this call adds the
- * transfers around it.  All of it is ordered on `stream`:
+ * memory.  The vLLM post ("Sparse Attention in K3.1 Pro") defines only the
+ * device-side step; this call adds the transfers around it.  All of it is
+ * ordered on `stream`:
  *  1. the host inputs are copied into the device buffers that the other arguments
  *     and `batch` name (q_req, q_pos, ctx_lens and block_table are overwritten on
  *     the device);
@@ -267,7 +268,7 @@ dsa_status dsa_layer_step_host(const dsa_kv_layout *layout, const dsa_batch *bat
  * dsa_topk without a workspace, for callers that cannot allocate device memory
  * (code running in a stream callback or host-function node, plugins whose host
  * framework owns all allocations, loops that forbid allocator use after start-up).
- * The pages describe no such call; it exists only for those callers.
+ * The vLLM post describes no such call; it exists only for those callers.
  *
  * Same arguments, results and guarantees as dsa_topk, minus the workspace: the
  * scratch (about T x (40 KiB + 8 B x ceil(max_ctx_len / 4096)) for histograms,
