@@ -8,8 +8,9 @@ raises ImportError if it is missing (build it with
 device memory and streams.
 
 Names mirror the C ABI: dsa_workspace_size, dsa_indexer_score, dsa_topk,
-dsa_sparse_mla, dsa_layer_step, dsa_layer_step_host, dsa_check,
-dsa_status_string, dsa_abi_version.
+dsa_sparse_mla, dsa_layer_step, dsa_layer_step_host (and
+prepare_layer_step_host, the same call with its arguments marshalled once),
+dsa_check, dsa_status_string, dsa_abi_version.
 """
 import ctypes
 import os
@@ -194,6 +195,23 @@ def dsa_layer_step_host(layout, batch, q_idx, w, q, topk, sm_scale, out, host, i
     _check(library().dsa_layer_step_host(ctypes.byref(layout), ctypes.byref(batch), _ptr(q_idx), _ptr(w), _ptr(q),
                                    int(topk), float(sm_scale), _ptr(idx_out), _ptr(out), _ptr(lse),
                                    ctypes.byref(host), _ptr(ws), ws.numel(), _stream(stream)), "dsa_layer_step_host")
+
+
+def prepare_layer_step_host(layout, batch, q_idx, w, q, topk, sm_scale, out, host, idx_out=None, lse=None, ws=None,
+                            stream=None):
+    """dsa_layer_step_host with its arguments marshalled once: returns a function
+    of no arguments that makes the call, for loops that repeat the same call.  The
+    descriptors, tensors and stream passed here must outlive it."""
+    fn = library().dsa_layer_step_host
+    args = (ctypes.byref(layout), ctypes.byref(batch), _ptr(q_idx), _ptr(w), _ptr(q), int(topk), float(sm_scale),
+            _ptr(idx_out), _ptr(out), _ptr(lse), ctypes.byref(host), _ptr(ws), ws.numel(), _stream(stream))
+
+    def call():
+        status = fn(*args)
+        if status != DSA_OK:
+            _check(status, "dsa_layer_step_host")
+
+    return call
 
 
 def dsa_check(ws, stream=None):

@@ -4,8 +4,8 @@ the computation happens here."""
 import numpy as np
 import torch
 
-from . import (alloc_workspace, dsa_indexer_score, dsa_layer_step, dsa_layer_step_host, dsa_sparse_mla, dsa_topk,
-               make_batch, make_host_io, make_layout)
+from . import (alloc_workspace, dsa_indexer_score, dsa_layer_step, dsa_sparse_mla, dsa_topk, make_batch,
+               make_host_io, make_layout, prepare_layer_step_host)
 
 
 class DeviceWorkload:
@@ -101,12 +101,22 @@ class HostStep:
         self.idx_host = torch.empty(T, dw.topk, dtype=torch.int32).pin_memory() if with_idx else None
         self.io = make_host_io(host[1], host[2], host[0], host[3], host[4], host[5], host[6], self.out_host,
                                self.lse_host, self.idx_host, packed=packed)
+        self._calls = {}
         self.h2d_bytes = sum(sizes)
         self.d2h_bytes = sum(t.numel() * t.element_size() for t in (self.out_host, self.lse_host, self.idx_host)
                              if t is not None)
 
     def step(self, stream=None, layout=None):
+        """One dsa_layer_step_host call (arguments marshalled once per layout and stream)."""
         dw = self.dw
-        dsa_layer_step_host(dw.layout if layout is None else layout, self.batch, self.q_idx, self.w, self.q, dw.topk,
-                            dw.wl.sm_scale, self.out, self.io, idx_out=self.idx, lse=self.lse, ws=dw.ws,
-                            stream=stream)
+        layout = dw.layout if layout is None else layout
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        key = (id(layout), stream.cuda_stream)
+        entry = self._calls.get(key)
+        if entry is None:
+            call = prepare_layer_step_host(layout, self.batch, self.q_idx, self.w, self.q, dw.topk, dw.wl.sm_scale,
+                                           self.out, self.io, idx_out=self.idx, lse=self.lse, ws=dw.ws,
+                                           stream=stream)
+            entry = self._calls[key] = (call, layout, stream)   # the layout and stream outlive the call
+        entry[0]()

@@ -170,3 +170,37 @@ def test_c_program_links_and_struct_layouts_match(lib, tmp_path):
     assert "abi" in seen
     for name, st in structs.items():   # every ctypes field was compared
         assert {(name, fn) for fn, _ in st._fields_} <= seen
+
+
+def test_prepared_host_step_passes_the_same_arguments(monkeypatch):
+    # the prepared call marshals once and then passes exactly what the plain call
+    # passes (checked against a recording stand-in for the library: no CUDA)
+    import torch
+
+    calls = []
+
+    class Rec:
+        def dsa_layer_step_host(self, *args):
+            norm = []
+            for a in args:
+                if type(a).__name__ == "CArgObject":
+                    norm.append(("byref", id(a._obj)))
+                elif isinstance(a, ctypes.c_void_p):
+                    norm.append(("stream", a.value))
+                else:
+                    norm.append(a)
+            calls.append(tuple(norm))
+            return 0
+
+    monkeypatch.setattr(dsa, "library", lambda: Rec())
+    stream = type("S", (), {"cuda_stream": 0x1234})()
+    t = [torch.zeros(16, dtype=torch.int32) for _ in range(7)]
+    lay, bat = _layout(), _batch()
+    h = dsa.make_host_io(*t[:7], t[0])
+    kw = dict(idx_out=t[4], lse=t[5], ws=t[6], stream=stream)
+    dsa.dsa_layer_step_host(lay, bat, t[0], t[1], t[2], 2048, 1 / 24, t[3], h, **kw)
+    prepared = dsa.prepare_layer_step_host(lay, bat, t[0], t[1], t[2], 2048, 1 / 24, t[3], h, **kw)
+    prepared()
+    prepared()
+    assert len(calls) == 3 and calls[0] == calls[1] == calls[2]
+    assert calls[0][-1] == ("stream", 0x1234) and calls[0][2] == t[0].data_ptr()
