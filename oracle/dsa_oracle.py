@@ -49,20 +49,26 @@ H_MLA, D_LAT, D_V = 96, 576, 512  # MLA heads, latent dims, value dims
 # ---------------------------------------------------------------- byte model
 
 def idx_bytes_per_token(idx_fmt: int) -> int:
-    """132 = 128 e4m3 + 4-byte scale; 68 = 64 packed e2m1 + 4 E8M0."""
+    """132 = 128 e4m3 + 4-byte scale ("Sparse Attention in K3.1 Pro": one FP8 key
+    of 132 bytes with its scale); 68 = 64 packed e2m1 + 4 E8M0 ("AMD /
+    Quantization: Native MXFP4 indexer": 68 bytes including scales)."""
     return {IDX_FP8: D_IDX + 4, IDX_MXFP4: D_IDX // 2 + D_IDX // 32}[idx_fmt]
 
 
 def lat_bytes_per_token(lat_fmt: int) -> int:
-    """576 e4m3, or 288 packed e2m1 + 36 e4m3 scales padded to 352."""
+    """576 e4m3, or 288 packed e2m1 + 36 e4m3 scales padded to 352 ("KV cache
+    footprint": 576 B FP8 and 352 B NVFP4 latents per token and layer)."""
     return {LAT_FP8: D_LAT, LAT_NVFP4: 352}[lat_fmt]
 
 
 def idx_page_bytes(idx_fmt: int, bs: int) -> int:
+    """Bytes of one block's index page ("A KV cache for three kinds of state": each
+    block's pages sit at fixed offsets in its row)."""
     return bs * idx_bytes_per_token(idx_fmt)
 
 
 def lat_page_bytes(lat_fmt: int, bs: int) -> int:
+    """Bytes of one block's latent page (same section)."""
     return bs * lat_bytes_per_token(lat_fmt)
 
 
@@ -75,19 +81,23 @@ def kv_bytes_per_token_all_layers(idx_fmt, lat_fmt, n_layers=24) -> int:
 
 def decode_bytes_model(ctx_len: int, topk: int = 2048, idx_fmt=IDX_FP8, lat_fmt=LAT_FP8) -> int:
     """Bytes one decode query reads from the cache in one DSA layer: every index
-    key of the context plus the latents of the selected tokens."""
+    key of the context plus the latents of the selected tokens ("Sparse Attention
+    in K3.1 Pro": the indexer scans every key, attention reads 2,048 latents)."""
     return ctx_len * idx_bytes_per_token(idx_fmt) + min(topk, ctx_len) * lat_bytes_per_token(lat_fmt)
 
 
 def dense_mla_bytes(ctx_len: int, lat_fmt=LAT_FP8) -> int:
-    """Bytes dense MLA reads per query per layer: the latent of every token."""
+    """Bytes dense MLA reads per query per layer: the latent of every token (the
+    dense baseline the same section compares against)."""
     return ctx_len * lat_bytes_per_token(lat_fmt)
 
 
 # ------------------------------------------------------------ page reading
 
 class Layout:
-    """One DSA layer's view of a packed pool held in host memory (uint8)."""
+    """One DSA layer's view of a packed pool held in host memory (uint8): one
+    contiguous row per cache block with that block's index-key and latent pages at
+    fixed offsets ("A KV cache for three kinds of state")."""
 
     def __init__(self, pool, row_stride, idx_page_offset, lat_page_offset,
                  block_size=64, idx_fmt=IDX_FP8, lat_fmt=LAT_FP8):
@@ -107,7 +117,10 @@ class Layout:
 
 
 def _decode_index_page(layout: Layout, page: np.ndarray, n: int) -> np.ndarray:
-    """First ``n`` keys of one index page -> float64 [n, 128]."""
+    """First ``n`` keys of one index page -> float64 [n, 128].  FP8: e4m3 code times
+    the token's fp32 scale ("Sparse Attention in K3.1 Pro"); MXFP4: e2m1 code times
+    2^(E-127), one E8M0 exponent per 32 dims ("AMD / Quantization: Native MXFP4
+    indexer").  The byte order inside the page is the layout stated above."""
     bs = layout.bs
     if layout.idx_fmt == IDX_FP8:
         vals = decode_e4m3(page[:bs * D_IDX].reshape(bs, D_IDX)[:n])
@@ -123,7 +136,9 @@ def _decode_index_page(layout: Layout, page: np.ndarray, n: int) -> np.ndarray:
 
 
 def _decode_latent_page(layout: Layout, page: np.ndarray, slots: np.ndarray) -> np.ndarray:
-    """Latents of the given slots of one latent page -> float64 [len(slots), 576]."""
+    """Latents of the given slots of one latent page -> float64 [len(slots), 576].
+    FP8: 576 e4m3 values with no scale ("KV cache footprint": 576 bytes); NVFP4:
+    e2m1 code times an e4m3 scale per 16 values (352-byte records)."""
     bs = layout.bs
     if layout.lat_fmt == LAT_FP8:
         return decode_e4m3(page.reshape(bs, D_LAT)[slots])
@@ -137,7 +152,8 @@ def _decode_latent_page(layout: Layout, page: np.ndarray, slots: np.ndarray) -> 
 
 def gather_index_keys(layout: Layout, bt_row: np.ndarray, n_tokens: int) -> np.ndarray:
     """Dequantised index keys of tokens 0 .. n_tokens-1 of one request -> [n, 128].
-    Page translation: token s is slot s % bs of row bt_row[s // bs]."""
+    Page translation ("A KV cache for three kinds of state": block tables are
+    translated into page addresses): token s is slot s % bs of row bt_row[s // bs]."""
     bs = layout.bs
     out = np.empty((n_tokens, D_IDX), dtype=np.float64)
     pb = idx_page_bytes(layout.idx_fmt, bs)
@@ -149,7 +165,8 @@ def gather_index_keys(layout: Layout, bt_row: np.ndarray, n_tokens: int) -> np.n
 
 
 def gather_latents(layout: Layout, bt_row: np.ndarray, tokens: np.ndarray) -> np.ndarray:
-    """Dequantised latents of the given token positions of one request -> [n, 576]."""
+    """Dequantised latents of the given token positions of one request -> [n, 576]
+    (page translation as in gather_index_keys)."""
     bs = layout.bs
     tokens = np.asarray(tokens, dtype=np.int64)
     out = np.empty((tokens.size, D_LAT), dtype=np.float64)
@@ -165,7 +182,9 @@ def gather_latents(layout: Layout, bt_row: np.ndarray, tokens: np.ndarray) -> np
 # ------------------------------------------------------------------ indexer
 
 def indexer_scores_for_token(keys: np.ndarray, q_idx_codes: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """score[s] = sum_h w[h] * max(0, q_idx[h] . k[s]) for every row of ``keys``.
+    """score[s] = sum_h w[h] * max(0, q_idx[h] . k[s]) for every row of ``keys``
+    ("Sparse Attention in K3.1 Pro": each earlier token is scored with 32 light
+    heads against its index key; the formula is the plain reading of that prose).
 
     keys: float64 [n, 128] dequantised index keys; q_idx_codes: uint8 e4m3 codes
     [32, 128] (used as-is: any query-side scale is folded into w); w: [32]."""
@@ -176,7 +195,9 @@ def indexer_scores_for_token(keys: np.ndarray, q_idx_codes: np.ndarray, w: np.nd
 
 def indexer_scores(layout: Layout, block_table, q_req, q_pos, q_idx, w):
     """Scores of every token of a batch: list over query tokens of float64 arrays
-    of length q_pos[t] + 1 (positions 0 .. q_pos[t] of its request)."""
+    of length q_pos[t] + 1 (positions 0 .. q_pos[t] of its request: "every earlier
+    token", inclusive because the new token's key is written before scoring, per
+    "Low-latency decode: a fused DSA decode path")."""
     out = []
     cache = {}
     for t in range(len(q_req)):
@@ -190,9 +211,11 @@ def indexer_scores(layout: Layout, block_table, q_req, q_pos, q_idx, w):
 # -------------------------------------------------------------------- top-k
 
 def topk_select(scores: np.ndarray, k: int) -> np.ndarray:
-    """Exact top-k: the k highest scores, equal scores ordered by lower token
-    index first.  Returns the selected token indices in ascending order; when
-    fewer than k tokens exist every token is selected."""
+    """Exact top-k ("Sparse Attention in K3.1 Pro": the 2,048 best tokens are
+    kept): the k highest scores, equal scores ordered by lower token index first
+    (the tie rule of the benchmark definition).  Returns the selected token
+    indices in ascending order; when fewer than k tokens exist every token is
+    selected."""
     scores = np.asarray(scores, dtype=np.float64)
     n = scores.size
     order = np.lexsort((np.arange(n), -scores))   # primary: score desc; then index asc
@@ -200,7 +223,8 @@ def topk_select(scores: np.ndarray, k: int) -> np.ndarray:
 
 
 def kth_score(scores: np.ndarray, k: int) -> float:
-    """The k-th highest score (the selection threshold); the lowest if n <= k."""
+    """The k-th highest score (the selection threshold, around which the parity
+    bar's tie band lies); the lowest if n <= k."""
     s = np.sort(np.asarray(scores, dtype=np.float64))[::-1]
     return float(s[min(k, s.size) - 1])
 
@@ -208,7 +232,10 @@ def kth_score(scores: np.ndarray, k: int) -> float:
 # --------------------------------------------------------------- sparse MLA
 
 def sparse_mla(q_bf16: np.ndarray, latents: np.ndarray, sm_scale: float):
-    """Exact softmax attention of each of the 96 heads over the given latents.
+    """Exact softmax attention of each of the 96 heads over the given latents
+    ("Sparse Attention in K3.1 Pro": MLA runs exactly, but only over the selected
+    tokens; "What's new in Kimi K3.1 Pro": 96 absorbed heads, 576-dim latent, NoPE,
+    so the value is the first 512 dims and no part of the product is rotary).
 
     q_bf16: uint16 bf16 bit patterns [96, 576]; latents: float64 [n, 576].
     logits[h, s] = sm_scale * q[h] . c[s]  (all 576 dims, no rotary part);
@@ -228,7 +255,9 @@ def sparse_mla(q_bf16: np.ndarray, latents: np.ndarray, sm_scale: float):
 
 def layer_step(layout: Layout, block_table, ctx_lens, q_req, q_pos, q_idx, w, q,
                topk=2048, sm_scale=1.0 / 24.0, tokens=None):
-    """One DSA layer for the query tokens listed in ``tokens`` (default: all).
+    """One DSA layer for the query tokens listed in ``tokens`` (default: all):
+    indexer scores, exact top-k, sparse MLA, in the order of Figure 1 of "Sparse
+    Attention in K3.1 Pro".
 
     Returns dict with per-token lists: 'scores' (float64 arrays), 'idx' (selected
     positions, ascending), and arrays 'out' [n, 96, 512], 'lse' [n, 96]."""

@@ -21,6 +21,8 @@ import numpy as np
 
 
 def _e4m3_value(code: int) -> float:
+    """Value of an e4m3 code from its fields (OCP 8-bit floating point
+    specification, E4M3 encoding: bias 7, no infinity, S.1111.111 is NaN)."""
     s = (code >> 7) & 1
     e = (code >> 3) & 0xF
     m = code & 0x7
@@ -34,6 +36,8 @@ def _e4m3_value(code: int) -> float:
 
 
 def _e2m1_value(code: int) -> float:
+    """Value of an e2m1 code from its fields (OCP Microscaling Formats v1.0, FP4
+    E2M1 element: bias 1, no infinity or NaN)."""
     s = (code >> 3) & 1
     e = (code >> 1) & 0x3
     m = code & 0x1
@@ -61,18 +65,22 @@ def decode_e2m1(nibbles: np.ndarray) -> np.ndarray:
 
 
 def decode_e8m0(b: np.ndarray) -> np.ndarray:
-    """uint8 biased exponents -> float64 scale factors 2^(b-127)."""
+    """uint8 biased exponents -> float64 scale factors 2^(b-127) (OCP Microscaling
+    Formats v1.0, E8M0 shared scale; 255 is NaN)."""
     return _E8M0_TABLE[np.asarray(b, dtype=np.uint8)]
 
 
 def decode_bf16(u16: np.ndarray) -> np.ndarray:
-    """uint16 bf16 bit patterns -> float64 values."""
+    """uint16 bf16 bit patterns -> float64 values (bfloat16 is the upper half of
+    an IEEE 754 binary32)."""
     u = np.asarray(u16, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return u.view(np.float32).astype(np.float64)
 
 
 def unpack_nibbles(packed: np.ndarray) -> np.ndarray:
-    """Packed e2m1 bytes -> codes, element 2i from the low nibble of byte i."""
+    """Packed e2m1 bytes -> codes, element 2i from the low nibble of byte i (the
+    post gives sizes only; this order is the layout reading the library's header
+    states, pinned by a hand-written byte test)."""
     p = np.asarray(packed, dtype=np.uint8)
     out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
     out[..., 0::2] = p & 0xF
