@@ -204,3 +204,17 @@ def test_prepared_host_step_passes_the_same_arguments(monkeypatch):
     prepared()
     assert len(calls) == 3 and calls[0] == calls[1] == calls[2]
     assert calls[0][-1] == ("stream", 0x1234) and calls[0][2] == t[0].data_ptr()
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no fallback: without the built CUDA library every call raises, none computes
+    import torch
+    monkeypatch.setattr(dsa, "_LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(dsa, "_LIB", None)
+    with pytest.raises(ImportError):
+        dsa.library()
+    t = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ImportError):
+        dsa.dsa_layer_step(_layout(), _batch(), t, t, t, 2048, 1 / 24, t, ws=t)
+    with pytest.raises(ImportError):
+        dsa.dsa_workspace_size(_layout(), _batch(), 2048)
