@@ -469,7 +469,7 @@ def main():
         torch.cuda.synchronize()
         e2e_ms, h2d, d2h, e2e_how = e2e_torch_copies()
         e2e_how += f" (dsa_layer_step_host failed: {type(err).__name__}: {err})"
-    e2e_value = world * 1000.0 / statistics.mean(e2e_ms)
+    _, e2e_value = job_rate(statistics.mean(e2e_ms), world, device="cuda")   # slowest rank, like `value`
     assert dsa.dsa_check(dw.ws, stream) == 0
 
     cpu = None
