@@ -10,7 +10,8 @@ device memory and streams.
 Names mirror the C ABI: dsa_workspace_size, dsa_indexer_score, dsa_topk,
 dsa_sparse_mla, dsa_layer_step, dsa_layer_step_host (and
 prepare_layer_step_host, the same call with its arguments marshalled once),
-dsa_check, dsa_status_string, dsa_abi_version.
+dsa_topk_noalloc, dsa_selftest_wait_timeout, dsa_check, dsa_status_string,
+dsa_abi_version.
 """
 import ctypes
 import os
@@ -72,6 +73,8 @@ def _load():
         "dsa_layer_step_host": (i32, [L, B, vp, vp, vp, i32, f32, vp, vp, vp, P(dsa_host_io), vp, sz, vp]),
         "dsa_check": (i32, [vp, sz, vp]),
         "dsa_last_cuda_error": (i32, [P(ctypes.c_char_p)]),
+        "dsa_topk_noalloc": (i32, [L, B, vp, i64, i32, vp, vp, vp]),
+        "dsa_selftest_wait_timeout": (i32, [vp, sz, i64, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -212,6 +215,20 @@ def prepare_layer_step_host(layout, batch, q_idx, w, q, topk, sm_scale, out, hos
             _check(status, "dsa_layer_step_host")
 
     return call
+
+
+def dsa_topk_noalloc(layout, batch, scores, ld, topk, idx, phys_slots=None, stream=None):
+    """dsa_topk with the library's own fixed scratch instead of a workspace."""
+    lay = ctypes.byref(layout) if layout is not None else None
+    _check(library().dsa_topk_noalloc(lay, ctypes.byref(batch), _ptr(scores), int(ld), int(topk), _ptr(idx),
+                                      _ptr(phys_slots), _stream(stream)), "dsa_topk_noalloc")
+
+
+def dsa_selftest_wait_timeout(ws, limit_cycles, stream=None):
+    """Runs a bounded wait that nothing completes (the failure path); dsa_check
+    then reports DSA_ERR_TIMEOUT."""
+    _check(library().dsa_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_cycles), _stream(stream)),
+           "dsa_selftest_wait_timeout")
 
 
 def dsa_check(ws, stream=None):

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/dsa.h"
 
@@ -35,20 +36,24 @@ struct Ws {
   size_t total = 0;
 };
 
-// SM count of the device current at the first call, for grid and split sizing.
-// Any value gives correct results.  The default attention split follows it, and
-// with it the rounding of the split combine; DSA_BATCH_INVARIANT fixes the split.
-// Thread-safe static initialisation.  When no device answers (workspace sizing on
-// a host without one) it is 152, a GB300's count.
+// SM count of the current device, for grid and split sizing (looked up once per
+// device).  Any value gives correct results.  The default attention split follows
+// it, and with it the rounding of the split combine; DSA_BATCH_INVARIANT fixes the
+// split.  When no device answers (workspace sizing on a host without one) it is
+// 152, a GB300's count.
 int num_sms() {
-  static const int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 152;
-    return v;
-  }();
-  return n;
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+    cache[dev] = v;
+  }
+  return cache[dev];
 }
 
 bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -343,6 +348,59 @@ dsa_status run_step(const dsa_kv_layout* layout, const dsa_batch* batch, const v
 
 namespace dsa {
 dsa_status record_cuda_status(cudaError_t e) { return cuda_status(e); }
+
+// The CUDA context current on this thread (null before the runtime made one).
+void* current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// cudaFuncSetAttribute(fn, attr, value) once per context: a kernel's attributes
+// belong to the module loaded in a context, so another device (or a context made
+// after a device reset) needs them set again.
+cudaError_t set_func_attr_once(const void* fn, cudaFuncAttribute attr, int value) {
+  struct Done {
+    void* ctx;
+    const void* fn;
+    int attr, value;
+  };
+  static std::mutex mu;
+  static std::vector<Done> done;
+  void* ctx = current_context();
+  std::lock_guard<std::mutex> lock(mu);
+  if (ctx)
+    for (const Done& d : done)
+      if (d.ctx == ctx && d.fn == fn && d.attr == static_cast<int>(attr) && d.value == value) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, attr, value);
+  if (e == cudaSuccess) {
+    ctx = current_context();   // made by the call above if there was none
+    if (ctx) done.push_back({ctx, fn, static_cast<int>(attr), value});
+  }
+  return e;
+}
+
+// The argument checks of dsa_topk, shared with dsa_topk_noalloc.
+dsa_status validate_topk_args(const dsa_kv_layout* layout, const dsa_batch* batch, const float* scores,
+                              int64_t ld_scores, int32_t topk, const int32_t* idx, const int32_t* phys_slots) {
+  dsa_status s;
+  if (phys_slots && (s = check_layout(layout, false)) != DSA_OK) return s;
+  if ((s = check_batch(batch, layout ? layout->block_size : 0)) != DSA_OK) return s;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_INVALID_ARG;
+  if (batch->num_tokens > 0 && (!scores || !idx || !aligned16(scores))) return DSA_ERR_INVALID_ARG;
+  if (ld_scores < batch->max_ctx_len || (ld_scores & 3)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
 }  // namespace dsa
 
 extern "C" {
@@ -391,12 +449,8 @@ dsa_status dsa_indexer_score(const dsa_kv_layout* layout, const dsa_batch* batch
 dsa_status dsa_topk(const dsa_kv_layout* layout, const dsa_batch* batch, const float* scores, int64_t ld_scores,
                     int32_t topk, int32_t* idx, int32_t* phys_slots, void* workspace, size_t workspace_bytes,
                     dsa_stream_t stream) {
-  dsa_status s;
-  if (phys_slots && (s = check_layout(layout, false)) != DSA_OK) return s;
-  if ((s = check_batch(batch, layout ? layout->block_size : 0)) != DSA_OK) return s;
-  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_INVALID_ARG;
-  if (batch->num_tokens > 0 && (!scores || !idx || !aligned16(scores))) return DSA_ERR_INVALID_ARG;
-  if (ld_scores < batch->max_ctx_len || (ld_scores & 3)) return DSA_ERR_INVALID_ARG;
+  dsa_status s = validate_topk_args(layout, batch, scores, ld_scores, topk, idx, phys_slots);
+  if (s != DSA_OK) return s;
   dsa_kv_layout dummy{};
   dummy.num_rows = 1;
   dummy.block_size = 64;

@@ -704,13 +704,9 @@ template <int IDXF, int G>
 static cudaError_t launch_scorer_g(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p,
                                    int grid, cudaStream_t st) {
   using C = ScorerCfg<IDXF, G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(indexer_kernel<IDXF, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = set_func_attr_once(reinterpret_cast<const void*>(indexer_kernel<IDXF, G>),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   // chained: the set-up above the kernel's wait overlaps the end of the kernel before it
   return launch_ex(indexer_kernel<IDXF, G>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, true, 0u, kmap, qmap, p);
 }

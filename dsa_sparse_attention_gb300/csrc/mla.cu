@@ -808,13 +808,9 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
 
 template <int LATF>
 static cudaError_t launch_mla_fmt(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(sparse_mla_kernel<LATF>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = set_func_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<LATF>),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   return launch_ex(sparse_mla_kernel<LATF>, dim3(p.nsplit, p.b.T), dim3(mla::THREADS), mla::SMEM_BYTES, st, chained,
                    0u, qmap, p);
 }

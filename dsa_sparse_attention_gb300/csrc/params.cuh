@@ -145,6 +145,11 @@ inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Host helpers (capi.cu): the CUDA context current on this thread, and
+// cudaFuncSetAttribute done once per (context, kernel, attribute, value).
+void* current_context();
+cudaError_t set_func_attr_once(const void* fn, cudaFuncAttribute attr, int value);
+
 cudaError_t launch_plan_groups(const BatchView& b, int G, ScoreGroup* groups, PlanHeader* hdr, uint32_t* status,
                                cudaStream_t st);
 cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,

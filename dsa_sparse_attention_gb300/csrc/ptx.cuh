@@ -130,10 +130,12 @@ struct Abort {
 };
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
-// false) when another role of the CTA already gave up, or after
-// kWaitLimitCycles, in which case it records DEV_TIMEOUT.  Never traps.
+// false) when another role of the CTA already gave up, or after `limit` SM
+// cycles (kWaitLimitCycles unless a caller passes a shorter one), in which case
+// it records DEV_TIMEOUT.  Never traps.
 // Inlined form, for loops that keep many registers live (a call would spill them).
-__device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity, Abort ab) {
+__device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity, Abort ab,
+                                                 long long limit = kWaitLimitCycles) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const long long t0 = clock64();
@@ -141,7 +143,7 @@ __device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait(addr, parity)) return true;
     if ((it & 15u) == 0u) {
       if (*reinterpret_cast<volatile int*>(ab.flag)) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         *reinterpret_cast<volatile int*>(ab.flag) = 1;
         atomicOr(ab.status, DEV_TIMEOUT);
         return false;
@@ -150,8 +152,9 @@ __device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity,
   }
 }
 
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort ab) {
-  return mbar_wait_inline(bar, parity, ab);
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort ab,
+                                              long long limit = kWaitLimitCycles) {
+  return mbar_wait_inline(bar, parity, ab, limit);
 }
 
 // Wait ignoring the CTA abort flag, for draining copies/MMAs in flight before an

@@ -147,7 +147,7 @@ def _streams(seed: int, n: int = 10):
 
 def make_workload(ctx_lens, q_per_req=1, *, name="custom", seed=0, idx_fmt=IDX_FP8,
                   lat_fmt=LAT_FP8, block_size=64, pool_rows=None, row_stride=None,
-                  permute=True, topk=2048, q_pos=None, bt_stride=None):
+                  permute=True, topk=2048, q_pos=None, bt_stride=None, negative_scale_frac=0.0):
     """Build a workload.
 
     ctx_lens: tokens in cache per request (including that request's query tokens).
@@ -156,6 +156,9 @@ def make_workload(ctx_lens, q_per_req=1, *, name="custom", seed=0, idx_fmt=IDX_F
     pool_rows: rows in the pool (default: exactly the blocks needed).
     permute: map blocks to a random permutation of pool rows (else identity).
     q_pos: optional explicit positions (list of arrays, one per request).
+    negative_scale_frac: fraction of FP8 index keys whose fp32 scale is negated
+      (magnitudes still U(0.5, 2)); 0 keeps every scale positive.  The signs come
+      from their own random stream, so the other tensors do not change with it.
     """
     rs = _streams(seed)
     ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
@@ -183,7 +186,7 @@ def make_workload(ctx_lens, q_per_req=1, *, name="custom", seed=0, idx_fmt=IDX_F
 
     pool = np.zeros(pool_rows * row_stride, dtype=np.uint8)
     rows2d = pool.reshape(pool_rows, row_stride)
-    g_key, g_scale, g_lat = rs[1], rs[2], rs[3]
+    g_key, g_scale, g_lat, g_sign = rs[1], rs[2], rs[3], rs[7]
     chunk_blocks = 512
     for b in range(B):
         for j0 in range(0, int(nblk[b]), chunk_blocks):
@@ -195,6 +198,8 @@ def make_workload(ctx_lens, q_per_req=1, *, name="custom", seed=0, idx_fmt=IDX_F
                 k = np.clip(g_key.standard_normal((ntok, 128), dtype=np.float32), -8, 8)
                 page_v = to_e4m3(k).reshape(nb, bs * 128)
                 sc = g_scale.uniform(0.5, 2.0, size=ntok).astype(np.float32)
+                if negative_scale_frac > 0:
+                    sc[g_sign.random(ntok) < negative_scale_frac] *= -1.0
                 page_s = sc.view(np.uint8).reshape(nb, bs * 4)
                 rows2d[rows, 0:bs * 128] = page_v
                 rows2d[rows, bs * 128:bs * 132] = page_s

@@ -270,16 +270,19 @@ dsa_status dsa_layer_step_host(const dsa_kv_layout *layout, const dsa_batch *bat
  * framework owns all allocations, loops that forbid allocator use after start-up).
  * The vLLM post describes no such call; it exists only for those callers.
  *
- * Same arguments, results and guarantees as dsa_topk, minus the workspace: the
- * scratch (about T x (40 KiB + 8 B x ceil(max_ctx_len / 4096)) for histograms,
- * candidate lists and per-chunk counts) lives in a fixed DSA_NOALLOC_SCRATCH_BYTES
- * array of device memory inside the library, which every GPU that loads the
- * library holds until the process exits.  Batches that need more return
- * DSA_ERR_WORKSPACE (T <= 96 query tokens fit at any context up to 1M tokens).
- * The call allocates nothing.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress with that device current); make that first call
- *    before any stream capture.
+ * Same arguments, checks, results and guarantees as dsa_topk, minus the
+ * workspace.  Rows of at most 65,536 scores (max_ctx_len <= 65,536) need no
+ * scratch at all.  Longer rows need at most T x (40,988 + 8 x ceil(max_ctx_len /
+ * 4096)) + 1,280 bytes for histograms, candidate lists and per-chunk counts, which
+ * live in a fixed DSA_NOALLOC_SCRATCH_BYTES array of device memory inside the
+ * library; every GPU that loads the library holds that array until the process
+ * exits.  A batch with longer rows that needs more returns DSA_ERR_WORKSPACE
+ * (up to 97 query tokens fit at 1M-token contexts, 101 just above 65,536).  The
+ * call allocates nothing.
+ *  - The first call in each CUDA context looks up the array's device address
+ *    (cudaGetSymbolAddress with that context current); make that first call
+ *    before any stream capture.  A context created later (another device, or the
+ *    primary context re-created after cudaDeviceReset) gets its own lookup.
  *  - Every call uses the same array: the call clears the part that must start at
  *    zero on `stream`, but calls that overlap on the GPU (other streams, other
  *    host threads) race on it; issue them in order on one stream.
@@ -296,6 +299,20 @@ dsa_status dsa_topk_noalloc(const dsa_kv_layout *layout, const dsa_batch *batch,
  * calls, clears it, and returns DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK.
  */
 dsa_status dsa_check(void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * Diagnostic of the failure path.  Every wait inside the library's kernels is
+ * bounded: past its limit it gives up, records DSA_ERR_TIMEOUT in the workspace
+ * status word, and the kernel drains what it has in flight and returns instead of
+ * hanging.  A healthy step never reaches that limit (about 2 s), so this call runs
+ * the same bounded wait on a barrier that nothing completes, with a limit of
+ * `limit_cycles` SM clock cycles (1,000 .. 4e9).  Once the stream has passed it,
+ * dsa_check() returns DSA_ERR_TIMEOUT (and the device stays usable).  The vLLM
+ * post describes no such call; it exists to test the failure path.
+ *  workspace: device, >= 256 bytes, 256-byte aligned (only the status word is used)
+ */
+dsa_status dsa_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int64_t limit_cycles,
+                                     dsa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -111,23 +111,33 @@ def test_clock_record_median_max_and_reasons(tmp_path):
     assert _clock_record(tmp_path, ["nothing here"]) is None
 
 
-def _run_bench(extra_env, *args):
+def _run_bench(extra_env, *args, expect_rc=0, wall=None):
     import json
     import subprocess
     import sys
+    import time
     env = dict(os.environ, **extra_env)
+    t0 = time.perf_counter()
     r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), *args], capture_output=True, text=True,
                        env=env, timeout=600)
-    assert r.returncode == 0, r.stderr[-2000:]
+    if wall is not None:
+        wall.append(time.perf_counter() - t0)
+    assert r.returncode == expect_rc, r.stderr[-2000:]
+    if expect_rc:
+        return r.stderr
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     return [json.loads(ln) for ln in lines]
 
 
 def test_reference_arm_line():
-    # the oracle timed as the reference arm: one JSON line with the contract's keys
-    (line,) = _run_bench({}, "--impl", "reference", "--steps", "1", "--warmup", "0")
+    # the oracle timed as the reference arm: one JSON line with the contract's keys;
+    # each timed step is a whole layer step, so K steps fit inside the run's wall time
+    wall = []
+    (line,) = _run_bench({}, "--impl", "reference", "--steps", "2", "--warmup", "0", wall=wall)
+    assert line["ms_per_step"] * line["steps"] / 1000.0 < wall[0]
     assert line["impl"] == "reference" and line["unit"] == "layer-steps/s" and line["higher_is_better"] is True
-    assert line["value"] > 0 and line["steps"] == 1 and line["warmup"] == 0 and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 0 and line["n_gpus"] == 1
+    assert abs(line["value"] * line["ms_per_step"] - 1000.0) < 1e-6
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "layer-steps/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
@@ -135,7 +145,19 @@ def test_reference_arm_line():
 
 
 def test_reference_arm_other_ranks_exit_without_work():
-    assert _run_bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--impl", "reference") == []
+    assert _run_bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--impl", "reference", "--gpus",
+                      "2") == []
+
+
+def test_gpus_must_match_the_launch():
+    # --gpus N runs N replicas only when launched as N ranks; anything else is refused
+    args = lambda n: types.SimpleNamespace(gpus=n)
+    assert bench.check_world(args(1), 1) is None and bench.check_world(args(4), 4) is None
+    assert "torch.distributed.run" in bench.check_world(args(8), 1)
+    assert "WORLD_SIZE=2" in bench.check_world(args(4), 2)
+    assert bench.check_world(args(0), 1) is not None
+    err = _run_bench({"WORLD_SIZE": "1"}, "--gpus", "2", "--impl", "reference", expect_rc=2)
+    assert "--gpus 2 does not match 1 rank" in err
 
 
 def test_call_rooflines_decode_b8_64k():

@@ -79,6 +79,38 @@ def test_host_validation_errors(lib):
     assert L.dsa_check(None, 0, None) == -4
 
 
+def test_noalloc_topk_validation(lib):
+    # the same argument checks as dsa_topk, all on the host before any launch
+    f = dsa.library().dsa_topk_noalloc
+    b = ctypes.byref(_batch())
+    assert f(None, None, 0x1000, 1000, 2048, 0x2000, None, None) == -1           # no batch
+    assert f(None, b, 0x1000, 1000, 0, 0x2000, None, None) == -1                 # topk 0
+    assert f(None, b, 0x1000, 1000, 4096, 0x2000, None, None) == -1              # topk above 2048
+    assert f(None, b, 0x1000, 999, 2048, 0x2000, None, None) == -1               # ld below max_ctx_len
+    assert f(None, b, 0x1000, 1002, 2048, 0x2000, None, None) == -1              # ld not a multiple of 4
+    assert f(None, b, 0x1008, 1000, 2048, 0x2000, None, None) == -1              # misaligned scores
+    assert f(None, b, 0x1000, 1000, 2048, None, None, None) == -1                # no index output
+    assert f(None, b, 0x1000, 1000, 2048, 0x2000, 0x3000, None) == -1            # slots need a layout
+    assert f(ctypes.byref(_layout(block_size=48)), b, 0x1000, 1000, 2048, 0x2000, 0x3000, None) == -2
+    bad = _layout()
+    bad.reserved = 1
+    assert f(ctypes.byref(bad), b, 0x1000, 1000, 2048, 0x2000, 0x3000, None) == -1
+    assert f(ctypes.byref(_layout(idx_fmt=9)), b, 0x1000, 1000, 2048, 0x2000, 0x3000, None) == -1
+    assert f(None, ctypes.byref(_batch(flags=4)), 0x1000, 1000, 2048, 0x2000, None, None) == -1
+    # rows over 65,536 scores use the fixed array: 98 tokens at 1M context do not fit
+    big = _batch(T=98, max_ctx=1 << 20, bt_stride=(1 << 20) // 64)
+    assert f(None, ctypes.byref(big), 0x1000, 1 << 20, 2048, 0x2000, None, None) == -4
+
+
+def test_selftest_validation(lib):
+    f = dsa.library().dsa_selftest_wait_timeout
+    assert f(None, 4096, 100000, None) == -4            # no workspace
+    assert f(0x100010, 4096, 100000, None) == -4        # misaligned
+    assert f(0x100000, 128, 100000, None) == -4         # no room for the status word
+    assert f(0x100000, 4096, 10, None) == -1            # limit too short
+    assert f(0x100000, 4096, 10 ** 10, None) == -1      # limit longer than any wait of the kernels
+
+
 def _call_step_host(host, lse=None, idx=None):
     L = dsa.library()
     return L.dsa_layer_step_host(ctypes.byref(_layout()), ctypes.byref(_batch()), 0x70000, 0x80000, 0x60000, 2048,

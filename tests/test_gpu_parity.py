@@ -95,6 +95,22 @@ def test_block_sizes(bs):
     _run_all(wl)
 
 
+@pytest.mark.parametrize("bs,frac", [(64, 0.5), (256, 0.5), (64, 1.0)])
+def test_mixed_sign_key_scales(bs, frac):
+    # The key scale multiplies the decoded key, so a negative scale turns
+    # ReLU(q . code * scale) into scale * min(q . code, 0); the scorer takes that
+    # branch per key.  Half (or all) of the keys get a negative scale.
+    wl = W.make_workload([5000, 700, 2049, 129], 1, seed=44, block_size=bs, permute=True,
+                         pool_rows=(5000 + 700 + 2049 + 129) // bs + 8, negative_scale_frac=frac)
+    _run_all(wl)
+
+
+def test_mixed_sign_key_scales_mtp_groups():
+    # the same through the grouped scorer (six query tokens share each key tile)
+    wl = W.make_workload([3000, 4100], 6, seed=45, permute=True, pool_rows=120, negative_scale_frac=0.5)
+    _run_all(wl)
+
+
 @pytest.mark.parametrize("k", [1, 7, 100, 1000])
 def test_topk_sizes(k):
     wl = W.make_workload([4000, 90, 5], 1, seed=15, permute=True)

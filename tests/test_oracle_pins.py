@@ -250,6 +250,37 @@ def test_topk_brute_force_tiny(seed):
         assert tuple(O.topk_select(scores, k)) == want[0]
 
 
+# ------------------------------------------------------- the tie band's anchor
+
+def test_kth_score_hand_values():
+    # kth_score sets where the parity bar's tie band lies (scores within 1e-5 of
+    # the k-th best may be swapped).  Values worked out by hand: sorted
+    # descending [3, 2, 2, 1, -1]; k past n gives the lowest score.
+    s = np.array([3.0, 1.0, 2.0, 2.0, -1.0])
+    want = {1: 3.0, 2: 2.0, 3: 2.0, 4: 1.0, 5: -1.0, 6: -1.0, 2048: -1.0}
+    for k, v in want.items():
+        assert O.kth_score(s, k) == v, k
+    # signed zeros compare equal; negatives order below them
+    z = np.array([-0.0, 0.0, -2.0, -1.0])
+    assert [O.kth_score(z, k) for k in (1, 2, 3, 4, 7)] == [0.0, 0.0, -1.0, -2.0, -2.0]
+    assert O.kth_score(np.array([5.0]), 1) == 5.0 and O.kth_score(np.array([5.0]), 2048) == 5.0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_kth_score_is_the_order_statistic(seed):
+    # The k-th largest x of a list is defined by: fewer than k entries exceed x
+    # and at least k entries are >= x; it is also the smallest score the exact
+    # top-k keeps (topk_select is pinned by brute force above).
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 400))
+    s = rng.integers(-20, 21, size=n).astype(np.float64) / 4.0
+    for k in sorted({1, 2, n // 2 + 1, n, n + 3}):
+        x = O.kth_score(s, k)
+        kk = min(k, n)
+        assert np.count_nonzero(s > x) < kk <= np.count_nonzero(s >= x)
+        assert x == s[O.topk_select(s, k)].min()
+
+
 # ------------------------------------------------- dense special case (library)
 
 @pytest.mark.parametrize("L", [1, 64, 65, 200])
@@ -312,6 +343,25 @@ def test_key_scale_scales_score():
     mask = np.ones(300, bool)
     mask[69] = False
     assert np.array_equal(new[mask], base[mask])
+
+
+def test_negative_key_scale_reads_as_a_negated_key():
+    # A negative fp32 scale multiplies the decoded key: with the scale of token 69
+    # negated, its score equals the score of the unchanged key against the negated
+    # query codes (e4m3 negation flips the sign bit, an exact operation).
+    wl, lay = _small()
+    keys = O.gather_index_keys(lay, wl.block_table[0], 300)
+    pool = wl.pool.copy()
+    row = wl.block_table[0, 1]
+    off = row * wl.row_stride + 64 * 128 + 5 * 4        # token 64+5
+    s = pool[off:off + 4].view(np.float32)[0]
+    pool[off:off + 4] = np.array([-s], np.float32).view(np.uint8)
+    lay2 = O.Layout(pool, wl.row_stride, 0, wl.lat_page_offset)
+    new = O.indexer_scores(lay2, wl.block_table, wl.q_req, wl.q_pos, wl.q_idx, wl.w)[0]
+    flipped = O.indexer_scores_for_token(keys, wl.q_idx[0] ^ np.uint8(0x80), wl.w[0])[69]
+    assert new[69] == flipped
+    base = O.indexer_scores(lay, wl.block_table, wl.q_req, wl.q_pos, wl.q_idx, wl.w)[0]
+    assert new[69] != base[69]
 
 
 def test_block_table_permutation_changes_nothing():
