@@ -32,6 +32,7 @@ struct Ws {
   size_t idx = 0, phys = 0;
   size_t part_o = 0, part_ml = 0;
   int nsplit = 1, tps = 16;
+  bool fp8_mla = false;   // FP8 latents may take the one-tile-per-CTA cluster kernel
   int topk_nchunks = 1;
   size_t total = 0;
 };
@@ -122,12 +123,16 @@ Ws plan_ws(const dsa_kv_layout* l, const dsa_batch* b, int topk) {
   if (nsplit < 1) nsplit = 1;
   w.tps = static_cast<int>(cdiv(ntiles, nsplit));
   w.nsplit = static_cast<int>(cdiv(ntiles, w.tps));
+  // The cluster kernel gives every 128 selected tokens their own CTA; it is used
+  // when that fills the GPU at most about twice, and always with
+  // DSA_BATCH_INVARIANT (its split never depends on the batch).
+  w.fp8_mla = l->lat_fmt == DSA_LAT_FP8 &&
+              ((b->flags & DSA_BATCH_INVARIANT) || T * int64_t(ntiles) <= 2 * int64_t(num_sms()));
   w.part_o = off;
   if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * kVDim * 2);
   w.part_ml = off;
   if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * 8);
   w.total = off;
-  (void)l;
   return w;
 }
 
@@ -311,11 +316,10 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
                    cudaStream_t st, bool chained) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
-  CUtensorMap qmap;
-  if (!make_q_map(&qmap, q, T)) return encode_fail();
   MlaParams p;
   p.pool = pool_view(l);
   p.b = batch_view(b);
+  p.q = static_cast<const __nv_bfloat16*>(q);
   p.idx = idx;
   p.phys = phys;
   p.topk = topk;
@@ -327,6 +331,14 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   p.part_o = at<__half>(ws, wl.part_o);
   p.part_ml = at<float2>(ws, wl.part_ml);
   p.status = at<uint32_t>(ws, wl.status);
+  const int ntiles = static_cast<int>(cdiv(topk, kSelTile));
+  if (wl.fp8_mla && sparse_mla_fp8_available(ntiles)) {
+    p.nsplit = ntiles;
+    p.tps = 1;
+    return cuda_status(launch_sparse_mla_fp8(p, st, chained));
+  }
+  CUtensorMap qmap;
+  if (!make_q_map(&qmap, q, T)) return encode_fail();
   return cuda_status(launch_sparse_mla(qmap, p, st, chained));
 }
 

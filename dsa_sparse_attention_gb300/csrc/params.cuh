@@ -50,6 +50,7 @@ struct TopkParams {
 struct MlaParams {
   PoolView pool;
   BatchView b;
+  const __nv_bfloat16* q;  // [T, 96, 576] (read directly by the FP8 kernel)
   const int32_t* idx;      // [T, topk]
   const int32_t* phys;     // [T, topk] physical slots (row * bs + slot) of idx, or null
   int topk;
@@ -157,5 +158,9 @@ cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, con
 int indexer_group_size(int idx_fmt, bool one_token_per_request);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained);
 cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained);
+// FP8 latents, one 128-token tile per CTA, the nsplit CTAs of a token in one
+// cluster: whether this device can run it for `nsplit` splits, and the launch.
+bool sparse_mla_fp8_available(int nsplit);
+cudaError_t launch_sparse_mla_fp8(const MlaParams& p, cudaStream_t st, bool chained);
 
 }  // namespace dsa
