@@ -11,6 +11,7 @@
 
 #include "../../include/dsa.h"
 
+#include "mla_q.cuh"
 #include "params.cuh"
 
 using namespace dsa;
@@ -32,7 +33,8 @@ struct Ws {
   size_t idx = 0, phys = 0;
   size_t part_o = 0, part_ml = 0;
   int nsplit = 1, tps = 16;
-  bool fp8_mla = false;   // FP8 latents may take the one-tile-per-CTA cluster kernel
+  bool fp8_mla = false;   // FP8 latents may take the one-tile-per-CTA FP8 kernel
+  size_t m8_q = 0;        // its query terms (mla_q.cuh), [T] x 110,976 B
   int topk_nchunks = 1;
   size_t total = 0;
 };
@@ -123,15 +125,21 @@ Ws plan_ws(const dsa_kv_layout* l, const dsa_batch* b, int topk) {
   if (nsplit < 1) nsplit = 1;
   w.tps = static_cast<int>(cdiv(ntiles, nsplit));
   w.nsplit = static_cast<int>(cdiv(ntiles, w.tps));
-  // The cluster kernel gives every 128 selected tokens their own CTA; it is used
+  // The FP8 kernel gives every 128 selected tokens their own CTA; it is used
   // when that fills the GPU at most about twice, and always with
   // DSA_BATCH_INVARIANT (its split never depends on the batch).
   w.fp8_mla = l->lat_fmt == DSA_LAT_FP8 &&
               ((b->flags & DSA_BATCH_INVARIANT) || T * int64_t(ntiles) <= 2 * int64_t(num_sms()));
+  w.m8_q = off;
+  if (w.fp8_mla) {
+    off = align_up(off + size_t(T) * kQTokenBytes);
+  }
+  // split partials: the FP8 kernel writes one per tile
+  const int part_splits = w.fp8_mla && ntiles > w.nsplit ? ntiles : w.nsplit;
   w.part_o = off;
-  if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * kVDim * 2);
+  if (part_splits > 1) off = align_up(off + size_t(T) * part_splits * kMlaHeads * kVDim * 2);
   w.part_ml = off;
-  if (w.nsplit > 1) off = align_up(off + size_t(T) * w.nsplit * kMlaHeads * 8);
+  if (part_splits > 1) off = align_up(off + size_t(T) * part_splits * kMlaHeads * 8);
   w.total = off;
   return w;
 }
@@ -256,8 +264,11 @@ dsa_status encode_fail() {
 }
 
 // `row_hist`: the top-k hint histograms to add to, or null.
+// `mla_q`: the layer step's absorbed query when its attention runs on FP8 latents
+// (the scorer then also writes the attention's query terms), else null.
 dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q_idx, const float* w, float* scores,
-                       int64_t ld, void* ws, const Ws& wl, cudaStream_t st, uint32_t* row_hist = nullptr) {
+                       int64_t ld, void* ws, const Ws& wl, cudaStream_t st, uint32_t* row_hist = nullptr,
+                       const void* mla_q = nullptr) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
   CUtensorMap kmap, qmap;
@@ -284,6 +295,8 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   p.status = status;
   p.direct = direct ? 1 : 0;
   p.row_hist = G == 1 ? row_hist : nullptr;
+  p.mla_q = static_cast<const __nv_bfloat16*>(mla_q);
+  p.mla_q_terms = mla_q ? at<uint8_t>(ws, wl.m8_q) : nullptr;
   return cuda_status(launch_indexer(kmap, qmap, p, G, num_sms(), st));
 }
 
@@ -311,9 +324,14 @@ dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* sco
   return cuda_status(launch_topk(p, st, chained));
 }
 
+// Whether the attention of this plan takes the FP8 kernel on this device.
+bool use_fp8_mla(const Ws& wl) { return wl.fp8_mla && sparse_mla_fp8_available(); }
+
+// `in_step`: inside a layer step, whose scorer has written the FP8 kernel's query
+// terms; otherwise a small kernel writes them first.
 dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, const int32_t* idx,
                    const int32_t* phys, int topk, float sm_scale, void* out, float* lse, void* ws, const Ws& wl,
-                   cudaStream_t st, bool chained) {
+                   cudaStream_t st, bool chained, bool in_step = false) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
   MlaParams p;
@@ -331,10 +349,14 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   p.part_o = at<__half>(ws, wl.part_o);
   p.part_ml = at<float2>(ws, wl.part_ml);
   p.status = at<uint32_t>(ws, wl.status);
-  const int ntiles = static_cast<int>(cdiv(topk, kSelTile));
-  if (wl.fp8_mla && sparse_mla_fp8_available(ntiles)) {
-    p.nsplit = ntiles;
+  if (use_fp8_mla(wl)) {
+    p.nsplit = static_cast<int>(cdiv(topk, kSelTile));   // one tile per CTA (the plan sized the partials so)
     p.tps = 1;
+    p.q_terms = at<uint8_t>(ws, wl.m8_q);
+    if (!in_step) {
+      const cudaError_t e = launch_mla_qprep(p.q, at<uint8_t>(ws, wl.m8_q), T, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
     return cuda_status(launch_sparse_mla_fp8(p, st, chained));
   }
   CUtensorMap qmap;
@@ -571,13 +593,17 @@ dsa_status run_step(const dsa_kv_layout* layout, const dsa_batch* batch, const v
   int32_t* idx = idx_out ? idx_out : at<int32_t>(workspace, wl.idx);
   // rows that the one-launch top-k takes start from the scorer's top-digit histograms
   uint32_t* row_hist = batch->max_ctx_len <= kTopkClusterMaxRow ? at<uint32_t>(workspace, wl.row_hist) : nullptr;
-  if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream, row_hist)) != DSA_OK) return s;
+  // with FP8 latents the scorer also prepares the attention's query terms
+  const bool fp8 = use_fp8_mla(wl);
+  if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream, row_hist,
+                       fp8 ? q : nullptr)) != DSA_OK)
+    return s;
   // the top-k also emits each selection's physical cache slot, which the attention gathers directly
   int32_t* phys = at<int32_t>(workspace, wl.phys);
   // the top-k and the attention start while their predecessor drains (programmatic launch)
   if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream, true, row_hist)) != DSA_OK)
     return s;
-  return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream, true);
+  return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream, true, fp8);
 }
 
 }  // namespace

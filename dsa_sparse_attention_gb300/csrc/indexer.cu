@@ -26,6 +26,7 @@
 // digit of the top-k's radix select, so the top-k starts from that histogram.
 #include <cuda.h>
 
+#include "mla_q.cuh"
 #include "params.cuh"
 
 namespace dsa {
@@ -359,6 +360,18 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
     tile_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
   }
   const Abort ab{abortf, p.status};
+  // Layer step with FP8 latents: the epilogue warps, idle until their first tile
+  // lands, also write the attention's query terms (one head per warp in turn).
+  if (p.mla_q && warp >= 2 && warp < 10) {
+    const int total = p.b.T * kMlaHeads, stride = static_cast<int>(gridDim.x) * 8;
+#pragma unroll 1
+    for (int i = static_cast<int>(blockIdx.x) * 8 + (warp - 2); i < total; i += stride) {
+      const int t = i / kMlaHeads, h = i - t * kMlaHeads;
+      uint8_t* tok = p.mla_q_terms + static_cast<int64_t>(t) * kQTokenBytes;
+      q_head_to_terms(p.mla_q + static_cast<int64_t>(t) * kMlaHeads * kLatDim, h, tok,
+                      reinterpret_cast<int32_t*>(tok + kQTermBytes));
+    }
+  }
   const int bs = p.pool.bs;
   const int box = bs < kKeyTile ? bs : kKeyTile;   // keys per TMA box
   const int nbox = kKeyTile / box;

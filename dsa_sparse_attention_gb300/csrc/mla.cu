@@ -806,6 +806,10 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
   *reinterpret_cast<uint4*>(o + h * kVDim + 8 * q) = *reinterpret_cast<const uint4*>(&tile[h][8 * q]);
 }
 
+cudaError_t launch_mla_combine(const MlaParams& p, cudaStream_t st) {
+  return launch_ex(mla_combine_kernel, dim3(kVDim / kCombDims, p.b.T), dim3(kCombThreads), 0, st, true, 0u, p);
+}
+
 template <int LATF>
 static cudaError_t launch_mla_fmt(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained) {
   cudaError_t e = set_func_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<LATF>),
@@ -820,7 +824,7 @@ cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaS
   cudaError_t e =
       p.pool.lat_fmt == 1 ? launch_mla_fmt<1>(qmap, p, st, chained) : launch_mla_fmt<0>(qmap, p, st, chained);
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  return launch_ex(mla_combine_kernel, dim3(kVDim / kCombDims, p.b.T), dim3(kCombThreads), 0, st, true, 0u, p);
+  return launch_mla_combine(p, st);
 }
 
 }  // namespace dsa

@@ -1,6 +1,5 @@
-// mla_fp8.cu — sparse MLA over FP8 latents with the latents read once, straight
-// into the tensor cores' operand tiles, and the splits of a token reduced inside
-// a thread-block cluster.
+// mla_fp8.cu — sparse MLA over FP8 latents, the latents read once, straight into
+// the tensor cores' operand tiles.
 //
 // vLLM K3.1 Pro day-0 post, "Sparse Attention in K3.1 Pro" (+ Figure 1): every
 // query head attends exactly over only the selected tokens' 576-byte FP8
@@ -8,42 +7,32 @@
 // latent dims, NoPE ("What's new in Kimi K3.1 Pro").  Partial results of the
 // splits of the selection are merged by log-sum-exp, as the post's DCP section
 // merges partial outputs across GPUs ("Long context: decode context
-// parallelism with a sparse indexer"); here the splits are the CTAs of a
-// cluster and the merge runs through distributed shared memory.
+// parallelism with a sparse indexer").
 //
-// One CTA per (query token, 128 selected tokens); the nsplit CTAs of a token
-// form one cluster.  Per CTA:
-//  1. The 128 selected latent records (576 B each) are gathered with 16-byte
-//     cp.async copies directly into five 128-byte-swizzled K-chunks of
-//     [128 tokens x 128 B] (dims 0..511 in chunks 0..3; chunk 4 holds dims
-//     512..575 twice, see 2).  No conversion: e4m3 is the MMA's operand type.
-//  2. While those copies fly, the query [96 heads x 576] bf16 is split per head
-//     into two e4m3 terms: with a power-of-two scale s_h putting the head's
-//     largest |q| in [224, 448], hi = e4m3(s_h q) and lo = e4m3(s_h q - hi).  A
-//     bf16 value has 8 significant bits and each e4m3 term holds 4, so hi + lo
-//     equals s_h q exactly for every |s_h q| >= 1/4 (below that the error is at
-//     most 2^-10 / s_h).  K-chunks of the query operand: hi dims 0..511 (four
-//     chunks), [hi 512..575 | lo 512..575] (chunk 4), lo dims 0..511.
-//  3. S[head, token] = sum_k q_term[head, k] . latent[token, k] over the nine
-//     chunks: tcgen05.mma kind::f8f6f4, M = 128 (heads 0..95; lanes 96..127 are
-//     padding nobody reads), N = 128 tokens, K = 1152, fp32 in TMEM.  Heads on
-//     TMEM lanes make the softmax thread-local: four threads per head, 32
-//     tokens each.
-//  4. p = 2^(logit2 - max + 8) is rounded once to fp16 (11 significant bits),
+// One CTA per (query token, 128 selected tokens).  Per CTA:
+//  1. Four threads per selected entry translate it to its latent record and
+//     copy the 576 bytes with 16-byte cp.async directly into five
+//     128-byte-swizzled K-chunks of [128 tokens x 128 B] (dims 0..511 in chunks
+//     0..3; chunk 4 holds dims 512..575 twice).  No conversion: e4m3 is the
+//     MMA's operand type.  The query arrives as two exact e4m3 terms per value
+//     (mla_q.cuh), prepared once per token, with bulk copies.
+//  2. S[head, token] = sum_k q_term[head, k] . latent[token, k] over the nine
+//     query chunks: tcgen05.mma kind::f8f6f4, M = 128 (heads 0..95; lanes
+//     96..127 are padding nobody reads), N = 128 tokens, K = 1152, fp32 in TMEM.
+//     Heads on TMEM lanes make the softmax thread-local: four threads per head,
+//     32 tokens each.
+//  3. p = 2^(logit2 - max + 8) is rounded once to fp16 (11 significant bits),
 //     then split exactly into three e4m3 terms (4 + 4 + 3 bits), written as
 //     three K-major [96 heads x 128 tokens] operand tiles; the row sum is the
 //     sum of the same fp16 values, so the normalisation matches the weights.
-//  5. O^T[dim, head] += V^T[dim, token] . P^T[token, head] for the four 128-dim
+//  4. O^T[dim, head] += V^T[dim, token] . P^T[token, head] for the four 128-dim
 //     blocks of the value, three terms each: M = 128 dims, N = 96 heads, K =
 //     3 x 128; A is the gathered latent tile itself read MN-major (the same
-//     bytes as step 3's B operand), B the P tiles.  TMEM: S in columns
+//     bytes as step 2's B operand), B the P tiles.  TMEM: S in columns
 //     [0, 128), O^T blocks at 128 + 96 v: 512 columns.
-//  6. One split: O / l in bf16.  Several: each CTA stores its normalised fp16
-//     partial and its per-head (max, sum) in its own shared memory; after one
-//     cluster barrier, CTA r sums the 32-dim blocks b with b % nsplit == r over
-//     all CTAs of the cluster (weights 2^(m_j - M) l_j / L) and writes them;
-//     rank 0 writes lse.  A second barrier keeps every CTA alive until the
-//     others have read it.
+//  5. One split: O / l in bf16.  Several: the normalised fp16 partial and the
+//     per-head (max, sum) go to the workspace, and the split combine of mla.cu
+//     merges them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,6 +41,7 @@
 #include <mutex>
 #include <vector>
 
+#include "mla_q.cuh"
 #include "params.cuh"
 
 namespace dsa {
@@ -69,23 +59,18 @@ constexpr int OFF_SRC = OFF_SMALL;                // [128] int64 byte offset of 
 constexpr int OFF_QEXP = OFF_SRC + 128 * 8;       // [96] int: log2 of the query scale of each head
 constexpr int OFF_REDM = OFF_QEXP + 96 * 4;       // [4][96] float: tile max per token quarter
 constexpr int OFF_REDL = OFF_REDM + 4 * 96 * 4;   // [4][96] float: sum per token quarter
-constexpr int OFF_ML = OFF_REDL + 4 * 96 * 4;     // [96] float2: this CTA's (max, sum), read by the cluster
+constexpr int OFF_ML = OFF_REDL + 4 * 96 * 4;     // [96] float2: this CTA's (max, sum)
 constexpr int OFF_INV = OFF_ML + 96 * 8;          // [96] float: 1 / sum
 constexpr int OFF_BARS = OFF_INV + 96 * 4;
 constexpr int OFF_MISC = OFF_BARS + 8 * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 constexpr int P_TERM = 96 * 128;                  // one e4m3 term of P^T (12 KB), at OFF_Q
-constexpr int STG_PITCH = 208;                    // fp16 partial row: 96 heads (192 B) + padding
-constexpr int OFF_WGT = OFF_LAT;                  // merge: [16][96] float weights
-constexpr int OFF_TILE = OFF_LAT + 16 * 96 * 4;   // merge: [96 heads][32 dims] bf16
 constexpr int MAX_SPLITS = 16;
 constexpr int S_COL = 0;
 constexpr int O_COL = 128;
 constexpr int MMA_WARP = 3;                       // a warp of lane quarter 3, which has no softmax role
 static_assert(OFF_LAT % 1024 == 0 && OFF_SMALL % 1024 == 0, "operand tiles are 1024-byte aligned");
 static_assert(3 * P_TERM <= OFF_LAT, "P fits the query region");
-static_assert(kVDim * STG_PITCH <= OFF_LAT, "the fp16 partial fits the query region");
-static_assert(OFF_TILE + 96 * 32 * 2 <= OFF_SMALL, "merge scratch fits the latent region");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace mla8
 
@@ -99,14 +84,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Two floats -> two e4m3 codes (round to nearest even, saturating), element 0 in the low byte.
-__device__ __forceinline__ uint32_t f2_to_e4m3x2(float a, float b) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFFu), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
 __device__ __forceinline__ uint32_t h2_to_e4m3x2(__half2 v) {
   return static_cast<uint32_t>(
       __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&v), __NV_SATFINITE, __NV_E4M3));
@@ -123,27 +100,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// log2 of the power-of-two scale that puts amax in [224, 448] (0 for amax = 0).
-__device__ __forceinline__ int q_scale_log2(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int e = static_cast<int>((b >> 23) & 0xFF) - 127;
-  if ((b & 0x7FFFFFFFu) == 0 || e < -126) return 0;          // zero or subnormal maximum: leave unscaled
-  const bool above = (b & 0x7FFFFFu) > 0x600000u;            // mantissa above 1.75
-  int k = (above ? 7 : 8) - e;
-  return k < -126 ? -126 : (k > 126 ? 126 : k);
-}
-
 template <int DUMMY>
 __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaParams p) {
   using namespace mla8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024_m8(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
-  uint64_t* ready = bars + 0;    // the latent tile and the query terms are in shared memory (512 arrivals)
   uint64_t* s_full = bars + 1;   // QK done
   uint64_t* p_full = bars + 2;   // P written (12 softmax warps)
   uint64_t* o_done = bars + 3;   // PV done
   uint64_t* drain = bars + 4;
+  uint64_t* q_full = bars + 5;   // the query terms and exponents are in shared memory (bulk copies)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + OFF_MISC + 8);
   int* has_work = reinterpret_cast<int*>(smem + OFF_MISC + 16);
@@ -156,62 +123,91 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int t = blockIdx.y;
-  const int split = blockIdx.x;   // = rank in the cluster (cluster dims = (nsplit, 1, 1))
+  const int split = blockIdx.x;
   const int nsplit = p.nsplit;
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.topk;
   const int32_t* phys_row = p.phys ? p.phys + static_cast<int64_t>(t) * p.topk : nullptr;
   if (tid == 0) {
-    mbar_init(ready, THREADS);
     mbar_init(s_full, 1);
     mbar_init(p_full, 12);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(q_full, 1);
     *abortf = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, 512);
-  // Everything above touches only this CTA; the selection comes from the kernel before.
+  // Everything above touches only this CTA; the selection (and, in a layer step, the
+  // query terms) come from the kernels before.
   grid_dep_wait();
   grid_dep_launch();
-
-  // ---- selected entries of this split -> byte offsets of their latent records
-  const int e0 = split * kSelTile;
-  if (tid < kSelTile) {
-    const int e = e0 + tid;
-    int64_t off = -1;
-    const int sv = e < p.topk ? __ldcg((phys_row ? phys_row : idx_row) + e) : -1;
-    if (sv >= 0) {
-      int prow = -1;
-      int slot = 0;
-      bool present = true;
-      if (phys_row) {
-        prow = sv >> p.pool.log2_bs;
-        slot = sv & (p.pool.bs - 1);
-      } else {
-        int req = __ldg(p.b.q_req + t);
-        const int pos = __ldg(p.b.q_pos + t);
-        if (req < 0 || req >= p.b.B) {
-          atomicOr(p.status, DEV_BAD_BATCH);
-          req = req < 0 ? 0 : p.b.B - 1;
-        }
-        const int64_t s_lim = static_cast<int64_t>(p.b.bt_stride) << p.pool.log2_bs;
-        present = sv <= pos && sv < s_lim;
-        if (present)
-          prow = __ldg(p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride + (sv >> p.pool.log2_bs));
-        else
-          atomicOr(p.status, DEV_BAD_BATCH);
-        slot = sv & (p.pool.bs - 1);
-      }
-      if (present) {
-        if (prow < 0 || prow >= p.pool.num_rows)
-          atomicOr(p.status, DEV_BAD_BLOCK);
-        else
-          off = static_cast<int64_t>(prow) * p.pool.row_stride + p.pool.lat_off + static_cast<int64_t>(slot) * kLatDim;
-      }
-    }
-    src_off[tid] = off;
-    if (tid == 0) *has_work = sv >= 0;   // valid entries come first: the split has work iff its first is selected
+  if (tid == 0) {   // the token's query terms (issued by the thread that set up the barriers)
+    const uint8_t* src = p.q_terms + static_cast<int64_t>(t) * kQTokenBytes;
+    mbar_arrive_expect_tx(q_full, kQTokenBytes);
+#pragma unroll 1
+    for (int c = 0; c < kQChunks; ++c) bulk_load(smem + OFF_Q + c * QCHUNK, src + c * QCHUNK, QCHUNK, q_full);
+    bulk_load(qexp, src + kQTermBytes, kMlaHeads * 4, q_full);
   }
+
+  // ---- selection -> latent record -> gather.  Warp w takes the selected entries
+  // (rows of the tile) w + 16 j, j < 8: lanes 0..7 translate them (lane j row w + 16 j),
+  // then for each row all lanes copy its 576 bytes with 16-byte cp.async straight into
+  // the operand tiles, 512 contiguous bytes per instruction: pieces 0..31 are dims
+  // 0..511 (chunks 0..3), then lanes 0..3 copy dims 512..575 into chunk 4 and lanes
+  // 4..7 the same dims again into chunk 4's upper half (the query's chunk 4 holds
+  // hi | lo of those dims).
+  {
+    int64_t off = -1;
+    int sv = -1;
+    if (lane < 8) {
+      const int rrow = warp + 16 * lane;
+      const int e = split * kSelTile + rrow;
+      sv = e < p.topk ? __ldcg((phys_row ? phys_row : idx_row) + e) : -1;
+      if (sv >= 0) {
+        int prow = -1;
+        bool present = true;
+        if (phys_row) {
+          prow = sv >> p.pool.log2_bs;
+        } else {
+          int req = __ldg(p.b.q_req + t);
+          const int pos = __ldg(p.b.q_pos + t);
+          if (req < 0 || req >= p.b.B) {
+            atomicOr(p.status, DEV_BAD_BATCH);
+            req = req < 0 ? 0 : p.b.B - 1;
+          }
+          const int64_t s_lim = static_cast<int64_t>(p.b.bt_stride) << p.pool.log2_bs;
+          present = sv <= pos && sv < s_lim;
+          if (present)
+            prow = __ldg(p.b.bt + static_cast<int64_t>(req) * p.b.bt_stride + (sv >> p.pool.log2_bs));
+          else
+            atomicOr(p.status, DEV_BAD_BATCH);
+        }
+        if (present) {
+          if (prow < 0 || prow >= p.pool.num_rows)
+            atomicOr(p.status, DEV_BAD_BLOCK);
+          else
+            off = static_cast<int64_t>(prow) * p.pool.row_stride + p.pool.lat_off +
+                  static_cast<int64_t>(sv & (p.pool.bs - 1)) * kLatDim;
+        }
+      }
+      src_off[rrow] = off;
+    }
+    if (warp == 0 && lane == 0) *has_work = sv >= 0;   // valid entries come first: work iff the first is selected
+    const uint32_t lat_s = smem_u32(smem + OFF_LAT);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t o = __shfl_sync(0xffffffffu, off, j);
+      const int rrow = warp + 16 * j;
+      const uint8_t* rec = p.pool.pool + (o >= 0 ? o : 0);
+      const uint32_t nb = o >= 0 ? 16u : 0u;
+      const uint32_t rb = lat_s + rrow * 128;
+      const uint32_t sw = static_cast<uint32_t>(rrow & 7);
+      cp_async16(rb + (lane >> 3) * LCHUNK + (((lane & 7) ^ sw) << 4), rec + 16 * lane, nb);
+      if (lane < 8) cp_async16(rb + 4 * LCHUNK + ((lane ^ sw) << 4), rec + 512 + 16 * (lane & 3), nb);
+    }
+  }
+  cp_async_wait_all();
+  fence_proxy_async_smem();   // the copies are read by the tensor core
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -220,79 +216,6 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
   const bool work = *has_work != 0;
 
   if (work) {
-    // ---- 1. gather: 128 records x 40 pieces of 16 B (pieces 36..39 repeat dims 512..575)
-    const uint32_t lat_s = smem_u32(smem + OFF_LAT);
-#pragma unroll 2
-    for (int pc = tid; pc < kSelTile * 40; pc += THREADS) {
-      const int tok = pc / 40, k = pc - tok * 40;
-      const int64_t off = src_off[tok];
-      const int c = k < 32 ? (k >> 3) : 4;
-      const int ci = k < 32 ? (k & 7) : (k - 32);
-      const int sb = k < 36 ? k : k - 4;
-      const uint8_t* src = p.pool.pool + (off >= 0 ? off + 16 * sb : 0);
-      const uint32_t dst = lat_s + c * LCHUNK + tok * 128 + ((ci ^ (tok & 7)) << 4);
-      cp_async16(dst, src, off >= 0 ? 16u : 0u);
-    }
-    // ---- 2. query terms (12 warps x 8 heads; 4 lanes per head, 144 dims each)
-    if (warp < 12) {
-      const int h = warp * 8 + (lane >> 2), m = lane & 3;
-      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(t) * kMlaHeads + h) * kLatDim +
-                                                         144 * m);
-      // pass 1: the head's largest |q| (18 loads in flight); pass 2 reloads from L1
-      float amax = 0.f;
-      {
-        uint4 v[18];
-#pragma unroll
-        for (int i = 0; i < 18; ++i) v[i] = __ldg(qsrc + i);
-#pragma unroll
-        for (int i = 0; i < 18; ++i) {
-          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[j] << 16)));
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[j] & 0xFFFF0000u)));
-        }
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      const int k2 = q_scale_log2(amax);
-      const float sc = __uint_as_float(static_cast<uint32_t>(k2 + 127) << 23);
-      if (m == 0) qexp[h] = k2;
-      uint8_t* qrow = smem + OFF_Q + (h >> 3) * 1024 + (h & 7) * 128;
-#pragma unroll 3
-      for (int g = 0; g < 9; ++g) {        // 16 dims per group: loads 2g, 2g + 1
-        const int G = 9 * m + g;           // global 16-dim group, 0..35
-        uint32_t hi[4], lo[4];
-        const uint4 xv[2] = {__ldg(qsrc + 2 * g), __ldg(qsrc + 2 * g + 1)};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint4 x = xv[half];
-          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {     // 4 values -> 4 bytes of each term
-            const float a0 = __uint_as_float(w4[2 * j] << 16) * sc;
-            const float a1 = __uint_as_float(w4[2 * j] & 0xFFFF0000u) * sc;
-            const float a2 = __uint_as_float(w4[2 * j + 1] << 16) * sc;
-            const float a3 = __uint_as_float(w4[2 * j + 1] & 0xFFFF0000u) * sc;
-            const uint32_t h01 = f2_to_e4m3x2(a0, a1), h23 = f2_to_e4m3x2(a2, a3);
-            const float2 b01 = e4m3x2_to_f2(h01), b23 = e4m3x2_to_f2(h23);
-            const uint32_t l01 = f2_to_e4m3x2(a0 - b01.x, a1 - b01.y), l23 = f2_to_e4m3x2(a2 - b23.x, a3 - b23.y);
-            hi[2 * half + j] = h01 | (h23 << 16);
-            lo[2 * half + j] = l01 | (l23 << 16);
-          }
-        }
-        const int hc = G < 32 ? (G >> 3) : 4, hi_i = G < 32 ? (G & 7) : (G - 32);
-        const int lc = G < 32 ? 5 + (G >> 3) : 4, lo_i = G < 32 ? (G & 7) : (G - 28);
-        *reinterpret_cast<uint4*>(qrow + hc * QCHUNK + ((hi_i ^ (h & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(qrow + lc * QCHUNK + ((lo_i ^ (h & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
-    cp_async_wait_all();
-    fence_proxy_async_smem();   // the copies and the query terms are read by the tensor core
-    mbar_arrive(ready);
-
     if (warp == MMA_WARP && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc_qk = make_idesc(0, 0, false, false, 128, 128);
@@ -301,7 +224,7 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
       const uint64_t dl = make_sdesc_sw128(smem_u32(smem + OFF_LAT), 16, 1024);     // latents, K-major (QK)
       const uint64_t dv = make_sdesc_sw128(smem_u32(smem + OFF_LAT), LCHUNK, 1024); // latents, MN-major (PV)
       const uint64_t dp = make_sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);       // P terms, K-major
-      bool ok = mbar_wait(ready, 0, ab);
+      bool ok = mbar_wait(q_full, 0, ab);
       if (ok) {
         tc_fence_after();
 #pragma unroll 1
@@ -335,7 +258,7 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
       const int quarter = warp & 3, u = warp >> 2;   // heads 32 quarter.., tokens 32 u ..
       const int h = quarter * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-      if (__all_sync(0xffffffffu, mbar_wait(s_full, 0, ab))) {   // uniform over the warp (aligned loads below)
+      if (__all_sync(0xffffffffu, mbar_wait(s_full, 0, ab) && mbar_wait(q_full, 0, ab))) {   // uniform (aligned loads below)
         tc_fence_after();
         uint32_t rr[32];
         DSA_TMEM_LD32(tmem + S_COL + 32 * u + lane_off, rr);
@@ -417,6 +340,17 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
   const int quarter = warp & 3, vb = warp >> 2;   // TMEM lanes = dims 128 vb + 32 quarter + lane
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const int dim = vb * 128 + quarter * 32 + lane;
+  // 32 consecutive heads' reciprocal sums (8 vector loads)
+  auto inv32 = [&](int c, float (&iv)[32]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 x = *reinterpret_cast<const float4*>(inv_l + 32 * c + 4 * i);
+      iv[4 * i] = x.x;
+      iv[4 * i + 1] = x.y;
+      iv[4 * i + 2] = x.z;
+      iv[4 * i + 3] = x.w;
+    }
+  };
   if (nsplit == 1) {
     if (good) {
       uint16_t* stage = reinterpret_cast<uint16_t*>(smem + OFF_Q);   // [96 heads][512 dims] bf16
@@ -424,10 +358,12 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
       for (int c = 0; c < 3; ++c) {
         uint32_t rr[32];
         DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 32 * c + lane_off, rr);
+        float iv[32];
+        inv32(c, iv);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(rr[i]) * inv_l[32 * c + i]);
+          const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(rr[i]) * iv[i]);
           stage[(32 * c + i) * kVDim + dim] = *reinterpret_cast<const uint16_t*>(&bv);
         }
       }
@@ -439,164 +375,72 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
         p.lse[static_cast<int64_t>(t) * kMlaHeads + tid] = (ml[tid].x - 8.f + log2f(ml[tid].y)) * 0.69314718055994531f;
     }
   } else {
-    // normalised fp16 partial, [512 dims][96 heads] at a 208-byte pitch, in this CTA's shared memory
+    // normalised fp16 partial [512 dims][96 heads] and (max - 8, sum) for the split
+    // combine.  A split with nothing selected writes (-inf, 0) only.
+    const int64_t ts = static_cast<int64_t>(t) * nsplit + split;
     if (good) {
-      uint8_t* row = smem + OFF_Q + dim * STG_PITCH;
-#pragma unroll 1
-      for (int c = 0; c < 3; ++c) {
-        uint32_t rr[32];
-        DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 32 * c + lane_off, rr);
-        tmem_wait_ld();
+      // thread = one dim row of the partial: its 96 heads (192 bytes) go straight out
+      uint4* grow = reinterpret_cast<uint4*>(p.part_o + (ts * kVDim + dim) * kMlaHeads);
+      auto store32 = [&](const uint32_t (&rr)[32], int c) {
+        float iv[32];
+        inv32(c, iv);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t w4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 8 * q + 2 * e;
-            const __half2 hv = __floats2half2_rn(__uint_as_float(rr[i]) * inv_l[32 * c + i],
-                                                 __uint_as_float(rr[i + 1]) * inv_l[32 * c + i + 1]);
-            w4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int i = 8 * q + 2 * e2;
+            const __half2 hv =
+                __floats2half2_rn(__uint_as_float(rr[i]) * iv[i], __uint_as_float(rr[i + 1]) * iv[i + 1]);
+            w4[e2] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-          *reinterpret_cast<uint4*>(row + 64 * c + 16 * q) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          grow[4 * c + q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
-      }
+      };
+      uint32_t r0[32], r1[32];
+      DSA_TMEM_LD32(tmem + O_COL + 96 * vb + lane_off, r0);   // two loads in flight, one wait
+      DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 32 + lane_off, r1);
+      tmem_wait_ld();
+      store32(r0, 0);
+      store32(r1, 1);
+      DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 64 + lane_off, r0);
+      tmem_wait_ld();
+      store32(r0, 2);
     }
-    cluster_arrive();   // release: the partial and (max, sum) are visible to the cluster after the wait
-    cluster_wait();
-    // weights of every split for every head: w_j = 2^(m_j - M) l_j / L
-    float* wgt = reinterpret_cast<float*>(smem + OFF_WGT);
-    if (tid < kMlaHeads) {
-      float2 v[MAX_SPLITS];
-      float M = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < MAX_SPLITS; ++j) {
-        v[j] = make_float2(-INFINITY, 0.f);
-        if (j < nsplit) {
-          const uint32_t a = cluster_map(smem_u32(&ml[tid]), static_cast<uint32_t>(j));
-          v[j].x = __uint_as_float(ld_cluster_u32(a));
-          v[j].y = __uint_as_float(ld_cluster_u32(a + 4));
-        }
-        if (v[j].y > 0.f) M = fmaxf(M, v[j].x);
-      }
-      float L = 0.f;
-#pragma unroll
-      for (int j = 0; j < MAX_SPLITS; ++j) {
-        const float w = v[j].y > 0.f ? exp2f(v[j].x - M) * v[j].y : 0.f;
-        v[j].y = w;
-        L += w;
-      }
-      const float inv = 1.f / L;
-#pragma unroll
-      for (int j = 0; j < MAX_SPLITS; ++j)
-        if (j < nsplit) wgt[j * kMlaHeads + tid] = v[j].y * inv;
-      if (split == 0 && p.lse)
-        p.lse[static_cast<int64_t>(t) * kMlaHeads + tid] = (M - 8.f + log2f(L)) * 0.69314718055994531f;
-    }
-    __syncthreads();
-    // the 32-dim blocks this CTA owns: sum over the cluster's partials, bf16 out
-    __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + OFF_TILE);   // [96 heads][32 dims]
-    const int d = tid / 12, g = tid % 12;   // dim of the block, group of 8 heads (384 threads)
-#pragma unroll 1
-    for (int blk = split; blk < kVDim / 32; blk += nsplit) {
-      if (tid < 384) {
-        const uint32_t own = smem_u32(smem + OFF_Q + (blk * 32 + d) * STG_PITCH + 16 * g);
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int j0 = 0; j0 < MAX_SPLITS; j0 += MAX_SPLITS / 2) {   // eight splits' loads in flight at a time
-          if (j0 >= nsplit) break;
-          uint4 part[MAX_SPLITS / 2];
-#pragma unroll
-          for (int j = 0; j < MAX_SPLITS / 2; ++j)
-            if (j0 + j < nsplit) part[j] = ld_cluster_v4(cluster_map(own, static_cast<uint32_t>(j0 + j)));
-#pragma unroll
-          for (int j = 0; j < MAX_SPLITS / 2; ++j) {
-            if (j0 + j >= nsplit) break;
-            const float4 wa = *reinterpret_cast<const float4*>(wgt + (j0 + j) * kMlaHeads + 8 * g);
-            const float4 wb = *reinterpret_cast<const float4*>(wgt + (j0 + j) * kMlaHeads + 8 * g + 4);
-            if (wa.x == 0.f && wa.y == 0.f && wa.z == 0.f && wa.w == 0.f && wb.x == 0.f && wb.y == 0.f &&
-                wb.z == 0.f && wb.w == 0.f)
-              continue;   // a split with nothing selected (its partial was never written)
-            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-            const uint32_t w4[4] = {part[j].x, part[j].y, part[j].z, part[j].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-              acc[2 * e] = fmaf(wv[2 * e], f.x, acc[2 * e]);
-              acc[2 * e + 1] = fmaf(wv[2 * e + 1], f.y, acc[2 * e + 1]);
-            }
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) tile[(8 * g + e) * 32 + d] = __float2bfloat16_rn(acc[e]);
-      }
-      __syncthreads();
-      if (tid < 384) {
-        const int hh = tid >> 2, q = tid & 3;
-        __nv_bfloat16* o = p.out + (static_cast<int64_t>(t) * kMlaHeads + hh) * kVDim + blk * 32 + 8 * q;
-        *reinterpret_cast<uint4*>(o) = *reinterpret_cast<const uint4*>(tile + hh * 32 + 8 * q);
-      }
-      __syncthreads();
-    }
-    cluster_arrive_relaxed();   // done reading the other CTAs
-    cluster_wait();             // and they are done reading this one
+    if (tid < kMlaHeads) p.part_ml[ts * kMlaHeads + tid] = make_float2(ml[tid].x - 8.f, ml[tid].y);
   }
+  if (tid == 0) drain_wait(q_full, 0);   // no copy into shared memory outlives the CTA
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// Largest cluster of this kernel the device can hold at once (0: none), per context.
-static int max_active_clusters(int csize) {
-  static std::mutex mu;
-  struct E {
-    void* ctx;
-    int csize, n;
-  };
-  static std::vector<E> cache;
-  void* ctx = current_context();
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (const E& e : cache)
-      if (e.ctx == ctx && e.csize == csize) return e.n;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(csize, 1);
-  cfg.blockDim = dim3(mla8::THREADS);
-  cfg.dynamicSmemBytes = mla8::SMEM_BYTES;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = csize;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_fp8_kernel<0>, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();
-    n = 0;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (ctx) cache.push_back({ctx, csize, n});
-  return n;
+// The query terms of every token (mla_q.cuh) for a standalone attention call: one
+// warp per head, grid (T, 3) of 32 warps.
+__global__ void __launch_bounds__(1024) mla_qprep_kernel(const __nv_bfloat16* q, uint8_t* terms) {
+  const int t = blockIdx.x, h = blockIdx.y * 32 + (threadIdx.x >> 5);
+  grid_dep_wait();
+  uint8_t* tok = terms + static_cast<int64_t>(t) * kQTokenBytes;
+  q_head_to_terms(q + static_cast<int64_t>(t) * kMlaHeads * kLatDim, h, tok, reinterpret_cast<int32_t*>(tok + kQTermBytes));
 }
 
-bool sparse_mla_fp8_available(int nsplit) {
-  if (nsplit < 1 || nsplit > mla8::MAX_SPLITS) return false;
-  if (set_func_attr_once(reinterpret_cast<const void*>(sparse_mla_fp8_kernel<0>),
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, mla8::SMEM_BYTES) != cudaSuccess)
-    return false;
-  if (nsplit > 8 && set_func_attr_once(reinterpret_cast<const void*>(sparse_mla_fp8_kernel<0>),
-                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    return false;
-  return nsplit == 1 || max_active_clusters(nsplit) > 0;
+cudaError_t launch_mla_qprep(const __nv_bfloat16* q, uint8_t* terms, int T, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  return launch_ex(mla_qprep_kernel, dim3(T, 3), dim3(1024), 0, st, false, 0u, q, terms);
 }
 
+bool sparse_mla_fp8_available() {
+  return set_func_attr_once(reinterpret_cast<const void*>(sparse_mla_fp8_kernel<0>),
+                            cudaFuncAttributeMaxDynamicSharedMemorySize, mla8::SMEM_BYTES) == cudaSuccess;
+}
+
+// One CTA per (token, 128 selected tokens), then (several splits) the split combine.
 cudaError_t launch_sparse_mla_fp8(const MlaParams& p, cudaStream_t st, bool chained) {
   if (p.b.T == 0) return cudaSuccess;
-  return launch_ex(sparse_mla_fp8_kernel<0>, dim3(p.nsplit, p.b.T), dim3(mla8::THREADS), mla8::SMEM_BYTES, st,
-                   chained, p.nsplit > 1 ? static_cast<unsigned>(p.nsplit) : 0u, p);
+  const cudaError_t e = launch_ex(sparse_mla_fp8_kernel<0>, dim3(p.nsplit, p.b.T), dim3(mla8::THREADS),
+                                  mla8::SMEM_BYTES, st, chained, 0u, p);
+  if (e != cudaSuccess || p.nsplit == 1) return e;
+  return launch_mla_combine(p, st);
 }
 
 }  // namespace dsa

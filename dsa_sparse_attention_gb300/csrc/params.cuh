@@ -20,6 +20,8 @@ struct IndexerParams {
   int direct;              // 1: one token per group, planned inside the scorer (hdr/groups unused)
   uint32_t* row_hist;      // [T, 2048] or null: per-token counts of the scores' top 11 key bits are
                            // added here (one token per group only); a hint for the top-k
+  const __nv_bfloat16* mla_q = nullptr;   // [T, 96, 576] or null: in a layer step whose attention runs on
+  uint8_t* mla_q_terms = nullptr;         // FP8 latents, the epilogue warps also write its query terms here
 };
 
 struct TopkParams {
@@ -61,6 +63,7 @@ struct MlaParams {
   float* lse;              // [T, 96] or null    (nsplit == 1)
   __half* part_o;          // [T, nsplit, 512, 96] (nsplit > 1), dim-major, each normalised by its own sum
   float2* part_ml;         // [T, nsplit, 96]      (nsplit > 1): (max in log2 units, sum)
+  const uint8_t* q_terms = nullptr;   // FP8 kernel: [T] query terms (mla_q.cuh layout)
   uint32_t* status;
 };
 
@@ -158,9 +161,13 @@ cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, con
 int indexer_group_size(int idx_fmt, bool one_token_per_request);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained);
 cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained);
-// FP8 latents, one 128-token tile per CTA, the nsplit CTAs of a token in one
-// cluster: whether this device can run it for `nsplit` splits, and the launch.
-bool sparse_mla_fp8_available(int nsplit);
+// FP8 latents, one 128-token tile per CTA (p.nsplit = tiles of the selection, p.tps
+// = 1), followed by the split combine: whether it can run here, and the launch.
+bool sparse_mla_fp8_available();
 cudaError_t launch_sparse_mla_fp8(const MlaParams& p, cudaStream_t st, bool chained);
+// The log-sum-exp merge of p.nsplit normalised partials into p.out / p.lse.
+cudaError_t launch_mla_combine(const MlaParams& p, cudaStream_t st);
+// The query terms of a batch for the FP8 attention (a standalone call; a layer step's scorer writes them).
+cudaError_t launch_mla_qprep(const __nv_bfloat16* q, uint8_t* terms, int T, cudaStream_t st);
 
 }  // namespace dsa

@@ -422,6 +422,7 @@ struct ClShared {
   uint32_t wsh[8][32];            // scratch of the scans and searches, one row per call site
   uint32_t res[2];
   uint32_t meta[kClMaxCtas];      // per CTA: (keys above digit b1) << 16 | (keys in digit b1)
+  uint32_t meta_b1[kClMaxCtas];   // per CTA: the digit b1 those counts refer to
   uint32_t counts[kClMaxCtas];    // per CTA: (keys above T) << 16 | (keys equal to T)
 };
 constexpr int kClZeroWords = kBins + kClOwn + kBins + 1024 + kClOwn + kClOwn / 2;
@@ -641,17 +642,25 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
       cluster_wait();
       pending = false;
     }
-    if (tid < static_cast<int>(csize)) st_cluster_u32(cluster_map(smem_u32(&S.meta[rank]), tid), tot);
+    if (tid < static_cast<int>(csize)) {
+      st_cluster_u32(cluster_map(smem_u32(&S.meta[rank]), tid), tot);
+      st_cluster_u32(cluster_map(smem_u32(&S.meta_b1[rank]), tid), static_cast<uint32_t>(b1));
+    }
     if (multi) cluster_sync();
     else __syncthreads();
     if (PRE && round == 0 && rank == 0) gh[tid] = make_uint4(0u, 0u, 0u, 0u);   // every CTA has read it
     G = 0;
     Cc = 0;
+    bool agree = true;
     for (uint32_t r = 0; r < csize; ++r) {
       G += S.meta[r] >> 16;
       Cc += S.meta[r] & 0xFFFFu;
+      agree = agree && S.meta_b1[r] == static_cast<uint32_t>(b1);
     }
-    if (!PRE || (G < k && k <= G + Cc)) break;   // uniform over the cluster
+    // A hint that is not an exact histogram (a workspace not left zeroed) can make
+    // the bin search ambiguous, so the CTAs may have picked different digits: the
+    // counts decide only when every CTA used the same one.
+    if (!PRE || (agree && G < k && k <= G + Cc)) break;   // uniform over the cluster
     exchange = true;
   }
 
