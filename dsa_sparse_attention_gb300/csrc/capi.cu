@@ -203,6 +203,20 @@ bool make_q_map(CUtensorMap* m, const void* q, int T) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The FP8 attention's split partials [rows = T * nsplit * 512 dims][96 heads] fp16,
+// box 32 heads x 256 rows, 64-byte swizzle (tensor stores from shared memory).
+bool make_part_map(CUtensorMap* m, void* part_o, int64_t rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cuuint64_t(kMlaHeads), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(kMlaHeads) * 2};
+  cuuint32_t box[2] = {32, 256};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, part_o, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 PoolView pool_view(const dsa_kv_layout* l) {
   PoolView v;
   v.pool = static_cast<const uint8_t*>(l->pool);
@@ -357,7 +371,10 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
       const cudaError_t e = launch_mla_qprep(p.q, at<uint8_t>(ws, wl.m8_q), T, st);
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    return cuda_status(launch_sparse_mla_fp8(p, st, chained));
+    CUtensorMap pmap;
+    std::memset(&pmap, 0, sizeof(pmap));
+    if (p.nsplit > 1 && !make_part_map(&pmap, p.part_o, int64_t(T) * p.nsplit * kVDim)) return encode_fail();
+    return cuda_status(launch_sparse_mla_fp8(pmap, p, st, chained));
   }
   CUtensorMap qmap;
   if (!make_q_map(&qmap, q, T)) return encode_fail();

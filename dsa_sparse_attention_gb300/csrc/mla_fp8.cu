@@ -71,6 +71,7 @@ constexpr int O_COL = 128;
 constexpr int MMA_WARP = 3;                       // a warp of lane quarter 3, which has no softmax role
 static_assert(OFF_LAT % 1024 == 0 && OFF_SMALL % 1024 == 0, "operand tiles are 1024-byte aligned");
 static_assert(3 * P_TERM <= OFF_LAT, "P fits the query region");
+static_assert(3 * kVDim * 64 <= OFF_LAT, "the staged fp16 partial fits the query region");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace mla8
 
@@ -100,8 +101,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// pmap: the split partials [T * nsplit * 512 dim rows][96 heads] fp16, box 32 heads x 256
+// rows, 64-byte swizzle (unused with one split).
 template <int DUMMY>
-__global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaParams p) {
+__global__ void __launch_bounds__(mla8::THREADS, 1)
+    sparse_mla_fp8_kernel(const __grid_constant__ CUtensorMap pmap, MlaParams p) {
   using namespace mla8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024_m8(smem_raw);
@@ -379,11 +383,13 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
     // combine.  A split with nothing selected writes (-inf, 0) only.
     const int64_t ts = static_cast<int64_t>(t) * nsplit + split;
     if (good) {
-      // thread = one dim row of the partial: its 96 heads (192 bytes) go straight out
-      uint4* grow = reinterpret_cast<uint4*>(p.part_o + (ts * kVDim + dim) * kMlaHeads);
-      auto store32 = [&](const uint32_t (&rr)[32], int c) {
+      // Staged as three [512 dims x 32 heads] fp16 regions (64-byte rows, 64-byte
+      // swizzle: 16-byte piece q of row r at q ^ ((r / 2) % 4), conflict-free), then
+      // written by six tensor stores of 256 rows x 32 heads.
+      auto stage32 = [&](const uint32_t (&rr)[32], int c) {
         float iv[32];
         inv32(c, iv);
+        uint8_t* rowp = smem + OFF_Q + c * (kVDim * 64) + dim * 64;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t w4[4];
@@ -394,18 +400,30 @@ __global__ void __launch_bounds__(mla8::THREADS, 1) sparse_mla_fp8_kernel(MlaPar
                 __floats2half2_rn(__uint_as_float(rr[i]) * iv[i], __uint_as_float(rr[i + 1]) * iv[i + 1]);
             w4[e2] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-          grow[4 * c + q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          *reinterpret_cast<uint4*>(rowp + ((q ^ ((dim >> 1) & 3)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       };
       uint32_t r0[32], r1[32];
       DSA_TMEM_LD32(tmem + O_COL + 96 * vb + lane_off, r0);   // two loads in flight, one wait
       DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 32 + lane_off, r1);
       tmem_wait_ld();
-      store32(r0, 0);
-      store32(r1, 1);
+      stage32(r0, 0);
+      stage32(r1, 1);
       DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 64 + lane_off, r0);
       tmem_wait_ld();
-      store32(r0, 2);
+      stage32(r0, 2);
+      fence_proxy_async_smem();   // the staged partial is read by the tensor stores
+      __syncthreads();
+      if (tid == 0) {
+#pragma unroll 1
+        for (int c = 0; c < 3; ++c)
+#pragma unroll 1
+          for (int hr = 0; hr < 2; ++hr)
+            tma_store_2d(&pmap, smem + OFF_Q + c * (kVDim * 64) + hr * 256 * 64, 32 * c,
+                         static_cast<int>(ts * kVDim) + 256 * hr);
+        bulk_commit_group();
+        bulk_wait_group_all();   // the partial is in global memory before this CTA ends
+      }
     }
     if (tid < kMlaHeads) p.part_ml[ts * kMlaHeads + tid] = make_float2(ml[tid].x - 8.f, ml[tid].y);
   }
@@ -435,10 +453,10 @@ bool sparse_mla_fp8_available() {
 }
 
 // One CTA per (token, 128 selected tokens), then (several splits) the split combine.
-cudaError_t launch_sparse_mla_fp8(const MlaParams& p, cudaStream_t st, bool chained) {
+cudaError_t launch_sparse_mla_fp8(const CUtensorMap& pmap, const MlaParams& p, cudaStream_t st, bool chained) {
   if (p.b.T == 0) return cudaSuccess;
   const cudaError_t e = launch_ex(sparse_mla_fp8_kernel<0>, dim3(p.nsplit, p.b.T), dim3(mla8::THREADS),
-                                  mla8::SMEM_BYTES, st, chained, 0u, p);
+                                  mla8::SMEM_BYTES, st, chained, 0u, pmap, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
   return launch_mla_combine(p, st);
 }

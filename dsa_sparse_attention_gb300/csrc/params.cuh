@@ -164,7 +164,7 @@ cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaS
 // FP8 latents, one 128-token tile per CTA (p.nsplit = tiles of the selection, p.tps
 // = 1), followed by the split combine: whether it can run here, and the launch.
 bool sparse_mla_fp8_available();
-cudaError_t launch_sparse_mla_fp8(const MlaParams& p, cudaStream_t st, bool chained);
+cudaError_t launch_sparse_mla_fp8(const CUtensorMap& pmap, const MlaParams& p, cudaStream_t st, bool chained);
 // The log-sum-exp merge of p.nsplit normalised partials into p.out / p.lse.
 cudaError_t launch_mla_combine(const MlaParams& p, cudaStream_t st);
 // The query terms of a batch for the FP8 attention (a standalone call; a layer step's scorer writes them).
