@@ -80,6 +80,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true", help="measure only the headline configuration")
+    ap.add_argument("--profile-config", default=None,
+                    help="run configuration N's layer step (or 'prefill_small': 1024 queries on a 32,768-token "
+                         "cache) W + K times and print nothing (for a profiler)")
     return ap.parse_args()
 
 
@@ -242,6 +246,151 @@ def cpu_baseline(wl, budget_s=12.0):
                       f"BLAS threads = {threads} of {os.cpu_count()} host cores"}
 
 
+# The other benchmark configurations, measured beside the headline one (each on its
+# own synthetic workload, seed 0; one device copy of its pool).
+OTHER_CONFIGS = {
+    2: "MTP decode: 32 requests x 6 query tokens (causal among them), contexts log-uniform in [16384, 262144], "
+       "FP8 keys and latents, permuted block table, top-2048",
+    3: "decode 1 request x 1,048,576-token context, MXFP4 index keys + NVFP4 latents, permuted block table, top-2048",
+    4: "chunked prefill: 8192 new queries on a 131,072-token cache (causal), FP8 keys and latents, top-2048",
+}
+
+
+def fp8_peak_tflops(bf16_tflops):
+    """Dense FP8 tensor peak derived from the measured bf16 one by the nominal ratio
+    (4.5 : 2.25 PFLOP/s dense on GB300)."""
+    return 2.0 * bf16_tflops
+
+
+def scorer_flops(wl):
+    """Indexer MACs as FLOPs: every scored (query, key) pair costs 32 heads x 128 dims x 2."""
+    return 2.0 * 32 * 128 * float(np.sum(wl.q_pos.astype(np.int64) + 1))
+
+
+def oracle_query_sample(wl, tokens):
+    """Seconds the float64 oracle takes for the listed query tokens of a workload."""
+    from oracle import dsa_oracle as O
+    lay = O.Layout(wl.pool, wl.row_stride, wl.idx_page_offset, wl.lat_page_offset, wl.block_size, wl.idx_fmt,
+                   wl.lat_fmt)
+    t0 = time.perf_counter()
+    O.layer_step(lay, wl.block_table, wl.ctx_lens, wl.q_req, wl.q_pos, wl.q_idx, wl.w, wl.q, topk=wl.topk,
+                 sm_scale=wl.sm_scale, tokens=tokens)
+    return time.perf_counter() - t0
+
+
+def measure_config(n, args, stream, flush, hbm_gbs, bf16_tflops, cpu=True):
+    """Layer-step time of configuration n (a CUDA graph of one dsa_layer_step, the L2
+    flushed by a 256 MiB write before each timed replay; median of the steps), the
+    indexer scorer's roofline (HBM for decode, FP8 tensor for prefill) and an oracle
+    sample on the host."""
+    import torch
+    import dsa_sparse_attention_gb300 as dsa
+    from dsa_sparse_attention_gb300 import workloads as W
+    from dsa_sparse_attention_gb300.harness import DeviceWorkload
+
+    wl = W.config(n, seed=0)
+    dw = DeviceWorkload(wl)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            dw.layer_step(stream)
+    stream.synchronize()
+    assert dsa.dsa_check(dw.ws, stream) == 0
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def timed_ms(g, reps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                flush.zero_()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    reps = max(5, min(args.steps, 50))
+    step_g = graph_of(lambda: dw.layer_step(torch.cuda.current_stream()))
+    step_ms = timed_ms(step_g, reps)
+    scores = torch.empty(wl.num_tokens, dw.ld, dtype=torch.float32, device="cuda")
+    sc_g = graph_of(lambda: dsa.dsa_indexer_score(dw.layout, dw.batch, dw.q_idx, dw.w, scores, dw.ld, dw.ws,
+                                                  torch.cuda.current_stream()))
+    sc_ms = timed_ms(sc_g, reps)
+    idx = dw.idx.cpu().numpy()
+    alg = algorithmic_bytes(wl, idx)
+    sb = scorer_bytes(wl)
+    out = {"workload": OTHER_CONFIGS[n], "tokens": wl.num_tokens, "requests": wl.num_reqs,
+           "ms_per_step": step_ms, "layer_steps_per_s": 1000.0 / step_ms, "algorithmic_bytes_per_step": alg,
+           "achieved_hbm_tbs_step": alg / (step_ms * 1e-3) / 1e12,
+           "timing": f"median of {reps} graph replays of one layer step, L2 flushed (256 MiB write) before each",
+           "scorer_ms": sc_ms}
+    if n == 4:
+        fl = scorer_flops(wl)
+        tf = fl / (sc_ms * 1e-3) / 1e12
+        pk = fp8_peak_tflops(bf16_tflops)
+        out["roofline"] = {"bound": "tensor", "kernel": "indexer scorer (FP8 tcgen05, 8 queries share a key tile)",
+                           "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk, "flops": fl,
+                           "peak_kind": "measured bf16 burst x 2 (nominal FP8 : bf16 dense ratio)"}
+    else:
+        gbs = sb / (sc_ms * 1e-3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": "indexer scorer", "achieved": gbs, "peak": hbm_gbs,
+                           "unit": "GB/s", "frac": gbs / hbm_gbs, "bytes": sb,
+                           "peak_kind": "measured copy bandwidth (burst)"}
+    if n == 3:
+        # the same 1M-token context with FP8 index keys (132 B) instead of MXFP4 (68 B)
+        wf = W.make_workload([1 << 20], 1, name="decode_L1M_fp8keys", seed=0, idx_fmt=W.IDX_FP8,
+                             lat_fmt=W.LAT_NVFP4, permute=True)
+        df = DeviceWorkload(wf)
+        sf = torch.empty(1, df.ld, dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                dsa.dsa_indexer_score(df.layout, df.batch, df.q_idx, df.w, sf, df.ld, df.ws, stream)
+        fg = graph_of(lambda: dsa.dsa_indexer_score(df.layout, df.batch, df.q_idx, df.w, sf, df.ld, df.ws,
+                                                    torch.cuda.current_stream()))
+        f_ms = timed_ms(fg, reps)
+        out["mxfp4_vs_fp8_keys"] = {"scorer_ms_mxfp4": sc_ms, "scorer_ms_fp8": f_ms, "speedup": f_ms / sc_ms,
+                                    "fp8_gbs": scorer_bytes(wf) / (f_ms * 1e-3) / 1e9}
+        del df, sf, fg
+    if cpu:
+        toks = [0]
+        secs = oracle_query_sample(wl, toks)
+        per_step = secs * wl.num_tokens / len(toks)
+        out["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "layer-steps/s",
+                               "cores": int(os.environ.get("OPENBLAS_NUM_THREADS") or os.cpu_count()),
+                               "kind": "oracle",
+                               "sample": f"{len(toks)} of {wl.num_tokens} query tokens in {secs:.2f} s, scaled to the "
+                                         f"whole step (extrapolated)"}
+    del dw, scores, step_g, sc_g
+    torch.cuda.synchronize()
+    return out
+
+
+def profile_config(args):
+    """Configuration N's layer step, W + K times on one stream, nothing timed or printed:
+    the command a profiler wraps to capture one configuration's kernels."""
+    import torch
+    import dsa_sparse_attention_gb300 as dsa
+    from dsa_sparse_attention_gb300 import workloads as W
+    from dsa_sparse_attention_gb300.build import build
+    from dsa_sparse_attention_gb300.harness import DeviceWorkload
+    build()
+    if args.profile_config == "prefill_small":   # the prefill scorer at a size a full profile can hold
+        wl = W.make_workload([32768 + 1024], 1024, name="prefill_1024_on_32768", seed=0, permute=True)
+    else:
+        wl = W.config(int(args.profile_config), seed=0)
+    dw = DeviceWorkload(wl)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup + args.steps):
+            dw.layer_step(stream)
+    stream.synchronize()
+    assert dsa.dsa_check(dw.ws, stream) == 0
+
+
 def run_reference(args, wl):
     _, world, _ = dist_info()
     # W untimed and K timed steps of the oracle, each a whole layer step of the
@@ -297,6 +446,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:   # the other ranks exit without work
             run_reference(args, W.config(1, seed=0))
+        return
+    if args.profile_config is not None:
+        profile_config(args)
         return
     wl = W.config(1, seed=0)
 
@@ -480,6 +632,18 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
 
+    # the other configurations, after the headline one's buffers are released
+    others = {}
+    if not args.skip_configs:
+        del graphs, chain, pools, layouts
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        peak_gbs, _ = load_peaks()
+        bf16_pk, _ = load_bf16_peak()
+        for n in sorted(OTHER_CONFIGS):
+            others[f"cfg{n}"] = measure_config(n, args, stream, flush, peak_gbs, bf16_pk,
+                                               cpu=rank == 0 and not args.no_cpu_baseline)
+
     if rank == 0:
         line = {
             "metric": "DSA decode layer-steps/s (64K context, batch 8)", "value": value, "unit": "layer-steps/s",
@@ -510,6 +674,7 @@ def main():
                                          f"({bf16_kind}, burst)"),
             "clocks": clk, "wall_s_timed": t_wall,
             "cpu_baseline": cpu,
+            "other_configs": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

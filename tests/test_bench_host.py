@@ -179,3 +179,13 @@ def test_call_rooflines_decode_b8_64k():
     r2 = bench.call_rooflines(wl, idx, {"indexer_score": 0.01, "topk": 0.01, "sparse_mla": 0.01}, 1000.0, 2000.0)
     assert r2["sparse_mla"]["flops"] * 2 == r["sparse_mla"]["flops"]
     assert r["sparse_mla"]["bytes"] - r2["sparse_mla"]["bytes"] == 8 * 1024 * LAT_FP8
+
+
+def test_prefill_scorer_flops_and_fp8_peak():
+    # every scored (query, key) pair costs 32 heads x 128 dims x 2 FLOP: for 8192
+    # queries at positions 131,072 + i that is 8192 x sum_i (131,073 + i) x 8192 = 9.07 TFLOP
+    wl = types.SimpleNamespace(q_pos=np.arange(131072, 131072 + 8192, dtype=np.int32))
+    want = 2.0 * 32 * 128 * (8192 * 131073 + 8191 * 8192 // 2)
+    assert bench.scorer_flops(wl) == want and abs(want - 9.07e12) < 0.01e12
+    assert bench.fp8_peak_tflops(1914.3) == 2 * 1914.3
+    assert set(bench.OTHER_CONFIGS) == {2, 3, 4}
