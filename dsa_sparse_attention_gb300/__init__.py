@@ -10,8 +10,8 @@ device memory and streams.
 Names mirror the C ABI: dsa_workspace_size, dsa_indexer_score, dsa_topk,
 dsa_sparse_mla, dsa_layer_step, dsa_layer_step_host (and
 prepare_layer_step_host, the same call with its arguments marshalled once),
-dsa_topk_noalloc, dsa_selftest_wait_timeout, dsa_check, dsa_status_string,
-dsa_abi_version.
+dsa_topk_noalloc, dsa_indexer_front, dsa_write_latent, dsa_selftest_wait_timeout,
+dsa_check, dsa_status_string, dsa_abi_version.
 """
 import ctypes
 import os
@@ -75,6 +75,8 @@ def _load():
         "dsa_last_cuda_error": (i32, [P(ctypes.c_char_p)]),
         "dsa_topk_noalloc": (i32, [L, B, vp, i64, i32, vp, vp, vp]),
         "dsa_selftest_wait_timeout": (i32, [vp, sz, i64, vp]),
+        "dsa_indexer_front": (i32, [L, B, vp, i32, vp, f32, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "dsa_write_latent": (i32, [L, B, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -229,6 +231,22 @@ def dsa_selftest_wait_timeout(ws, limit_cycles, stream=None):
     then reports DSA_ERR_TIMEOUT."""
     _check(library().dsa_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_cycles), _stream(stream)),
            "dsa_selftest_wait_timeout")
+
+
+def dsa_indexer_front(layout, batch, c_q, norm_weight, eps, w_qi, head_w, q_idx, w_out, k_new=None, ws=None,
+                      stream=None):
+    """The fused indexer front: q_idx / w_out for the scorer and, with k_new, the new
+    tokens' index keys written into the pool."""
+    _check(library().dsa_indexer_front(ctypes.byref(layout), ctypes.byref(batch), _ptr(c_q), int(c_q.shape[1]),
+                                       _ptr(norm_weight), float(eps), _ptr(w_qi), _ptr(head_w), _ptr(k_new),
+                                       _ptr(q_idx), _ptr(w_out), _ptr(ws), ws.numel(), _stream(stream)),
+           "dsa_indexer_front")
+
+
+def dsa_write_latent(layout, batch, latent, ws=None, stream=None):
+    """The new tokens' latents (bf16 [T, 576]) into their cache slots, in the pool's format."""
+    _check(library().dsa_write_latent(ctypes.byref(layout), ctypes.byref(batch), _ptr(latent), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "dsa_write_latent")
 
 
 def dsa_check(ws, stream=None):

@@ -627,6 +627,57 @@ dsa_status run_step(const dsa_kv_layout* layout, const dsa_batch* batch, const v
 
 extern "C" {
 
+dsa_status dsa_indexer_front(const dsa_kv_layout* layout, const dsa_batch* batch, const void* c_q, int32_t d_q,
+                             const void* norm_weight, float eps, const void* w_qi, const float* head_w,
+                             const void* k_new, void* q_idx, float* w_out, void* workspace, size_t workspace_bytes,
+                             dsa_stream_t stream) {
+  dsa_status s = check_layout(layout);
+  if (s != DSA_OK) return s;
+  if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
+  if (k_new && layout->idx_fmt != DSA_IDX_FP8) return DSA_ERR_UNSUPPORTED;
+  if (d_q < 8 || d_q > 4096 || (d_q & 7) || !std::isfinite(eps) || eps < 0.f) return DSA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) || workspace_bytes < kStatusBytes)
+    return DSA_ERR_WORKSPACE;
+  const int T = batch->num_tokens;
+  if (T == 0) return DSA_OK;
+  if (!c_q || !norm_weight || !w_qi || !head_w || !q_idx || !w_out || !aligned16(c_q) || !aligned16(norm_weight) ||
+      !aligned16(w_qi) || !aligned16(q_idx) || !aligned16(head_w) || !aligned16(w_out) || (k_new && !aligned16(k_new)))
+    return DSA_ERR_INVALID_ARG;
+  FrontParams p;
+  p.b = batch_view(batch);
+  p.pool = pool_view(layout);
+  p.c_q = static_cast<const __nv_bfloat16*>(c_q);
+  p.gamma = static_cast<const __nv_bfloat16*>(norm_weight);
+  p.w_qi = static_cast<const __nv_bfloat16*>(w_qi);
+  p.head_w = head_w;
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.q_idx = static_cast<uint8_t*>(q_idx);
+  p.w_out = w_out;
+  p.pool_w = static_cast<uint8_t*>(const_cast<void*>(layout->pool));
+  p.d_q = d_q;
+  p.eps = eps;
+  p.status = static_cast<uint32_t*>(workspace);
+  return cuda_status(launch_indexer_front(p, stream));
+}
+
+dsa_status dsa_write_latent(const dsa_kv_layout* layout, const dsa_batch* batch, const void* latent,
+                            void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  dsa_status s = check_layout(layout);
+  if (s != DSA_OK) return s;
+  if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) || workspace_bytes < kStatusBytes)
+    return DSA_ERR_WORKSPACE;
+  if (batch->num_tokens == 0) return DSA_OK;
+  if (!latent || !aligned16(latent)) return DSA_ERR_INVALID_ARG;
+  LatentWriteParams p;
+  p.b = batch_view(batch);
+  p.pool = pool_view(layout);
+  p.latent = static_cast<const __nv_bfloat16*>(latent);
+  p.pool_w = static_cast<uint8_t*>(const_cast<void*>(layout->pool));
+  p.status = static_cast<uint32_t*>(workspace);
+  return cuda_status(launch_write_latent(p, stream));
+}
+
 dsa_status dsa_check(void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
   if (!workspace || workspace_bytes < kStatusBytes) return DSA_ERR_WORKSPACE;
   uint32_t word = 0;

@@ -149,6 +149,34 @@ inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The fused indexer front and the latent write (front.cu).
+struct FrontParams {
+  BatchView b;
+  PoolView pool;
+  const __nv_bfloat16* c_q;    // [T, d_q]
+  const __nv_bfloat16* gamma;  // [d_q]
+  const __nv_bfloat16* w_qi;   // [4096, d_q]
+  const float* head_w;         // [T, 32]
+  const __nv_bfloat16* k_new;  // [T, 128] or null
+  uint8_t* q_idx;              // [T, 32, 128] e4m3
+  float* w_out;                // [T, 32]
+  uint8_t* pool_w;             // the pool, written at the new tokens' slots
+  int d_q;
+  float eps;
+  uint32_t* status;
+};
+
+struct LatentWriteParams {
+  BatchView b;
+  PoolView pool;
+  const __nv_bfloat16* latent;   // [T, 576]
+  uint8_t* pool_w;
+  uint32_t* status;
+};
+
+cudaError_t launch_indexer_front(const FrontParams& p, cudaStream_t st);
+cudaError_t launch_write_latent(const LatentWriteParams& p, cudaStream_t st);
+
 // Host helpers (capi.cu): the CUDA context current on this thread, and
 // cudaFuncSetAttribute done once per (context, kernel, attribute, value).
 void* current_context();

@@ -295,6 +295,51 @@ dsa_status dsa_topk_noalloc(const dsa_kv_layout *layout, const dsa_batch *batch,
                             dsa_stream_t stream);
 
 /*
+ * The fused indexer front ("Low-latency decode: a fused DSA decode path": the
+ * query norm, the indexer's query projection, its FP8 quantization with the head
+ * weights folded in, and the new token's index key, in one kernel).  The post
+ * prints no shapes; this call takes them as stated here.  For each query token t:
+ *   y = c_q[t] / sqrt(mean(c_q[t]^2) + eps) * norm_weight          (RMSNorm, fp32)
+ *   q[h, :] = w_qi[h * 128 .. h * 128 + 127, :] . y               (fp32)
+ *   s[h] = max|q[h, :]| / 448 (1 for an all-zero head)
+ *   q_idx[t, h, :] = e4m3(q[h, :] / s[h]),  w_out[t, h] = head_w[t, h] * s[h]
+ * so q_idx and w_out are the inputs dsa_indexer_score / dsa_layer_step take.
+ * With k_new given, the new token's index key is written into the pool at the
+ * token's own position (block_table[q_req[t]][q_pos[t] / bs], slot q_pos[t] % bs):
+ * s_k = max|k| / 448 in fp32 (1 when zero), 128 codes e4m3(k / s_k), then s_k in
+ * the page's scale area.  FP8 index pages only (DSA_ERR_UNSUPPORTED otherwise).
+ *  c_q        : device bf16 [T, d_q], d_q a multiple of 8 in 8..4096
+ *  norm_weight: device bf16 [d_q];  eps >= 0
+ *  w_qi       : device bf16 [32 * 128, d_q] (row h * 128 + d is output dim d of head h)
+ *  head_w     : device fp32 [T, 32];  k_new: device bf16 [T, 128] or NULL
+ *  q_idx      : device e4m3 [T, 32, 128] (written);  w_out: device fp32 [T, 32] (written)
+ *  workspace  : only its status word is used (>= 256 bytes); a block id or
+ *               position out of range is recorded there and nothing is written for it.
+ * Unlike the other calls this one writes the pool (the new tokens' slots only).
+ * All pointers 16-byte aligned.
+ */
+dsa_status dsa_indexer_front(const dsa_kv_layout *layout, const dsa_batch *batch, const void *c_q, int32_t d_q,
+                             const void *norm_weight, float eps, const void *w_qi, const float *head_w,
+                             const void *k_new, void *q_idx, float *w_out, void *workspace, size_t workspace_bytes,
+                             dsa_stream_t stream);
+
+/*
+ * The new tokens' latents into the cache ("Low-latency decode: a fused DSA decode
+ * path": the MLA query kernel writes the new token's latent into the KV cache;
+ * "KV cache footprint": 576-byte FP8 or 352-byte NVFP4 latents).  For each query
+ * token t the record at its own position (as in dsa_indexer_front) becomes
+ *   FP8  : e4m3(latent[t, :]) (576 bytes, no scale)
+ *   NVFP4: per 16 values j: scale_j = e4m3(max|x| / 6), codes e2m1(x / scale_j)
+ *          (zero for a zero scale), packed two per byte (element 2i in the low
+ *          nibble), 36 scale bytes, 28 zero bytes (352 bytes)
+ * with round-to-nearest-even, saturating conversions in fp32.
+ *  latent   : device bf16 [T, 576], 16-byte aligned
+ *  workspace: only its status word is used (>= 256 bytes), as above.
+ */
+dsa_status dsa_write_latent(const dsa_kv_layout *layout, const dsa_batch *batch, const void *latent,
+                            void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
  * Synchronises `stream`, reads the workspace status word written by earlier
  * calls, clears it, and returns DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK.
  */

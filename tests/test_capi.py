@@ -102,6 +102,26 @@ def test_noalloc_topk_validation(lib):
     assert f(None, ctypes.byref(big), 0x1000, 1 << 20, 2048, 0x2000, None, None) == -4
 
 
+def test_front_and_latent_write_validation(lib):
+    # every check runs on the host before a launch
+    L = dsa.library()
+    b = ctypes.byref(_batch())
+    front = lambda lay, d_q=1536, eps=1e-6, ws=0x100000, ws_bytes=4096, k=0x6000: L.dsa_indexer_front(
+        ctypes.byref(lay), b, 0x1000, d_q, 0x2000, eps, 0x3000, 0x4000, k, 0x7000, 0x8000, ws, ws_bytes, None)
+    assert front(_layout(), d_q=7) == -1                       # not a multiple of 8
+    assert front(_layout(), d_q=8192) == -1                    # wider than 4096
+    assert front(_layout(), eps=-1.0) == -1
+    assert front(_layout(), eps=float("nan")) == -1
+    assert front(_layout(), ws_bytes=16) == -4
+    assert front(_layout(), ws=0x100010) == -4
+    assert front(_layout(idx_fmt=1)) == -2                     # new keys need FP8 index pages
+    assert L.dsa_indexer_front(ctypes.byref(_layout()), b, 0x1008, 1536, 0x2000, 1e-6, 0x3000, 0x4000, None, 0x7000,
+                               0x8000, 0x100000, 4096, None) == -1   # misaligned query
+    assert L.dsa_write_latent(ctypes.byref(_layout()), b, None, 0x100000, 4096, None) == -1
+    assert L.dsa_write_latent(ctypes.byref(_layout()), b, 0x1000, 0x100000, 16, None) == -4
+    assert L.dsa_write_latent(None, b, 0x1000, 0x100000, 4096, None) == -1
+
+
 def test_selftest_validation(lib):
     f = dsa.library().dsa_selftest_wait_timeout
     assert f(None, 4096, 100000, None) == -4            # no workspace
