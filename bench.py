@@ -369,6 +369,42 @@ def measure_config(n, args, stream, flush, hbm_gbs, bf16_tflops, cpu=True):
     return out
 
 
+FRONT_DQ = 1536
+
+
+def front_bytes(T, d_q=FRONT_DQ):
+    """Bytes the indexer front must move: the projection weights once, each token's
+    compressed query, its head weights in and out, its q_idx and new key."""
+    return 4096 * d_q * 2 + d_q * 2 + T * (d_q * 2 + 32 * 4 * 2 + 4096 + 128 * 2 + 132)
+
+
+def measure_front(dw, stream, graph_timed_fn, hbm_gbs):
+    """Mean time of one dsa_indexer_front call (replayed from a graph of 8 calls over
+    the batch of `dw`), and its rate against the HBM peak."""
+    import torch
+    import dsa_sparse_attention_gb300 as dsa
+    T = dw.wl.num_tokens
+    g = torch.Generator(device="cuda").manual_seed(0)
+    c_q = torch.randn(T, FRONT_DQ, generator=g, device="cuda").to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(FRONT_DQ, generator=g, device="cuda")).to(torch.bfloat16)
+    w_qi = (torch.randn(4096, FRONT_DQ, generator=g, device="cuda") / FRONT_DQ ** 0.5).to(torch.bfloat16)
+    head_w = torch.randn(T, 32, generator=g, device="cuda") / 32 ** 0.5
+    k_new = torch.randn(T, 128, generator=g, device="cuda").to(torch.bfloat16)
+    pool = dw.pool.clone()   # the front writes the new keys: a copy of the pool
+    lay = dw.pool_copy_layout(pool)
+    q_idx = torch.empty(T, 32, 128, dtype=torch.uint8, device="cuda")
+    w_out = torch.empty(T, 32, dtype=torch.float32, device="cuda")
+    call = lambda _lay: dsa.dsa_indexer_front(lay, dw.batch, c_q, gamma, 1e-6, w_qi, head_w, q_idx, w_out,
+                                              k_new=k_new, ws=dw.ws, stream=stream)
+    ms = graph_timed_fn(call)
+    nbytes = front_bytes(T)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del pool
+    return {"ms": ms, "bytes": nbytes, "gbs": gbs, "frac_hbm": gbs / hbm_gbs, "d_q": FRONT_DQ,
+            "how": "mean over 8 calls replayed from one CUDA graph; weights are synthetic (seeded), the compressed "
+                   "query width 1,536 a reading"}
+
+
 def profile_config(args):
     """Configuration N's layer step, W + K times on one stream, nothing timed or printed:
     the command a profiler wraps to capture one configuration's kernels."""
@@ -601,6 +637,10 @@ def main():
         "eager_one_call": {"indexer_score": sc_ms_eager, "topk": timed(topk_call), "sparse_mla": timed(mla_call)},
     }
 
+    # the fused indexer front of the same batch (compressed query of 1,536 dims, seeded
+    # synthetic weights): a stream of the 4096 x 1536 bf16 projection weights
+    front = measure_front(dw, stream, graph_timed_fn=graph_timed, hbm_gbs=load_peaks()[0])
+
     # whole-step algorithmic bytes
     idx_np = dw.idx.cpu().numpy()
     alg = algorithmic_bytes(wl, idx_np)
@@ -669,6 +709,7 @@ def main():
                     "how": e2e_how},
             "gpu_launches": n_kernels_per_step * args.steps,
             "breakdown_ms": breakdown,
+            "indexer_front": front,
             "call_rooflines": dict(call_rooflines(wl, idx_np, breakdown["graph_replayed"], peak, bf16_peak),
                                    peaks=f"HBM {peak:.0f} GB/s ({peak_kind}), bf16 {bf16_peak:.0f} TFLOP/s "
                                          f"({bf16_kind}, burst)"),

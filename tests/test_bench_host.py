@@ -189,3 +189,9 @@ def test_prefill_scorer_flops_and_fp8_peak():
     assert bench.scorer_flops(wl) == want and abs(want - 9.07e12) < 0.01e12
     assert bench.fp8_peak_tflops(1914.3) == 2 * 1914.3
     assert set(bench.OTHER_CONFIGS) == {2, 3, 4}
+
+
+def test_front_bytes():
+    # 4096 x 1536 bf16 weights, gamma, and per token: query, head weights in and out,
+    # q_idx codes, the new key in (bf16) and out (132 B)
+    assert bench.front_bytes(8) == 4096 * 1536 * 2 + 1536 * 2 + 8 * (1536 * 2 + 256 + 4096 + 256 + 132)
