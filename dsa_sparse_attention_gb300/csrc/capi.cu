@@ -217,6 +217,21 @@ bool make_part_map(CUtensorMap* m, void* part_o, int64_t rows) {
          CUDA_SUCCESS;
 }
 
+// The split partials as [T * nsplit][512 dims][96 heads] fp16 for the combine: a box
+// is four consecutive splits of 32 dims x 96 heads (no swizzle, 192-byte rows).
+bool make_comb_map(CUtensorMap* m, void* part_o, int64_t T, int nsplit) {
+  constexpr cuuint32_t kBoxSplits = 4;   // the combine's splits per copy
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cuuint64_t(kMlaHeads), cuuint64_t(kVDim), cuuint64_t(T) * cuuint64_t(nsplit)};
+  cuuint64_t strides[2] = {cuuint64_t(kMlaHeads) * 2, cuuint64_t(kMlaHeads) * 2 * kVDim};
+  cuuint32_t box[3] = {cuuint32_t(kMlaHeads), 32, kBoxSplits};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, part_o, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 PoolView pool_view(const dsa_kv_layout* l) {
   PoolView v;
   v.pool = static_cast<const uint8_t*>(l->pool);
@@ -371,14 +386,19 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
       const cudaError_t e = launch_mla_qprep(p.q, at<uint8_t>(ws, wl.m8_q), T, st);
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    CUtensorMap pmap;
+    CUtensorMap pmap, cmap;
     std::memset(&pmap, 0, sizeof(pmap));
-    if (p.nsplit > 1 && !make_part_map(&pmap, p.part_o, int64_t(T) * p.nsplit * kVDim)) return encode_fail();
-    return cuda_status(launch_sparse_mla_fp8(pmap, p, st, chained));
+    std::memset(&cmap, 0, sizeof(cmap));
+    if (p.nsplit > 1 && (!make_part_map(&pmap, p.part_o, int64_t(T) * p.nsplit * kVDim) ||
+                         !make_comb_map(&cmap, p.part_o, T, p.nsplit)))
+      return encode_fail();
+    return cuda_status(launch_sparse_mla_fp8(pmap, cmap, p, st, chained));
   }
-  CUtensorMap qmap;
+  CUtensorMap qmap, cmap;
+  std::memset(&cmap, 0, sizeof(cmap));
   if (!make_q_map(&qmap, q, T)) return encode_fail();
-  return cuda_status(launch_sparse_mla(qmap, p, st, chained));
+  if (p.nsplit > 1 && !make_comb_map(&cmap, p.part_o, T, p.nsplit)) return encode_fail();
+  return cuda_status(launch_sparse_mla(qmap, cmap, p, st, chained));
 }
 
 // One host <-> device copy of dsa_layer_step_host.

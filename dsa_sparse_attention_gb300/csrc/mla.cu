@@ -723,40 +723,65 @@ __global__ void __launch_bounds__(mla::THREADS, 1)
 }
 
 // Log-sum-exp combine of the split partials (each partial normalised by its
-// own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m);
-// one thread per head computes the weights.
-// Grid (512 / 32 dims, T), 384 threads: thread = (dim of the block's 32, group of 8
-// heads); every split's 16 bytes are loaded at once, before the weights.  Splits
-// with nothing selected (sum 0) take no part in the sum.  The [96 heads x 32 dims] result is
-// staged in shared memory for row stores.
+// own sum): out = sum_j w_j l_j o_j / sum_j w_j l_j, w_j = 2^(m_j - max m).
+// Grid (512 / 32 dims, T), 12 warps.  The token's partials of the block's 32 dims
+// come into shared memory by TMA, four splits per copy (boxes of 96 heads x 32
+// dims x 4 splits, 192-byte rows; a box past the token's last split reads bytes
+// that are not used), each on its own barrier so the sums start while later
+// splits land; the nsplit x 96 (max, sum) pairs come by one bulk copy and
+// threads 0..95 turn them into weights (one thread per head).  Warp w takes the
+// 32 heads of quad w % 3 and the 8 dims of octet w / 3; lane = (dim, group of 8
+// heads), so a warp's reads of one split hit every bank equally and its weights
+// are four 32-byte rows.  Splits with nothing selected (sum 0) take no part in
+// the sum.  The [96 heads x 32 dims] result is staged for row stores.
 constexpr int kCombDims = 32;
-constexpr int kCombThreads = kCombDims * (kMlaHeads / 8);
+constexpr int kCombThreads = 384;
 constexpr int kMaxSplits = kMaxTopk / kSelTile;
-__global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) {
+constexpr int kCombBoxSplits = 4;                                   // splits per TMA copy
+constexpr int kCombMaxBoxes = kMaxSplits / kCombBoxSplits;
+constexpr int kCombSplitBytes = kCombDims * kMlaHeads * 2;          // 6144: one split's 32 dims x 96 heads
+static_assert(kMaxSplits % kCombBoxSplits == 0, "whole boxes");
+__global__ void __launch_bounds__(kCombThreads)
+    mla_combine_kernel(const __grid_constant__ CUtensorMap cmap, MlaParams p) {
+  extern __shared__ uint8_t csm_raw[];
+  uint8_t* csm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(csm_raw) + 127) & ~uintptr_t(127));
+  const int ns = p.nsplit;
+  const int nbox = (ns + kCombBoxSplits - 1) / kCombBoxSplits;
+  const float2* mls = reinterpret_cast<const float2*>(csm + nbox * kCombBoxSplits * kCombSplitBytes);   // [ns][96]
   __shared__ __align__(16) float wgt[kMaxSplits][kMlaHeads];   // normalised weight per split and head
   __shared__ __align__(16) __nv_bfloat16 tile[kMlaHeads][kCombDims];
-  __shared__ int used[kMaxSplits];
+  __shared__ uint32_t used_mask;   // bit j: split j holds selected tokens
+  __shared__ __align__(8) uint64_t bars[kCombMaxBoxes + 1];   // one per box, then the (max, sum) pairs
+  __shared__ int abortf;
+  const int t = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i <= kCombMaxBoxes; ++i) mbar_init(&bars[i], 1);
+    abortf = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&cmap);
+  }
+  __syncthreads();
   grid_dep_wait();
   grid_dep_launch();   // the next chained kernel (the next layer step's scorer) may be scheduled
-  const int t = blockIdx.y;
-  const int64_t base = static_cast<int64_t>(t) * p.nsplit;
-  const int g = threadIdx.x % (kMlaHeads / 8);            // heads [8g, 8g + 8)
-  const int dl = threadIdx.x / (kMlaHeads / 8);           // dim within the block
-  const int d = blockIdx.x * kCombDims + dl;
-  // every split's 16 bytes are requested first, so their latency covers the weights
-  // below; an empty split's slot (in bounds, never written) is loaded but not used
-  uint4 u[kMaxSplits];
-#pragma unroll
-  for (int j = 0; j < kMaxSplits; ++j)
-    if (j < p.nsplit) u[j] = __ldcg(reinterpret_cast<const uint4*>(p.part_o + ((base + j) * kVDim + d) * kMlaHeads + 8 * g));
-  // weights: thread h < 96 owns head h; its (max, sum) of every split come straight
-  // from global memory, all loads in flight at once (alongside the partials above)
-  if (threadIdx.x < kMlaHeads) {
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bars[kCombMaxBoxes], static_cast<uint32_t>(ns) * kMlaHeads * 8);
+    bulk_load(const_cast<float2*>(mls), p.part_ml + static_cast<int64_t>(t) * ns * kMlaHeads,
+              static_cast<uint32_t>(ns) * kMlaHeads * 8, &bars[kCombMaxBoxes]);
+  } else if (threadIdx.x >= 32 && threadIdx.x < 32 + nbox) {   // one box per thread of warp 1
+    const int bx = threadIdx.x - 32;
+    mbar_arrive_expect_tx(&bars[bx], kCombBoxSplits * kCombSplitBytes);
+    tma_load_3d(csm + bx * kCombBoxSplits * kCombSplitBytes, &cmap, &bars[bx], 0, blockIdx.x * kCombDims,
+                t * ns + bx * kCombBoxSplits);
+  }
+  const Abort ab{&abortf, p.status};
+  // Loops over the splits are unrolled to the maximum with the split count as a
+  // predicate: their shared-memory loads then issue together.
+  if (threadIdx.x < kMlaHeads && mbar_wait(&bars[kCombMaxBoxes], 0, ab)) {
     const int h = threadIdx.x;
     float2 ml[kMaxSplits];
 #pragma unroll
-    for (int j = 0; j < kMaxSplits; ++j)
-      ml[j] = j < p.nsplit ? __ldcg(p.part_ml + (base + j) * kMlaHeads + h) : make_float2(-INFINITY, 0.f);
+    for (int j = 0; j < kMaxSplits; ++j) ml[j] = j < ns ? mls[j * kMlaHeads + h] : make_float2(0.f, 0.f);
     float M = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kMaxSplits; ++j)
@@ -771,43 +796,69 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(MlaParams p) 
     const float inv = 1.f / L;
 #pragma unroll
     for (int j = 0; j < kMaxSplits; ++j)
-      if (j < p.nsplit) wgt[j][h] = w[j] * inv;
-    if (h == 0)
+      if (j < ns) wgt[j][h] = w[j] * inv;
+    if (h == 0) {   // a split is empty for all heads or for none
+      uint32_t m = 0;
 #pragma unroll
-      for (int j = 0; j < kMaxSplits; ++j)
-        if (j < p.nsplit) used[j] = ml[j].y > 0.f;   // a split is empty for all heads or for none
+      for (int j = 0; j < kMaxSplits; ++j) m |= static_cast<uint32_t>(ml[j].y > 0.f) << j;
+      used_mask = m;
+    }
     if (p.lse && blockIdx.x == 0)
       p.lse[static_cast<int64_t>(t) * kMlaHeads + h] = (M + log2f(L)) * 0.69314718055994531f;
   }
-  __syncthreads();
+  __syncthreads();   // the weights (or a timeout) are visible
+  const int grp = 4 * (warp % 3) + (lane & 3);   // heads 8 grp .. 8 grp + 7
+  const int dim = 8 * (warp / 3) + (lane >> 2);  // of the block's 32
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const uint32_t um = abortf ? 0u : used_mask;
+  bool ok = true;
 #pragma unroll
-  for (int j = 0; j < kMaxSplits; ++j) {
-    if (j >= p.nsplit || !used[j]) continue;
-    const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
-    const float4 wa = *reinterpret_cast<const float4*>(&wgt[j][8 * g]);       // this thread's 8 heads' weights
-    const float4 wb = *reinterpret_cast<const float4*>(&wgt[j][8 * g + 4]);
-    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+  for (int bx = 0; bx < kCombMaxBoxes; ++bx) {
+    if (bx >= nbox || !ok) break;
+    ok = mbar_wait(&bars[bx], 0, ab);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-      acc[2 * e] = fmaf(wv[2 * e], f.x, acc[2 * e]);
-      acc[2 * e + 1] = fmaf(wv[2 * e + 1], f.y, acc[2 * e + 1]);
+    for (int jj = 0; jj < kCombBoxSplits; ++jj) {
+      const int j = bx * kCombBoxSplits + jj;
+      // predicated loads (an unused split contributes zeros): no branch between them
+      const bool use = ok && ((um >> j) & 1u);
+      const uint8_t* src = csm + j * kCombSplitBytes + dim * (kMlaHeads * 2) + grp * 16;
+      const uint4 u = use ? *reinterpret_cast<const uint4*>(src) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+      const float4 wa = use ? *reinterpret_cast<const float4*>(&wgt[j][8 * grp]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 wb = use ? *reinterpret_cast<const float4*>(&wgt[j][8 * grp + 4]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+        acc[2 * e] = fmaf(wv[2 * e], f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(wv[2 * e + 1], f.y, acc[2 * e + 1]);
+      }
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) tile[8 * g + i][dl] = __float2bfloat16_rn(acc[i]);
+  for (int i = 0; i < 8; ++i) tile[8 * grp + i][dim] = __float2bfloat16_rn(acc[i]);
   __syncthreads();
-  // 96 rows of 32 dims (64 bytes): 4 x 16-byte stores per row
-  __nv_bfloat16* o = p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim + blockIdx.x * kCombDims;
-  const int h = threadIdx.x >> 2, q = threadIdx.x & 3;
-  *reinterpret_cast<uint4*>(o + h * kVDim + 8 * q) = *reinterpret_cast<const uint4*>(&tile[h][8 * q]);
+  if (!abortf) {   // uniform: read after the barrier
+    // 96 rows of 32 dims (64 bytes): 4 x 16-byte stores per row
+    __nv_bfloat16* o = p.out + static_cast<int64_t>(t) * kMlaHeads * kVDim + blockIdx.x * kCombDims;
+    const int h = threadIdx.x >> 2, q = threadIdx.x & 3;
+    *reinterpret_cast<uint4*>(o + h * kVDim + 8 * q) = *reinterpret_cast<const uint4*>(&tile[h][8 * q]);
+  }
+  if (threadIdx.x >= 32 && threadIdx.x < 32 + nbox) drain_wait(&bars[threadIdx.x - 32], 0);   // no copy outlives the CTA
+  if (threadIdx.x == 0) drain_wait(&bars[kCombMaxBoxes], 0);
 }
 
-cudaError_t launch_mla_combine(const MlaParams& p, cudaStream_t st) {
-  return launch_ex(mla_combine_kernel, dim3(kVDim / kCombDims, p.b.T), dim3(kCombThreads), 0, st, true, 0u, p);
+cudaError_t launch_mla_combine(const CUtensorMap& cmap, const MlaParams& p, cudaStream_t st) {
+  const int nbox = (p.nsplit + kCombBoxSplits - 1) / kCombBoxSplits;
+  const int smem = nbox * kCombBoxSplits * kCombSplitBytes + p.nsplit * kMlaHeads * 8 + 128;
+  cudaError_t e = set_func_attr_once(reinterpret_cast<const void*>(mla_combine_kernel),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kMaxSplits * (kCombSplitBytes + kMlaHeads * 8) + 128);
+  if (e != cudaSuccess) return e;
+  return launch_ex(mla_combine_kernel, dim3(kVDim / kCombDims, p.b.T), dim3(kCombThreads), smem, st, true, 0u, cmap,
+                   p);
 }
 
 template <int LATF>
@@ -819,12 +870,13 @@ static cudaError_t launch_mla_fmt(const CUtensorMap& qmap, const MlaParams& p, c
                    0u, qmap, p);
 }
 
-cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained) {
+cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const CUtensorMap& cmap, const MlaParams& p, cudaStream_t st,
+                              bool chained) {
   if (p.b.T == 0) return cudaSuccess;
   cudaError_t e =
       p.pool.lat_fmt == 1 ? launch_mla_fmt<1>(qmap, p, st, chained) : launch_mla_fmt<0>(qmap, p, st, chained);
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  return launch_mla_combine(p, st);
+  return launch_mla_combine(cmap, p, st);
 }
 
 }  // namespace dsa

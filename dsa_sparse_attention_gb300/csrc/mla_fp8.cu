@@ -453,12 +453,13 @@ bool sparse_mla_fp8_available() {
 }
 
 // One CTA per (token, 128 selected tokens), then (several splits) the split combine.
-cudaError_t launch_sparse_mla_fp8(const CUtensorMap& pmap, const MlaParams& p, cudaStream_t st, bool chained) {
+cudaError_t launch_sparse_mla_fp8(const CUtensorMap& pmap, const CUtensorMap& cmap, const MlaParams& p, cudaStream_t st,
+                                  bool chained) {
   if (p.b.T == 0) return cudaSuccess;
   const cudaError_t e = launch_ex(sparse_mla_fp8_kernel<0>, dim3(p.nsplit, p.b.T), dim3(mla8::THREADS),
                                   mla8::SMEM_BYTES, st, chained, 0u, pmap, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  return launch_mla_combine(p, st);
+  return launch_mla_combine(cmap, p, st);
 }
 
 }  // namespace dsa

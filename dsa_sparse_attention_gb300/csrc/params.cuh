@@ -188,13 +188,15 @@ cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, con
                            int grid, cudaStream_t st);
 int indexer_group_size(int idx_fmt, bool one_token_per_request);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained);
-cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const MlaParams& p, cudaStream_t st, bool chained);
+cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const CUtensorMap& cmap, const MlaParams& p, cudaStream_t st,
+                              bool chained);
 // FP8 latents, one 128-token tile per CTA (p.nsplit = tiles of the selection, p.tps
 // = 1), followed by the split combine: whether it can run here, and the launch.
 bool sparse_mla_fp8_available();
-cudaError_t launch_sparse_mla_fp8(const CUtensorMap& pmap, const MlaParams& p, cudaStream_t st, bool chained);
+cudaError_t launch_sparse_mla_fp8(const CUtensorMap& pmap, const CUtensorMap& cmap, const MlaParams& p, cudaStream_t st,
+                                  bool chained);
 // The log-sum-exp merge of p.nsplit normalised partials into p.out / p.lse.
-cudaError_t launch_mla_combine(const MlaParams& p, cudaStream_t st);
+cudaError_t launch_mla_combine(const CUtensorMap& cmap, const MlaParams& p, cudaStream_t st);
 // The query terms of a batch for the FP8 attention (a standalone call; a layer step's scorer writes them).
 cudaError_t launch_mla_qprep(const __nv_bfloat16* q, uint8_t* terms, int T, cudaStream_t st);
 

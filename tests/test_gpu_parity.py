@@ -111,7 +111,7 @@ def test_mixed_sign_key_scales_mtp_groups():
     _run_all(wl)
 
 
-@pytest.mark.parametrize("k", [1, 7, 100, 1000])
+@pytest.mark.parametrize("k", [1, 7, 100, 300, 700, 1000])
 def test_topk_sizes(k):
     wl = W.make_workload([4000, 90, 5], 1, seed=15, permute=True)
     _run_all(wl, topk=k)
@@ -301,6 +301,16 @@ def test_mxfp4_keys_fp8_latents():
 def test_fp8_keys_nvfp4_latents():
     wl = W.make_workload([5000, 700, 2049], 1, seed=42, lat_fmt=W.LAT_NVFP4, permute=True, pool_rows=200)
     _run_all(wl)
+
+
+def test_combine_split_count_not_a_multiple_of_four():
+    # 48 query tokens with NVFP4 latents: the attention runs 6 splits per token, so
+    # the combine's last 4-split copy of each token reaches past its splits (into the
+    # next token's, and past the end of the partials for the last token)
+    wl = W.make_workload([1500 + 211 * i for i in range(8)], 6, seed=46, lat_fmt=W.LAT_NVFP4, permute=True,
+                         pool_rows=400)
+    assert wl.num_tokens == 48
+    _run_all(wl, tokens=[0, 5, 17, 30, 46, 47])
 
 
 def test_mxfp4_nvfp4_mtp_groups():
