@@ -167,6 +167,54 @@ def test_layer_step_dirty_workspace_hint():
     check_topk(OracleCache(wl), ref_idx, list(range(wl.num_tokens)), dw.topk)
 
 
+def _copy_key(wl, b, src, dsts):
+    """Give positions `dsts` of request b the FP8 index key (codes and scale) of position `src`."""
+    rows = wl.pool.reshape(wl.num_rows, wl.row_stride)
+    bs = wl.block_size
+
+    def loc(pos):
+        return int(wl.block_table[b, pos // bs]), pos % bs
+
+    r, sl = loc(src)
+    page = rows[r, wl.idx_page_offset:]
+    codes = page[sl * 128: sl * 128 + 128].copy()
+    scale = page[bs * 128 + sl * 4: bs * 128 + sl * 4 + 4].copy()
+    for d in dsts:
+        r, sl = loc(int(d))
+        page = rows[r, wl.idx_page_offset:]
+        page[sl * 128: sl * 128 + 128] = codes
+        page[bs * 128 + sl * 4: bs * 128 + sl * 4 + 4] = scale
+
+
+@pytest.mark.parametrize("n_tied", [150, 400])
+def test_layer_step_threshold_ties(n_tied):
+    # Many positions of a row share the exact key whose score sits at the k-th
+    # place: the layer step's top-k (starting from the scorer's histogram) must cut
+    # them at the lowest positions, spread over several CTAs of the row, and equal
+    # the exact selection over the GPU's own scores.
+    from oracle import dsa_oracle as O
+    wl = W.make_workload([65536, 30000, 5000], 1, seed=61, permute=True)
+    oc = OracleCache(wl)
+    rng = np.random.default_rng(61)
+    for b in range(2):
+        t = int(np.nonzero(wl.q_req == b)[0][0])
+        n = int(wl.q_pos[t]) + 1
+        sc = oc.scores(t)
+        src = int(np.argsort(-sc, kind="stable")[wl.topk - 40])
+        _copy_key(wl, b, src, rng.choice(np.setdiff1d(np.arange(n), [src]), n_tied, replace=False))
+    dw = _dev(wl)
+    for _ in range(3):   # the first step may start from an unzeroed workspace; the next ones not
+        idx, out, lse = dw.layer_step()
+        torch.cuda.synchronize()
+        scores = _np(dw.indexer_scores())
+        g_idx = _np(idx)
+        for t in range(wl.num_tokens):
+            n = int(wl.q_pos[t]) + 1
+            ref = O.topk_select(scores[t, :n].astype(np.float64), dw.topk)
+            assert np.array_equal(g_idx[t, :ref.size], ref), f"token {t}"
+            assert np.all(g_idx[t, ref.size:] == -1)
+
+
 @pytest.mark.parametrize("lens", [[65536, 9000, 3000, 1, 2048, 2049, 40000], [70000, 12345, 5]])
 def test_topk_heavy_ties_exact(lens):
     # Scores with five distinct values (and both signs of zero): the threshold
