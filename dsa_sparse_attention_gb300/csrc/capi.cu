@@ -232,6 +232,21 @@ bool make_comb_map(CUtensorMap* m, void* part_o, int64_t T, int nsplit) {
          CUDA_SUCCESS;
 }
 
+// The indexer query projection W [4096 rows, d_q] bf16 for the front: a box is
+// 256 dims (fewer when d_q is smaller) of 32 rows, no swizzle; dims past d_q read
+// as zeros.
+bool make_front_w_map(CUtensorMap* m, const void* w, int d_q) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cuuint64_t(d_q), cuuint64_t(kIdxHeads) * kIdxDim};
+  cuuint64_t strides[1] = {cuuint64_t(d_q) * 2};
+  cuuint32_t box[2] = {cuuint32_t(d_q < 256 ? d_q : 256), 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 PoolView pool_view(const dsa_kv_layout* l) {
   PoolView v;
   v.pool = static_cast<const uint8_t*>(l->pool);
@@ -677,7 +692,9 @@ dsa_status dsa_indexer_front(const dsa_kv_layout* layout, const dsa_batch* batch
   p.d_q = d_q;
   p.eps = eps;
   p.status = static_cast<uint32_t*>(workspace);
-  return cuda_status(launch_indexer_front(p, stream));
+  CUtensorMap wmap;
+  if (!make_front_w_map(&wmap, w_qi, d_q)) return encode_fail();
+  return cuda_status(launch_indexer_front(wmap, p, stream));
 }
 
 dsa_status dsa_write_latent(const dsa_kv_layout* layout, const dsa_batch* batch, const void* latent,

@@ -12,11 +12,16 @@
 //
 // Indexer front.  At decode the projection is a weight stream (4096 x d_q bf16,
 // 12.6 MB at d_q = 1536) against a few queries, so it runs on the CUDA cores as a
-// GEMV, not on the tensor cores.  Grid (4 quarters x 32 heads, token chunks of 8)
-// in clusters of the 4 quarters of a head: each CTA normalises its chunk's
-// queries into shared memory (fp32), streams its 32 rows of W once (16-byte
-// loads, all of a row's loads in flight) and keeps the 32 x T dot products; the
-// head's maximum comes from the four CTAs through distributed shared memory,
+// blocked GEMV, not on the tensor cores (a tile of 8 tokens would leave them
+// idle and the fp32 query would need two bf16 terms).  Grid (4 quarters x 32
+// heads, token chunks of 8) in clusters of the 4 quarters of a head.  Each CTA
+// brings its 32 rows of W into a 4-slot ring by TMA, 256 dims a copy, while 8
+// warps normalise the chunk's queries into shared memory (fp32).  Thread (row
+// group g, lane kl of 128) accumulates 8 rows x 8 tokens over dims 2kl, 2kl + 1
+// of every 256-dim chunk with packed fp32 FMAs; the 128 partial sums of each
+// output are reduced by a butterfly inside the warps (each lane ends with 2 of
+// its warp's 64 outputs) and across the 4 warps of the group in shared memory.
+// The head's maximum comes from the four CTAs through distributed shared memory,
 // then each CTA quantizes its rows.  The first CTA of the first head also writes
 // the chunk's new index keys into their cache slots.
 #include <cuda.h>
@@ -34,7 +39,28 @@ constexpr int THREADS = 512;
 constexpr int CHUNK = 8;                 // query tokens per CTA
 constexpr int ROWS = 32;                 // output rows (dims of one head) per CTA
 constexpr int MAX_DQ = 4096;
+constexpr int KBOX = 256;                // dims of W per copy
+constexpr int RING = 4;                  // copies in flight
+constexpr int SLOT_BYTES = ROWS * KBOX * 2;
+// dynamic shared memory: ring | y [CHUNK][y_pitch] fp32 | red [16 warps][64] | qv [ROWS][CHUNK] |
+// amax [CHUNK] x 2 | bars [RING] | abort flag
+__host__ __device__ constexpr int y_pitch(int dq) { return (dq + KBOX - 1) / KBOX * KBOX; }
+__host__ __device__ constexpr int smem_bytes(int dq) {
+  return RING * SLOT_BYTES + CHUNK * y_pitch(dq) * 4 + 16 * 64 * 4 + ROWS * CHUNK * 4 + 2 * CHUNK * 4 + RING * 8 + 16 +
+         128;
+}
+static_assert(smem_bytes(MAX_DQ) <= 232448, "front shared memory");
 }  // namespace front
+
+// d = a * b + c on two fp32 lanes at once (one packed FMA, round to nearest)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
 
 // Physical row and slot of token t's position (checked); false when out of range.
 __device__ __forceinline__ bool new_token_slot(const BatchView& b, const PoolView& pool, int t, uint32_t* status,
@@ -61,106 +87,161 @@ __device__ __forceinline__ uint32_t f4_to_e4m3x4(float a, float b, float c, floa
   return lo | (hi << 16);
 }
 
-__global__ void __launch_bounds__(front::THREADS) indexer_front_kernel(FrontParams p) {
+__global__ void __launch_bounds__(front::THREADS, 1)
+    indexer_front_kernel(const __grid_constant__ CUtensorMap wmap, FrontParams p) {
   using namespace front;
-  extern __shared__ __align__(16) float fsm[];
-  float* y = fsm;                                     // [CHUNK][d_q] normalised queries
-  float* qv = fsm + CHUNK * p.d_q;                    // [ROWS][CHUNK] projections of this CTA
-  float* amax_sh = qv + ROWS * CHUNK;                 // [CHUNK] this CTA's per-token max |q|
-  float* amax_all = amax_sh + CHUNK;                  // [CHUNK] the head's
+  extern __shared__ uint8_t fsm_raw[];
+  uint8_t* fsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fsm_raw) + 127) & ~uintptr_t(127));
+  const int dq = p.d_q;
+  const int ypitch = y_pitch(dq);
+  const int nk = ypitch / KBOX;                                       // 256-dim chunks of W
+  const int kbox = dq < KBOX ? dq : KBOX;                             // dims per copy
+  uint8_t* ring = fsm;                                                // [RING][ROWS][kbox] bf16
+  float* y = reinterpret_cast<float*>(fsm + RING * SLOT_BYTES);       // [CHUNK][ypitch] normalised queries
+  float* red = y + CHUNK * ypitch;                                    // [16 warps][64] partial sums
+  float* qv = red + 16 * 64;                                          // [ROWS][CHUNK] projections of this CTA
+  float* amax_sh = qv + ROWS * CHUNK;                                 // [CHUNK] this CTA's per-token max |q|
+  float* amax_all = amax_sh + CHUNK;                                  // [CHUNK] the head's
+  uint64_t* bars = reinterpret_cast<uint64_t*>(amax_all + CHUNK);     // [RING]
+  int* abortf = reinterpret_cast<int*>(bars + RING);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = blockIdx.x & 3, h = blockIdx.x >> 2;
+  const int row0 = h * 128 + quarter * ROWS;
   const int t0 = blockIdx.y * CHUNK;
   const int nt = min(CHUNK, p.b.T - t0);
-  const int dq = p.d_q;
-  grid_dep_wait();
-  // 1. RMSNorm of each token of the chunk (one warp per token)
-  if (warp < nt) {
-    const __nv_bfloat16* x = p.c_q + static_cast<int64_t>(t0 + warp) * dq;
-    float ss = 0.f;
-    for (int i = lane * 8; i < dq; i += 256) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + i));
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = __uint_as_float(w4[j] << 16), c = __uint_as_float(w4[j] & 0xFFFF0000u);
-        ss = fmaf(a, a, fmaf(c, c, ss));
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = 1.0f / sqrtf(ss / static_cast<float>(dq) + p.eps);
-    for (int i = lane * 8; i < dq; i += 256) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + i));
-      const uint4 g = __ldg(reinterpret_cast<const uint4*>(p.gamma + i));
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w}, g4[4] = {g.x, g.y, g.z, g.w};
-      float o8[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        o8[2 * j] = __uint_as_float(w4[j] << 16) * r * __uint_as_float(g4[j] << 16);
-        o8[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u) * r * __uint_as_float(g4[j] & 0xFFFF0000u);
-      }
-      float4* dst = reinterpret_cast<float4*>(y + warp * dq + i);
-      dst[0] = make_float4(o8[0], o8[1], o8[2], o8[3]);
-      dst[1] = make_float4(o8[4], o8[5], o8[6], o8[7]);
-    }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RING; ++i) mbar_init(&bars[i], 1);
+    *abortf = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&wmap);
   }
   __syncthreads();
-  // 2. this CTA's 32 rows (dims 32 quarter .. of head h), two per warp; lane l takes
-  // the 16-byte pieces l, l + 32, ... of a row (d_q / 8 pieces)
-  for (int rr = warp; rr < ROWS; rr += THREADS / 32) {
-    const int row = h * 128 + quarter * ROWS + rr;
-    const uint4* wrow = reinterpret_cast<const uint4*>(p.w_qi + static_cast<int64_t>(row) * dq);
-    const int npc = dq / 8;
-    float acc[CHUNK];
-#pragma unroll
-    for (int t = 0; t < CHUNK; ++t) acc[t] = 0.f;
-    for (int base = 0; base < npc; base += 32 * 8) {
-      uint4 wv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {   // up to eight pieces of the row in flight per lane
-        const int pc = base + lane + 32 * u;
-        wv[u] = pc < npc ? __ldg(wrow + pc) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int pc = base + lane + 32 * u;
-        if (pc >= npc) break;
-        const uint32_t w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
-        float wf[8];
+  grid_dep_wait();
+  // 1. the first W copies, then RMSNorm of each token of the chunk (one warp per
+  // token; y past d_q and the rows of absent tokens are zero)
+  if (threadIdx.x == 0)
+    for (int c = 0; c < RING && c < nk; ++c) {
+      mbar_arrive_expect_tx(&bars[c], ROWS * kbox * 2);
+      tma_load_2d(ring + c * SLOT_BYTES, &wmap, &bars[c], c * KBOX, row0);
+    }
+  if (warp < CHUNK) {
+    float* yt = y + warp * ypitch;
+    if (warp < nt) {
+      const __nv_bfloat16* x = p.c_q + static_cast<int64_t>(t0 + warp) * dq;
+      float ss = 0.f;
+      for (int i = lane * 8; i < dq; i += 256) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + i));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float o8[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          wf[2 * j] = __uint_as_float(w4[j] << 16);
-          wf[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+          o8[2 * j] = __uint_as_float(w4[j] << 16);
+          o8[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+          ss = fmaf(o8[2 * j], o8[2 * j], fmaf(o8[2 * j + 1], o8[2 * j + 1], ss));
         }
-#pragma unroll
-        for (int t = 0; t < CHUNK; ++t) {
-          if (t >= nt) break;
-          const float4 a = *reinterpret_cast<const float4*>(y + t * dq + pc * 8);
-          const float4 c = *reinterpret_cast<const float4*>(y + t * dq + pc * 8 + 4);
-          float s = acc[t];
-          s = fmaf(wf[0], a.x, s);
-          s = fmaf(wf[1], a.y, s);
-          s = fmaf(wf[2], a.z, s);
-          s = fmaf(wf[3], a.w, s);
-          s = fmaf(wf[4], c.x, s);
-          s = fmaf(wf[5], c.y, s);
-          s = fmaf(wf[6], c.z, s);
-          s = fmaf(wf[7], c.w, s);
-          acc[t] = s;
-        }
+        reinterpret_cast<float4*>(yt + i)[0] = make_float4(o8[0], o8[1], o8[2], o8[3]);
+        reinterpret_cast<float4*>(yt + i)[1] = make_float4(o8[4], o8[5], o8[6], o8[7]);
       }
-    }
 #pragma unroll
-    for (int t = 0; t < CHUNK; ++t) {
-      float s = acc[t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) qv[rr * CHUNK + t] = s;
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float r = 1.0f / sqrtf(ss / static_cast<float>(dq) + p.eps);
+      __syncwarp();
+      for (int i = lane * 8; i < dq; i += 256) {
+        const uint4 gm = __ldg(reinterpret_cast<const uint4*>(p.gamma + i));
+        const uint32_t g4[4] = {gm.x, gm.y, gm.z, gm.w};
+        float4* dst = reinterpret_cast<float4*>(yt + i);
+        float4 a = dst[0], c = dst[1];
+        a.x = a.x * r * __uint_as_float(g4[0] << 16);
+        a.y = a.y * r * __uint_as_float(g4[0] & 0xFFFF0000u);
+        a.z = a.z * r * __uint_as_float(g4[1] << 16);
+        a.w = a.w * r * __uint_as_float(g4[1] & 0xFFFF0000u);
+        c.x = c.x * r * __uint_as_float(g4[2] << 16);
+        c.y = c.y * r * __uint_as_float(g4[2] & 0xFFFF0000u);
+        c.z = c.z * r * __uint_as_float(g4[3] << 16);
+        c.w = c.w * r * __uint_as_float(g4[3] & 0xFFFF0000u);
+        dst[0] = a;
+        dst[1] = c;
+      }
+      for (int i = dq + lane; i < ypitch; i += 32) yt[i] = 0.f;
+    } else {
+      for (int i = lane; i < ypitch; i += 32) yt[i] = 0.f;
     }
   }
   __syncthreads();
-  // 3. the head's max |q| per token: this CTA's 32 rows, then the cluster's four quarters
+  // 2. thread (group g of 8 rows, kl of 128) over dims 2 kl, 2 kl + 1 of each chunk
+  const int g = warp >> 2, kl = ((warp & 3) << 5) | lane;
+  float2 acc[8][CHUNK / 2];   // [row][token pair]
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int t = 0; t < CHUNK / 2; ++t) acc[i][t] = make_float2(0.f, 0.f);
+  const Abort ab{abortf, p.status};
+  bool ok = true;
+#pragma unroll 1
+  for (int c = 0; c < nk; ++c) {
+    const int slot = c % RING;
+    if (ok) ok = mbar_wait(&bars[slot], (c / RING) & 1, ab);
+    if (ok && 2 * kl < kbox) {
+      const uint8_t* wsl = ring + slot * SLOT_BYTES + (8 * g) * (kbox * 2) + 4 * kl;
+      float2 w2[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(wsl + i * (kbox * 2));
+        w2[i] = make_float2(__uint_as_float(wb << 16), __uint_as_float(wb & 0xFFFF0000u));
+      }
+      const float* yc = y + c * KBOX + 2 * kl;
+#pragma unroll
+      for (int tp = 0; tp < CHUNK / 2; ++tp) {
+        const float2 ya = *reinterpret_cast<const float2*>(yc + (2 * tp) * ypitch);       // token 2tp, dims d, d+1
+        const float2 yb = *reinterpret_cast<const float2*>(yc + (2 * tp + 1) * ypitch);   // token 2tp+1
+        const float2 y0 = make_float2(ya.x, yb.x), y1 = make_float2(ya.y, yb.y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[i][tp] = ffma2(make_float2(w2[i].x, w2[i].x), y0, acc[i][tp]);
+          acc[i][tp] = ffma2(make_float2(w2[i].y, w2[i].y), y1, acc[i][tp]);
+        }
+      }
+    }
+    __syncthreads();   // every warp is done with this slot
+    if (threadIdx.x == 0 && c + RING < nk && !*reinterpret_cast<volatile int*>(abortf)) {
+      mbar_arrive_expect_tx(&bars[slot], ROWS * kbox * 2);
+      tma_load_2d(ring + slot * SLOT_BYTES, &wmap, &bars[slot], (c + RING) * KBOX, row0);
+    }
+  }
+  // 3. reduce each output's 128 partial sums: a butterfly over the lanes leaves lane l
+  // with outputs 2l, 2l + 1 (output v = row * 8 + token) of the warp, then the 4 warps
+  // of the group add in shared memory
+  float v[64];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int tp = 0; tp < CHUNK / 2; ++tp) {
+      v[i * 8 + 2 * tp] = acc[i][tp].x;
+      v[i * 8 + 2 * tp + 1] = acc[i][tp].y;
+    }
+#pragma unroll
+  for (int o = 16, n = 64; o > 0; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float send = upper ? v[j] : v[j + n / 2];
+      const float keep = upper ? v[j + n / 2] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  red[warp * 64 + 2 * lane] = v[0];
+  red[warp * 64 + 2 * lane + 1] = v[1];
+  __syncthreads();
+  if (threadIdx.x < ROWS * CHUNK) {
+    const int r = threadIdx.x >> 3, t = threadIdx.x & 7;   // row of the CTA, token
+    const int gg = r >> 3, vi = (r & 7) * 8 + t;
+    float sum = 0.f;
+#pragma unroll
+    for (int w4 = 0; w4 < 4; ++w4) sum += red[(gg * 4 + w4) * 64 + vi];
+    qv[r * CHUNK + t] = sum;
+  }
+  __syncthreads();
+  // 4. the head's max |q| per token: this CTA's 32 rows, then the cluster's four quarters
   if (threadIdx.x < CHUNK) {
     float m = 0.f;
     for (int rr = 0; rr < ROWS; ++rr) m = fmaxf(m, fabsf(qv[rr * CHUNK + threadIdx.x]));
@@ -176,7 +257,7 @@ __global__ void __launch_bounds__(front::THREADS) indexer_front_kernel(FrontPara
   }
   cluster_arrive_relaxed();   // done reading the other quarters
   __syncthreads();
-  // 4. codes e4m3(q / s), s = max / 448 (1 for an all-zero head); folded weights by quarter 0
+  // 5. codes e4m3(q / s), s = max / 448 (1 for an all-zero head); folded weights by quarter 0
   if (threadIdx.x < CHUNK * ROWS / 4) {
     const int t = threadIdx.x / (ROWS / 4), r4 = (threadIdx.x % (ROWS / 4)) * 4;   // 4 rows per thread
     if (t < nt) {
@@ -189,7 +270,7 @@ __global__ void __launch_bounds__(front::THREADS) indexer_front_kernel(FrontPara
       if (quarter == 0 && r4 == 0) p.w_out[static_cast<int64_t>(t0 + t) * kIdxHeads + h] = p.head_w[(t0 + t) * kIdxHeads + h] * s;
     }
   }
-  // 5. the chunk's new index keys (first quarter of head 0): one warp per token,
+  // 6. the chunk's new index keys (first quarter of head 0): one warp per token,
   // four values per lane, s_k = max |k| / 448 in fp32
   if (p.k_new && blockIdx.x == 0 && warp < nt) {
     const int t = t0 + warp;
@@ -209,6 +290,9 @@ __global__ void __launch_bounds__(front::THREADS) indexer_front_kernel(FrontPara
     }
   }
   cluster_wait();   // no CTA leaves while another may still read its maxima
+  // no copy into shared memory outlives the CTA (the last copy of each slot)
+  if (threadIdx.x < RING && static_cast<int>(threadIdx.x) < nk)
+    drain_wait(&bars[threadIdx.x], ((nk - 1 - static_cast<int>(threadIdx.x)) / RING) & 1);
 }
 
 // The new tokens' latents into their cache slots: one CTA of 64 threads per
@@ -268,13 +352,13 @@ __global__ void __launch_bounds__(64) write_latent_kernel(LatentWriteParams p) {
   if (i < 7) *reinterpret_cast<uint32_t*>(rec + 324 + 4 * i) = 0u;
 }
 
-cudaError_t launch_indexer_front(const FrontParams& p, cudaStream_t st) {
-  const size_t smem = (static_cast<size_t>(front::CHUNK) * p.d_q + front::ROWS * front::CHUNK + 2 * front::CHUNK) * 4;
+cudaError_t launch_indexer_front(const CUtensorMap& wmap, const FrontParams& p, cudaStream_t st) {
   cudaError_t e = set_func_attr_once(reinterpret_cast<const void*>(indexer_front_kernel),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, front::smem_bytes(front::MAX_DQ));
   if (e != cudaSuccess) return e;
   const dim3 grid(kIdxHeads * 4, static_cast<unsigned>(cdiv(p.b.T, front::CHUNK)));
-  return launch_ex(indexer_front_kernel, grid, dim3(front::THREADS), smem, st, false, 4u, p);
+  return launch_ex(indexer_front_kernel, grid, dim3(front::THREADS), front::smem_bytes(p.d_q), st, false, 4u, wmap,
+                   p);
 }
 
 cudaError_t launch_write_latent(const LatentWriteParams& p, cudaStream_t st) {

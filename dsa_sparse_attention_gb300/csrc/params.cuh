@@ -174,7 +174,7 @@ struct LatentWriteParams {
   uint32_t* status;
 };
 
-cudaError_t launch_indexer_front(const FrontParams& p, cudaStream_t st);
+cudaError_t launch_indexer_front(const CUtensorMap& wmap, const FrontParams& p, cudaStream_t st);
 cudaError_t launch_write_latent(const LatentWriteParams& p, cudaStream_t st);
 
 // Host helpers (capi.cu): the CUDA context current on this thread, and

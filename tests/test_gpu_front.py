@@ -2,8 +2,12 @@
 through the C ABI, against the float64 oracle (oracle/front.py):
 
 * the folded head weights within 1e-5 relative; the query's e4m3 codes equal
-  except where the oracle's scaled value lies within 1e-4 (relative) of the
-  midpoint between two neighbouring codes (the kernel accumulates in fp32);
+  except where the oracle's scaled value x = q / s lies within tau of the
+  midpoint between two neighbouring codes.  The kernel sums the d_q products of
+  each output in fp32, so its q differs from the exact one by about
+  sqrt(d_q) * 2^-24 * sqrt(sum of the squared products) (rounding errors of
+  random sign); tau is 8 times that, in units of x, plus 2^-20 |x| for the fp32
+  division by s;
 * the pool after the call equals the oracle's pool byte for byte (the new index
   keys, and for dsa_write_latent the new FP8 / NVFP4 latent records: those are
   computed in fp32 on both sides, so the bytes are exact);
@@ -38,16 +42,25 @@ def _dev_u16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
 
 
-def _codes_match(got, want, x):
-    """e4m3 codes equal, or neighbours around a midpoint within 1e-4 of x."""
+def _codes_match(got, want, x, tau):
+    """e4m3 codes equal, or neighbours around a midpoint within tau of x."""
     if np.array_equal(got, want):
         return 0
     diff = np.nonzero(got != want)
     a, b, v = decode_e4m3(got[diff]), decode_e4m3(want[diff]), x[diff]
     mid = (a + b) / 2
-    ok = np.abs(v - mid) <= 1e-4 * np.maximum(np.abs(v), 1e-30)
+    ok = np.abs(v - mid) <= tau[diff]
     assert np.all(ok), f"{np.count_nonzero(~ok)} codes differ away from a rounding midpoint"
     return diff[0].size
+
+
+def _tau(c_q, gamma, w_qi, eps, s, x):
+    """Tolerance of x = q / s for the fp32 sums of the kernel (see the module docstring)."""
+    from oracle.formats import decode_bf16
+    y = F.rmsnorm(decode_bf16(c_q), decode_bf16(gamma), eps)
+    wd = decode_bf16(w_qi).reshape(32 * 128, -1)
+    rss = np.sqrt(((wd * y) ** 2).sum(axis=1)).reshape(32, 128)
+    return 8 * np.sqrt(wd.shape[1]) * 2.0 ** -24 * rss / s[:, None] + 2.0 ** -20 * np.abs(x)
 
 
 def _front_case(lens, d_q, seed):
@@ -83,7 +96,8 @@ def test_indexer_front_and_new_keys(lens, d_q):
     for t in range(T):
         codes, wf, s, q = F.indexer_front(c_q[t], gamma, w_qi, head_w[t], eps)
         np.testing.assert_allclose(g_w[t], wf, rtol=1e-5, atol=1e-30)
-        flips += _codes_match(g_codes[t], codes, q / s[:, None])
+        x = q / s[:, None]
+        flips += _codes_match(g_codes[t], codes, x, _tau(c_q[t], gamma, w_qi, eps, s, x))
         kc, ks = F.index_key_fp8(k_new[t])
         p = int(wl.q_pos[t])
         F.write_index_key(pool_ref, wl.row_stride, wl.idx_page_offset, wl.block_size,
