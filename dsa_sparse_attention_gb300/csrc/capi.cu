@@ -232,18 +232,18 @@ bool make_comb_map(CUtensorMap* m, void* part_o, int64_t T, int nsplit) {
          CUDA_SUCCESS;
 }
 
-// The indexer query projection W [4096 rows, d_q] bf16 for the front: a box is
-// 256 dims (fewer when d_q is smaller) of 32 rows, no swizzle; dims past d_q read
-// as zeros.
+// The indexer query projection W [4096 rows, d_q] bf16 for the front: a box is 64
+// dims (128 bytes) of one head's 128 rows, 128-byte swizzle (the MMA's A operand,
+// K-major); dims past d_q read as zeros.
 bool make_front_w_map(CUtensorMap* m, const void* w, int d_q) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cuuint64_t(d_q), cuuint64_t(kIdxHeads) * kIdxDim};
   cuuint64_t strides[1] = {cuuint64_t(d_q) * 2};
-  cuuint32_t box[2] = {cuuint32_t(d_q < 256 ? d_q : 256), 32};
+  cuuint32_t box[2] = {64, 128};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -670,7 +670,7 @@ dsa_status dsa_indexer_front(const dsa_kv_layout* layout, const dsa_batch* batch
   if (s != DSA_OK) return s;
   if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
   if (k_new && layout->idx_fmt != DSA_IDX_FP8) return DSA_ERR_UNSUPPORTED;
-  if (d_q < 8 || d_q > 4096 || (d_q & 7) || !std::isfinite(eps) || eps < 0.f) return DSA_ERR_INVALID_ARG;
+  if (d_q < 64 || d_q > 4096 || (d_q & 7) || !std::isfinite(eps) || eps < 0.f) return DSA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) || workspace_bytes < kStatusBytes)
     return DSA_ERR_WORKSPACE;
   const int T = batch->num_tokens;

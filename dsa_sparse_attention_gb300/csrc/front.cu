@@ -1,29 +1,28 @@
 // front.cu — the fused indexer front and the new tokens' cache writes.
 //
-// vLLM K3.1 Pro day-0 post, "Low-latency decode: a fused DSA decode path": "a
-// fused indexer front: the query norm, the indexer's query projection, its FP8
-// or MXFP4 quantization with the head weights folded in, and the new token's
-// index key, in one kernel"; the MLA query kernel "writing the new token's
-// latent into the KV cache".  Readings (the post prints no shapes): RMSNorm over
-// the compressed query of width d_q, q = W . norm(c_q) with W [32 * 128, d_q],
-// FP8 per (token, head) with s = max|q_h| / 448 folded into the head weight,
-// the new key FP8 with s_k = max|k| / 448, latents FP8 (plain e4m3) or NVFP4
-// (e4m3 scale max|x| / 6 per 16 values, e2m1 values).
+// vLLM K3.1 Pro day-0 post, "Low-latency decode: a fused DSA decode path": one
+// kernel applies the query norm, projects the indexer query, quantizes it (FP8 or
+// MXFP4) with the head weights absorbing the scales, and writes the new token's
+// index key; the new token's latent enters the cache from the MLA query side.
+// The post gives no shapes.  Readings: RMSNorm over the compressed query of
+// width d_q, q = W . norm(c_q) with W [32 * 128, d_q], FP8 per (token, head) with
+// s = max|q_h| / 448 folded into the head weight, the new key FP8 with
+// s_k = max|k| / 448, latents FP8 (plain e4m3) or NVFP4 (e4m3 scale max|x| / 6
+// per 16 values, e2m1 values).
 //
 // Indexer front.  At decode the projection is a weight stream (4096 x d_q bf16,
-// 12.6 MB at d_q = 1536) against a few queries, so it runs on the CUDA cores as a
-// blocked GEMV, not on the tensor cores (a tile of 8 tokens would leave them
-// idle and the fp32 query would need two bf16 terms).  Grid (4 quarters x 32
-// heads, token chunks of 8) in clusters of the 4 quarters of a head.  Each CTA
-// brings its 32 rows of W into a 4-slot ring by TMA, 256 dims a copy, while 8
-// warps normalise the chunk's queries into shared memory (fp32).  Thread (row
-// group g, lane kl of 128) accumulates 8 rows x 8 tokens over dims 2kl, 2kl + 1
-// of every 256-dim chunk with packed fp32 FMAs; the 128 partial sums of each
-// output are reduced by a butterfly inside the warps (each lane ends with 2 of
-// its warp's 64 outputs) and across the 4 warps of the group in shared memory.
-// The head's maximum comes from the four CTAs through distributed shared memory,
-// then each CTA quantizes its rows.  The first CTA of the first head also writes
-// the chunk's new index keys into their cache slots.
+// 12.6 MB at d_q = 1536) against a few queries.  It runs on the tensor cores:
+// grid (32 heads x 4 quarters of d_q, token chunks of 8) in clusters of the 4
+// quarters of a head.  Each CTA streams its head's 128 rows of W over its quarter
+// of d_q into a 6-slot ring by TMA (64 dims, 128-byte swizzle, the K-major A
+// operand), while 8 warps normalise the chunk's queries and write them as the B
+// operand: per token two bf16 rows, hi = bf16(y) and lo = bf16(y - hi), so that
+// W . y is carried to about 2^-17 of each product.  One thread issues
+// tcgen05.mma kind::f16 (M = 128 rows, N = 16, fp32 accumulation in TMEM); the
+// epilogue adds the hi and lo columns, and after one cluster barrier the first
+// CTA adds the four quarters, takes each token's maximum over the head and writes
+// the codes and folded weights; the second CTA of the first head meanwhile writes
+// the chunk's new index keys.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp4.h>
@@ -35,32 +34,28 @@
 namespace dsa {
 
 namespace front {
-constexpr int THREADS = 512;
+constexpr int THREADS = 320;             // warps 0..7: queries, 0..3 also the epilogue; 8: W copies; 9: MMA
+constexpr int PROD_WARP = 8;
+constexpr int MMA_WARP = 9;
 constexpr int CHUNK = 8;                 // query tokens per CTA
-constexpr int ROWS = 32;                 // output rows (dims of one head) per CTA
+constexpr int ROWS = 32;                 // rows (dims of one head) a CTA finalises
 constexpr int MAX_DQ = 4096;
-constexpr int KBOX = 256;                // dims of W per copy
-constexpr int RING = 4;                  // copies in flight
-constexpr int SLOT_BYTES = ROWS * KBOX * 2;
-// dynamic shared memory: ring | y [CHUNK][y_pitch] fp32 | red [16 warps][64] | qv [ROWS][CHUNK] |
-// amax [CHUNK] x 2 | bars [RING] | abort flag
-__host__ __device__ constexpr int y_pitch(int dq) { return (dq + KBOX - 1) / KBOX * KBOX; }
-__host__ __device__ constexpr int smem_bytes(int dq) {
-  return RING * SLOT_BYTES + CHUNK * y_pitch(dq) * 4 + 16 * 64 * 4 + ROWS * CHUNK * 4 + 2 * CHUNK * 4 + RING * 8 + 16 +
-         128;
-}
-static_assert(smem_bytes(MAX_DQ) <= 232448, "front shared memory");
+constexpr int KC = 64;                   // dims per W copy and B chunk (one 128-byte row of bf16)
+constexpr int RING = 6;                  // W copies in flight
+constexpr int MAX_CPQ = (MAX_DQ / KC + 3) / 4;   // chunks of one quarter of d_q
+constexpr int A_BYTES = 128 * KC * 2;    // 128 rows of W x 64 dims
+constexpr int B_CHUNK = 16 * KC * 2;     // 16 rows (8 tokens, hi | lo) x 64 dims
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + RING * A_BYTES;
+constexpr int OFF_RED = OFF_B + MAX_CPQ * B_CHUNK;
+constexpr int OFF_QV = OFF_RED + 4 * ROWS * CHUNK * 4;
+constexpr int OFF_AMAX = OFF_QV + ROWS * CHUNK * 4;
+constexpr int OFF_BARS = OFF_AMAX + 2 * CHUNK * 4;
+constexpr int OFF_MISC = OFF_BARS + (2 * RING + 1) * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+static_assert(OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_CHUNK % 1024 == 0, "swizzled operands");
+static_assert(OFF_BARS % 8 == 0, "barriers");
 }  // namespace front
-
-// d = a * b + c on two fp32 lanes at once (one packed FMA, round to nearest)
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
-        "l"(*reinterpret_cast<const uint64_t*>(&c)));
-  return *reinterpret_cast<const float2*>(&d);
-}
 
 // Physical row and slot of token t's position (checked); false when out of range.
 __device__ __forceinline__ bool new_token_slot(const BatchView& b, const PoolView& pool, int t, uint32_t* status,
@@ -91,188 +86,206 @@ __global__ void __launch_bounds__(front::THREADS, 1)
     indexer_front_kernel(const __grid_constant__ CUtensorMap wmap, FrontParams p) {
   using namespace front;
   extern __shared__ uint8_t fsm_raw[];
-  uint8_t* fsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fsm_raw) + 127) & ~uintptr_t(127));
-  const int dq = p.d_q;
-  const int ypitch = y_pitch(dq);
-  const int nk = ypitch / KBOX;                                       // 256-dim chunks of W
-  const int kbox = dq < KBOX ? dq : KBOX;                             // dims per copy
-  uint8_t* ring = fsm;                                                // [RING][ROWS][kbox] bf16
-  float* y = reinterpret_cast<float*>(fsm + RING * SLOT_BYTES);       // [CHUNK][ypitch] normalised queries
-  float* red = y + CHUNK * ypitch;                                    // [16 warps][64] partial sums
-  float* qv = red + 16 * 64;                                          // [ROWS][CHUNK] projections of this CTA
-  float* amax_sh = qv + ROWS * CHUNK;                                 // [CHUNK] this CTA's per-token max |q|
+  uint8_t* fsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fsm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = fsm + OFF_A;                                        // [RING][128 rows x 128 B] (swizzled)
+  uint8_t* bq = fsm + OFF_B;                                          // [MAX_CPQ][16 rows x 128 B] (swizzled)
+  float* red = reinterpret_cast<float*>(fsm + OFF_RED);               // [4 quarters][32 rows][8] partial sums
+  float* qv = reinterpret_cast<float*>(fsm + OFF_QV);                 // [ROWS][CHUNK] this CTA's rows
+  float* amax_sh = reinterpret_cast<float*>(fsm + OFF_AMAX);          // [CHUNK] this CTA's per-token max |q|
   float* amax_all = amax_sh + CHUNK;                                  // [CHUNK] the head's
-  uint64_t* bars = reinterpret_cast<uint64_t*>(amax_all + CHUNK);     // [RING]
-  int* abortf = reinterpret_cast<int*>(bars + RING);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(fsm + OFF_BARS);
+  uint64_t* full = bars;                                              // [RING] W chunk landed
+  uint64_t* empty = bars + RING;                                      // [RING] its MMAs are done
+  uint64_t* done = bars + 2 * RING;                                   // every MMA is done (one phase)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(fsm + OFF_MISC);
+  int* abortf = reinterpret_cast<int*>(fsm + OFF_MISC + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quarter = blockIdx.x & 3, h = blockIdx.x >> 2;
-  const int row0 = h * 128 + quarter * ROWS;
+  const int quarter = static_cast<int>(cluster_rank()), h = blockIdx.x >> 2;
   const int t0 = blockIdx.y * CHUNK;
   const int nt = min(CHUNK, p.b.T - t0);
+  const int dq = p.d_q;
+  // this CTA's 64-dim chunks of d_q: [c_first, c_first + ncv)
+  const int nch = (dq + KC - 1) / KC, cpq = (nch + 3) / 4;
+  const int c_first = quarter * cpq;
+  const int ncv = max(0, min(cpq, nch - c_first));
+  int issued = 0;   // W copies issued (by thread 0 first, then by the producer warp)
   if (threadIdx.x == 0) {
-    for (int i = 0; i < RING; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 2 * RING + 1; ++i) mbar_init(&bars[i], 1);
     *abortf = 0;
     fence_mbar_init();
-    prefetch_tensormap(&wmap);
-  }
-  __syncthreads();
-  grid_dep_wait();
-  // 1. the first W copies, then RMSNorm of each token of the chunk (one warp per
-  // token; y past d_q and the rows of absent tokens are zero)
-  if (threadIdx.x == 0)
-    for (int c = 0; c < RING && c < nk; ++c) {
-      mbar_arrive_expect_tx(&bars[c], ROWS * kbox * 2);
-      tma_load_2d(ring + c * SLOT_BYTES, &wmap, &bars[c], c * KBOX, row0);
+    // The weights are an input of the call that no kernel before writes: their first
+    // RING copies start at once (the rest as the MMAs free their slots, below).
+    for (; issued < ncv && issued < RING; ++issued) {
+      mbar_arrive_expect_tx(&full[issued], A_BYTES);
+      tma_load_2d(ring + issued * A_BYTES, &wmap, &full[issued], (c_first + issued) * KC, h * 128);
     }
+  }
+  if (warp == MMA_WARP) tmem_alloc(tslot, 32);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (warp == PROD_WARP && lane == 0) issued = min(ncv, RING);
+  grid_dep_wait();
+  const Abort ab{abortf, p.status};
   if (warp < CHUNK) {
-    float* yt = y + warp * ypitch;
-    if (warp < nt) {
-      const __nv_bfloat16* x = p.c_q + static_cast<int64_t>(t0 + warp) * dq;
+    // ---- RMSNorm of token `warp` over all of d_q, then its normalised values in
+    // this CTA's dims as two bf16 terms (row warp: hi, row 8 + warp: lo) of the
+    // MMA's B operand, K-major with the 128-byte swizzle; zeros past d_q and for
+    // absent tokens
+    const int t = warp;
+    float r = 0.f;
+    const __nv_bfloat16* x = p.c_q + static_cast<int64_t>(t0 + t) * dq;
+    if (t < nt) {
       float ss = 0.f;
-      for (int i = lane * 8; i < dq; i += 256) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + i));
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-        float o8[8];
+#pragma unroll 1
+      for (int i0 = lane * 8; i0 < dq; i0 += 256 * 4) {   // four 16-byte loads in flight per lane
+        uint4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          o8[2 * j] = __uint_as_float(w4[j] << 16);
-          o8[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
-          ss = fmaf(o8[2 * j], o8[2 * j], fmaf(o8[2 * j + 1], o8[2 * j + 1], ss));
+        for (int u = 0; u < 4; ++u)
+          v[u] = i0 + 256 * u < dq ? __ldg(reinterpret_cast<const uint4*>(x + i0 + 256 * u)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float a = __uint_as_float(w4[j] << 16), c = __uint_as_float(w4[j] & 0xFFFF0000u);
+            ss = fmaf(a, a, fmaf(c, c, ss));
+          }
         }
-        reinterpret_cast<float4*>(yt + i)[0] = make_float4(o8[0], o8[1], o8[2], o8[3]);
-        reinterpret_cast<float4*>(yt + i)[1] = make_float4(o8[4], o8[5], o8[6], o8[7]);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float r = 1.0f / sqrtf(ss / static_cast<float>(dq) + p.eps);
-      __syncwarp();
-      for (int i = lane * 8; i < dq; i += 256) {
-        const uint4 gm = __ldg(reinterpret_cast<const uint4*>(p.gamma + i));
-        const uint32_t g4[4] = {gm.x, gm.y, gm.z, gm.w};
-        float4* dst = reinterpret_cast<float4*>(yt + i);
-        float4 a = dst[0], c = dst[1];
-        a.x = a.x * r * __uint_as_float(g4[0] << 16);
-        a.y = a.y * r * __uint_as_float(g4[0] & 0xFFFF0000u);
-        a.z = a.z * r * __uint_as_float(g4[1] << 16);
-        a.w = a.w * r * __uint_as_float(g4[1] & 0xFFFF0000u);
-        c.x = c.x * r * __uint_as_float(g4[2] << 16);
-        c.y = c.y * r * __uint_as_float(g4[2] & 0xFFFF0000u);
-        c.z = c.z * r * __uint_as_float(g4[3] << 16);
-        c.w = c.w * r * __uint_as_float(g4[3] & 0xFFFF0000u);
-        dst[0] = a;
-        dst[1] = c;
-      }
-      for (int i = dq + lane; i < ypitch; i += 32) yt[i] = 0.f;
-    } else {
-      for (int i = lane; i < ypitch; i += 32) yt[i] = 0.f;
+      r = 1.0f / sqrtf(ss / static_cast<float>(dq) + p.eps);
     }
-  }
-  __syncthreads();
-  // 2. thread (group g of 8 rows, kl of 128) over dims 2 kl, 2 kl + 1 of each chunk
-  const int g = warp >> 2, kl = ((warp & 3) << 5) | lane;
-  float2 acc[8][CHUNK / 2];   // [row][token pair]
+    const int k0 = c_first * KC;
+    for (int j = lane; j < cpq * (KC / 8); j += 32) {   // 16-byte pieces of the CTA's dims
+      const int idx = k0 + 8 * j;
+      uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
+      if (t < nt && idx < dq) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + idx));
+        const uint4 gm = __ldg(reinterpret_cast<const uint4*>(p.gamma + idx));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w}, g4[4] = {gm.x, gm.y, gm.z, gm.w};
+        uint32_t h4[4], l4[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int t = 0; t < CHUNK / 2; ++t) acc[i][t] = make_float2(0.f, 0.f);
-  const Abort ab{abortf, p.status};
-  bool ok = true;
-#pragma unroll 1
-  for (int c = 0; c < nk; ++c) {
-    const int slot = c % RING;
-    if (ok) ok = mbar_wait(&bars[slot], (c / RING) & 1, ab);
-    if (ok && 2 * kl < kbox) {
-      const uint8_t* wsl = ring + slot * SLOT_BYTES + (8 * g) * (kbox * 2) + 4 * kl;
-      float2 w2[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(wsl + i * (kbox * 2));
-        w2[i] = make_float2(__uint_as_float(wb << 16), __uint_as_float(wb & 0xFFFF0000u));
-      }
-      const float* yc = y + c * KBOX + 2 * kl;
-#pragma unroll
-      for (int tp = 0; tp < CHUNK / 2; ++tp) {
-        const float2 ya = *reinterpret_cast<const float2*>(yc + (2 * tp) * ypitch);       // token 2tp, dims d, d+1
-        const float2 yb = *reinterpret_cast<const float2*>(yc + (2 * tp + 1) * ypitch);   // token 2tp+1
-        const float2 y0 = make_float2(ya.x, yb.x), y1 = make_float2(ya.y, yb.y);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc[i][tp] = ffma2(make_float2(w2[i].x, w2[i].x), y0, acc[i][tp]);
-          acc[i][tp] = ffma2(make_float2(w2[i].y, w2[i].y), y1, acc[i][tp]);
+        for (int e = 0; e < 4; ++e) {
+          const float ya = __uint_as_float(w4[e] << 16) * r * __uint_as_float(g4[e] << 16);
+          const float yb = __uint_as_float(w4[e] & 0xFFFF0000u) * r * __uint_as_float(g4[e] & 0xFFFF0000u);
+          const __nv_bfloat162 hh = __floats2bfloat162_rn(ya, yb);
+          const float2 hf = __bfloat1622float2(hh);
+          const __nv_bfloat162 ll = __floats2bfloat162_rn(ya - hf.x, yb - hf.y);
+          h4[e] = *reinterpret_cast<const uint32_t*>(&hh);
+          l4[e] = *reinterpret_cast<const uint32_t*>(&ll);
         }
+        hi = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+        lo = make_uint4(l4[0], l4[1], l4[2], l4[3]);
       }
+      const int c = j / (KC / 8), piece = j % (KC / 8);
+      uint8_t* chunk = bq + c * B_CHUNK;
+      *reinterpret_cast<uint4*>(chunk + sw128_off(t, piece)) = hi;                 // row t (rows 0..7: atom 0)
+      *reinterpret_cast<uint4*>(chunk + 1024 + sw128_off(t, piece)) = lo;          // row 8 + t (atom 1)
     }
-    __syncthreads();   // every warp is done with this slot
-    if (threadIdx.x == 0 && c + RING < nk && !*reinterpret_cast<volatile int*>(abortf)) {
-      mbar_arrive_expect_tx(&bars[slot], ROWS * kbox * 2);
-      tma_load_2d(ring + slot * SLOT_BYTES, &wmap, &bars[slot], (c + RING) * KBOX, row0);
-    }
+    fence_proxy_async_smem();   // visible to the tensor core
   }
-  // 3. reduce each output's 128 partial sums: a butterfly over the lanes leaves lane l
-  // with outputs 2l, 2l + 1 (output v = row * 8 + token) of the warp, then the 4 warps
-  // of the group add in shared memory
-  float v[64];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int tp = 0; tp < CHUNK / 2; ++tp) {
-      v[i * 8 + 2 * tp] = acc[i][tp].x;
-      v[i * 8 + 2 * tp + 1] = acc[i][tp].y;
+  __syncthreads();   // the B operand is complete
+  if (warp == PROD_WARP && lane == 0) {
+    for (; issued < ncv; ++issued) {
+      const int s = issued % RING;
+      if (!mbar_wait(&empty[s], ((issued / RING) - 1) & 1, ab)) break;
+      mbar_arrive_expect_tx(&full[s], A_BYTES);
+      tma_load_2d(ring + s * A_BYTES, &wmap, &full[s], (c_first + issued) * KC, h * 128);
     }
+  } else if (warp == MMA_WARP && lane == 0) {
+    // ---- D[128 rows][16] (+)= W chunk x B chunk, four K = 16 steps per chunk
+    const uint32_t idesc = make_idesc(1, 1, false, false, 128, 16);
+    for (int c = 0; c < ncv; ++c) {
+      const int s = c % RING;
+      if (!mbar_wait(&full[s], (c / RING) & 1, ab)) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(ring + s * A_BYTES), b0 = smem_u32(bq + c * B_CHUNK);
 #pragma unroll
-  for (int o = 16, n = 64; o > 0; o >>= 1, n >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int j = 0; j < n / 2; ++j) {
-      const float send = upper ? v[j] : v[j + n / 2];
-      const float keep = upper ? v[j + n / 2] : v[j];
-      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      for (int k = 0; k < KC / 16; ++k)
+        mma_f16(tmem, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
+                (c > 0 || k > 0) ? 1u : 0u);
+      tc_commit(&empty[s]);
     }
+    tc_commit(done);   // completes when every MMA issued above has (at once with none)
   }
-  red[warp * 64 + 2 * lane] = v[0];
-  red[warp * 64 + 2 * lane + 1] = v[1];
-  __syncthreads();
-  if (threadIdx.x < ROWS * CHUNK) {
-    const int r = threadIdx.x >> 3, t = threadIdx.x & 7;   // row of the CTA, token
-    const int gg = r >> 3, vi = (r & 7) * 8 + t;
-    float sum = 0.f;
+  __syncwarp();
+  // ---- epilogue: warp w < 4 holds rows 32w.. of the head: this quarter's 8 sums per
+  // row (hi + lo columns) into its own shared memory; after one cluster barrier the
+  // first CTA adds the four quarters, takes the head's maximum per token and writes
+  // the codes and the folded weights
+  if (warp < 4) {
+    float q8[CHUNK];
+    const bool ok = mbar_wait(done, 0, ab);
+    tc_fence_after();
+    if (ok && ncv > 0) {
+      uint32_t a[8], b[8];
+      DSA_TMEM_LD8(tmem + (static_cast<uint32_t>(warp * 32) << 16), a);
+      DSA_TMEM_LD8(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 8, b);
+      tmem_wait_ld();
 #pragma unroll
-    for (int w4 = 0; w4 < 4; ++w4) sum += red[(gg * 4 + w4) * 64 + vi];
-    qv[r * CHUNK + t] = sum;
-  }
-  __syncthreads();
-  // 4. the head's max |q| per token: this CTA's 32 rows, then the cluster's four quarters
-  if (threadIdx.x < CHUNK) {
-    float m = 0.f;
-    for (int rr = 0; rr < ROWS; ++rr) m = fmaxf(m, fabsf(qv[rr * CHUNK + threadIdx.x]));
-    amax_sh[threadIdx.x] = m;
+      for (int t = 0; t < CHUNK; ++t) q8[t] = __uint_as_float(a[t]) + __uint_as_float(b[t]);
+    } else {
+#pragma unroll
+      for (int t = 0; t < CHUNK; ++t) q8[t] = 0.f;
+    }
+    float4* dst = reinterpret_cast<float4*>(red + threadIdx.x * CHUNK);   // [128 rows][8]
+    dst[0] = make_float4(q8[0], q8[1], q8[2], q8[3]);
+    dst[1] = make_float4(q8[4], q8[5], q8[6], q8[7]);
   }
   cluster_arrive();
-  cluster_wait();
-  if (threadIdx.x < CHUNK) {
-    float m = 0.f;
-    for (uint32_t r = 0; r < 4; ++r)
-      m = fmaxf(m, __uint_as_float(ld_cluster_u32(cluster_map(smem_u32(&amax_sh[threadIdx.x]), r))));
-    amax_all[threadIdx.x] = m;
-  }
-  cluster_arrive_relaxed();   // done reading the other quarters
-  __syncthreads();
-  // 5. codes e4m3(q / s), s = max / 448 (1 for an all-zero head); folded weights by quarter 0
-  if (threadIdx.x < CHUNK * ROWS / 4) {
-    const int t = threadIdx.x / (ROWS / 4), r4 = (threadIdx.x % (ROWS / 4)) * 4;   // 4 rows per thread
-    if (t < nt) {
-      const float m = amax_all[t];
-      const float s = m > 0.f ? m / 448.0f : 1.0f;
-      const uint32_t code = f4_to_e4m3x4(qv[(r4 + 0) * CHUNK + t] / s, qv[(r4 + 1) * CHUNK + t] / s,
-                                         qv[(r4 + 2) * CHUNK + t] / s, qv[(r4 + 3) * CHUNK + t] / s);
-      *reinterpret_cast<uint32_t*>(p.q_idx + (static_cast<int64_t>(t0 + t) * kIdxHeads + h) * kIdxDim + quarter * ROWS +
-                                   r4) = code;
-      if (quarter == 0 && r4 == 0) p.w_out[static_cast<int64_t>(t0 + t) * kIdxHeads + h] = p.head_w[(t0 + t) * kIdxHeads + h] * s;
+  cluster_wait();   // every quarter's partial sums are in its shared memory
+  if (quarter == 0 && warp < 4) {
+    const int row = threadIdx.x;   // dim of head h
+    const float hw = row < nt ? __ldg(p.head_w + (t0 + row) * kIdxHeads + h) : 0.f;   // token row's head weight
+    float q8[CHUNK];
+#pragma unroll
+    for (int t = 0; t < CHUNK; ++t) q8[t] = 0.f;
+#pragma unroll
+    for (uint32_t src = 0; src < 4; ++src) {
+      const uint32_t at = cluster_map(smem_u32(red + row * CHUNK), src);
+      const uint4 v0 = ld_cluster_v4(at), v1 = ld_cluster_v4(at + 16);
+      q8[0] += __uint_as_float(v0.x);
+      q8[1] += __uint_as_float(v0.y);
+      q8[2] += __uint_as_float(v0.z);
+      q8[3] += __uint_as_float(v0.w);
+      q8[4] += __uint_as_float(v1.x);
+      q8[5] += __uint_as_float(v1.y);
+      q8[6] += __uint_as_float(v1.z);
+      q8[7] += __uint_as_float(v1.w);
     }
+    // the head's max |q| per token: within the warp, then over the 4 warps
+#pragma unroll
+    for (int t = 0; t < CHUNK; ++t) {
+      float m = fabsf(q8[t]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) qv[warp * CHUNK + t] = m;
+    }
+    named_bar_sync(1, 128);
+    // s = max / 448 (1 for an all-zero head): thread t < 8 takes token t's scale, its
+    // reciprocal and its folded weight
+    if (row < CHUNK) {
+      const float m = fmaxf(fmaxf(qv[row], qv[CHUNK + row]), fmaxf(qv[2 * CHUNK + row], qv[3 * CHUNK + row]));
+      const float sc = m > 0.f ? m / 448.0f : 1.0f;
+      amax_all[row] = 1.0f / sc;
+      if (row < nt) p.w_out[static_cast<int64_t>(t0 + row) * kIdxHeads + h] = hw * sc;
+    }
+    named_bar_sync(1, 128);
+    // codes e4m3(q / s), one byte per token and dim
+    uint8_t* qdst = p.q_idx + (static_cast<int64_t>(t0) * kIdxHeads + h) * kIdxDim + row;
+#pragma unroll
+    for (int t = 0; t < CHUNK; ++t)
+      if (t < nt)
+        qdst[static_cast<int64_t>(t) * kIdxHeads * kIdxDim] =
+            static_cast<uint8_t>(__nv_cvt_float_to_fp8(q8[t] * amax_all[t], __NV_SATFINITE, __NV_E4M3));
   }
-  // 6. the chunk's new index keys (first quarter of head 0): one warp per token,
-  // four values per lane, s_k = max |k| / 448 in fp32
-  if (p.k_new && blockIdx.x == 0 && warp < nt) {
+  if (quarter != 0) cluster_arrive_relaxed();   // the first CTA reads this one's sums until the end
+  // the chunk's new index keys (second quarter of head 0, while the first finalises
+  // the head): one warp per token, four values per lane, s_k = max |k| / 448 in fp32
+  if (p.k_new && blockIdx.x == 1 && warp < nt) {
     const int t = t0 + warp;
     const uint2 kv = __ldg(reinterpret_cast<const uint2*>(p.k_new + static_cast<int64_t>(t) * kIdxDim) + lane);
     const float k0 = __uint_as_float(kv.x << 16), k1 = __uint_as_float(kv.x & 0xFFFF0000u);
@@ -289,10 +302,15 @@ __global__ void __launch_bounds__(front::THREADS, 1)
       if (lane == 0) *reinterpret_cast<float*>(page + static_cast<int64_t>(p.pool.bs) * kIdxDim + slot * 4) = s;
     }
   }
-  cluster_wait();   // no CTA leaves while another may still read its maxima
-  // no copy into shared memory outlives the CTA (the last copy of each slot)
-  if (threadIdx.x < RING && static_cast<int>(threadIdx.x) < nk)
-    drain_wait(&bars[threadIdx.x], ((nk - 1 - static_cast<int>(threadIdx.x)) / RING) & 1);
+  if (quarter == 0) cluster_arrive_relaxed();
+  cluster_wait();   // no CTA leaves while the first may still read its sums
+  // no copy or MMA outlives the CTA (after a timeout some may still run)
+  if (warp == PROD_WARP && lane == 0)
+    for (int c = max(0, issued - RING); c < issued; ++c) drain_wait(&full[c % RING], (c / RING) & 1);
+  if (warp == MMA_WARP && lane == 0) drain_wait(done, 0);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) tmem_dealloc(tmem, 32);
 }
 
 // The new tokens' latents into their cache slots: one CTA of 64 threads per
@@ -354,11 +372,10 @@ __global__ void __launch_bounds__(64) write_latent_kernel(LatentWriteParams p) {
 
 cudaError_t launch_indexer_front(const CUtensorMap& wmap, const FrontParams& p, cudaStream_t st) {
   cudaError_t e = set_func_attr_once(reinterpret_cast<const void*>(indexer_front_kernel),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, front::smem_bytes(front::MAX_DQ));
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, front::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid(kIdxHeads * 4, static_cast<unsigned>(cdiv(p.b.T, front::CHUNK)));
-  return launch_ex(indexer_front_kernel, grid, dim3(front::THREADS), front::smem_bytes(p.d_q), st, false, 4u, wmap,
-                   p);
+  return launch_ex(indexer_front_kernel, grid, dim3(front::THREADS), front::SMEM_BYTES, st, false, 4u, wmap, p);
 }
 
 cudaError_t launch_write_latent(const LatentWriteParams& p, cudaStream_t st) {

@@ -300,7 +300,7 @@ dsa_status dsa_topk_noalloc(const dsa_kv_layout *layout, const dsa_batch *batch,
  * weights folded in, and the new token's index key, in one kernel).  The post
  * prints no shapes; this call takes them as stated here.  For each query token t:
  *   y = c_q[t] / sqrt(mean(c_q[t]^2) + eps) * norm_weight          (RMSNorm, fp32)
- *   q[h, :] = w_qi[h * 128 .. h * 128 + 127, :] . y               (fp32)
+ *   q[h, :] = w_qi[h * 128 .. h * 128 + 127, :] . y   (fp32 sums; y enters as bf16 hi + lo terms)
  *   s[h] = max|q[h, :]| / 448 (1 for an all-zero head)
  *   q_idx[t, h, :] = e4m3(q[h, :] / s[h]),  w_out[t, h] = head_w[t, h] * s[h]
  * so q_idx and w_out are the inputs dsa_indexer_score / dsa_layer_step take.
@@ -308,7 +308,7 @@ dsa_status dsa_topk_noalloc(const dsa_kv_layout *layout, const dsa_batch *batch,
  * token's own position (block_table[q_req[t]][q_pos[t] / bs], slot q_pos[t] % bs):
  * s_k = max|k| / 448 in fp32 (1 when zero), 128 codes e4m3(k / s_k), then s_k in
  * the page's scale area.  FP8 index pages only (DSA_ERR_UNSUPPORTED otherwise).
- *  c_q        : device bf16 [T, d_q], d_q a multiple of 8 in 8..4096
+ *  c_q        : device bf16 [T, d_q], d_q a multiple of 8 in 64..4096
  *  norm_weight: device bf16 [d_q];  eps >= 0
  *  w_qi       : device bf16 [32 * 128, d_q] (row h * 128 + d is output dim d of head h)
  *  head_w     : device fp32 [T, 32];  k_new: device bf16 [T, 128] or NULL

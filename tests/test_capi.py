@@ -110,6 +110,7 @@ def test_front_and_latent_write_validation(lib):
         ctypes.byref(lay), b, 0x1000, d_q, 0x2000, eps, 0x3000, 0x4000, k, 0x7000, 0x8000, ws, ws_bytes, None)
     assert front(_layout(), d_q=7) == -1                       # not a multiple of 8
     assert front(_layout(), d_q=8192) == -1                    # wider than 4096
+    assert front(_layout(), d_q=56) == -1                      # narrower than 64
     assert front(_layout(), eps=-1.0) == -1
     assert front(_layout(), eps=float("nan")) == -1
     assert front(_layout(), ws_bytes=16) == -4

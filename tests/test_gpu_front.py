@@ -3,11 +3,12 @@ through the C ABI, against the float64 oracle (oracle/front.py):
 
 * the folded head weights within 1e-5 relative; the query's e4m3 codes equal
   except where the oracle's scaled value x = q / s lies within tau of the
-  midpoint between two neighbouring codes.  The kernel sums the d_q products of
-  each output in fp32, so its q differs from the exact one by about
-  sqrt(d_q) * 2^-24 * sqrt(sum of the squared products) (rounding errors of
-  random sign); tau is 8 times that, in units of x, plus 2^-20 |x| for the fp32
-  division by s;
+  midpoint between two neighbouring codes.  The kernel multiplies W by y carried
+  as two bf16 terms (hi = bf16(y), lo = bf16(y - hi): within 2^-17 |y| of y) and
+  sums the d_q products in fp32 on the tensor cores, so its q differs from the
+  exact one by about (2^-17 + sqrt(d_q) * 2^-24) * sqrt(sum of the squared
+  products) (errors of random sign); tau is 8 times that, in units of x, plus
+  2^-20 |x| for the fp32 division by s;
 * the pool after the call equals the oracle's pool byte for byte (the new index
   keys, and for dsa_write_latent the new FP8 / NVFP4 latent records: those are
   computed in fp32 on both sides, so the bytes are exact);
@@ -60,7 +61,7 @@ def _tau(c_q, gamma, w_qi, eps, s, x):
     y = F.rmsnorm(decode_bf16(c_q), decode_bf16(gamma), eps)
     wd = decode_bf16(w_qi).reshape(32 * 128, -1)
     rss = np.sqrt(((wd * y) ** 2).sum(axis=1)).reshape(32, 128)
-    return 8 * np.sqrt(wd.shape[1]) * 2.0 ** -24 * rss / s[:, None] + 2.0 ** -20 * np.abs(x)
+    return 8 * (2.0 ** -17 + np.sqrt(wd.shape[1]) * 2.0 ** -24) * rss / s[:, None] + 2.0 ** -20 * np.abs(x)
 
 
 def _front_case(lens, d_q, seed):
