@@ -20,7 +20,7 @@ Readings taken where the post is silent:
    (0xFFFF - g), g = the candidate's rank-major, position-ascending index in the
    gathered set, so a larger word is a better candidate and equal scores go to
    the lower position; the ids stay local (g indexes the sender's list).
- * "Holds more than it sent" is detected as: every candidate the rank sent was
+ * A rank that may hold more top-k members than it sent is detected as: every candidate the rank sent was
    selected and the rank has tokens it did not send.  Then none of its unsent
    tokens can be excluded, so it resends its full local top-k for that row; a
    rank with an unselected candidate cannot hold a better unsent one.

@@ -164,7 +164,7 @@ dsa_status dsa_indexer_score(const dsa_kv_layout *layout, const dsa_batch *batch
                              dsa_stream_t stream);
 
 /*
- * Exact top-k ("Then it keeps the top 2,048 tokens"): for each token t, the k
+ * Exact top-k ("Sparse Attention in K3.1 Pro": the best 2,048 tokens are kept): for each token t, the k
  * largest of scores[t, 0..q_pos[t]]; equal scores are ordered by lower position
  * first (-0.0 equals +0.0).  idx[t, :] receives the selected positions in
  * ascending order; when q_pos[t] + 1 < k every position is selected and the
@@ -182,7 +182,7 @@ dsa_status dsa_topk(const dsa_kv_layout *layout, const dsa_batch *batch, const f
                     void *workspace, size_t workspace_bytes, dsa_stream_t stream);
 
 /*
- * Sparse MLA ("MLA attention then runs exactly, but only over those 2,048 tokens"):
+ * Sparse MLA ("Sparse Attention in K3.1 Pro": exact attention restricted to the kept tokens):
  * for each token t and head h < 96, over the positions S_t = {idx[t, i] >= 0}:
  *   logit(s) = sm_scale * q[t,h,:] . c(s)          (all 576 dims)
  *   out[t,h,:] = sum_s softmax(logit)(s) * c(s)[0:512]
@@ -295,9 +295,9 @@ dsa_status dsa_topk_noalloc(const dsa_kv_layout *layout, const dsa_batch *batch,
                             dsa_stream_t stream);
 
 /*
- * The fused indexer front ("Low-latency decode: a fused DSA decode path": the
- * query norm, the indexer's query projection, its FP8 quantization with the head
- * weights folded in, and the new token's index key, in one kernel).  The post
+ * The fused indexer front ("Low-latency decode: a fused DSA decode path": one
+ * kernel normalises the query, projects the indexer query, quantizes it with the
+ * scales absorbed by the head weights and writes the new token's index key).  The post
  * prints no shapes; this call takes them as stated here.  For each query token t:
  *   y = c_q[t] / sqrt(mean(c_q[t]^2) + eps) * norm_weight          (RMSNorm, fp32)
  *   q[h, :] = w_qi[h * 128 .. h * 128 + 127, :] . y   (fp32 sums; y enters as bf16 hi + lo terms)

@@ -9,7 +9,7 @@ The method (vLLM blog post "vLLM delivers day-0 support for Kimi K3.1 Pro"):
 * "Sparse Attention in K3.1 Pro": an indexer keeps one FP8 key per token
   (128 e4m3 values plus a 4-byte scale, 132 bytes) and scores every earlier
   token for each query with 32 light heads; the 2,048 best tokens are kept and
-  MLA attention then runs exactly over only those tokens' 576-byte latents.
+  exact MLA attention reads only their 576-byte latents.
   The score is  score(t, s) = sum_h w[t, h] * ReLU(q_idx[t, h, :] . k_idx[s, :])
   with k_idx the dequantised key (code * scale).  Causal and inclusive: token t
   at position p scores s = 0 .. p.

@@ -4,11 +4,11 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 vLLM K3.1 Pro day-0 post, "Low-latency decode: a fused DSA decode path": a DSA
 layer runs one packed input projection (query, KV latent, output gate, the
-indexer's key and head weights), then a fused indexer front: "the query norm,
-the indexer's query projection, its FP8 or MXFP4 quantization with the head
-weights folded in, and the new token's index key, in one kernel"; the MLA query
-kernel writes the new token's latent into the KV cache.  The post gives no
-shapes or formulas beyond that sentence.  Readings taken (stated in the
+indexer's key and head weights), then one kernel that normalises the query,
+projects the indexer query, quantizes it (FP8 or MXFP4) with the scales absorbed
+by the head weights, and writes the new token's index key; the new token's
+latent enters the KV cache from the MLA query side.  The post gives no shapes or
+formulas for these steps.  Readings taken (stated in the
 library's header as well):
 
 * query norm: RMSNorm, y = x / sqrt(mean(x^2) + eps) * gamma, over the

@@ -128,7 +128,7 @@ def test_nvfp4_latent_record_read_from_hand_written_bytes():
 # --------------------------------------------------------- byte arithmetic
 
 def test_per_token_widths():
-    # "132 bytes with its scale"; 68 B MXFP4 "including scales"; 576 / 352 B latents
+    # an FP8 index key takes 132 B with its scale, an MXFP4 one 68 B with its scales; latents 576 / 352 B
     assert O.idx_bytes_per_token(O.IDX_FP8) == 132 == 128 + 4
     assert O.idx_bytes_per_token(O.IDX_MXFP4) == 68 == 64 + 4
     assert O.lat_bytes_per_token(O.LAT_FP8) == 576
@@ -141,13 +141,13 @@ def test_kv_footprint_table():
     assert O.kv_bytes_per_token_all_layers(None, O.LAT_FP8) == 13824
     assert O.kv_bytes_per_token_all_layers(O.IDX_FP8, O.LAT_FP8) == 16992
     assert O.kv_bytes_per_token_all_layers(O.IDX_MXFP4, O.LAT_NVFP4) == 10080
-    # "cutting index-cache storage by 48.5%"; "1.7x as many tokens as with FP8"
+    # MXFP4 keys need 48.5% less index storage; the MXFP4 + NVFP4 cache holds 1.7x the tokens of FP8
     assert round(100 * (1 - 68 / 132), 1) == 48.5
     assert round(16992 / 10080, 1) == 1.7
 
 
 def test_decode_byte_ratio_about_23_percent():
-    # "At long context, that is about 23% of the bytes dense MLA reads per layer."
+    # at long context a decode step reads about 23% of the bytes dense MLA would, per layer
     r = lambda L: O.decode_bytes_model(L) / O.dense_mla_bytes(L)
     assert abs(r(65536) - 0.2604) < 1e-4
     assert abs(r(1 << 20) - 0.2311) < 1e-4
