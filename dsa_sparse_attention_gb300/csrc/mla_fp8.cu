@@ -403,27 +403,31 @@ __global__ void __launch_bounds__(mla8::THREADS, 1)
           *reinterpret_cast<uint4*>(rowp + ((q ^ ((dim >> 1) & 3)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       };
+      // each 32-head region leaves by its two tensor stores as soon as it is staged
+      auto store32 = [&](int c) {
+        fence_proxy_async_smem();   // the staged region is read by the tensor stores
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll 1
+          for (int hr = 0; hr < 2; ++hr)
+            tma_store_2d(&pmap, smem + OFF_Q + c * (kVDim * 64) + hr * 256 * 64, 32 * c,
+                         static_cast<int>(ts * kVDim) + 256 * hr);
+          bulk_commit_group();
+        }
+      };
       uint32_t r0[32], r1[32];
       DSA_TMEM_LD32(tmem + O_COL + 96 * vb + lane_off, r0);   // two loads in flight, one wait
       DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 32 + lane_off, r1);
       tmem_wait_ld();
       stage32(r0, 0);
-      stage32(r1, 1);
       DSA_TMEM_LD32(tmem + O_COL + 96 * vb + 64 + lane_off, r0);
+      store32(0);
+      stage32(r1, 1);
+      store32(1);
       tmem_wait_ld();
       stage32(r0, 2);
-      fence_proxy_async_smem();   // the staged partial is read by the tensor stores
-      __syncthreads();
-      if (tid == 0) {
-#pragma unroll 1
-        for (int c = 0; c < 3; ++c)
-#pragma unroll 1
-          for (int hr = 0; hr < 2; ++hr)
-            tma_store_2d(&pmap, smem + OFF_Q + c * (kVDim * 64) + hr * 256 * 64, 32 * c,
-                         static_cast<int>(ts * kVDim) + 256 * hr);
-        bulk_commit_group();
-        bulk_wait_group_all();   // the partial is in global memory before this CTA ends
-      }
+      store32(2);
+      if (tid == 0) bulk_wait_group_read_all();   // the staging is read before the CTA's memory is released
     }
     if (tid < kMlaHeads) p.part_ml[ts * kMlaHeads + tid] = make_float2(ml[tid].x - 8.f, ml[tid].y);
   }
