@@ -146,13 +146,15 @@ def test_layer_step_all_scores_tied_long_rows(lens):
     check_mla(OracleCache(wl), g, _np(out), _np(lse), toks)
 
 
-def test_layer_step_dirty_workspace_hint():
+@pytest.mark.parametrize("lens", [[65536, 40000, 9000, 3000, 2049], [70000, 12345, 5, 66000]])
+def test_layer_step_dirty_workspace_hint(lens):
     # Inside a layer step the top-k starts from top-digit histograms the scorer
     # leaves in the workspace, and leaves them zeroed.  A workspace whose bytes
     # past the status word hold garbage (here all ones) gives the top-k a wrong
     # hint, which it must detect and replace; the next step starts clean.  All
-    # three steps must equal the separate calls exactly.
-    wl = W.make_workload([65536, 40000, 9000, 3000, 2049], 1, seed=23)
+    # three steps must equal the separate calls exactly.  The second case takes the
+    # multi-pass path (rows over 65,536 scores), with a row selected whole.
+    wl = W.make_workload(lens, 1, seed=23)
     dw = _dev(wl)
     ref_scores = dw.indexer_scores()
     ref_idx = _np(dw.topk_of(ref_scores))
