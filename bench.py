@@ -83,7 +83,8 @@ def parse():
     ap.add_argument("--skip-configs", action="store_true", help="measure only the headline configuration")
     ap.add_argument("--profile-config", default=None,
                     help="run configuration N's layer step (or 'prefill_small': 1024 queries on a 32,768-token "
-                         "cache) W + K times and print nothing (for a profiler)")
+                         "cache; or 'front': the indexer front of the headline batch, one weight copy per call) "
+                         "W + K times and print nothing (for a profiler)")
     return ap.parse_args()
 
 
@@ -426,6 +427,27 @@ def profile_config(args):
     from dsa_sparse_attention_gb300.build import build
     from dsa_sparse_attention_gb300.harness import DeviceWorkload
     build()
+    if args.profile_config == "front":   # the indexer front (d_q = 1,536) on the headline batch
+        wl = W.config(1, seed=0)
+        dw = DeviceWorkload(wl)
+        T = wl.num_tokens
+        g = torch.Generator(device="cuda").manual_seed(0)
+        c_q = torch.randn(T, FRONT_DQ, generator=g, device="cuda").to(torch.bfloat16)
+        gamma = (1 + 0.1 * torch.randn(FRONT_DQ, generator=g, device="cuda")).to(torch.bfloat16)
+        n = args.warmup + args.steps
+        w_qis = [(torch.randn(4096, FRONT_DQ, generator=g, device="cuda") / FRONT_DQ ** 0.5).to(torch.bfloat16)
+                 for _ in range(min(n, FRONT_W_COPIES))]
+        head_w = torch.randn(T, 32, generator=g, device="cuda") / 32 ** 0.5
+        k_new = torch.randn(T, 128, generator=g, device="cuda").to(torch.bfloat16)
+        q_idx = torch.empty(T, 32, 128, dtype=torch.uint8, device="cuda")
+        w_out = torch.empty(T, 32, dtype=torch.float32, device="cuda")
+        stream = torch.cuda.Stream()
+        for i in range(n):
+            dsa.dsa_indexer_front(dw.layout, dw.batch, c_q, gamma, 1e-6, w_qis[i % len(w_qis)], head_w, q_idx, w_out,
+                                  k_new=k_new, ws=dw.ws, stream=stream)
+        stream.synchronize()
+        assert dsa.dsa_check(dw.ws, stream) == 0
+        return
     if args.profile_config == "prefill_small":   # the prefill scorer at a size a full profile can hold
         wl = W.make_workload([32768 + 1024], 1024, name="prefill_1024_on_32768", seed=0, permute=True)
     else:
