@@ -285,6 +285,9 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
     }
     *abortf = 0;
     fence_mbar_init();
+    // the descriptors are launch parameters: fetched while the kernel before drains
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&qmap);
   }
   if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
   // Everything above touches only this CTA; the inputs may come from the kernel before.
@@ -384,10 +387,6 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       // before any is used); lane 0 walks the group cursor over all tiles and
       // issues its tiles' copies.
       const int pid = warp == 0 ? 0 : 1 + warp - C::PROD_WARP0;
-      if (lane == 0 && pid == 0) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&qmap);
-      }
       const uint64_t stream_pol = l2_evict_first_policy();
       GroupCursor cur;
       cur.init(groups, ng, total, tile_lo);

@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(mla8::THREADS, 1)
     mbar_init(q_full, 1);
     *abortf = 0;
     fence_mbar_init();
+    if (nsplit > 1) prefetch_tensormap(&pmap);   // a launch parameter: fetched before the wait
   }
   if (warp == 0) tmem_alloc(tslot, 512);
   // Everything above touches only this CTA; the selection (and, in a layer step, the
