@@ -142,7 +142,7 @@ struct ScorerCfg {
   static constexpr bool MX = IDXF == 1;
   // Key stages are freed as soon as their MMA completes; the per-key scales the
   // epilogue reads live in a separate, longer ring of SSLOTS slots.
-  static constexpr int STAGES = MX ? 6 : ((G == 1) ? 12 : 8);
+  static constexpr int STAGES = MX ? 6 : 8;
   static constexpr int SSLOTS = STAGES + 4;
   static constexpr int NBLK = MX ? 4 : 1;                   // accumulators per tile (scale blocks)
   static constexpr int ACC_COLS = 32 * G * NBLK;
