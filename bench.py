@@ -16,9 +16,10 @@ reads; that variant is reported too, as `ms_per_step_after_l2_flush`.)  The
 timed steps replay a CUDA graph of four consecutive C-ABI layer-step calls (one
 per pool copy), as a multi-layer forward pass would capture them; one pair of
 CUDA events brackets all K steps.  `e2e` instead runs the host-buffer C-ABI call
-(dsa_layer_step_host) each step: the step's inputs are copied from page-locked
-host memory and the output is copied back inside the timed region, and the host
-waits for each step before issuing the next.
+(dsa_layer_step_host) each step, captured once into a CUDA graph as a decode loop
+with fixed buffers would: the step's inputs are copied from page-locked host
+memory and the output is copied back inside the timed region, and the host waits
+for each step before issuing the next (`eager_value`: the same call made eagerly).
 
 `--impl reference` times the float64 CPU oracle on the same workload (the
 reference arm: the vLLM post describing the method ships no runnable code of it).
@@ -683,23 +684,44 @@ def main():
     # end to end through the C ABI with host buffers (dsa_layer_step_host): every step
     # copies its inputs from page-locked host memory (packed back to back, so one
     # copy), runs, and copies its output back; the host waits for each step, as a
-    # decode loop whose next input depends on this output does
+    # decode loop whose next input depends on this output does.  The call is
+    # captured once per pool copy into a CUDA graph, as a decode loop with fixed
+    # buffers captures it, and each step replays one (the copies run on every
+    # replay); the same call made eagerly is reported beside it.
     def e2e_host_call():
         hs = HostStep(dw, packed=True, with_lse=False, with_idx=False)
         for i in range(4):
             hs.step(stream, layouts[i % len(layouts)])
         torch.cuda.synchronize()
-        ms_list = []
-        for i in range(args.steps):
-            t0 = time.perf_counter()
-            hs.step(stream, layouts[i % len(layouts)])
-            stream.synchronize()
-            ms_list.append((time.perf_counter() - t0) * 1000)
-        return ms_list, hs.h2d_bytes, hs.d2h_bytes, ("dsa_layer_step_host per step: inputs from one page-locked "
-                                                     "buffer, output back, host waits for each step")
 
-    e2e_ms, h2d, d2h, e2e_how = e2e_host_call()
+        def wall(step_fn):
+            for i in range(4):
+                step_fn(i)
+                stream.synchronize()
+            ms_list = []
+            for i in range(args.steps):
+                t0 = time.perf_counter()
+                step_fn(i)
+                stream.synchronize()
+                ms_list.append((time.perf_counter() - t0) * 1000)
+            return ms_list
+
+        eager_ms = wall(lambda i: hs.step(stream, layouts[i % len(layouts)]))
+        hgraphs = []
+        for lay in layouts:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                hs.step(torch.cuda.current_stream(), lay)
+            hgraphs.append(g)
+        with torch.cuda.stream(stream):
+            graph_ms = wall(lambda i: hgraphs[i % len(hgraphs)].replay())
+        return graph_ms, eager_ms, hs.h2d_bytes, hs.d2h_bytes, (
+            "dsa_layer_step_host captured into a CUDA graph (one per pool copy), one replay per step: inputs "
+            "copied from one page-locked buffer, output copied back, host waits for each step")
+
+    e2e_ms, e2e_eager_ms, h2d, d2h, e2e_how = e2e_host_call()
     _, e2e_value = job_rate(statistics.mean(e2e_ms), world, device="cuda")   # slowest rank, like `value`
+    _, e2e_eager = job_rate(statistics.mean(e2e_eager_ms), world, device="cuda")
     assert dsa.dsa_check(dw.ws, stream) == 0
 
     cpu = None
@@ -740,7 +762,8 @@ def main():
                          "launch_ms_how": "mean over 8 scorer calls replayed from one CUDA graph (pool copies rotated)",
                          "launch_ms_eager": sc_ms_eager},
             "e2e": {"value": e2e_value, "unit": "layer-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "how": e2e_how},
+                    "how": e2e_how, "eager_value": e2e_eager,
+                    "eager_how": "the same call made eagerly each step (the launches' host latency included)"},
             "gpu_launches": n_kernels_per_step * args.steps,
             "breakdown_ms": breakdown,
             "indexer_front": front,

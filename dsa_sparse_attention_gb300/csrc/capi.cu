@@ -11,6 +11,7 @@
 
 #include "../../include/dsa.h"
 
+#include "hostcopy.cuh"
 #include "mla_q.cuh"
 #include "params.cuh"
 
@@ -70,6 +71,10 @@ dsa_status check_layout(const dsa_kv_layout* l, bool need_pool = true) {
   if (l->lat_fmt != DSA_LAT_FP8 && l->lat_fmt != DSA_LAT_NVFP4) return DSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(l->pool) & 15) || (l->row_stride_bytes & 15) || (l->idx_page_offset & 15) ||
       (l->lat_page_offset & 15))
+    return DSA_ERR_INVALID_ARG;
+  // MXFP4 index pages are read by a packed 4-bit tensor copy: 32-byte alignment
+  if (l->idx_fmt == DSA_IDX_MXFP4 &&
+      ((reinterpret_cast<uintptr_t>(l->pool) & 31) || (l->row_stride_bytes & 31) || (l->idx_page_offset & 31)))
     return DSA_ERR_INVALID_ARG;
   const int64_t idx_pb = int64_t(l->block_size) * (l->idx_fmt == DSA_IDX_FP8 ? 132 : 68);
   const int64_t lat_pb = int64_t(l->block_size) * (l->lat_fmt == DSA_LAT_FP8 ? 576 : 352);
@@ -158,22 +163,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over the index-key value bytes of every page: {value bytes per key,
-// block slots, rows}.  FP8 keys (128 B) land 128-byte swizzled, ready for the
-// MMA; packed MXFP4 keys (64 B) land row-major for the converter warps.
+// 3-D map over the index-key values of every page: {128 dims, block slots, rows},
+// 128-byte swizzle, 128 B per key in shared memory, ready for the MMA.  FP8 keys
+// are 128 e4m3 bytes.  MXFP4 keys (64 bytes of packed e2m1 in the page) use the
+// 16 x 4-bit element type that pads every 8 bytes of codes to 16 (the MMA's E2M1
+// operand layout); it needs the page and the row stride 32-byte aligned, and a
+// copy counts the 64 packed bytes per key.
 bool make_key_map(CUtensorMap* m, const dsa_kv_layout* l) {
   auto enc = encode_fn();
   if (!enc) return false;
   const bool mx = l->idx_fmt == DSA_IDX_MXFP4;
-  const cuuint64_t vb = mx ? 64 : 128;
   const int box_rows = l->block_size < kKeyTile ? l->block_size : kKeyTile;
-  cuuint64_t dims[3] = {vb, cuuint64_t(l->block_size), cuuint64_t(l->num_rows)};
-  cuuint64_t strides[2] = {vb, cuuint64_t(l->row_stride_bytes)};
-  cuuint32_t box[3] = {cuuint32_t(vb), cuuint32_t(box_rows), 1};
+  cuuint64_t dims[3] = {128, cuuint64_t(l->block_size), cuuint64_t(l->num_rows)};
+  cuuint64_t strides[2] = {cuuint64_t(mx ? 64 : 128), cuuint64_t(l->row_stride_bytes)};
+  cuuint32_t box[3] = {128, cuuint32_t(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(l->pool)) + l->idx_page_offset;
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             mx ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(m, mx ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -416,6 +423,38 @@ dsa_status run_mla(const dsa_kv_layout* l, const dsa_batch* b, const void* q, co
   return cuda_status(launch_sparse_mla(qmap, cmap, p, st, chained));
 }
 
+// The device address of the host range [host, host + bytes) when the whole range
+// lies inside one page-locked allocation that the current device can address
+// (cudaHostAlloc, cudaMallocHost or cudaHostRegister), else null: only such a
+// range is handed to the copy kernel; anything else goes through cudaMemcpyAsync.
+void* mapped_device_ptr(const void* host, size_t bytes) {
+  using Fn = CUresult (*)(void*, CUpointer_attribute, CUdeviceptr);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(f);
+  });
+  if (!fn || !host || !bytes) return nullptr;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    (void)cudaGetLastError();   // not a pointer the runtime knows: no error left behind
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  const CUdeviceptr d = reinterpret_cast<CUdeviceptr>(a.devicePointer);
+  CUdeviceptr start = 0;
+  size_t size = 0;
+  if (fn(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, d) != CUDA_SUCCESS ||
+      fn(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, d) != CUDA_SUCCESS)
+    return nullptr;
+  if (d < start || d - start > size || bytes > size - (d - start)) return nullptr;
+  return a.devicePointer;
+}
+
 // One host <-> device copy of dsa_layer_step_host.
 struct Copy {
   void* dst;
@@ -599,13 +638,28 @@ dsa_status dsa_layer_step_host(const dsa_kv_layout* layout, const dsa_batch* bat
         return DSA_ERR_INVALID_ARG;
       total += in[i].bytes;
     }
+  // page-locked ranges move in one copy kernel per direction (SM loads and stores
+  // over the host link); other host memory through cudaMemcpyAsync
+  const int nsm = num_sms();
   cudaError_t e = cudaSuccess;
+  auto add = [&](HostCopyParams& hp, const Copy& c, bool to_host) {
+    if (!c.bytes || e != cudaSuccess) return;
+    void* m = mapped_device_ptr(to_host ? c.dst : c.src, c.bytes);
+    if (m && hp.nseg < kHostCopyMaxSegs) {
+      hp.seg[hp.nseg++] = {static_cast<uint8_t*>(to_host ? m : c.dst),
+                           static_cast<const uint8_t*>(to_host ? c.src : m), c.bytes};
+      return;
+    }
+    e = cudaMemcpyAsync(c.dst, c.src, c.bytes, to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice, stream);
+  };
+  HostCopyParams hin{};
   if (packed) {
-    e = cudaMemcpyAsync(in[0].dst, in[0].src, total, cudaMemcpyHostToDevice, stream);
+    add(hin, {in[0].dst, in[0].src, total}, false);
   } else {
-    for (int i = 0; i < 7 && e == cudaSuccess; ++i)
-      if (in[i].bytes) e = cudaMemcpyAsync(in[i].dst, in[i].src, in[i].bytes, cudaMemcpyHostToDevice, stream);
+    for (int i = 0; i < 7; ++i) add(hin, in[i], false);
   }
+  // chained: its dependency wait covers the kernels before it; the scorer's set-up overlaps it
+  if (e == cudaSuccess && hin.nseg) e = launch_host_copy(hin, nsm, stream, true);
   if (e != cudaSuccess) return cuda_fail(e);
   if ((s = run_step(layout, batch, q_idx, w, q, topk, sm_scale, idx_out, out, lse, workspace, wl, stream)) != DSA_OK)
     return s;
@@ -614,8 +668,9 @@ dsa_status dsa_layer_step_host(const dsa_kv_layout* layout, const dsa_batch* bat
       {host->lse, lse, host->lse ? size_t(T) * kMlaHeads * 4 : 0},
       {host->idx, idx_out, host->idx ? size_t(T) * size_t(topk) * 4 : 0},
   };
-  for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-    if (back[i].bytes) e = cudaMemcpyAsync(back[i].dst, back[i].src, back[i].bytes, cudaMemcpyDeviceToHost, stream);
+  HostCopyParams hout{};
+  for (int i = 0; i < 3; ++i) add(hout, back[i], true);
+  if (e == cudaSuccess && hout.nseg) e = launch_host_copy(hout, nsm, stream, true);
   return e == cudaSuccess ? DSA_OK : cuda_fail(e);
 }
 

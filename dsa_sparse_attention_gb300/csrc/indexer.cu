@@ -18,8 +18,11 @@
 //    loads each group's queries; two MMA warps take tiles in turn; warps 2..9,
 //    two sets of four taking alternate tiles, read the accumulators (thread = key)
 //    and reduce sum_h w * ReLU(acc) * scale into fp32 scores.  FP8 keys: producers
-//    0 and 10..12, MMA warps 1 and 13; MXFP4 keys: converter warps 10..17,
-//    producers 0 and 18, MMA warps 1 and 19.
+//    0 and 10..12, MMA warps 1 and 13.  MXFP4 keys: the tensor copy widens each
+//    16 packed e2m1 codes to a 16-byte unit (8 bytes of codes, 8 of padding), the
+//    operand layout of the block-scaled kind::mxf8f6f4 MMA with E2M1 keys; scale
+//    warps 10..13 move each tile's E8M0 exponents into TMEM, where the MMA
+//    applies them per 32-dim block; producers 0 and 14..16, MMA warps 1 and 17.
 // Page translation (row = block_table[req][s / bs]) happens in the producer.
 // Inside a layer step (one token per group) the epilogue also counts each
 // token's scores by the top 11 bits of their order-preserving key, the first
@@ -133,32 +136,40 @@ constexpr int kRowBatch = 32;      // tiles whose block-table rows a producer wa
 constexpr int kHistBins = 2048;    // top-digit bins of the score histogram handed to the top-k
 
 // Shared-memory / TMEM plan of the scorer.  IDXF = DSA_IDX_FP8 (0) or
-// DSA_IDX_MXFP4 (1); G = max tokens per group (N = 32 G).  MXFP4 keys arrive
-// packed (64 B/key) and converter warps expand them to e4m3 (exact); each
-// 32-dim scale block gets its own accumulator so the E8M0 scales are applied
-// exactly in the epilogue.
+// DSA_IDX_MXFP4 (1); G = max tokens per group (N = 32 G).  MXFP4 keys (64 B of
+// codes per key in the pool) land as 128 B per key, each 8 bytes of codes padded
+// to 16; scale warps move each key's four E8M0 exponents into TMEM, where the
+// block-scaled MMA applies exponent b to the products of dims 32b..32b+31 (exact
+// powers of two), so one accumulator holds the scaled score terms.
 template <int IDXF, int G>
 struct ScorerCfg {
   static constexpr bool MX = IDXF == 1;
   // Key stages are freed as soon as their MMA completes; the per-key scales the
   // epilogue reads live in a separate, longer ring of SSLOTS slots.
-  static constexpr int STAGES = MX ? 6 : 8;
+  static constexpr int STAGES = 8;
   static constexpr int SSLOTS = STAGES + 4;
-  static constexpr int NBLK = MX ? 4 : 1;                   // accumulators per tile (scale blocks)
-  static constexpr int ACC_COLS = 32 * G * NBLK;
-  static constexpr int NACC = (G == 1 && !MX) ? 4 : 2;      // TMEM accumulators (even: set = tile parity)
+  static constexpr int ACC_COLS = 32 * G;
+  static constexpr int NACC = G == 1 ? 4 : 2;               // TMEM accumulators (even: set = tile parity)
   // MMA issue costs the issuing thread a few hundred cycles per tile, so NMMA
   // warps take tiles in turn (each with its own accumulators).
   static constexpr int NMMA = 2;
-  static constexpr int TMEM_COLS = NACC * ACC_COLS;         // 128 / 256 / 512 (powers of two)
-  static constexpr int KEY_BYTES = kKeyTile * kIdxDim;      // 16 KB of e4m3 (MMA operand)
-  static constexpr int PACK_BYTES = MX ? kKeyTile * 64 : 0; // 8 KB of packed e2m1 per stage
+  // MXFP4: the block scales of the MMA, A (keys) 4 columns per key stage (key r of
+  // the stage at lane r, column r / 32), B (the query, all 2^0) G columns
+  static constexpr int SFA_COL = NACC * ACC_COLS;
+  static constexpr int SFB_COL = SFA_COL + 4 * STAGES;
+  static constexpr int TMEM_USED = MX ? SFB_COL + G : NACC * ACC_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                   : TMEM_USED <= 64  ? 64
+                                   : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256
+                                                      : 512;   // allocations are powers of two
+  // 16 KB of MMA operand per stage: e4m3 codes, or e2m1 codes with every 8 bytes padded to 16
+  static constexpr int KEY_BYTES = kKeyTile * kIdxDim;
   static constexpr int SCALE_BYTES = kKeyTile * 4;
   static constexpr int Q_BYTES = G * kIdxHeads * kIdxDim;
   static constexpr int W_BYTES = G * kIdxHeads * 4;
   static constexpr int OFF_Q = STAGES * KEY_BYTES;
-  static constexpr int OFF_PACK = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_SCALES = OFF_PACK + STAGES * PACK_BYTES;
+  static constexpr int OFF_SCALES = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_W = OFF_SCALES + SSLOTS * SCALE_BYTES;   // 2 x [G][32] fp32
   static constexpr int OFF_POS = OFF_W + 2 * W_BYTES;                // 2 x [G] int
   static constexpr int OFF_BARS = OFF_POS + 2 * G * 4 + 64;
@@ -168,17 +179,17 @@ struct ScorerCfg {
   // Copies are issued by NPROD producer warps taking tiles in turn: one thread
   // issues a bulk or tensor copy in about 150 cycles, several warps in parallel
   // several times faster.
-  static constexpr int NPROD = MX ? 2 : 4;   // MXFP4: the converter warps leave fewer registers
+  static constexpr int NPROD = 4;
   static constexpr int OFF_ROWS = OFF_PLAN + kDirectMaxT * 32 + 64;   // producers: [NPROD][kRowBatch][8] block ids
   // One token per group: the epilogue counts the top 11 key bits of its first
   // token's scores in shared memory (later tokens go straight to global memory).
   static constexpr bool HIST = G == 1;
   static constexpr int OFF_HIST = (OFF_ROWS + NPROD * kRowBatch * 8 * 4 + 15) & ~15;   // zeroed 16 bytes at a time
   static constexpr int SMEM_BYTES = OFF_HIST + (HIST ? kHistBins * 4 : 0) + 1024;  // + slack for alignment
-  static constexpr int CONV_WARPS = MX ? 8 : 0;
-  static constexpr int PROD_WARP0 = 10 + CONV_WARPS;     // producer warps: 0 and PROD_WARP0 ..
+  static constexpr int SCALE_WARPS = MX ? 4 : 0;           // one per TMEM lane quarter
+  static constexpr int PROD_WARP0 = 10 + SCALE_WARPS;     // producer warps: 0 and PROD_WARP0 ..
   static constexpr int MMA_WARP1 = PROD_WARP0 + NPROD - 1;   // MMA warps: 1 and MMA_WARP1 ..
-  static constexpr int THREADS = 320 + 32 * CONV_WARPS + 32 * (NPROD - 1) + 32 * (NMMA - 1);
+  static constexpr int THREADS = 320 + 32 * SCALE_WARPS + 32 * (NPROD - 1) + 32 * (NMMA - 1);
   static_assert(NACC % NMMA == 0, "accumulators per MMA warp");
   // Tile i uses stage i % STAGES, producer i % NPROD, MMA warp i % NMMA and scale
   // slot i % SSLOTS.  Each ring's length is a multiple of the number of warps
@@ -187,21 +198,11 @@ struct ScorerCfg {
   static_assert(STAGES % NPROD == 0 && STAGES % NMMA == 0, "key stages per producer and MMA warp");
   static_assert(SSLOTS % NPROD == 0 && SSLOTS % 2 == 0, "scale slots per producer and epilogue set");
   static_assert(NACC % 2 == 0, "accumulators per epilogue set");
-  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512, "tmem columns");
+  static_assert(TMEM_USED <= 512, "tmem columns");
   static_assert(SMEM_BYTES <= 232448, "smem");
   static_assert(OFF_HIST % 16 == 0 && OFF_Q % 1024 == 0 && OFF_SCALES % 16 == 0 && OFF_W % 16 == 0 && OFF_BARS % 8 == 0,
                 "alignment of the shared-memory regions");
 };
-
-// 4 e2m1 codes (low 16 bits of w, element 0 in the lowest nibble) -> 4 e4m3 bytes.
-// Magnitudes {0,.5,1,1.5,2,3,4,6} map to e4m3 codes {00,30,38,3C,40,44,48,4C}
-// through a byte permute; the sign bit moves from nibble bit 3 to byte bit 7.
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t w) {
-  uint32_t mag;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(mag) : "r"(0x3C383000u), "r"(0x4C484440u), "r"(w & 0x7777u));
-  const uint32_t sg = ((w & 0x8u) << 4) | ((w & 0x80u) << 8) | ((w & 0x800u) << 12) | ((w & 0x8000u) << 16);
-  return mag | sg;
-}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -256,8 +257,8 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   uint64_t* qfull = tempty + C::NACC;
   uint64_t* qempty = qfull + 2;
   uint64_t* drain = qempty + 2;               // [NMMA]
-  uint64_t* cvt = drain + C::NMMA;            // [STAGES] MXFP4: converted keys ready
-  uint64_t* sfull = cvt + C::STAGES;          // [SSLOTS] scales landed
+  uint64_t* sready = drain + C::NMMA;         // [STAGES] MXFP4: the stage's key exponents are in TMEM
+  uint64_t* sfull = sready + C::STAGES;       // [SSLOTS] scales landed
   uint64_t* sempty = sfull + C::SSLOTS;       // [SSLOTS] scales read by the epilogue
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);   // the MMA's commit (MXFP4: the converters finished before it)
+      mbar_init(&empty[s], 1);   // the MMA's commit
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       mbar_init(&qempty[i], C::NMMA + 8);   // every MMA warp's commit, every epilogue warp
     }
     for (int m = 0; m < C::NMMA; ++m) mbar_init(&drain[m], 1);
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(&cvt[s], C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&sready[s], C::SCALE_WARPS > 0 ? C::SCALE_WARPS : 1);
     for (int s = 0; s < C::SSLOTS; ++s) {
       mbar_init(&sfull[s], 1);
       mbar_init(&sempty[s], 4);   // the epilogue warps of the tile's set
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
             if (it >= C::SSLOTS && !(ok = mbar_wait(&sempty[ss], ((it / C::SSLOTS) - 1) & 1, ab))) break;
             const int* rows = rows_sm + jj * 8;
             const int64_t key0 = static_cast<int64_t>(i - grp.tile_begin) * kKeyTile;
-            constexpr int VB = C::MX ? kIdxDim / 2 : kIdxDim;   // value bytes per key in the page
+            constexpr int VB = C::MX ? kIdxDim / 2 : kIdxDim;   // value bytes per key in the page (counted)
             uint32_t nkeys = 0;
             for (int bx = 0; bx < nbox; ++bx)
               if (rows[bx] >= 0) nkeys += static_cast<uint32_t>(box);
@@ -489,8 +490,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
               if (row < 0) continue;
               const int64_t k0 = key0 + static_cast<int64_t>(bx) * box;
               const int slot0 = static_cast<int>(k0 & (bs - 1));
-              uint8_t* vdst = C::MX ? smem + C::OFF_PACK + s * C::PACK_BYTES + bx * box * VB
-                                    : smem + s * C::KEY_BYTES + bx * box * kIdxDim;
+              uint8_t* vdst = smem + s * C::KEY_BYTES + bx * box * kIdxDim;   // 128 B per key in shared memory
               tma_load_3d_hint(vdst, &kmap, &full[s], 0, slot0, row, stream_pol);
               const uint8_t* src = p.pool.pool + static_cast<int64_t>(row) * p.pool.row_stride + p.pool.idx_off +
                                    static_cast<int64_t>(bs) * VB + static_cast<int64_t>(slot0) * 4;
@@ -527,18 +527,23 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       if (lane == 0) {
         GroupCursor cur;
         cur.init(groups, ng, total, tile_lo);
-        uint32_t idesc = make_idesc(0, 0, false, false, kKeyTile, cur.grp.n * kIdxHeads);
+        auto idesc_of = [](int n) {
+          return C::MX ? make_idesc_bs(5, 0, kKeyTile, n * kIdxHeads, 0, 0)   // E2M1 keys, e4m3 queries
+                       : make_idesc(0, 0, false, false, kKeyTile, n * kIdxHeads);
+        };
+        uint32_t idesc = idesc_of(cur.grp.n);
         bool ok = mbar_wait(&qfull[0], 0, ab);
         for (int i = tile_lo; i < tile_hi && ok; ++i) {
           if (cur.advance(i)) {
-            idesc = make_idesc(0, 0, false, false, kKeyTile, cur.grp.n * kIdxHeads);
+            idesc = idesc_of(cur.grp.n);
             if (!(ok = mbar_wait(&qfull[cur.count & 1], (cur.count >> 1) & 1, ab))) break;
           }
           const int it = i - tile_lo;
           if (it % C::NMMA == mid) {
             const int s = it % C::STAGES;
             const int acc = it % C::NACC;
-            if (!(ok = mbar_wait_inline(C::MX ? &cvt[s] : &full[s], (it / C::STAGES) & 1, ab))) break;
+            if (!(ok = mbar_wait_inline(&full[s], (it / C::STAGES) & 1, ab))) break;
+            if (C::MX && !(ok = mbar_wait_inline(&sready[s], (it / C::STAGES) & 1, ab))) break;
             if (it >= C::NACC && !(ok = mbar_wait_inline(&tempty[acc], ((it / C::NACC) - 1) & 1, ab))) break;
             tc_fence_after();
             const uint32_t d = tmem + acc * C::ACC_COLS;
@@ -546,11 +551,15 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
             const uint32_t b0 = smem_u32(smem + C::OFF_Q + (cur.count & 1) * C::Q_BYTES);
 #pragma unroll
             for (int k = 0; k < kIdxDim / 32; ++k) {
-              // FP8: one accumulator over K = 128.  MXFP4: block k (dims 32k..32k+31) alone
-              // into accumulator k, scaled by its E8M0 exponent in the epilogue.
-              const uint32_t dk = C::MX ? d + k * (32 * G) : d;
-              mma_f8f6f4(dk, make_sdesc_sw128(a0 + 32 * k, 16, 1024), make_sdesc_sw128(b0 + 32 * k, 16, 1024), idesc,
-                         C::MX ? 0u : (k > 0 ? 1u : 0u));
+              // one accumulator over K = 128; MXFP4: block k (dims 32k..32k+31) scaled by
+              // byte k of each key's exponent cell
+              const uint64_t ad = make_sdesc_sw128(a0 + 32 * k, 16, 1024);
+              const uint64_t bd = make_sdesc_sw128(b0 + 32 * k, 16, 1024);
+              if (C::MX)
+                mma_mxf8f6f4_bs(d, ad, bd, idesc | (static_cast<uint32_t>(k) << 29), tmem + C::SFA_COL + 4 * s,
+                                tmem + C::SFB_COL, k > 0 ? 1u : 0u);
+              else
+                mma_f8f6f4(d, ad, bd, idesc, k > 0 ? 1u : 0u);
             }
             tc_commit(&empty[s]);
             tc_commit(&tfull[acc]);
@@ -563,30 +572,28 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         }
       }
     } else if (C::MX && warp >= 10 && warp < C::PROD_WARP0) {
-      // ------------------------------------------------- converters (MXFP4)
-      // Thread pair per key: packed e2m1 (64 B, row-major) -> e4m3 K-major,
-      // 128-byte swizzle, as the TMA would have laid out FP8 keys.
-      const int ct = threadIdx.x - 320;       // 0..255
-      const int row = ct >> 1, hf = ct & 1;
+      // ------------------------------------------------- scale warps (MXFP4)
+      // The warp of lane quarter q writes the E8M0 cells of keys 32q .. 32q+31 of
+      // each tile into TMEM (lane = key, column SFA_COL + 4 s + q: the layout the
+      // block-scaled MMA reads) once the stage's previous MMA is done with them,
+      // and, before its first tile, the query's unit scales in its quarter.
+      const int q = warp & 3;
+      const uint32_t lq = static_cast<uint32_t>(32 * q) << 16;
+      for (int c = 0; c < G; ++c) tmem_st1(tmem + lq + C::SFB_COL + c, 0x7F7F7F7Fu);   // 2^0 in every byte
       bool ok = true;
       for (int i = tile_lo; i < tile_hi && ok; ++i) {
         const int it = i - tile_lo;
-        const int s = it % C::STAGES;
-        if (!(ok = mbar_wait(&full[s], (it / C::STAGES) & 1, ab))) break;
-        const uint8_t* src = smem + C::OFF_PACK + s * C::PACK_BYTES + row * 64 + hf * 32;
-        uint8_t* dst = smem + s * C::KEY_BYTES + (row >> 3) * 1024;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(src + 8 * c4);   // 16 codes = dims 16c .. 16c+15
-          const int c = hf * 4 + c4;
-          const uint4 o = make_uint4(e2m1x4_to_e4m3x4(w.x), e2m1x4_to_e4m3x4(w.x >> 16), e2m1x4_to_e4m3x4(w.y),
-                                     e2m1x4_to_e4m3x4(w.y >> 16));
-          *reinterpret_cast<uint4*>(dst + sw128_off(row & 7, c)) = o;
-        }
-        fence_proxy_async_smem();
+        const int s = it % C::STAGES, ss = it % C::SSLOTS;
+        if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;
+        if (!(ok = mbar_wait(&sfull[ss], (it / C::SSLOTS) & 1, ab))) break;
+        const uint32_t e8 = reinterpret_cast<const uint32_t*>(smem + C::OFF_SCALES + ss * C::SCALE_BYTES)[32 * q + lane];
+        tmem_st1(tmem + lq + C::SFA_COL + 4 * s + q, e8);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&cvt[s]);
+        if (lane == 0) mbar_arrive(&sready[s]);
       }
+      tmem_wait_st();   // none in flight at the deallocation (also after an abort)
     } else {
       // ------------------------------------------------------------ epilogue
       // Two sets of four warps take alternate tiles; in a set, warp w reads TMEM
@@ -615,37 +622,12 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         const int qb = cur.count & 1;
         const int kloc = quarter * 32 + lane;
         const int key = (i - grp.tile_begin) * kKeyTile + kloc;
-        float scale = 1.f;
-        float bsc[4] = {1.f, 1.f, 1.f, 1.f};
-        if (C::MX) {
-          const uint32_t e8 = reinterpret_cast<const uint32_t*>(smem + C::OFF_SCALES + ss * C::SCALE_BYTES)[kloc];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const uint32_t e = (e8 >> (8 * b)) & 0xFFu;   // 2^(e-127); e = 0 is 2^-127, e = 255 NaN
-            bsc[b] = __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : e << 23));
-          }
-        } else {
-          scale = reinterpret_cast<const float*>(smem + C::OFF_SCALES + ss * C::SCALE_BYTES)[kloc];
-        }
+        // FP8: the key's fp32 scale; MXFP4: already applied by the MMA
+        const float scale = C::MX ? 1.f : reinterpret_cast<const float*>(smem + C::OFF_SCALES + ss * C::SCALE_BYTES)[kloc];
         for (int j = 0; j < grp.n; ++j) {
           uint32_t r[32];
           DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + j * kIdxHeads + (static_cast<uint32_t>(quarter * 32) << 16), r);
           tmem_wait_ld();
-          if (C::MX) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bsc[0]);
-#pragma unroll
-            for (int b = 1; b < 4; ++b) {
-              uint32_t rb[32];
-              DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + b * (32 * G) + j * kIdxHeads +
-                                (static_cast<uint32_t>(quarter * 32) << 16),
-                            rb);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                r[i] = __float_as_uint(fmaf(__uint_as_float(rb[i]), bsc[b], __uint_as_float(r[i])));
-            }
-          }
           const float4* wv = reinterpret_cast<const float4*>(wsm + (qb * G + j) * kIdxHeads);
           float sum = 0.f;
           if (scale >= 0.f) {

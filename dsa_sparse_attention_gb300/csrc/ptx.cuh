@@ -296,6 +296,34 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
       : "memory");
 }
 
+// D(tmem) (+)= sum over the 32-wide K blocks of SFA * SFB * (A_blk * B_blk): 8/6/4-bit
+// operands with UE8M0 block scales read from TMEM (kind::mxf8f6f4, one scale per
+// row and operand for the instruction's K = 32).  Scale layout, per operand: the
+// scale of row r (A: M index; B: N index) is byte `id` of the 32-bit TMEM cell at
+// column sf + r / 32, lane 32 q + r % 32, where q is the lane quarter of the output
+// row being computed (A: q = r / 32; B: the same copy in every quarter).
+__device__ __forceinline__ void mma_mxf8f6f4_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], "
+      "%1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4.block_scale (fp32 D, UE8M0 scales):
+// formats as make_idesc; a_id / b_id pick the byte of each operand's scale cell.
+__host__ __device__ constexpr uint32_t make_idesc_bs(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N,
+                                                     uint32_t a_id, uint32_t b_id) {
+  return (b_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+         (a_id << 29);
+}
+
+// One 32-bit TMEM column of the calling warp's lane quarter (thread i: lane quarter*32 + i).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
 // Instruction descriptor (kind::f16 / kind::f8f6f4, dense).  Formats:
 //   D: 1 = f32.  A/B for kind::f16: 0 = f16, 1 = bf16; for kind::f8f6f4: 0 = e4m3, 5 = e2m1.
 //   *_mn: operand is MN-major (else K-major).

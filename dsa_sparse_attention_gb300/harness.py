@@ -68,15 +68,23 @@ class HostStep:
     packed=True lays the inputs out back to back, in the order DSA_HOST_PACKED
     names, in one host buffer and one device buffer, and sets that flag (the call
     moves them with one copy); packed=False gives every input its own allocation
-    on both sides and one copy each."""
+    on both sides and one copy each.  pinned=False keeps the host side in pageable
+    memory; misalign > 0 (a multiple of 4) starts every host array that many bytes
+    into its allocation."""
 
-    def __init__(self, dw, packed=True, with_lse=True, with_idx=True):
+    def __init__(self, dw, packed=True, with_lse=True, with_idx=True, pinned=True, misalign=0):
         self.dw = dw
         src = [dw.q.view(torch.uint8), dw.q_idx, dw.w, dw.q_req, dw.q_pos, dw.ctx, dw.bt]
         sizes = [t.numel() * t.element_size() for t in src]
+        def host_empty(shape, dtype):
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            buf = torch.empty(n + misalign, dtype=torch.uint8)
+            buf = buf.pin_memory() if pinned else buf
+            return buf[misalign:].view(dtype).view(shape)
+
         if packed:
             dev_all = torch.empty(sum(sizes), dtype=torch.uint8, device=dw.device)
-            host_all = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+            host_all = host_empty((sum(sizes),), torch.uint8)
             dev, host, off = [], [], 0
             for t, n in zip(src, sizes):
                 dev.append(dev_all[off:off + n].view(t.dtype).view(t.shape))
@@ -85,7 +93,7 @@ class HostStep:
             self._keep = (dev_all, host_all)
         else:
             dev = [torch.empty_like(t) for t in src]
-            host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in src]
+            host = [host_empty(t.shape, t.dtype) for t in src]
         for h, t in zip(host, src):
             h.copy_(t.cpu())
         self.dev, self.host = dev, host
@@ -96,9 +104,9 @@ class HostStep:
         self.out = torch.empty(T, 96, 512, dtype=torch.bfloat16, device=dw.device)
         self.lse = torch.empty(T, 96, dtype=torch.float32, device=dw.device) if with_lse else None
         self.idx = torch.empty(T, dw.topk, dtype=torch.int32, device=dw.device) if with_idx else None
-        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.lse_host = torch.empty(T, 96, dtype=torch.float32).pin_memory() if with_lse else None
-        self.idx_host = torch.empty(T, dw.topk, dtype=torch.int32).pin_memory() if with_idx else None
+        self.out_host = host_empty(self.out.shape, self.out.dtype)
+        self.lse_host = host_empty((T, 96), torch.float32) if with_lse else None
+        self.idx_host = host_empty((T, dw.topk), torch.int32) if with_idx else None
         self.io = make_host_io(host[1], host[2], host[0], host[3], host[4], host[5], host[6], self.out_host,
                                self.lse_host, self.idx_host, packed=packed)
         self._calls = {}

@@ -77,7 +77,8 @@ enum { DSA_LAT_FP8 = 0, DSA_LAT_NVFP4 = 1 };  /* latent page formats */
  *          (scale j covers dims 16j..16j+15), 28 bytes of padding (352 B/token)
  * Token s of request b lives in row block_table[b][s / block_size], slot
  * s % block_size.  pool, row_stride_bytes and both offsets must be multiples of
- * 16 bytes.  Index-key scales must be finite; latents and keys must hold no NaN
+ * 16 bytes; with MXFP4 index keys pool, row_stride_bytes and idx_page_offset must
+ * be multiples of 32 bytes.  Index-key scales must be finite; latents and keys must hold no NaN
  * codes.  The pool is device memory owned by the caller and only read.
  */
 typedef struct {

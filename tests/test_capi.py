@@ -73,6 +73,15 @@ def test_host_validation_errors(lib):
     assert _call_step(_layout(), _batch(), q=0x60008) == -1            # misaligned q
     assert _call_step(_layout(idx_fmt=7), _batch()) == -1
     assert _call_step(_layout(block_size=512), _batch()) == -2
+    # MXFP4 index pages (read by a packed 4-bit tensor copy) need 32-byte alignment of
+    # the pool, the row stride and the index page; FP8 ones only 16
+    mx = dict(idx_fmt=1, row_stride=4352 + 36864, lat_page_offset=4352)
+    assert dsa.dsa_workspace_size(_layout(**mx), _batch(), 2048) > 0
+    assert dsa.dsa_workspace_size(_layout(**dict(mx, row_stride=4352 + 36864 + 16)), _batch(), 2048) == 0
+    assert dsa.dsa_workspace_size(_layout(**dict(mx, idx_page_offset=16, lat_page_offset=4368,
+                                                 row_stride=4352 + 36864 + 32)), _batch(), 2048) == 0
+    assert dsa.dsa_workspace_size(_layout(row_stride=45312 + 16), _batch(), 2048) > 0
+    assert _call_step(_layout(pool=0x10010, **mx), _batch()) == -1
     L = dsa.library()
     assert L.dsa_layer_step(None, ctypes.byref(_batch()), 0, 0, 0, 2048, 1.0, None, 0, None, 0, 0, None) == -1
     assert L.dsa_topk(None, ctypes.byref(_batch()), 0x1000, 1000, 0, 0x2000, None, 0x100000, 1 << 30, None) == -1

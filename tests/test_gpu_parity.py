@@ -377,18 +377,27 @@ def test_full_cfg3_decode_1m_mxfp4_nvfp4():
     print(r)
 
 
-@pytest.mark.parametrize("packed", [True, False])
-def test_layer_step_from_host_buffers(packed):
+@pytest.mark.parametrize("packed,pinned,misalign,lens", [
+    (True, True, 0, [5000, 1, 2049, 300]),
+    (False, True, 0, [5000, 1, 2049, 300]),
+    (False, False, 0, [5000, 1, 2049, 300]),
+    (True, True, 0, [700, 3001, 1]),
+    (False, True, 4, [700, 3001, 1]),
+    (True, True, 4, [700, 3001, 1]),
+])
+def test_layer_step_from_host_buffers(packed, pinned, misalign, lens):
     # the host-buffer call copies in, runs the same step and copies out: its host
-    # results equal the device call's bit for bit (inputs packed into one buffer
-    # each side, so they move as one copy, or each in its own allocation)
+    # results equal the device call's bit for bit.  Inputs packed into one buffer
+    # each side (one copy) or each in its own allocation; page-locked host memory
+    # (moved by the library's copy kernel) or pageable (cudaMemcpyAsync); host
+    # arrays 16-byte aligned or 4 bytes off; three tokens leave byte tails (12-byte
+    # position arrays, a packed total that is not a multiple of 16)
     from dsa_sparse_attention_gb300 import dsa_check
     from dsa_sparse_attention_gb300.harness import HostStep
-    lens = [5000, 1, 2049, 300]
     wl = W.make_workload(lens, 1, seed=17, permute=True, pool_rows=120)
     dw = _dev(wl)
     idx, out, lse = (_np(x) for x in dw.layer_step())
-    hs = HostStep(dw, packed=packed)
+    hs = HostStep(dw, packed=packed, pinned=pinned, misalign=misalign)
     for t in hs.dev:   # the step must read what the call copied in, not what was there
         t.zero_()
     torch.cuda.synchronize()
