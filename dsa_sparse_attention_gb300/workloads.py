@@ -27,6 +27,7 @@ import numpy as np
 import torch
 
 IDX_FP8, IDX_MXFP4 = 0, 1
+Q_FP8, Q_MXFP4 = 0, 1               # index-query formats
 LAT_FP8, LAT_NVFP4 = 0, 1
 _IDX_TOKEN_BYTES = {IDX_FP8: 132, IDX_MXFP4: 68}
 _LAT_TOKEN_BYTES = {LAT_FP8: 576, LAT_NVFP4: 352}
@@ -121,12 +122,13 @@ class Workload:
     ctx_lens: np.ndarray        # int32 [B]
     q_req: np.ndarray           # int32 [T]
     q_pos: np.ndarray           # int32 [T]
-    q_idx: np.ndarray           # uint8 e4m3 [T, 32, 128]
+    q_idx: np.ndarray           # uint8 e4m3 [T, 32, 128]; MXFP4 queries: [T * 32 * 68] (codes, then E8M0)
     w: np.ndarray               # float32 [T, 32]
     q: np.ndarray               # uint16 bf16 bits [T, 96, 576]
     topk: int = 2048
     sm_scale: float = 1.0 / 24.0
     meta: dict = field(default_factory=dict)
+    q_fmt: int = Q_FP8
 
     @property
     def num_tokens(self):
@@ -147,7 +149,7 @@ def _streams(seed: int, n: int = 10):
 
 def make_workload(ctx_lens, q_per_req=1, *, name="custom", seed=0, idx_fmt=IDX_FP8,
                   lat_fmt=LAT_FP8, block_size=64, pool_rows=None, row_stride=None,
-                  permute=True, topk=2048, q_pos=None, bt_stride=None, negative_scale_frac=0.0):
+                  permute=True, topk=2048, q_pos=None, bt_stride=None, negative_scale_frac=0.0, q_fmt=Q_FP8):
     """Build a workload.
 
     ctx_lens: tokens in cache per request (including that request's query tokens).
@@ -159,6 +161,8 @@ def make_workload(ctx_lens, q_per_req=1, *, name="custom", seed=0, idx_fmt=IDX_F
     negative_scale_frac: fraction of FP8 index keys whose fp32 scale is negated
       (magnitudes still U(0.5, 2)); 0 keeps every scale positive.  The signs come
       from their own random stream, so the other tensors do not change with it.
+    q_fmt: Q_MXFP4 draws the index queries N(0,1) and stores them MXFP4 in the
+      library's query layout: T x 32 x 64 packed e2m1 bytes, then T x 32 x 4 E8M0.
     """
     rs = _streams(seed)
     ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
@@ -223,14 +227,19 @@ def make_workload(ctx_lens, q_per_req=1, *, name="custom", seed=0, idx_fmt=IDX_F
         q_pos_arr = np.concatenate([np.asarray(q_pos[b]) for b in range(B)])
     q_pos_arr = q_pos_arr.astype(np.int32)
     T = q_req.size
-    q_idx = to_e4m3(np.clip(rs[4].standard_normal((T, 32, 128), dtype=np.float32), -8, 8))
+    qd = rs[4].standard_normal((T, 32, 128), dtype=np.float32)
+    if q_fmt == Q_MXFP4:
+        packed, e8 = quantize_mxfp4(qd.reshape(T * 32, 128))
+        q_idx = np.concatenate([packed.reshape(-1), e8.reshape(-1)])
+    else:
+        q_idx = to_e4m3(np.clip(qd, -8, 8))
     w = (rs[5].standard_normal((T, 32)) * np.sqrt(1.0 / 32.0)).astype(np.float32)
     q = to_bf16_bits(rs[6].standard_normal((T, 96, 576), dtype=np.float32))
     return Workload(name=name, pool=pool, num_rows=pool_rows, row_stride=row_stride,
                     idx_page_offset=0, lat_page_offset=idx_pb, block_size=bs,
                     idx_fmt=idx_fmt, lat_fmt=lat_fmt, block_table=bt,
                     ctx_lens=ctx_lens.astype(np.int32), q_req=q_req, q_pos=q_pos_arr,
-                    q_idx=q_idx, w=w, q=q, topk=int(topk))
+                    q_idx=q_idx, w=w, q=q, topk=int(topk), q_fmt=int(q_fmt))
 
 
 # --------------------------------------------------- the five configurations

@@ -35,6 +35,15 @@ Byte layout read here (the same contract the library header states):
      NVFP4: bs x 352 bytes per token = 288 packed e2m1 bytes, 36 e4m3 scales
             (scale j covers dims 16j .. 16j+15), 28 zero bytes of padding
   token s of request b lives in row block_table[b, s // bs], slot s % bs.
+
+Index queries ("Low-latency decode: a fused DSA decode path": the indexer query
+is quantized to FP8 or MXFP4):
+     FP8  : e4m3 codes [T, 32, 128], used as-is (a per-head scale is folded
+            into the head weights)
+     MXFP4: T x 32 x 64 packed e2m1 bytes (element 2i in the low nibble), then
+            T x 32 x 4 E8M0 bytes (scale j covers dims 32j .. 32j+31); per token
+            the oracle takes them as [32, 68]: a head's 64 code bytes, then its 4
+            exponents (``mxfp4_query_tokens``).
 """
 import numpy as np
 
@@ -42,6 +51,7 @@ from .formats import decode_e4m3, decode_e2m1, decode_e8m0, decode_bf16, unpack_
 
 IDX_FP8, IDX_MXFP4 = 0, 1
 LAT_FP8, LAT_NVFP4 = 0, 1
+Q_FP8, Q_MXFP4 = 0, 1
 H_IDX, D_IDX = 32, 128          # indexer heads x dims
 H_MLA, D_LAT, D_V = 96, 576, 512  # MLA heads, latent dims, value dims
 
@@ -181,19 +191,45 @@ def gather_latents(layout: Layout, bt_row: np.ndarray, tokens: np.ndarray) -> np
 
 # ------------------------------------------------------------------ indexer
 
-def indexer_scores_for_token(keys: np.ndarray, q_idx_codes: np.ndarray, w: np.ndarray) -> np.ndarray:
+def mxfp4_query_tokens(buf: np.ndarray, T: int) -> np.ndarray:
+    """The library's MXFP4 query buffer (T x 32 x 64 code bytes, then T x 32 x 4
+    E8M0 bytes) -> per token [T, 32, 68]: each head's 64 code bytes, then its 4
+    exponents."""
+    buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    codes = buf[:T * H_IDX * 64].reshape(T, H_IDX, 64)
+    e8 = buf[T * H_IDX * 64:T * H_IDX * 68].reshape(T, H_IDX, 4)
+    return np.concatenate([codes, e8], axis=2)
+
+
+def decode_query(q_idx_token: np.ndarray, q_fmt: int = Q_FP8) -> np.ndarray:
+    """One token's index query -> float64 [32, 128].  FP8: the e4m3 codes [32, 128]
+    as-is; MXFP4: [32, 68] per head 64 packed e2m1 bytes and 4 E8M0 exponents, the
+    value e2m1(code) * 2^(E - 127) with exponent j covering dims 32j .. 32j+31 (the
+    MX block format the post names for the indexer, as for the MXFP4 keys)."""
+    if q_fmt == Q_FP8:
+        return decode_e4m3(np.asarray(q_idx_token).reshape(H_IDX, D_IDX))
+    if q_fmt == Q_MXFP4:
+        t = np.asarray(q_idx_token, dtype=np.uint8).reshape(H_IDX, 68)
+        vals = decode_e2m1(unpack_nibbles(t[:, :64]))
+        return vals * np.repeat(decode_e8m0(t[:, 64:68]), 32, axis=1)
+    raise ValueError("unknown index-query format")
+
+
+def indexer_scores_for_token(keys: np.ndarray, q_idx_codes: np.ndarray, w: np.ndarray,
+                             q_fmt: int = Q_FP8) -> np.ndarray:
     """score[s] = sum_h w[h] * max(0, q_idx[h] . k[s]) for every row of ``keys``
     ("Sparse Attention in K3.1 Pro": each earlier token is scored with 32 light
     heads against its index key; the formula is the plain reading of that prose).
 
-    keys: float64 [n, 128] dequantised index keys; q_idx_codes: uint8 e4m3 codes
-    [32, 128] (used as-is: any query-side scale is folded into w); w: [32]."""
-    q = decode_e4m3(np.asarray(q_idx_codes).reshape(H_IDX, D_IDX))
+    keys: float64 [n, 128] dequantised index keys; q_idx_codes: one token's index
+    query in format q_fmt (see decode_query; FP8 codes are used as-is: any
+    query-side scale is folded into w); w: [32]."""
+    q = decode_query(q_idx_codes, q_fmt)
     dots = keys @ q.T                       # [n, 32]
     return np.maximum(dots, 0.0) @ np.asarray(w, dtype=np.float64).reshape(H_IDX)
 
 
-def indexer_scores(layout: Layout, block_table, q_req, q_pos, q_idx, w):
+def indexer_scores(layout: Layout, block_table, q_req, q_pos, q_idx, w, q_fmt=Q_FP8):
     """Scores of every token of a batch: list over query tokens of float64 arrays
     of length q_pos[t] + 1 (positions 0 .. q_pos[t] of its request: "every earlier
     token", inclusive because the new token's key is written before scoring, per
@@ -204,7 +240,7 @@ def indexer_scores(layout: Layout, block_table, q_req, q_pos, q_idx, w):
         b, p = int(q_req[t]), int(q_pos[t])
         if b not in cache or cache[b].shape[0] < p + 1:
             cache[b] = gather_index_keys(layout, block_table[b], p + 1)
-        out.append(indexer_scores_for_token(cache[b][:p + 1], q_idx[t], w[t]))
+        out.append(indexer_scores_for_token(cache[b][:p + 1], q_idx[t], w[t], q_fmt))
     return out
 
 
@@ -254,13 +290,15 @@ def sparse_mla(q_bf16: np.ndarray, latents: np.ndarray, sm_scale: float):
 # --------------------------------------------------------------- layer step
 
 def layer_step(layout: Layout, block_table, ctx_lens, q_req, q_pos, q_idx, w, q,
-               topk=2048, sm_scale=1.0 / 24.0, tokens=None):
+               topk=2048, sm_scale=1.0 / 24.0, tokens=None, q_fmt=Q_FP8):
     """One DSA layer for the query tokens listed in ``tokens`` (default: all):
     indexer scores, exact top-k, sparse MLA, in the order of Figure 1 of "Sparse
     Attention in K3.1 Pro".
 
     Returns dict with per-token lists: 'scores' (float64 arrays), 'idx' (selected
-    positions, ascending), and arrays 'out' [n, 96, 512], 'lse' [n, 96]."""
+    positions, ascending), and arrays 'out' [n, 96, 512], 'lse' [n, 96].
+    q_idx holds one entry per token in format q_fmt (MXFP4: [T, 32, 68], see
+    mxfp4_query_tokens)."""
     T = len(q_req)
     tokens = list(range(T)) if tokens is None else list(tokens)
     res = {"tokens": tokens, "scores": [], "idx": [], "out": [], "lse": []}
@@ -271,7 +309,7 @@ def layer_step(layout: Layout, block_table, ctx_lens, q_req, q_pos, q_idx, w, q,
             raise ValueError(f"token {t}: position {p} outside context {ctx_lens[b]}")
         if b not in key_cache or key_cache[b].shape[0] < p + 1:
             key_cache[b] = gather_index_keys(layout, block_table[b], p + 1)
-        sc = indexer_scores_for_token(key_cache[b][:p + 1], q_idx[t], w[t])
+        sc = indexer_scores_for_token(key_cache[b][:p + 1], q_idx[t], w[t], q_fmt)
         sel = topk_select(sc, topk)
         lat = gather_latents(layout, block_table[b], sel)
         o, l = sparse_mla(q[t], lat, sm_scale)

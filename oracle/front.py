@@ -21,6 +21,12 @@ library's header as well):
   computed in fp32 (1 when zero), codes = e4m3(fp32(k) / s_k), written at the
   token's slot of its block's index page (132 bytes: 128 codes, then the scale
   in the page's scale area);
+* MXFP4 quantization (of the query per (token, head), and of the new token's
+  index key when the pool holds MXFP4 keys), per block of 32 dims with the OCP MX
+  rule: E = floor(log2(max|x|)) - 2 + 127 (2 is the largest e2m1 exponent),
+  clamped to 0 .. 254, E = 0 for an all-zero block; codes = e2m1(x * 2^(127 - E))
+  rounded to nearest even and saturated at +-6; the exponents travel with the
+  codes (E8M0), so the head weights stay as given;
 * the new token's latent: FP8 pages hold e4m3(x) (no scale); NVFP4 records hold,
   per 16 values, the scale e4m3(max|x| / 6) and e2m1(x / scale), packed two per
   byte (element 2i in the low nibble), 36 scale bytes, 28 zero bytes.
@@ -86,10 +92,43 @@ def quantize_query_fp8(q):
     return encode_e4m3(q / s[:, None]), s
 
 
-def indexer_front(c_q_bf16, gamma_bf16, w_qi_bf16, head_w, eps):
-    """One token's q_idx codes [32, 128] and folded head weights w' [32]
-    (float64), plus the scales and the unquantized query for the parity check."""
+def mx_exponents(x):
+    """E8M0 exponents of the 32-value blocks along the last axis of x [..., 32 m]:
+    floor(log2(max|x|)) - 2 + 127 clamped to 0 .. 254, 0 for an all-zero block."""
+    x = np.asarray(x, dtype=np.float64)
+    blocks = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    amax = np.abs(blocks).max(axis=-1)
+    _, ex = np.frexp(amax)                 # amax = f * 2^ex, 0.5 <= f < 1: floor(log2 amax) = ex - 1
+    e = np.where(amax > 0, ex - 1 - 2 + 127, 0)
+    return np.clip(e, 0, 254).astype(np.uint8)
+
+
+def quantize_mxfp4(x):
+    """MXFP4 of x [..., 128] (float64 or float32 values): (packed codes [..., 64],
+    element 2i in the low nibble; E8M0 [..., 4]).  The scaling by 2^(127 - E) is
+    exact, so the arithmetic's width does not matter."""
+    x = np.asarray(x, dtype=np.float64)
+    e = mx_exponents(x)
+    scale = np.repeat(np.ldexp(1.0, 127 - e.astype(np.int64)), 32, axis=-1)
+    codes = encode_e2m1(x * scale)
+    return (codes[..., 0::2] & 0xF) | ((codes[..., 1::2] & 0xF) << 4), e
+
+
+def quantize_query_mxfp4(q):
+    """Per-(head, 32-dim block) MXFP4 quantization of q [32, 128]: the library's
+    per-token query form [32, 68] (each head's 64 code bytes, then its 4 E8M0)."""
+    packed, e = quantize_mxfp4(q)
+    return np.concatenate([packed, e], axis=1).astype(np.uint8)
+
+
+def indexer_front(c_q_bf16, gamma_bf16, w_qi_bf16, head_w, eps, q_fmt=0):
+    """One token's index query and head weights, plus the scales and the
+    unquantized query for the parity check.  FP8 (q_fmt 0): codes [32, 128], w'
+    = w * s folded (float64), s [32].  MXFP4 (q_fmt 1): [32, 68] (codes and E8M0),
+    w unchanged, s = None."""
     q = indexer_query(c_q_bf16, gamma_bf16, w_qi_bf16, eps)
+    if q_fmt == 1:
+        return quantize_query_mxfp4(q), np.asarray(head_w, dtype=np.float64), None, q
     codes, s = quantize_query_fp8(q)
     return codes, np.asarray(head_w, dtype=np.float64) * s, s, q
 
@@ -101,6 +140,13 @@ def index_key_fp8(k_bf16):
     amax = np.float32(np.abs(k).max())
     s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
     return encode_e4m3((k / s).astype(np.float64)), s
+
+
+def index_key_mxfp4(k_bf16):
+    """The new token's MXFP4 index key: (packed codes uint8 [64], E8M0 uint8 [4]).
+    bf16 inputs are exact in fp32 and the scaling is by a power of two, so this
+    equals the fp32 computation."""
+    return quantize_mxfp4(decode_bf16(k_bf16).reshape(128))
 
 
 def latent_record(x_bf16, lat_fmt):
@@ -130,6 +176,14 @@ def write_index_key(pool, row_stride, idx_page_offset, bs, row, slot, codes, sca
     base = int(row) * row_stride + idx_page_offset
     pool[base + slot * 128: base + slot * 128 + 128] = codes
     pool[base + bs * 128 + slot * 4: base + bs * 128 + slot * 4 + 4] = np.float32(scale).reshape(1).view(np.uint8)
+
+
+def write_index_key_mxfp4(pool, row_stride, idx_page_offset, bs, row, slot, packed, e8):
+    """Place an MXFP4 key in its block's index page: 64 code bytes at slot * 64,
+    the 4 exponents at bs * 64 + slot * 4 (the library's index-page layout)."""
+    base = int(row) * row_stride + idx_page_offset
+    pool[base + slot * 64: base + slot * 64 + 64] = packed
+    pool[base + bs * 64 + slot * 4: base + bs * 64 + slot * 4 + 4] = e8
 
 
 def write_latent(pool, row_stride, lat_page_offset, row, slot, record):

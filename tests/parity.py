@@ -35,6 +35,9 @@ class OracleCache:
         self.lay = oracle_layout(wl)
         self._keys = {}
         self._scores = {}
+        self.q_fmt = getattr(wl, "q_fmt", O.Q_FP8)
+        # one entry per token in the oracle's per-token query form
+        self.q_tok = (O.mxfp4_query_tokens(wl.q_idx, wl.num_tokens) if self.q_fmt == O.Q_MXFP4 else wl.q_idx)
 
     def keys(self, b, n):
         # one request's keys at a time (contexts of the large workloads are big)
@@ -46,7 +49,7 @@ class OracleCache:
         if t not in self._scores:
             wl = self.wl
             b, p = int(wl.q_req[t]), int(wl.q_pos[t])
-            self._scores[t] = O.indexer_scores_for_token(self.keys(b, p + 1), wl.q_idx[t], wl.w[t])
+            self._scores[t] = O.indexer_scores_for_token(self.keys(b, p + 1), self.q_tok[t], wl.w[t], self.q_fmt)
         return self._scores[t]
 
     def mla(self, t, sel):

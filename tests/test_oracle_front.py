@@ -11,6 +11,7 @@ import torch
 from oracle import dsa_oracle as O
 from oracle import front as F
 from oracle.formats import E4M3_TABLE, decode_e4m3
+from dsa_sparse_attention_gb300 import workloads as W
 
 
 def _bf16(x):
@@ -110,3 +111,91 @@ def test_index_key_and_latent_writes_read_back():
     lay4 = O.Layout(pool4, wl4.row_stride, wl4.idx_page_offset, wl4.lat_page_offset, 64, lat_fmt=1)
     back = O.gather_latents(lay4, wl4.block_table[0], np.array([pos]))[0]
     np.testing.assert_array_equal(back[:18], y[:18].astype(np.float64))
+
+
+# ------------------------------------------------------------------ MXFP4
+
+def test_mx_exponent_rule_hand_worked():
+    # OCP MX: E = floor(log2 max|x|) - 2 + 127 per 32 values (2 = the largest e2m1
+    # exponent, so the block's largest value lands in [4, 8) before saturation at 6)
+    x = np.zeros(128)
+    x[0], x[1], x[2] = 0.75, 0.3, -0.1875          # block 0: floor(log2 .75) = -1 -> E = 124, scale 1/8
+    x[32] = 6.0                                      # block 1: E = 127, 6 exactly
+    x[64] = -7.0                                     # block 2: E = 127, 7 saturates to 6
+    packed, e = F.quantize_mxfp4(x)                  # block 3: all zero -> E = 0
+    assert e.tolist() == [124, 127, 127, 0]
+    # 0.75 * 8 = 6 -> code 7; 0.3 * 8 = 2.4 -> 2 (code 4); -0.1875 * 8 = -1.5 -> code 0x8 | 3
+    assert packed[0] == (7 | 4 << 4) and packed[1] == (0x8 | 3)
+    assert packed[16] == 7 and packed[32] == 0x8 | 7 and np.count_nonzero(packed) == 4
+    # powers of two at the boundary: max|x| = 4 -> E = 127; just below 4 -> E = 126 (scale 2)
+    assert F.mx_exponents(np.r_[4.0, np.zeros(31)]).tolist() == [127]
+    assert F.mx_exponents(np.r_[np.nextafter(4.0, 0), np.zeros(31)]).tolist() == [126]
+    assert F.mx_exponents(np.r_[1e-45, np.zeros(31)]).tolist() == [0]    # clamped at the bottom
+
+
+def test_mxfp4_quantizer_roundtrips_representable_blocks():
+    # a block of e2m1 values times 2^j, whose largest magnitude is 4 or 6, comes back
+    # exactly with E = 127 + j (decoded by the oracle's own, separately pinned readers)
+    rng = np.random.default_rng(5)
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6])
+    for j in (-20, -3, 0, 5, 40):
+        v = rng.choice(grid, size=(32, 128)) * rng.choice([-1, 1], size=(32, 128))
+        v[:, ::32] = 6.0                                          # each block's max
+        tok = F.quantize_query_mxfp4(np.ldexp(v, j))
+        assert np.all(tok[:, 64:] == 127 + j)
+        np.testing.assert_array_equal(O.decode_query(tok, O.Q_MXFP4), np.ldexp(v, j))
+
+
+def test_mxfp4_query_error_within_half_a_step():
+    # scaled by 2^(127-E) every value lies in [0, 8); the e2m1 grid spacing is 0.5 below
+    # 2, 1 below 4 and 2 up to 6, so rounding errs by at most half of it, and values in
+    # (6, 8) saturate to 6; large random queries over a wide range of magnitudes
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((32, 128)) * np.exp(rng.uniform(-5, 5, size=(32, 1)))
+    tok = F.quantize_query_mxfp4(q)
+    back = O.decode_query(tok, O.Q_MXFP4)
+    unit = np.repeat(np.ldexp(1.0, tok[:, 64:].astype(int) - 127), 32, axis=1)
+    v = np.abs(q) / unit
+    assert np.all(v < 8)
+    bound = np.where(v < 2, 0.25, np.where(v < 4, 0.5, np.where(v <= 6, 1.0, v - 6)))
+    assert np.all(np.abs(back - q) <= bound * unit * (1 + 1e-12))
+
+
+def test_mxfp4_query_buffer_layout_and_score():
+    # the library's buffer: T x 32 x 64 code bytes, then T x 32 x 4 exponents; a
+    # hand-worked score: head 0 = 1.5 * 2^-2 at dim 0 and head 1 = -3 at dim 40,
+    # key = (2, 0, ..., dim 40 = 0.5), w = (1, 0.25, 0 ...): score = 1 * ReLU(0.75)
+    # + 0.25 * ReLU(-1.5) = 0.75
+    T = 2
+    codes = np.zeros((T, 32, 64), np.uint8)
+    e8 = np.full((T, 32, 4), 127, np.uint8)
+    codes[1, 0, 0] = 3                               # token 1, head 0, dim 0: e2m1 1.5
+    e8[1, 0, 0] = 125                                #   block 0 of head 0: 2^-2
+    codes[1, 1, 20] = 0x8 | 5                        # head 1, dim 40 (low nibble of byte 20): -3
+    buf = np.concatenate([codes.reshape(-1), e8.reshape(-1)])
+    tok = O.mxfp4_query_tokens(buf, T)
+    assert tok.shape == (T, 32, 68) and np.all(tok[0] == np.r_[np.zeros(64), np.full(4, 127)])
+    key = np.zeros((1, 128))
+    key[0, 0], key[0, 40] = 2.0, 0.5
+    w = np.zeros(32)
+    w[0], w[1] = 1.0, 0.25
+    assert O.indexer_scores_for_token(key, tok[1], w, O.Q_MXFP4).tolist() == [0.75]
+    assert O.indexer_scores_for_token(key, tok[0], w, O.Q_MXFP4).tolist() == [0.0]
+
+
+def test_mxfp4_key_write_reads_back():
+    # the new token's MXFP4 key written into a page and read back by the page reader
+    wl = W.make_workload([200], 1, seed=9, idx_fmt=W.IDX_MXFP4)
+    pool = wl.pool.copy()
+    k = np.random.default_rng(3).standard_normal(128).astype(np.float32)
+    kb = _bf16(k)
+    packed, e8 = F.index_key_mxfp4(kb)
+    row, slot = int(wl.block_table[0, 3]), 7
+    F.write_index_key_mxfp4(pool, wl.row_stride, wl.idx_page_offset, 64, row, slot, packed, e8)
+    lay = O.Layout(pool, wl.row_stride, wl.idx_page_offset, wl.lat_page_offset, 64, idx_fmt=O.IDX_MXFP4)
+    got = O.gather_index_keys(lay, wl.block_table[0], 200)[3 * 64 + slot]
+    want = O.decode_query(np.r_[packed, e8].reshape(1, 68).repeat(32, 0), O.Q_MXFP4)[0]
+    np.testing.assert_array_equal(got, want)
+    kf = torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).float().numpy().astype(np.float64)
+    unit = np.repeat(np.ldexp(1.0, e8.astype(int) - 127), 32)
+    assert np.all(np.abs(got - kf) <= unit)
