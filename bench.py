@@ -127,7 +127,8 @@ def algorithmic_bytes(wl, idx):
 
 def scorer_bytes(wl):
     key_b = 132 if wl.idx_fmt == 0 else 68
-    return int(sum(int(L) for L in wl.ctx_lens)) * key_b + wl.num_tokens * (4096 + 128)
+    q_b = 32 * 68 if getattr(wl, "q_fmt", 0) == 1 else 4096   # MXFP4 or e4m3 index query
+    return int(sum(int(L) for L in wl.ctx_lens)) * key_b + wl.num_tokens * (q_b + 128)
 
 
 class ClockSampler:
@@ -357,6 +358,21 @@ def measure_config(n, args, stream, flush, hbm_gbs, bf16_tflops, cpu=True):
         out["mxfp4_vs_fp8_keys"] = {"scorer_ms_mxfp4": sc_ms, "scorer_ms_fp8": f_ms, "speedup": f_ms / sc_ms,
                                     "fp8_gbs": scorer_bytes(wf) / (f_ms * 1e-3) / 1e9}
         del df, sf, fg
+        # the same MXFP4 keys scored by MXFP4 queries (DSA_BATCH_QIDX_MXFP4: E2M1 x E2M1
+        # block-scaled MMA, both operands' exponents from TMEM)
+        wq = W.make_workload([1 << 20], 1, name="decode_L1M_mxfp4_queries", seed=0, idx_fmt=W.IDX_MXFP4,
+                             lat_fmt=W.LAT_NVFP4, permute=True, q_fmt=W.Q_MXFP4)
+        dq = DeviceWorkload(wq)
+        sq = torch.empty(1, dq.ld, dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                dsa.dsa_indexer_score(dq.layout, dq.batch, dq.q_idx, dq.w, sq, dq.ld, dq.ws, stream)
+        qg = graph_of(lambda: dsa.dsa_indexer_score(dq.layout, dq.batch, dq.q_idx, dq.w, sq, dq.ld, dq.ws,
+                                                    torch.cuda.current_stream()))
+        q_ms = timed_ms(qg, reps)
+        out["mxfp4_queries"] = {"scorer_ms": q_ms, "gbs": scorer_bytes(wq) / (q_ms * 1e-3) / 1e9,
+                                "how": "the 1M MXFP4 keys scored by MXFP4 index queries, L2 flushed before each"}
+        del dq, sq, qg
     if cpu:
         toks = [0]
         secs = oracle_query_sample(wl, toks)

@@ -25,6 +25,7 @@ DSA_IDX_FP8, DSA_IDX_MXFP4 = 0, 1
 DSA_LAT_FP8, DSA_LAT_NVFP4 = 0, 1
 DSA_MAX_TOPK = 2048
 DSA_BATCH_INVARIANT = 1
+DSA_BATCH_QIDX_MXFP4 = 2
 DSA_HOST_PACKED = 1
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED", -3: "DSA_ERR_CUDA",
                 -4: "DSA_ERR_WORKSPACE", -5: "DSA_ERR_TIMEOUT", -6: "DSA_ERR_DEVICE_CHECK"}

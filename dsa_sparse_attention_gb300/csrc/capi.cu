@@ -84,9 +84,23 @@ dsa_status check_layout(const dsa_kv_layout* l, bool need_pool = true) {
   return DSA_OK;
 }
 
+// Bytes of q_idx for a batch: e4m3 codes, or MXFP4 codes and exponents.
+size_t q_idx_bytes(const dsa_batch* b) {
+  return size_t(b->num_tokens) * kIdxHeads * ((b->flags & DSA_BATCH_QIDX_MXFP4) ? kIdxDim / 2 + 4 : kIdxDim);
+}
+
+// MXFP4 queries need MXFP4 keys and a 32-byte aligned q_idx (a packed 4-bit tensor copy).
+dsa_status check_qidx(const dsa_kv_layout* l, const dsa_batch* b, const void* q_idx) {
+  if (!(b->flags & DSA_BATCH_QIDX_MXFP4)) return DSA_OK;
+  if (l->idx_fmt != DSA_IDX_MXFP4) return DSA_ERR_UNSUPPORTED;
+  if (b->num_tokens > 0 && (reinterpret_cast<uintptr_t>(q_idx) & 31)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
 dsa_status check_batch(const dsa_batch* b, int block_size) {
   if (!b) return DSA_ERR_INVALID_ARG;
-  if (b->num_tokens < 0 || b->num_reqs < 1 || (b->flags & ~DSA_BATCH_INVARIANT) || b->bt_stride < 1)
+  if (b->num_tokens < 0 || b->num_reqs < 1 || (b->flags & ~(DSA_BATCH_INVARIANT | DSA_BATCH_QIDX_MXFP4)) ||
+      b->bt_stride < 1)
     return DSA_ERR_INVALID_ARG;
   if (b->num_tokens > 0 && (!b->q_req || !b->q_pos)) return DSA_ERR_INVALID_ARG;
   if (!b->ctx_lens || !b->block_table) return DSA_ERR_INVALID_ARG;
@@ -184,16 +198,19 @@ bool make_key_map(CUtensorMap* m, const dsa_kv_layout* l) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// q_idx [T*32 rows, 128 B], box = one token's 32 heads.
-bool make_qidx_map(CUtensorMap* m, const void* q_idx, int T) {
+// q_idx [T*32 rows of 128 dims], box = one token's 32 heads, 128 B per head in shared
+// memory (128-byte swizzle): e4m3 codes, or MXFP4 codes (64 packed bytes per head)
+// through the 16 x 4-bit element type that pads each 8 bytes of codes to 16.
+bool make_qidx_map(CUtensorMap* m, const void* q_idx, int T, bool mx) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {128, cuuint64_t(T) * kIdxHeads};
-  cuuint64_t strides[1] = {128};
+  cuuint64_t strides[1] = {cuuint64_t(mx ? 64 : 128)};
   cuuint32_t box[2] = {128, kIdxHeads};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(q_idx), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+  return enc(m, mx ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<void*>(q_idx), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -322,8 +339,9 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
                        const void* mla_q = nullptr) {
   const int T = b->num_tokens;
   if (T == 0) return DSA_OK;
+  const bool qmx = (b->flags & DSA_BATCH_QIDX_MXFP4) != 0;
   CUtensorMap kmap, qmap;
-  if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T)) return encode_fail();
+  if (!make_key_map(&kmap, l) || !make_qidx_map(&qmap, q_idx, T, qmx)) return encode_fail();
   const int G = indexer_group_size(l->idx_fmt, T == b->num_reqs);
   const bool direct = G == 1 && T <= kDirectMaxT;
   uint32_t* status = at<uint32_t>(ws, wl.status);
@@ -348,6 +366,8 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
   p.row_hist = G == 1 ? row_hist : nullptr;
   p.mla_q = static_cast<const __nv_bfloat16*>(mla_q);
   p.mla_q_terms = mla_q ? at<uint8_t>(ws, wl.m8_q) : nullptr;
+  p.qmx = qmx ? 1 : 0;
+  p.q_scales = qmx ? static_cast<const uint8_t*>(q_idx) + size_t(T) * kIdxHeads * (kIdxDim / 2) : nullptr;
   return cuda_status(launch_indexer(kmap, qmap, p, G, num_sms(), st));
 }
 
@@ -566,6 +586,7 @@ dsa_status dsa_indexer_score(const dsa_kv_layout* layout, const dsa_batch* batch
   if (batch->num_tokens > 0 && (!q_idx || !w || !scores || !aligned16(q_idx) || !aligned16(w) || !aligned16(scores)))
     return DSA_ERR_INVALID_ARG;
   if (ld_scores < batch->max_ctx_len || (ld_scores & 3)) return DSA_ERR_INVALID_ARG;
+  if ((s = check_qidx(layout, batch, q_idx)) != DSA_OK) return s;
   const Ws wl = plan_ws(layout, batch, 1);
   if ((s = check_ws(workspace, workspace_bytes, wl)) != DSA_OK) return s;
   return run_indexer(layout, batch, q_idx, w, scores, ld_scores, workspace, wl, stream);
@@ -622,7 +643,7 @@ dsa_status dsa_layer_step_host(const dsa_kv_layout* layout, const dsa_batch* bat
   // in the order a packed layout follows
   const Copy in[7] = {
       {q, host->q, size_t(T) * kMlaHeads * kLatDim * 2},
-      {q_idx, host->q_idx, size_t(T) * kIdxHeads * kIdxDim},
+      {q_idx, host->q_idx, q_idx_bytes(batch)},
       {w, host->w, size_t(T) * kIdxHeads * 4},
       {const_cast<int32_t*>(batch->q_req), host->q_req, size_t(T) * 4},
       {const_cast<int32_t*>(batch->q_pos), host->q_pos, size_t(T) * 4},
@@ -688,6 +709,7 @@ dsa_status check_step(const dsa_kv_layout* layout, const dsa_batch* batch, const
   if (batch->num_tokens > 0 && (!q_idx || !w || !q || !out || !aligned16(q_idx) || !aligned16(w) ||
                                 !aligned16(q) || !aligned16(out)))
     return DSA_ERR_INVALID_ARG;
+  if ((s = check_qidx(layout, batch, q_idx)) != DSA_OK) return s;
   wl = plan_ws(layout, batch, topk);
   return check_ws(workspace, workspace_bytes, wl);
 }
@@ -724,7 +746,6 @@ dsa_status dsa_indexer_front(const dsa_kv_layout* layout, const dsa_batch* batch
   dsa_status s = check_layout(layout);
   if (s != DSA_OK) return s;
   if ((s = check_batch(batch, layout->block_size)) != DSA_OK) return s;
-  if (k_new && layout->idx_fmt != DSA_IDX_FP8) return DSA_ERR_UNSUPPORTED;
   if (d_q < 64 || d_q > 4096 || (d_q & 7) || !std::isfinite(eps) || eps < 0.f) return DSA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) || workspace_bytes < kStatusBytes)
     return DSA_ERR_WORKSPACE;
@@ -733,6 +754,7 @@ dsa_status dsa_indexer_front(const dsa_kv_layout* layout, const dsa_batch* batch
   if (!c_q || !norm_weight || !w_qi || !head_w || !q_idx || !w_out || !aligned16(c_q) || !aligned16(norm_weight) ||
       !aligned16(w_qi) || !aligned16(q_idx) || !aligned16(head_w) || !aligned16(w_out) || (k_new && !aligned16(k_new)))
     return DSA_ERR_INVALID_ARG;
+  if ((s = check_qidx(layout, batch, q_idx)) != DSA_OK) return s;
   FrontParams p;
   p.b = batch_view(batch);
   p.pool = pool_view(layout);
@@ -747,6 +769,7 @@ dsa_status dsa_indexer_front(const dsa_kv_layout* layout, const dsa_batch* batch
   p.d_q = d_q;
   p.eps = eps;
   p.status = static_cast<uint32_t*>(workspace);
+  p.qmx = (batch->flags & DSA_BATCH_QIDX_MXFP4) ? 1 : 0;
   CUtensorMap wmap;
   if (!make_front_w_map(&wmap, w_qi, d_q)) return encode_fail();
   return cuda_status(launch_indexer_front(wmap, p, stream));

@@ -256,6 +256,31 @@ __global__ void __launch_bounds__(front::THREADS, 1)
       q8[6] += __uint_as_float(v1.z);
       q8[7] += __uint_as_float(v1.w);
     }
+    if (p.qmx) {
+      // MXFP4 (uniform over the CTA): warp w holds the head's 32-dim block w of each
+      // token, so the block's maximum is a warp maximum.  E = floor(log2 max) - 2 + 127
+      // clamped to 0..254 (0 for a zero block), codes e2m1(q * 2^(127 - E)) (an exact
+      // power-of-two scaling, then round to nearest even, saturating at 6), two per
+      // byte with the even dim in the low nibble; the exponents follow all the codes.
+      const int64_t nT = p.b.T;
+      uint8_t* cdst = p.q_idx + (static_cast<int64_t>(t0) * kIdxHeads + h) * (kIdxDim / 2) + (row >> 1);
+      uint8_t* edst = p.q_idx + nT * kIdxHeads * (kIdxDim / 2) + (static_cast<int64_t>(t0) * kIdxHeads + h) * 4 + warp;
+#pragma unroll
+      for (int t = 0; t < CHUNK; ++t) {
+        float m = fabsf(q8[t]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int e = m > 0.f ? min(max(ilogbf(m) - 2 + 127, 0), 254) : 0;
+        const float v = q8[t] * __uint_as_float(static_cast<uint32_t>(254 - e) << 23);
+        const uint32_t c = __nv_cvt_float_to_fp4(v, __NV_E2M1, cudaRoundNearest) & 0xFu;
+        const uint32_t c_odd = __shfl_down_sync(0xffffffffu, c, 1);
+        if (t < nt) {
+          if ((lane & 1) == 0) cdst[static_cast<int64_t>(t) * kIdxHeads * (kIdxDim / 2)] = static_cast<uint8_t>(c | (c_odd << 4));
+          if (lane == 0) edst[static_cast<int64_t>(t) * kIdxHeads * 4] = static_cast<uint8_t>(e);
+        }
+      }
+      if (row < nt) p.w_out[static_cast<int64_t>(t0 + row) * kIdxHeads + h] = hw;   // the scales travel with the codes
+    } else {
     // the head's max |q| per token: within the warp, then over the 4 warps
 #pragma unroll
     for (int t = 0; t < CHUNK; ++t) {
@@ -281,11 +306,35 @@ __global__ void __launch_bounds__(front::THREADS, 1)
       if (t < nt)
         qdst[static_cast<int64_t>(t) * kIdxHeads * kIdxDim] =
             static_cast<uint8_t>(__nv_cvt_float_to_fp8(q8[t] * amax_all[t], __NV_SATFINITE, __NV_E4M3));
+    }
   }
   if (quarter != 0) cluster_arrive_relaxed();   // the first CTA reads this one's sums until the end
   // the chunk's new index keys (second quarter of head 0, while the first finalises
-  // the head): one warp per token, four values per lane, s_k = max |k| / 448 in fp32
-  if (p.k_new && blockIdx.x == 1 && warp < nt) {
+  // the head): one warp per token, four values per lane.  FP8 pages: s_k = max |k| /
+  // 448 in fp32.  MXFP4 pages: per 32 dims (8 lanes) the MX exponent and e2m1 codes
+  // as for the queries, 64 code bytes at the slot, the 4 exponents in the scale area.
+  if (p.k_new && blockIdx.x == 1 && warp < nt && p.pool.idx_fmt == DSA_IDX_MXFP4) {
+    const int t = t0 + warp;
+    const uint2 kv = __ldg(reinterpret_cast<const uint2*>(p.k_new + static_cast<int64_t>(t) * kIdxDim) + lane);
+    const float kk[4] = {__uint_as_float(kv.x << 16), __uint_as_float(kv.x & 0xFFFF0000u),
+                         __uint_as_float(kv.y << 16), __uint_as_float(kv.y & 0xFFFF0000u)};
+    float m = fmaxf(fmaxf(fabsf(kk[0]), fabsf(kk[1])), fmaxf(fabsf(kk[2]), fabsf(kk[3])));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));   // over the block's 8 lanes
+    const int e = m > 0.f ? min(max(ilogbf(m) - 2 + 127, 0), 254) : 0;
+    const float mul = __uint_as_float(static_cast<uint32_t>(254 - e) << 23);
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = __nv_cvt_float_to_fp4(kk[i] * mul, __NV_E2M1, cudaRoundNearest) & 0xFu;
+    int64_t row = 0;
+    int slot = 0;
+    if (new_token_slot(p.b, p.pool, t, p.status, row, slot)) {
+      uint8_t* page = p.pool_w + row * p.pool.row_stride + p.pool.idx_off;
+      *reinterpret_cast<uint16_t*>(page + slot * (kIdxDim / 2) + 2 * lane) =
+          static_cast<uint16_t>(c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12));
+      if ((lane & 7) == 0) page[static_cast<int64_t>(p.pool.bs) * (kIdxDim / 2) + slot * 4 + (lane >> 3)] = static_cast<uint8_t>(e);
+    }
+  } else if (p.k_new && blockIdx.x == 1 && warp < nt) {
     const int t = t0 + warp;
     const uint2 kv = __ldg(reinterpret_cast<const uint2*>(p.k_new + static_cast<int64_t>(t) * kIdxDim) + lane);
     const float k0 = __uint_as_float(kv.x << 16), k1 = __uint_as_float(kv.x & 0xFFFF0000u);

@@ -154,10 +154,14 @@ struct ScorerCfg {
   // warps take tiles in turn (each with its own accumulators).
   static constexpr int NMMA = 2;
   // MXFP4: the block scales of the MMA, A (keys) 4 columns per key stage (key r of
-  // the stage at lane r, column r / 32), B (the query, all 2^0) G columns
+  // the stage at lane r, column r / 32), B (the queries: all 2^0, or with MXFP4
+  // queries their exponents) SFB_STRIDE columns per query buffer (token j at column
+  // j).  The MMA takes scale addresses at even columns only (an odd one faults with
+  // a misaligned address); every scale region here starts at a multiple of 4.
   static constexpr int SFA_COL = NACC * ACC_COLS;
   static constexpr int SFB_COL = SFA_COL + 4 * STAGES;
-  static constexpr int TMEM_USED = MX ? SFB_COL + G : NACC * ACC_COLS;
+  static constexpr int SFB_STRIDE = (G + 3) / 4 * 4;
+  static constexpr int TMEM_USED = MX ? SFB_COL + 2 * SFB_STRIDE : NACC * ACC_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
                                    : TMEM_USED <= 64  ? 64
                                    : TMEM_USED <= 128 ? 128
@@ -169,11 +173,12 @@ struct ScorerCfg {
   static constexpr int Q_BYTES = G * kIdxHeads * kIdxDim;
   static constexpr int W_BYTES = G * kIdxHeads * 4;
   static constexpr int OFF_Q = STAGES * KEY_BYTES;
-  static constexpr int OFF_SCALES = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_QS = OFF_Q + 2 * Q_BYTES;              // MXFP4 queries: 2 x [G][32] E8M0 words
+  static constexpr int OFF_SCALES = OFF_QS + (MX ? 2 * G * kIdxHeads * 4 : 0);
   static constexpr int OFF_W = OFF_SCALES + SSLOTS * SCALE_BYTES;   // 2 x [G][32] fp32
   static constexpr int OFF_POS = OFF_W + 2 * W_BYTES;                // 2 x [G] int
   static constexpr int OFF_BARS = OFF_POS + 2 * G * 4 + 64;
-  static constexpr int N_BARS = 3 * STAGES + 2 * NACC + 4 + NMMA + 2 * SSLOTS;
+  static constexpr int N_BARS = 3 * STAGES + 2 * NACC + 4 + NMMA + 2 * SSLOTS + 2;
   static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;
   static constexpr int OFF_PLAN = OFF_MISC + 64;            // direct mode: groups [kDirectMaxT] + total
   // Copies are issued by NPROD producer warps taking tiles in turn: one thread
@@ -199,6 +204,7 @@ struct ScorerCfg {
   static_assert(SSLOTS % NPROD == 0 && SSLOTS % 2 == 0, "scale slots per producer and epilogue set");
   static_assert(NACC % 2 == 0, "accumulators per epilogue set");
   static_assert(TMEM_USED <= 512, "tmem columns");
+  static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SFB_STRIDE % 4 == 0, "scale addresses at multiples of 4");
   static_assert(SMEM_BYTES <= 232448, "smem");
   static_assert(OFF_HIST % 16 == 0 && OFF_Q % 1024 == 0 && OFF_SCALES % 16 == 0 && OFF_W % 16 == 0 && OFF_BARS % 8 == 0,
                 "alignment of the shared-memory regions");
@@ -260,6 +266,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
   uint64_t* sready = drain + C::NMMA;         // [STAGES] MXFP4: the stage's key exponents are in TMEM
   uint64_t* sfull = sready + C::STAGES;       // [SSLOTS] scales landed
   uint64_t* sempty = sfull + C::SSLOTS;       // [SSLOTS] scales read by the epilogue
+  uint64_t* qsready = sempty + C::SSLOTS;     // [2] MXFP4 queries: the group's exponents are in TMEM
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   int* abortf = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
   float* wsm = reinterpret_cast<float*>(smem + C::OFF_W);
@@ -284,6 +291,7 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       mbar_init(&sfull[s], 1);
       mbar_init(&sempty[s], 4);   // the epilogue warps of the tile's set
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&qsready[i], C::SCALE_WARPS > 0 ? C::SCALE_WARPS : 1);
     *abortf = 0;
     fence_mbar_init();
     // the descriptors are launch parameters: fetched while the kernel before drains
@@ -411,12 +419,19 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
           }
           possm[qb * G + j] = pos;
         }
-        mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * (kIdxHeads * kIdxDim + kIdxHeads * 4));
+        // codes (MXFP4: the 4-bit copy counts 64 packed bytes per head), head weights,
+        // and with MXFP4 queries their exponents
+        const uint32_t code_bytes = C::MX && p.qmx ? kIdxHeads * kIdxDim / 2 : kIdxHeads * kIdxDim;
+        const uint32_t qs_bytes = C::MX && p.qmx ? kIdxHeads * 4 : 0;
+        mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(grp.n) * (code_bytes + kIdxHeads * 4 + qs_bytes));
         for (int j = 0; j < grp.n; ++j)
           tma_load_2d(smem + C::OFF_Q + qb * C::Q_BYTES + j * kIdxHeads * kIdxDim, &qmap, &qfull[qb], 0,
                       (grp.t0 + j) * kIdxHeads);
         bulk_load(wsm + qb * G * kIdxHeads, p.w + static_cast<int64_t>(grp.t0) * kIdxHeads,
                   static_cast<uint32_t>(grp.n) * kIdxHeads * 4, &qfull[qb]);
+        if (qs_bytes)
+          bulk_load(smem + C::OFF_QS + qb * G * kIdxHeads * 4, p.q_scales + static_cast<int64_t>(grp.t0) * kIdxHeads * 4,
+                    static_cast<uint32_t>(grp.n) * qs_bytes, &qfull[qb]);
         return true;
       };
       int walked = tile_lo;                                          // tile the cursor is at
@@ -527,16 +542,18 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       if (lane == 0) {
         GroupCursor cur;
         cur.init(groups, ng, total, tile_lo);
-        auto idesc_of = [](int n) {
-          return C::MX ? make_idesc_bs(5, 0, kKeyTile, n * kIdxHeads, 0, 0)   // E2M1 keys, e4m3 queries
+        const bool qmx = C::MX && p.qmx;
+        auto idesc_of = [qmx](int n) {   // E2M1 keys with e4m3 (or E2M1) queries
+          return C::MX ? make_idesc_bs(5, qmx ? 5 : 0, kKeyTile, n * kIdxHeads, 0, 0)
                        : make_idesc(0, 0, false, false, kKeyTile, n * kIdxHeads);
         };
         uint32_t idesc = idesc_of(cur.grp.n);
-        bool ok = mbar_wait(&qfull[0], 0, ab);
+        bool ok = mbar_wait(&qfull[0], 0, ab) && (!qmx || mbar_wait(&qsready[0], 0, ab));
         for (int i = tile_lo; i < tile_hi && ok; ++i) {
           if (cur.advance(i)) {
             idesc = idesc_of(cur.grp.n);
             if (!(ok = mbar_wait(&qfull[cur.count & 1], (cur.count >> 1) & 1, ab))) break;
+            if (qmx && !(ok = mbar_wait(&qsready[cur.count & 1], (cur.count >> 1) & 1, ab))) break;
           }
           const int it = i - tile_lo;
           if (it % C::NMMA == mid) {
@@ -555,9 +572,10 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
               // byte k of each key's exponent cell
               const uint64_t ad = make_sdesc_sw128(a0 + 32 * k, 16, 1024);
               const uint64_t bd = make_sdesc_sw128(b0 + 32 * k, 16, 1024);
-              if (C::MX)
-                mma_mxf8f6f4_bs(d, ad, bd, idesc | (static_cast<uint32_t>(k) << 29), tmem + C::SFA_COL + 4 * s,
-                                tmem + C::SFB_COL, k > 0 ? 1u : 0u);
+              if (C::MX)   // scale byte k: the keys' (and MXFP4 queries') exponent of block k
+                mma_mxf8f6f4_bs(d, ad, bd, idesc | (static_cast<uint32_t>(k) << 29) | (qmx ? k << 4 : 0u),
+                                tmem + C::SFA_COL + 4 * s, tmem + C::SFB_COL + (cur.count & 1) * C::SFB_STRIDE,
+                                k > 0 ? 1u : 0u);
               else
                 mma_f8f6f4(d, ad, bd, idesc, k > 0 ? 1u : 0u);
             }
@@ -579,9 +597,28 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
       // and, before its first tile, the query's unit scales in its quarter.
       const int q = warp & 3;
       const uint32_t lq = static_cast<uint32_t>(32 * q) << 16;
-      for (int c = 0; c < G; ++c) tmem_st1(tmem + lq + C::SFB_COL + c, 0x7F7F7F7Fu);   // 2^0 in every byte
-      bool ok = true;
+      const bool qmx = p.qmx != 0;
+      if (!qmx)
+        for (int c = 0; c < 2 * C::SFB_STRIDE; ++c) tmem_st1(tmem + lq + C::SFB_COL + c, 0x7F7F7F7Fu);   // 2^0 in every byte
+      // MXFP4 queries: a group's head exponents (head h at lane h of every quarter,
+      // token j at column SFB_COL + buffer * SFB_STRIDE + j), once its query has landed
+      GroupCursor gc;
+      gc.init(groups, ng, total, tile_lo);
+      auto group_scales = [&](int count) -> bool {
+        const int qb = count & 1;
+        if (!mbar_wait(&qfull[qb], (count >> 1) & 1, ab)) return false;
+        const uint32_t* qs = reinterpret_cast<const uint32_t*>(smem + C::OFF_QS) + qb * G * kIdxHeads;
+        for (int j = 0; j < gc.grp.n; ++j)
+          tmem_st1(tmem + lq + C::SFB_COL + qb * C::SFB_STRIDE + j, qs[j * kIdxHeads + lane]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qsready[qb]);
+        return true;
+      };
+      bool ok = !qmx || tile_lo >= tile_hi || group_scales(0);
       for (int i = tile_lo; i < tile_hi && ok; ++i) {
+        if (gc.advance(i) && qmx && !(ok = group_scales(gc.count))) break;
         const int it = i - tile_lo;
         const int s = it % C::STAGES, ss = it % C::SSLOTS;
         if (it >= C::STAGES && !(ok = mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1, ab))) break;

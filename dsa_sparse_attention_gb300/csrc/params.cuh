@@ -22,6 +22,8 @@ struct IndexerParams {
                            // added here (one token per group only); a hint for the top-k
   const __nv_bfloat16* mla_q = nullptr;   // [T, 96, 576] or null: in a layer step whose attention runs on
   uint8_t* mla_q_terms = nullptr;         // FP8 latents, the epilogue warps also write its query terms here
+  int qmx = 0;                            // 1: MXFP4 queries (MXFP4 keys only): codes through the query map,
+  const uint8_t* q_scales = nullptr;      //    and their E8M0 exponents [T, 32, 4] here
 };
 
 struct TopkParams {
@@ -164,6 +166,7 @@ struct FrontParams {
   int d_q;
   float eps;
   uint32_t* status;
+  int qmx = 0;                 // 1: q_idx in MXFP4 (codes [T, 32, 64], then E8M0 [T, 32, 4]), w_out = head_w
 };
 
 struct LatentWriteParams {

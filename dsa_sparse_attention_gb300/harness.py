@@ -23,6 +23,8 @@ class DeviceWorkload:
         self.q = torch.from_numpy(wl.q.view(np.int16)).to(device).view(torch.bfloat16)
         self.layout = make_layout(self.pool, wl.num_rows, wl.row_stride, wl.idx_page_offset, wl.lat_page_offset,
                                   wl.block_size, wl.idx_fmt, wl.lat_fmt)
+        if getattr(wl, "q_fmt", 0) == 1:   # MXFP4 index queries in q_idx
+            flags |= 2
         self.batch = make_batch(self.q_req, self.q_pos, self.ctx, self.bt, wl.max_ctx_len, flags)
         self.ws = alloc_workspace(self.layout, self.batch, self.topk, device)
         T = wl.num_tokens

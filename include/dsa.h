@@ -112,6 +112,18 @@ typedef struct {
  * cost of more partial traffic for large batches.
  */
 #define DSA_BATCH_INVARIANT 1
+/*
+ * MXFP4 index queries ("Low-latency decode: a fused DSA decode path": the index
+ * query is quantized to FP8 or MXFP4).  With this flag q_idx of every call that
+ * takes it holds T x 32 x 64 bytes of packed e2m1 codes (head h of token t at
+ * (t * 32 + h) * 64, element 2i in the low nibble of byte i), then T x 32 x 4 E8M0
+ * exponents (byte j of head h of token t at T * 2048 + (t * 32 + h) * 4 + j covers
+ * dims 32j..32j+31): 68 bytes per head, 32-byte aligned.  The query value is
+ * e2m1(code) * 2^(E - 127); the head weights are used as given.  Only with MXFP4
+ * index keys (DSA_ERR_UNSUPPORTED otherwise); dsa_indexer_front then writes this
+ * form.  Without the flag q_idx holds e4m3 codes [T, 32, 128].
+ */
+#define DSA_BATCH_QIDX_MXFP4 2
 typedef struct {
   int32_t num_tokens;        /* T >= 0 */
   int32_t num_reqs;          /* B >= 1 */
@@ -305,15 +317,22 @@ dsa_status dsa_topk_noalloc(const dsa_kv_layout *layout, const dsa_batch *batch,
  *   s[h] = max|q[h, :]| / 448 (1 for an all-zero head)
  *   q_idx[t, h, :] = e4m3(q[h, :] / s[h]),  w_out[t, h] = head_w[t, h] * s[h]
  * so q_idx and w_out are the inputs dsa_indexer_score / dsa_layer_step take.
+ * With DSA_BATCH_QIDX_MXFP4 (MXFP4 index pages only) q_idx is written in that
+ * flag's layout instead: per head and 32-dim block b, E = floor(log2 max|q|) - 2
+ * + 127 clamped to 0..254 (0 for a zero block), codes e2m1(q * 2^(127 - E))
+ * (round to nearest even, saturating at 6); w_out[t, h] = head_w[t, h].
  * With k_new given, the new token's index key is written into the pool at the
- * token's own position (block_table[q_req[t]][q_pos[t] / bs], slot q_pos[t] % bs):
- * s_k = max|k| / 448 in fp32 (1 when zero), 128 codes e4m3(k / s_k), then s_k in
- * the page's scale area.  FP8 index pages only (DSA_ERR_UNSUPPORTED otherwise).
+ * token's own position (block_table[q_req[t]][q_pos[t] / bs], slot q_pos[t] % bs).
+ * FP8 pages: s_k = max|k| / 448 in fp32 (1 when zero), 128 codes e4m3(k / s_k),
+ * then s_k in the page's scale area.  MXFP4 pages: per 32 dims the exponent and
+ * e2m1 codes by the rule above, 64 code bytes at the slot, 4 exponents in the
+ * scale area.
  *  c_q        : device bf16 [T, d_q], d_q a multiple of 8 in 64..4096
  *  norm_weight: device bf16 [d_q];  eps >= 0
  *  w_qi       : device bf16 [32 * 128, d_q] (row h * 128 + d is output dim d of head h)
  *  head_w     : device fp32 [T, 32];  k_new: device bf16 [T, 128] or NULL
- *  q_idx      : device e4m3 [T, 32, 128] (written);  w_out: device fp32 [T, 32] (written)
+ *  q_idx      : device e4m3 [T, 32, 128], or MXFP4 (68 bytes per head, 32-byte
+ *               aligned) with DSA_BATCH_QIDX_MXFP4 (written);  w_out: device fp32 [T, 32] (written)
  *  workspace  : only its status word is used (>= 256 bytes); a block id or
  *               position out of range is recorded there and nothing is written for it.
  * Unlike the other calls this one writes the pool (the new tokens' slots only).

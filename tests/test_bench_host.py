@@ -46,6 +46,9 @@ def test_fp4_widths():
     idx = np.arange(8, dtype=np.int32)[None]
     assert bench.algorithmic_bytes(wl, idx) == 1000 * KEY_MXFP4 + 8 * LAT_NVFP4 + Q_AND_OUT
     assert bench.scorer_bytes(wl) == 1000 * KEY_MXFP4 + 4096 + 128
+    wq = _wl([1000], [0], idx_fmt=1, lat_fmt=1)
+    wq.q_fmt = 1                                                  # MXFP4 index queries: 68 B per head
+    assert bench.scorer_bytes(wq) == 1000 * KEY_MXFP4 + 32 * 68 + 128
 
 
 def _copy_sources(tmp_path):

@@ -54,7 +54,7 @@ def test_workspace_size_and_validation(lib):
     assert dsa.dsa_workspace_size(_layout(block_size=48), _batch(), 2048) == 0
     assert dsa.dsa_workspace_size(_layout(row_stride=45300), _batch(), 2048) == 0
     assert dsa.dsa_workspace_size(_layout(), _batch(max_ctx=16 * 64 + 1), 2048) == 0
-    assert dsa.dsa_workspace_size(_layout(), _batch(flags=2), 2048) == 0
+    assert dsa.dsa_workspace_size(_layout(), _batch(flags=4), 2048) == 0
     inv = dsa.dsa_workspace_size(_layout(), _batch(T=64, flags=dsa.DSA_BATCH_INVARIANT), 2048)
     dflt = dsa.dsa_workspace_size(_layout(), _batch(T=64), 2048)
     assert inv > dflt
@@ -82,6 +82,15 @@ def test_host_validation_errors(lib):
                                                  row_stride=4352 + 36864 + 32)), _batch(), 2048) == 0
     assert dsa.dsa_workspace_size(_layout(row_stride=45312 + 16), _batch(), 2048) > 0
     assert _call_step(_layout(pool=0x10010, **mx), _batch()) == -1
+    # MXFP4 index queries: only with MXFP4 keys, and q_idx 32-byte aligned
+    qmx = _batch(flags=dsa.DSA_BATCH_QIDX_MXFP4)
+    assert _call_step(_layout(), qmx) == -2
+    L = dsa.library()
+    call = lambda q_idx: L.dsa_layer_step(ctypes.byref(_layout(**mx)), ctypes.byref(qmx), q_idx, 0x80000, 0x60000,
+                                          2048, 1 / 24, None, 0x90000, None, 0x100000, 1 << 30, None)
+    assert call(0x70010) == -1
+    assert dsa.dsa_workspace_size(_layout(**mx), qmx, 2048) > 0
+    assert dsa.dsa_workspace_size(_layout(**mx), _batch(flags=4), 2048) == 0
     L = dsa.library()
     assert L.dsa_layer_step(None, ctypes.byref(_batch()), 0, 0, 0, 2048, 1.0, None, 0, None, 0, 0, None) == -1
     assert L.dsa_topk(None, ctypes.byref(_batch()), 0x1000, 1000, 0, 0x2000, None, 0x100000, 1 << 30, None) == -1
@@ -124,7 +133,13 @@ def test_front_and_latent_write_validation(lib):
     assert front(_layout(), eps=float("nan")) == -1
     assert front(_layout(), ws_bytes=16) == -4
     assert front(_layout(), ws=0x100010) == -4
-    assert front(_layout(idx_fmt=1)) == -2                     # new keys need FP8 index pages
+    # MXFP4 index queries need MXFP4 index pages and a 32-byte aligned q_idx
+    bq = ctypes.byref(_batch(flags=dsa.DSA_BATCH_QIDX_MXFP4))
+    mx = _layout(idx_fmt=1, row_stride=4352 + 36864, lat_page_offset=4352)
+    frontq = lambda lay, q_idx: L.dsa_indexer_front(ctypes.byref(lay), bq, 0x1000, 1536, 0x2000, 1e-6, 0x3000, 0x4000,
+                                                    None, q_idx, 0x8000, 0x100000, 4096, None)
+    assert frontq(_layout(), 0x7000) == -2
+    assert frontq(mx, 0x7010) == -1
     assert L.dsa_indexer_front(ctypes.byref(_layout()), b, 0x1008, 1536, 0x2000, 1e-6, 0x3000, 0x4000, None, 0x7000,
                                0x8000, 0x100000, 4096, None) == -1   # misaligned query
     assert L.dsa_write_latent(ctypes.byref(_layout()), b, None, 0x100000, 4096, None) == -1

@@ -369,6 +369,28 @@ def test_mxfp4_nvfp4_mtp_groups():
     _run_all(wl)
 
 
+def test_mxfp4_queries_and_keys():
+    # MXFP4 index queries (codes through the 4-bit tensor copy, exponents as the
+    # MMA's B scales) against MXFP4 keys, one token per request; 165 key tiles over
+    # 152 CTAs, so some CTAs cross from one token's tiles to the next (the second
+    # query buffer and its scale columns)
+    wl = W.make_workload([5000, 700, 2049, 129, 3000, 3000, 4000, 2500], 1, seed=51, idx_fmt=W.IDX_MXFP4,
+                         q_fmt=W.Q_MXFP4, permute=True, pool_rows=400)
+    _run_all(wl)
+
+
+def test_mxfp4_queries_wide_exponents_mtp_groups():
+    # every (token, head, block) exponent redrawn over 2^-9 .. 2^9: a wrong head,
+    # block or token column of the B scales would show; six tokens per request
+    # (groups of two tokens in the scorer) and NVFP4 latents
+    wl = W.make_workload([3000, 4100, 333], 6, seed=52, idx_fmt=W.IDX_MXFP4, lat_fmt=W.LAT_NVFP4, q_fmt=W.Q_MXFP4,
+                         permute=True, pool_rows=200)
+    T = wl.num_tokens
+    rng = np.random.default_rng(3)
+    wl.q_idx[T * 32 * 64:] = rng.integers(118, 137, size=T * 32 * 4).astype(np.uint8)
+    _run_all(wl)
+
+
 @pytest.mark.slow
 def test_full_cfg3_decode_1m_mxfp4_nvfp4():
     # one request, 1,048,576-token context, MXFP4 index keys and NVFP4 latents
