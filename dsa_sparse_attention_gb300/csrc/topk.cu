@@ -299,12 +299,31 @@ __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParam
       return true;
     };
     select_low21(gen, static_cast<int>(count), r, Tlow, aboveT, h, sh);
-    cut = select_cut(gen, static_cast<int>(count), Tlow, r - aboveT, h, sh);
+    // h still holds the last digit's counts: h[Tlow & 1023] keys equal T.  When all of
+    // them are taken (the usual case) no position cut is needed.
+    const uint32_t eq = h[Tlow & 1023u];
+    cut = eq == r - aboveT ? 0x7FFFFFFF : select_cut(gen, static_cast<int>(count), Tlow, r - aboveT, h, sh);
+    // selections per chunk: counted in shared memory (this CTA alone writes the row's
+    // counts, which start at zero), or with global atomics for rows of more chunks
+    const bool in_smem = nch <= kBins;
+    if (in_smem) {
+      __syncthreads();   // every thread is done reading h
+      for (int c = threadIdx.x; c < nch; c += kTopkThreads) h[c] = 0;
+      __syncthreads();
+    }
     for (uint32_t i = threadIdx.x; i < count; i += kTopkThreads) {
       const uint2 c = lc[i];
       const uint32_t lo = c.x & 0x1FFFFFu;
-      if (lo > Tlow || (lo == Tlow && static_cast<int32_t>(c.y) <= cut))
-        atomicAdd(taken + c.y / static_cast<uint32_t>(p.chunk), 1u);
+      if (lo > Tlow || (lo == Tlow && static_cast<int32_t>(c.y) <= cut)) {
+        const uint32_t ch = c.y / static_cast<uint32_t>(p.chunk);
+        if (in_smem) atomicAdd(&h[ch], 1u);
+        else atomicAdd(taken + ch, 1u);
+      }
+    }
+    if (in_smem) {
+      __syncthreads();
+      for (int c = threadIdx.x; c < nch; c += kTopkThreads)
+        if (h[c]) taken[c] = h[c];
     }
   } else {
     // heavy ties: redo the resolution over the whole row in this CTA
