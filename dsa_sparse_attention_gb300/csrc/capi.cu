@@ -375,7 +375,7 @@ dsa_status run_indexer(const dsa_kv_layout* l, const dsa_batch* b, const void* q
 // `pre_hist`: histograms the scorer left for these scores, or null.
 dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* scores, int64_t ld, int topk,
                     int32_t* idx, int32_t* phys, void* ws, const Ws& wl, cudaStream_t st, bool chained,
-                    uint32_t* pre_hist = nullptr) {
+                    uint32_t* pre_hist = nullptr, bool zeroed = false) {
   if (b->num_tokens == 0) return DSA_OK;
   TopkParams p;
   p.b = batch_view(b);
@@ -392,7 +392,7 @@ dsa_status run_topk(const dsa_kv_layout* l, const dsa_batch* b, const float* sco
   p.log2_bs = lg;
   p.status = at<uint32_t>(ws, wl.status);
   p.pre_hist = pre_hist;
-  return cuda_status(launch_topk(p, st, chained));
+  return cuda_status(launch_topk(p, st, chained, zeroed));
 }
 
 // Whether the attention of this plan takes the FP8 kernel on this device.
@@ -724,13 +724,22 @@ dsa_status run_step(const dsa_kv_layout* layout, const dsa_batch* batch, const v
   uint32_t* row_hist = batch->max_ctx_len <= kTopkClusterMaxRow ? at<uint32_t>(workspace, wl.row_hist) : nullptr;
   // with FP8 latents the scorer also prepares the attention's query terms
   const bool fp8 = use_fp8_mla(wl);
+  // rows beyond the one-launch top-k take three passes whose scratch must start at
+  // zero: cleared before the scorer, so the passes follow the scorer directly
+  const bool long_rows = batch->max_ctx_len > kTopkClusterMaxRow && batch->num_tokens > 0;
+  if (long_rows) {
+    const TopkScratch L = topk_scratch_layout(batch->num_tokens, wl.topk_nchunks);
+    const cudaError_t e = cudaMemsetAsync(at<uint8_t>(workspace, wl.topk) + L.hist, 0, L.zero_end - L.hist, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   if ((s = run_indexer(layout, batch, q_idx, w, scores, wl.ld, workspace, wl, stream, row_hist,
                        fp8 ? q : nullptr)) != DSA_OK)
     return s;
   // the top-k also emits each selection's physical cache slot, which the attention gathers directly
   int32_t* phys = at<int32_t>(workspace, wl.phys);
   // the top-k and the attention start while their predecessor drains (programmatic launch)
-  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream, true, row_hist)) != DSA_OK)
+  if ((s = run_topk(layout, batch, scores, wl.ld, topk, idx, phys, workspace, wl, stream, true, row_hist, long_rows)) !=
+      DSA_OK)
     return s;
   return run_mla(layout, batch, q, idx, phys, topk, sm_scale, out, lse, workspace, wl, stream, true, fp8);
 }

@@ -190,7 +190,9 @@ cudaError_t launch_plan_groups(const BatchView& b, int G, ScoreGroup* groups, Pl
 cudaError_t launch_indexer(const CUtensorMap& kmap, const CUtensorMap& qmap, const IndexerParams& p, int G,
                            int grid, cudaStream_t st);
 int indexer_group_size(int idx_fmt, bool one_token_per_request);
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained);
+// `zeroed`: the scratch [hist .. zero_end) was cleared on the stream already
+// (otherwise the launch clears it first).
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained, bool zeroed = false);
 cudaError_t launch_sparse_mla(const CUtensorMap& qmap, const CUtensorMap& cmap, const MlaParams& p, cudaStream_t st,
                               bool chained);
 // FP8 latents, one 128-token tile per CTA (p.nsplit = tiles of the selection, p.tps

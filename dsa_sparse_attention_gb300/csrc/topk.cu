@@ -145,7 +145,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(TopkParams p) {
   __shared__ uint32_t sh[48];
   const int t = blockIdx.y;
   int c0, c1, n;
-  if (!row_range(p, t, c0, c1, n) || n <= p.k) return;
+  const bool work = row_range(p, t, c0, c1, n) && n > p.k;   // inputs of the call, read before the wait
+  grid_dep_wait();     // the scores (and the zeroed scratch) of the work before
+  grid_dep_launch();
+  if (!work) return;
   for (int i = threadIdx.x; i < kBins; i += kTopkThreads) h[i] = 0;
   __syncthreads();
   const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
@@ -249,7 +252,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParam
   __shared__ uint2 lc[4096];       // this chunk's candidates (key, position)
   const int t = blockIdx.y;
   int c0, c1, n;
-  if (!row_range(p, t, c0, c1, n) || n <= p.k) return;
+  const bool work = row_range(p, t, c0, c1, n) && n > p.k;
+  grid_dep_wait();     // the histogram pass
+  grid_dep_launch();
+  if (!work) return;
   const uint32_t b1 = p.thr[4 * t + 0];
   const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
   if (threadIdx.x == 0) lcount = 0;
@@ -356,6 +362,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_emit_kernel(TopkParams p) {
   const int t = blockIdx.y;
   int req, pos;
   load_token(p.b, t, p.status, req, pos);
+  grid_dep_wait();     // the candidate pass
+  grid_dep_launch();
   const int n = pos + 1;
   const int c0 = blockIdx.x * p.chunk;
   const int c1 = min(n, c0 + p.chunk);
@@ -855,7 +863,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(TopkParams p) 
   if (gathered && multi) cluster_wait();   // no CTA leaves while another may still read its candidates
 }
 
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained) {
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained, bool zeroed) {
   if (p.b.T == 0) return cudaSuccess;
   if (p.b.max_ctx <= kClMaxRow) {
     const unsigned csize = static_cast<unsigned>(cdiv(p.b.max_ctx, kClSlice));
@@ -864,12 +872,14 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained) {
     return launch_ex(topk_cluster_kernel<false>, dim3(csize, p.b.T), dim3(kClThreads), 0, st, chained, csize, p);
   }
   const dim3 grid(p.nchunks, p.b.T);
-  cudaError_t e = cudaMemsetAsync(p.zero_begin, 0, p.zero_bytes, st);
-  if (e != cudaSuccess) return e;
-  topk_hist_kernel<<<grid, kTopkThreads, 0, st>>>(p);
-  topk_candidates_kernel<<<grid, kTopkThreads, 0, st>>>(p);
-  topk_emit_kernel<<<grid, kTopkThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (!zeroed && (e = cudaMemsetAsync(p.zero_begin, 0, p.zero_bytes, st)) != cudaSuccess) return e;
+  // each pass starts while the one before drains (programmatic launch; each waits
+  // for the one before before it reads anything that one writes)
+  if ((e = launch_ex(topk_hist_kernel, grid, dim3(kTopkThreads), 0, st, chained && zeroed, 0u, p)) != cudaSuccess)
+    return e;
+  if ((e = launch_ex(topk_candidates_kernel, grid, dim3(kTopkThreads), 0, st, true, 0u, p)) != cudaSuccess) return e;
+  return launch_ex(topk_emit_kernel, grid, dim3(kTopkThreads), 0, st, true, 0u, p);
 }
 
 }  // namespace dsa
