@@ -607,9 +607,9 @@ def main():
     t_wall = time.perf_counter() - t_wall
     ms, value = job_rate(ev0.elapsed_time(ev1) / args.steps, world, device="cuda")
 
-    # the same K-step replay repeated until about 0.25 s of replays: their median
+    # the same K-step replay repeated until about 1 s of replays: their median
     # (and spread), beside the single measurement above; the clock record covers both
-    n_rep = max(3, min(400, int(250.0 / max(ms * args.steps, 1e-3))))
+    n_rep = max(3, min(2000, int(1000.0 / max(ms * args.steps, 1e-3))))
     rep = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
     with torch.cuda.stream(stream):
         for a, b in rep:
