@@ -247,8 +247,12 @@ dsa_status dsa_layer_step(const dsa_kv_layout *layout, const dsa_batch *batch,
  * that each array starts where the one before it ends, on both sides, and returns
  * DSA_ERR_INVALID_ARG where one does not.  Whether the arrays share an allocation
  * cannot be checked: a copy must not span two allocations.  Host memory should be
- * page-locked.  With pageable memory the results are the same, but the host waits
- * for each copy.
+ * page-locked: a range that lies inside one page-locked allocation the device can
+ * address (cudaHostAlloc, cudaMallocHost, cudaHostRegister; checked with the
+ * driver's pointer attributes) is moved by the library's copy kernel through its
+ * mapped device address, all such inputs in one launch and all such outputs in
+ * another.  Any other host memory goes through cudaMemcpyAsync: the results are
+ * the same, but with pageable memory the host waits for each copy.
  * The call returns once everything is enqueued.  The host outputs hold the results
  * only once the stream has passed them (cudaStreamSynchronize or an event).  Every
  * argument is validated before anything is enqueued.
