@@ -661,10 +661,8 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
         const int key = (i - grp.tile_begin) * kKeyTile + kloc;
         // FP8: the key's fp32 scale; MXFP4: already applied by the MMA
         const float scale = C::MX ? 1.f : reinterpret_cast<const float*>(smem + C::OFF_SCALES + ss * C::SCALE_BYTES)[kloc];
-        for (int j = 0; j < grp.n; ++j) {
-          uint32_t r[32];
-          DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + j * kIdxHeads + (static_cast<uint32_t>(quarter * 32) << 16), r);
-          tmem_wait_ld();
+        // one token's 32 head sums -> its score (and the histogram hand-off)
+        auto finish = [&](const uint32_t (&r)[32], int j) {
           const float4* wv = reinterpret_cast<const float4*>(wsm + (qb * G + j) * kIdxHeads);
           float sum = 0.f;
           if (scale >= 0.f) {
@@ -696,6 +694,20 @@ __global__ void __launch_bounds__(ScorerCfg<IDXF, G>::THREADS, 1)
               else atomicAdd(p.row_hist + static_cast<int64_t>(grp.t0 + j) * kHistBins + bin, 1u);
             }
           }
+        };
+        // groups of several tokens: two tokens' sums per TMEM wait (a wait covers
+        // every load before it, so loads issued together share one latency)
+        constexpr bool PAIR = !C::MX && G > 1;   // MXFP4 kernels have no registers to spare
+        for (int j = 0; j < grp.n; j += PAIR ? 2 : 1) {
+          const bool two = PAIR && j + 1 < grp.n;   // warp-uniform
+          uint32_t r[32], r2[32];
+          DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + j * kIdxHeads + (static_cast<uint32_t>(quarter * 32) << 16), r);
+          if (two)
+            DSA_TMEM_LD32(tmem + acc * C::ACC_COLS + (j + 1) * kIdxHeads + (static_cast<uint32_t>(quarter * 32) << 16),
+                          r2);
+          tmem_wait_ld();
+          finish(r, j);
+          if (two) finish(r2, j + 1);
         }
         tc_fence_before();
         __syncwarp();
