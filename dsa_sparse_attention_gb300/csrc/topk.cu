@@ -11,12 +11,12 @@
 //                 preserving key; the last CTA of the row finds the digit b1 that
 //                 holds the k-th largest key and the count above it.
 //  2. candidates: each chunk counts its keys above digit b1 and appends the keys
-//                 in digit b1 (the candidates) to a per-row list; the last CTA
-//                 of the row resolves the exact threshold key T among them, and
-//                 the position cut for keys equal to T (lowest positions first),
-//                 then counts per chunk how many candidates are taken.  If the
-//                 list overflows (heavy ties), that CTA redoes this step exactly
-//                 over the whole row.
+//                 in digit b1 (the candidates) to a per-row list; then one CTA
+//                 of 1,024 threads per row resolves the exact threshold key T
+//                 among them, and the position cut for keys equal to T (lowest
+//                 positions first), then counts per chunk how many candidates
+//                 are taken.  If the list overflows (heavy ties), that CTA
+//                 redoes this step exactly over the whole row.
 //  3. emit:       ordered compaction: chunk c writes its selected positions after
 //                 those of chunks < c, so the output is ascending, deterministic
 //                 and independent of the rest of the batch.
@@ -246,7 +246,6 @@ __device__ int32_t select_cut(Gen gen, int count, uint32_t T, uint32_t m, uint32
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParams p) {
-  __shared__ uint32_t h[kBins];
   __shared__ uint32_t sh[48];
   __shared__ uint32_t lcount, lbase;
   __shared__ uint2 lc[4096];       // this chunk's candidates (key, position)
@@ -284,10 +283,27 @@ __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParam
   uint2* cand = p.cands + static_cast<int64_t>(t) * p.cap;
   for (uint32_t i = threadIdx.x; i < lcount; i += kTopkThreads)
     if (lbase + i < static_cast<uint32_t>(p.cap)) cand[lbase + i] = lc[i];
-  const int nch = static_cast<int>(cdiv(n, p.chunk));
-  if (!last_of_row(p.done + 2 * t + 1, nch, sh)) return;
+}
 
-  // ---- last CTA of the row: exact threshold and position cut
+// Exact resolution of each row's threshold among its candidates: one CTA of
+// kResolveThreads per row, after every chunk of the row has listed its candidates.
+constexpr int kResolveThreads = 1024;
+
+__global__ void __launch_bounds__(kResolveThreads) topk_resolve_kernel(TopkParams p) {
+  __shared__ uint32_t h[kBins];
+  __shared__ uint32_t sh[48];
+  __shared__ uint2 lc[4096];       // the row's candidates (key, position)
+  const int t = blockIdx.x;
+  int req, pos;
+  load_token(p.b, t, p.status, req, pos);   // inputs of the call, read before the wait
+  grid_dep_wait();     // the candidate pass
+  grid_dep_launch();
+  const int n = pos + 1;
+  if (n <= p.k) return;
+  const int nch = static_cast<int>(cdiv(n, p.chunk));
+  const uint32_t b1 = p.thr[4 * t + 0];
+  const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
+  const uint2* cand = p.cands + static_cast<int64_t>(t) * p.cap;
   const uint32_t r = static_cast<uint32_t>(p.k) - p.thr[4 * t + 1];   // to take from digit b1
   const uint32_t count = __ldcg(p.cand_count + t);
   uint32_t Tlow, aboveT;
@@ -296,7 +312,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParam
   if (count <= static_cast<uint32_t>(p.cap)) {
     // the whole candidate list fits this CTA's staging buffer (cap == 4096)
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < count; i += kTopkThreads) lc[i] = __ldcg(cand + i);
+    for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) lc[i] = __ldcg(cand + i);
     __syncthreads();
     auto gen = [&](int i, uint32_t& key, int32_t& idx) {
       const uint2 c = lc[i];
@@ -314,10 +330,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParam
     const bool in_smem = nch <= kBins;
     if (in_smem) {
       __syncthreads();   // every thread is done reading h
-      for (int c = threadIdx.x; c < nch; c += kTopkThreads) h[c] = 0;
+      for (int c = threadIdx.x; c < nch; c += static_cast<int>(blockDim.x)) h[c] = 0;
       __syncthreads();
     }
-    for (uint32_t i = threadIdx.x; i < count; i += kTopkThreads) {
+    for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) {
       const uint2 c = lc[i];
       const uint32_t lo = c.x & 0x1FFFFFu;
       if (lo > Tlow || (lo == Tlow && static_cast<int32_t>(c.y) <= cut)) {
@@ -328,7 +344,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParam
     }
     if (in_smem) {
       __syncthreads();
-      for (int c = threadIdx.x; c < nch; c += kTopkThreads)
+      for (int c = threadIdx.x; c < nch; c += static_cast<int>(blockDim.x))
         if (h[c]) taken[c] = h[c];
     }
   } else {
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_candidates_kernel(TopkParam
     };
     select_low21(gen, n, r, Tlow, aboveT, h, sh);
     cut = select_cut(gen, n, Tlow, r - aboveT, h, sh);
-    for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+    for (int i = threadIdx.x; i < n; i += static_cast<int>(blockDim.x)) {
       uint32_t key;
       int32_t idx;
       if (gen(i, key, idx) && (key > Tlow || (key == Tlow && idx <= cut)))
@@ -879,6 +895,8 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool chained, bool
   if ((e = launch_ex(topk_hist_kernel, grid, dim3(kTopkThreads), 0, st, chained && zeroed, 0u, p)) != cudaSuccess)
     return e;
   if ((e = launch_ex(topk_candidates_kernel, grid, dim3(kTopkThreads), 0, st, true, 0u, p)) != cudaSuccess) return e;
+  if ((e = launch_ex(topk_resolve_kernel, dim3(p.b.T), dim3(kResolveThreads), 0, st, true, 0u, p)) != cudaSuccess)
+    return e;
   return launch_ex(topk_emit_kernel, grid, dim3(kTopkThreads), 0, st, true, 0u, p);
 }
 
