@@ -581,8 +581,8 @@ def main():
     torch.cuda.synchronize()
 
     # scorer, top-k (one cluster launch for rows up to 65,536 scores, else histogram,
-    # candidates and emit), attention, split combine
-    n_kernels_per_step = 1 + (1 if int(wl.ctx_lens.max()) <= 65536 else 3) + 1 + 1
+    # candidates, resolution and emit), attention, split combine
+    n_kernels_per_step = 1 + (1 if int(wl.ctx_lens.max()) <= 65536 else 4) + 1 + 1
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
