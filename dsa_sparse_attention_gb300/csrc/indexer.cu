@@ -156,8 +156,9 @@ struct ScorerCfg {
   // MXFP4: the block scales of the MMA, A (keys) 4 columns per key stage (key r of
   // the stage at lane r, column r / 32), B (the queries: all 2^0, or with MXFP4
   // queries their exponents) SFB_STRIDE columns per query buffer (token j at column
-  // j).  The MMA takes scale addresses at even columns only (an odd one faults with
-  // a misaligned address); every scale region here starts at a multiple of 4.
+  // j).  A scale address at an odd column (161) faulted with a misaligned address
+  // where columns 160 and 162 worked; every scale region here starts at a multiple
+  // of 4.
   static constexpr int SFA_COL = NACC * ACC_COLS;
   static constexpr int SFB_COL = SFA_COL + 4 * STAGES;
   static constexpr int SFB_STRIDE = (G + 3) / 4 * 4;
