@@ -134,7 +134,9 @@ def make_layout(pool, num_rows, row_stride, idx_page_offset, lat_page_offset, bl
 
 
 def make_batch(q_req, q_pos, ctx_lens, block_table, max_ctx_len, flags=0):
-    """Batch descriptor over device int32 tensors (kept alive by the caller)."""
+    """Batch descriptor over device int32 tensors (kept alive by the caller).  flags:
+    DSA_BATCH_INVARIANT and/or DSA_BATCH_QIDX_MXFP4 (q_idx holds MXFP4 index
+    queries: T x 32 x 64 code bytes, then T x 32 x 4 E8M0 bytes)."""
     return dsa_batch(int(q_req.shape[0]), int(ctx_lens.shape[0]), _ptr(q_req), _ptr(q_pos), _ptr(ctx_lens),
                      _ptr(block_table), int(block_table.shape[1]), int(flags), int(max_ctx_len))
 
@@ -236,8 +238,9 @@ def dsa_selftest_wait_timeout(ws, limit_cycles, stream=None):
 
 def dsa_indexer_front(layout, batch, c_q, norm_weight, eps, w_qi, head_w, q_idx, w_out, k_new=None, ws=None,
                       stream=None):
-    """The fused indexer front: q_idx / w_out for the scorer and, with k_new, the new
-    tokens' index keys written into the pool."""
+    """The fused indexer front: q_idx / w_out for the scorer (e4m3 with folded head
+    weights, or MXFP4 when the batch has DSA_BATCH_QIDX_MXFP4) and, with k_new, the
+    new tokens' index keys written into the pool (FP8 or MXFP4 pages)."""
     _check(library().dsa_indexer_front(ctypes.byref(layout), ctypes.byref(batch), _ptr(c_q), int(c_q.shape[1]),
                                        _ptr(norm_weight), float(eps), _ptr(w_qi), _ptr(head_w), _ptr(k_new),
                                        _ptr(q_idx), _ptr(w_out), _ptr(ws), ws.numel(), _stream(stream)),
